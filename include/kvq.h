@@ -1,0 +1,209 @@
+/*
+ * kvq.h -- C ABI of libkvq.so: decode-phase attention over a quantized KV cache
+ * on one GB300 (sm_103a).
+ *
+ * What is computed.  K is kept as an 8-bit payload, four codes packed per
+ * 32-bit word, with one fp16 scale per 32 head-dim elements ("Flash Attention
+ * for llama.cpp on RDNA3", first paragraph: only the 8-bit K payload and fp16
+ * scales are stored, and four 8-bit values fill one 32-bit word for the dot4
+ * instruction).  V is kept as q4_0 or q8_0 blocks of 32 with an fp16 scale (the
+ * V formats of that page's VRAM and KLD tables).  The cache of a sequence is a
+ * list of append-only segments: new tokens go into the last one, filled tokens
+ * are never copied or moved (BitLLM summary, "What differs").  A query is
+ * quantized per 32-block with the K rule, so q.k is a sum over blocks of exact
+ * int32 dot products scaled by the two fp16 scales (BitLLM summary, "How to
+ * use": the MatMul stays in the integer domain and casts are deferred);
+ * softmax and the P.V product over dequantized V are then evaluated in fp32.
+ *
+ * Quantization rules (bit-exact contract):
+ *   int8 (K, Q, q8_0 V): s = fp16_rn(absmax/127); c = clamp(round_half_away(x/s), -127, 127);
+ *                        s == 0 gives all-zero codes.
+ *   q4_0 (V):            d = fp16_rn(absmax/8); q = clamp(round_half_away(x/d) + 8, 0, 15);
+ *                        value (q-8)*d; d == 0 gives q = 8.
+ * x/s is the correctly rounded fp32 quotient; absmax is over the 32 fp16 inputs.
+ *
+ * Memory.  The library allocates nothing.  Every pointer marked "device" is
+ * caller-owned device memory of the current CUDA device; every pointer marked
+ * "host" is caller-owned host memory read during the call only.  Work is
+ * enqueued on `stream` (a cudaStream_t; NULL = legacy default stream) and is
+ * asynchronous: no call synchronizes the host.  Kernels are chained with
+ * programmatic dependent launch (set KVQ_PDL=0 in the environment to launch
+ * them plainly); calls can be captured into CUDA graphs once the first call on
+ * the device has run outside capture (it caches device attributes).
+ *
+ * Errors.  Arguments are validated before anything is enqueued; a failed
+ * validation returns a status and changes no state (kvq_append bumps segment
+ * lengths only on success).  A launch failure returns KVQ_ERR_CUDA.  Faults
+ * during execution surface at the caller's next synchronization.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_QBLOCK 32          /* quantization block (head-dim elements)          */
+#define KVQ_HEAD_DIM 128       /* the only head_dim this build supports           */
+#define KVQ_SEG_ALIGN 64       /* segment capacity must be a multiple of this     */
+#define KVQ_MAX_ROWS 32        /* query rows per kv head: t_q * (q heads of it)   */
+#define KVQ_MAX_T_Q 8          /* query tokens per sequence per call              */
+#define KVQ_MAX_HEADS 256      /* n_q_heads and n_kv_heads limit                  */
+
+typedef enum kvq_status {
+    KVQ_OK = 0,
+    KVQ_ERR_INVALID_ARG = 1,   /* a pointer, size or layout rule is violated      */
+    KVQ_ERR_UNSUPPORTED = 2,   /* no sm_103 device, or a size this build lacks    */
+    KVQ_ERR_CAPACITY = 3,      /* kvq_append: the open segment is too small       */
+    KVQ_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required      */
+    KVQ_ERR_CUDA = 5           /* a CUDA runtime call or kernel launch failed     */
+} kvq_status;
+
+typedef enum kvq_vtype {
+    KVQ_V_Q4_0 = 0,            /* 16 bytes of nibbles + fp16 scale per 32 values  */
+    KVQ_V_Q8_0 = 1             /* 32 int8 + fp16 scale per 32 values              */
+} kvq_vtype;
+
+/*
+ * One append-only segment of one sequence.  All four arrays are device memory,
+ * 16-byte aligned, head-major, indexed [kv_head][token][...] with token in
+ * [0, cap):
+ *   k_q  int8  [n_kv_heads][cap][head_dim]      (little-endian words: byte i of
+ *                                                word w is element 4w+i)
+ *   k_s  fp16  [n_kv_heads][cap][head_dim/32]
+ *   v_q  q4_0: uint8 [n_kv_heads][cap][head_dim/2], in each 32-block byte j holds
+ *              element j (low nibble) and element j+16 (high nibble);
+ *        q8_0: int8  [n_kv_heads][cap][head_dim]
+ *   v_s  fp16  [n_kv_heads][cap][head_dim/32]
+ * cap  : capacity in tokens, a positive multiple of KVQ_SEG_ALIGN.
+ * len  : tokens filled, 0..cap (host bookkeeping; kvq_append advances it).
+ * pos0 : absolute position of the segment's token 0.  Segment k+1 of a sequence
+ *        must start where segment k ends: pos0[k+1] == pos0[k] + len[k]; the
+ *        first segment starts at 0.  Only the last segment of a sequence is
+ *        open for appends.
+ */
+typedef struct kvq_segment {
+    void *k_q;
+    void *k_s;
+    void *v_q;
+    void *v_s;
+    int32_t cap;
+    int32_t len;
+    int32_t pos0;
+    int32_t reserved;
+} kvq_segment;
+
+/*
+ * Host descriptor of a batch of caches that share shape and V format.
+ * segs is a host array [n_seqs * max_segs]; sequence b uses segs[b*max_segs ..
+ * b*max_segs + n_segs[b] - 1].  n_segs is a host array [n_seqs], each in
+ * 0..max_segs and at most 64 (a sequence with no segment has no positions).
+ * All of it is caller-owned.
+ */
+typedef struct kvq_cache {
+    int32_t n_seqs;
+    int32_t n_kv_heads;
+    int32_t head_dim;          /* must be KVQ_HEAD_DIM                            */
+    int32_t v_type;            /* kvq_vtype                                       */
+    int32_t max_segs;
+    int32_t *n_segs;
+    kvq_segment *segs;
+} kvq_cache;
+
+/*
+ * kvq_append -- quantize new fp16 K/V tokens into the open (last) segment of
+ * each listed sequence (steps "append-quantize K" and "append-quantize V"; the
+ * int8 rule above for K and q8_0 V, the q4_0 rule for q4_0 V).
+ *
+ *  c        host descriptor; on success segs[last].len of every listed sequence
+ *           grows by its n_new.
+ *  n_seqs_in number of listed sequences (0 is a no-op).
+ *  seq_ids  host [n_seqs_in], distinct sequence indices in [0, c->n_seqs).
+ *  n_new    host [n_seqs_in], tokens to append per listed sequence (>= 0).
+ *  k16, v16 device fp16 [sum(n_new)][n_kv_heads][head_dim], token-major, the
+ *           tokens of seq_ids[0] first, 16-byte aligned.
+ *  stream   cudaStream_t.
+ * Every listed sequence with n_new > 0 needs at least one segment.
+ * Returns KVQ_ERR_CAPACITY (nothing enqueued, nothing changed) if some open
+ * segment lacks room; the caller then adds a segment and retries.
+ */
+kvq_status kvq_append(kvq_cache *c, int32_t n_seqs_in, const int32_t *seq_ids,
+                      const int32_t *n_new, const void *k16, const void *v16,
+                      void *stream);
+
+/*
+ * kvq_decode_attn -- split-KV decode attention of every sequence of c.
+ *
+ *  q16       device fp16 [n_seqs][t_q][n_q_heads][head_dim], 16-byte aligned.
+ *            The t_q query tokens of a sequence are its last t_q positions.
+ *  n_q_heads query heads.
+ *  t_q       query tokens per sequence, 1..KVQ_MAX_T_Q.
+ *  causal_tail nonzero: query token i sees positions 0 .. L-t_q+i (a causal mask
+ *            among the t_q newest positions); zero: every query token sees
+ *            0 .. L-1.
+ *  seq_lens  device int32 [n_seqs]: L of each sequence (positions, including
+ *            the t_q new ones).  Positions at or beyond max_len, or beyond the
+ *            last segment's capacity, are ignored.
+ *  max_len   host: upper bound of seq_lens, sizes the grid.
+ *  head_map  host int32 [n_q_heads]: kv head read by each query head, or NULL
+ *            for contiguous groups (query head h reads kv head
+ *            h / (n_q_heads/n_kv_heads)).  t_q times the largest group must
+ *            not exceed KVQ_MAX_ROWS.
+ *  sm_scale  softmax scale applied to q.k (e.g. 1/sqrt(head_dim)).
+ *  out       device fp32 [n_seqs][t_q][n_q_heads][head_dim]: softmax(q.k*sm_scale).v
+ *  lse       device fp32 [n_seqs][t_q][n_q_heads]: natural log of
+ *            sum_t exp(sm_scale*q.k_t).  A row that sees no position gets
+ *            out = 0 and lse = -inf.
+ *  workspace device scratch for the split partials, 256-byte aligned, at
+ *            least kvq_decode_workspace_size() bytes; NULL is allowed when
+ *            that size is 0.
+ *  workspace_bytes size of workspace; KVQ_ERR_WORKSPACE if it is too small.
+ * Launches (per group of at most 64 sequences): the split-KV attention kernel
+ * and, when a sequence is split, the log-sum-exp combine kernel.
+ */
+kvq_status kvq_decode_attn(const kvq_cache *c, const void *q16, int32_t n_q_heads,
+                           int32_t t_q, int32_t causal_tail, const int32_t *seq_lens,
+                           int32_t max_len, const int32_t *head_map, float sm_scale,
+                           float *out, float *lse, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
+ * kvq_decode_workspace_size -- bytes of workspace kvq_decode_attn needs for
+ * these arguments on the current device (0 when no sequence is split).  It
+ * depends on the device's SM count, n_seqs, the heads, t_q, max_len and the
+ * host segment lengths, so query it again after any of them changes.
+ *  bytes  host out.
+ */
+kvq_status kvq_decode_workspace_size(const kvq_cache *c, int32_t n_q_heads, int32_t t_q,
+                                     int32_t max_len, const int32_t *head_map, size_t *bytes);
+
+/* Short English text of a status code (static storage). */
+const char *kvq_status_string(kvq_status s);
+
+/*
+ * kvq_debug_qk -- TEST HOOK, not part of the decode path: runs the same
+ * split-KV attention kernel as kvq_decode_attn with its outputs replaced by
+ * dumps of the quantized query and the raw per-block integer scores, so tests
+ * can compare them bit for bit with an independent implementation.
+ *
+ *  q_codes   device int8 [n_seqs][t_q][n_q_heads][head_dim]
+ *  q_scales  device fp16 bits [n_seqs][t_q][n_q_heads][head_dim/32]
+ *  scores    device int32 [n_seqs][t_q][n_q_heads][max_len][head_dim/32]:
+ *            I_b = sum over the 32 elements of block b of q_code*k_code, for
+ *            every position < L of the sequence (causal masking is not applied
+ *            here); other entries are left untouched.
+ * Other arguments as kvq_decode_attn.
+ */
+kvq_status kvq_debug_qk(const kvq_cache *c, const void *q16, int32_t n_q_heads,
+                        int32_t t_q, const int32_t *seq_lens, int32_t max_len,
+                        const int32_t *head_map, int8_t *q_codes, uint16_t *q_scales,
+                        int32_t *scores, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,171 @@
+// kvq_internal.cuh -- launch-parameter structs and sm_103a device helpers shared
+// by the CUDA translation units of libkvq.so.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kD = KVQ_HEAD_DIM;        // head dim
+constexpr int kNB = kD / KVQ_QBLOCK;    // 32-blocks per head row (4)
+constexpr int kTile = 64;               // tokens per pipeline stage
+constexpr int kWarps = 4;               // warps per split CTA, 16 tokens each per stage
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 4;              // cp.async ring depth
+constexpr int kMaxSegsLaunch = 64;      // segment-table entries per launch
+constexpr int kMaxSeqsLaunch = 64;      // sequences per launch
+
+// One segment as the attention kernel sees it (device pointers of kv head 0;
+// head h starts h*cap tokens further).
+struct SegDesc {
+    const uint32_t *kq;   // [Hkv][cap][kD/4] words
+    const uint16_t *ks;   // [Hkv][cap][kNB] fp16 bits
+    const uint8_t *vq;    // [Hkv][cap][kD/2 or kD]
+    const uint16_t *vs;   // [Hkv][cap][kNB]
+    int pos0;             // absolute position of token 0
+    int cap;              // tokens, multiple of kTile
+};
+
+struct AttnParams {
+    SegDesc seg[kMaxSegsLaunch];
+    uint8_t seq_seg0[kMaxSeqsLaunch];      // first table entry of each sequence
+    uint8_t seq_nseg[kMaxSeqsLaunch];
+    uint8_t grp_q[KVQ_MAX_HEADS];          // query heads listed kv head by kv head
+    uint16_t grp_begin[KVQ_MAX_HEADS + 1]; // kv head h owns grp_q[grp_begin[h] .. grp_begin[h+1])
+    const uint16_t *q;                     // [n_seqs][t_q][Hq][kD] fp16 bits
+    const int *seq_lens;                   // [n_seqs]
+    float *out;                            // [n_seqs][t_q][Hq][kD]       (n_split == 1)
+    float *lse;                            // [n_seqs][t_q][Hq]
+    float *ws_o;                           // [n_seqs][t_q][Hq][n_split][kD] (n_split > 1)
+    float *ws_lse;                         // [n_seqs][t_q][Hq][n_split]
+    int8_t *dbg_qc;                        // test hook outputs (DUMP kernels only)
+    uint16_t *dbg_qs;
+    int32_t *dbg_scores;
+    int n_seqs, n_kv_heads, n_q_heads, t_q, causal;
+    int max_len;                           // positions >= max_len are ignored
+    int n_split, chunk;                    // split s covers [s*chunk, (s+1)*chunk)
+    float qk_scale_log2;                   // sm_scale * log2(e)
+};
+
+struct CombineParams {
+    const float *ws_o;
+    const float *ws_lse;
+    float *out;
+    float *lse;
+    int n_rows;                            // n_seqs * t_q * Hq
+    int n_split;
+};
+
+struct AppendEntry {
+    uint32_t *kq;
+    uint16_t *ks;
+    uint8_t *vq;
+    uint16_t *vs;
+    int cap;                               // tokens
+    int dst;                               // first token slot written
+    int src;                               // first input token row
+    int n;                                 // tokens
+};
+
+struct AppendParams {
+    AppendEntry e[kMaxSeqsLaunch];
+    const uint16_t *k16;                   // [sum n][Hkv][kD]
+    const uint16_t *v16;
+    int n_entries;
+    int n_kv_heads;
+};
+
+// ------------------------------------------------------------ host launchers --
+// Implemented in kvq_append.cu / kvq_attn_q4.cu / kvq_attn_q8.cu.
+// n_tiles8 = query rows per kv head rounded up to 1, 2 or 4 tiles of 8.
+cudaError_t launch_append(const AppendParams &p, int v_type, int max_rows, cudaStream_t s, bool pdl);
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t s, bool pdl);
+cudaError_t launch_split_q4(const AttnParams &p, int n_tiles8, bool dump, cudaStream_t s, bool pdl);
+cudaError_t launch_split_q8(const AttnParams &p, int n_tiles8, bool dump, cudaStream_t s, bool pdl);
+cudaError_t prepare_split_q4(int n_tiles8, bool dump, int *ctas_per_sm);
+cudaError_t prepare_split_q8(int n_tiles8, bool dump, int *ctas_per_sm);
+
+// ------------------------------------------------------------- device helpers --
+
+// Programmatic dependent launch: wait for the producing grid (and its memory)
+// before the first read of anything an earlier kernel wrote.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next PDL-launched grid in the stream to be scheduled.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte global->shared async copy; src_bytes 0 zero-fills without reading.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// D = A(16x32 s8, row) * B(32x8 s8, col) + C, int32 accumulate.
+__device__ __forceinline__ void mma_s8_16832(int (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                             int c)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};\n"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(c));
+}
+
+// D += A(16x16 f16, row) * B(16x8 f16, col), fp32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Transpose an 8x8 matrix of 16-bit elements held one row-pair per lane.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
+{
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint16_t b)
+{
+    return __half2float(__ushort_as_half(b));
+}
+
+// int8 rule of one element given its block scale s (fp32 copy of the fp16 scale).
+__device__ __forceinline__ int quant_i8(float x, float s)
+{
+    if (s == 0.f) return 0;
+    float c = roundf(__fdiv_rn(x, s));          // correctly rounded quotient, ties away
+    return (int)fminf(fmaxf(c, -127.f), 127.f);
+}
+
+// q4_0 rule of one element given d (fp32 copy of the fp16 scale).
+__device__ __forceinline__ int quant_q4(float x, float d)
+{
+    if (d == 0.f) return 8;
+    float c = roundf(__fdiv_rn(x, d)) + 8.f;
+    return (int)fminf(fmaxf(c, 0.f), 15.f);
+}
+
+}  // namespace kvq

@@ -1,0 +1,173 @@
+// kvq_small.cu -- the append/quantize kernel and the split-combine kernel.
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+// ---------------------------------------------------------------------------
+// Append-quantize.  One warp per (token, kv head) row of 128 fp16 values: lane
+// l holds elements 4l..4l+3 (one 8-byte load), so lanes 8b..8b+7 hold 32-block
+// b and a 3-step xor shuffle gives the block absmax.  K (and q8_0 V) codes are
+// packed four per word and stored as one coalesced 128-byte row; q4_0 lanes
+// 0..3 of each block pull the codes of elements 16.. from lanes 4..7 and store
+// byte j = q[j] | q[j+16] << 4.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float block_absmax(const float (&x)[4])
+{
+    float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+    return a;
+}
+
+__device__ __forceinline__ void load4h(const uint16_t *p, float (&x)[4])
+{
+    const uint2 raw = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+}
+
+// int8 rule on one row: returns this lane's packed word and the block scale bits.
+__device__ __forceinline__ uint32_t quant_row_i8(const float (&x)[4], uint16_t &s16)
+{
+    const float a = block_absmax(x);
+    const __half sh = __float2half_rn(__fdiv_rn(a, 127.f));
+    const float s = __half2float(sh);
+    s16 = __half_as_ushort(sh);
+    uint32_t w = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w |= (uint32_t)(quant_i8(x[k], s) & 0xff) << (8 * k);
+    return w;
+}
+
+template <int VT>
+__global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ AppendParams p)
+{
+    pdl_wait();      // inputs come from earlier kernels; the cache may still be read by one
+    pdl_trigger();
+    const AppendEntry &e = p.e[blockIdx.y];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = p.n_kv_heads;
+    const int row = blockIdx.x * 4 + warp;
+    const int tok = row / H, h = row - tok * H;
+    if (tok >= e.n) return;   // warp-uniform
+    const size_t src = ((size_t)(e.src + tok) * H + h) * kD + lane * 4;
+    const size_t dst = (size_t)h * e.cap + e.dst + tok;   // token row in the segment
+
+    float x[4];
+    uint16_t s16;
+    load4h(p.k16 + src, x);
+    const uint32_t kw = quant_row_i8(x, s16);
+    e.kq[dst * (kD / 4) + lane] = kw;
+    if ((lane & 7) == 0) e.ks[dst * kNB + (lane >> 3)] = s16;
+
+    load4h(p.v16 + src, x);
+    if (VT == KVQ_V_Q8_0) {
+        const uint32_t vw = quant_row_i8(x, s16);
+        reinterpret_cast<uint32_t *>(e.vq)[dst * (kD / 4) + lane] = vw;
+        if ((lane & 7) == 0) e.vs[dst * kNB + (lane >> 3)] = s16;
+    } else {
+        const float a = block_absmax(x);
+        const __half dh = __float2half_rn(a * 0.125f);   // absmax/8, exact before rounding
+        const float d = __half2float(dh);
+        uint32_t q = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) q |= (uint32_t)quant_q4(x[k], d) << (8 * k);
+        const uint32_t qhi = __shfl_down_sync(0xffffffffu, q, 4);   // elements 16.. of the block
+        if ((lane & 7) < 4)
+            reinterpret_cast<uint32_t *>(e.vq)[dst * (kD / 8) + (lane >> 3) * 4 + (lane & 3)] = q | (qhi << 4);
+        if ((lane & 7) == 0) e.vs[dst * kNB + (lane >> 3)] = __half_as_ushort(dh);
+    }
+}
+
+cudaError_t launch_append(const AppendParams &p, int v_type, int max_rows, cudaStream_t s, bool pdl)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((max_rows + 3) / 4, p.n_entries);
+    cfg.blockDim = dim3(128);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (v_type == KVQ_V_Q4_0) return cudaLaunchKernelEx(&cfg, append_kernel<KVQ_V_Q4_0>, p);
+    return cudaLaunchKernelEx(&cfg, append_kernel<KVQ_V_Q8_0>, p);
+}
+
+// ---------------------------------------------------------------------------
+// Split combine: per query row, M = max_s lse_s, w_s = exp(lse_s - M),
+// out = sum_s w_s o_s / sum_s w_s, lse = M + log(sum_s w_s).  One CTA per row,
+// thread = head dim; splits with lse = -inf (no visible position) weigh 0 and
+// their o is never read.
+// ---------------------------------------------------------------------------
+constexpr int kMaxSplit = 1024;
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float *red)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float t = __shfl_xor_sync(0xffffffffu, v, o);
+        v = is_max ? fmaxf(v, t) : v + t;
+    }
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    v = red[0];
+#pragma unroll
+    for (int w = 1; w < 4; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+    return v;
+}
+
+__global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ CombineParams p)
+{
+    __shared__ float w_s[kMaxSplit];
+    __shared__ float red[4];
+    pdl_wait();
+    pdl_trigger();
+    const int row = blockIdx.x, tid = threadIdx.x, n = p.n_split;
+    const float *ls = p.ws_lse + (size_t)row * n;
+    float M = -INFINITY;
+    for (int s = tid; s < n; s += 128) {
+        const float v = ls[s];
+        w_s[s] = v;
+        M = fmaxf(M, v);
+    }
+    M = block_reduce(M, true, red);
+    float W = 0.f;
+    for (int s = tid; s < n; s += 128) {
+        const float v = w_s[s];
+        const float w = (v == -INFINITY) ? 0.f : expf(v - M);
+        w_s[s] = w;
+        W += w;
+    }
+    W = block_reduce(W, false, red);   // the reduce's barriers also publish w_s
+    float acc = 0.f;
+    const float *o = p.ws_o + (size_t)row * n * kD + tid;
+    for (int s = 0; s < n; ++s) {
+        const float w = w_s[s];
+        if (w != 0.f) acc = fmaf(w, o[(size_t)s * kD], acc);
+    }
+    const bool any = W > 0.f;
+    p.out[(size_t)row * kD + tid] = any ? acc / W : 0.f;
+    if (tid == 0) p.lse[row] = any ? M + logf(W) : -INFINITY;
+}
+
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t s, bool pdl)
+{
+    if (p.n_split > kMaxSplit) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_rows);
+    cfg.blockDim = dim3(kD);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, p);
+}
+
+}  // namespace kvq

@@ -1,0 +1,214 @@
+"""ctypes binding of libkvq.so (include/kvq.h): argument marshalling only.
+
+Every step of the decode path runs in the library's CUDA kernels; torch only
+provides device memory and the stream handle.  Importing this module does not
+load the library; the first call does, and raises if libkvq.so is missing --
+there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from ctypes import POINTER, c_float, c_int32, c_size_t, c_void_p
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvq.so")
+
+KVQ_OK = 0
+KVQ_ERR_INVALID_ARG = 1
+KVQ_ERR_UNSUPPORTED = 2
+KVQ_ERR_CAPACITY = 3
+KVQ_ERR_WORKSPACE = 4
+KVQ_ERR_CUDA = 5
+V_Q4_0 = 0
+V_Q8_0 = 1
+HEAD_DIM = 128
+SEG_ALIGN = 64
+QBLOCK = 32
+
+EXPORTED = ("kvq_append", "kvq_decode_attn", "kvq_decode_workspace_size", "kvq_status_string", "kvq_debug_qk")
+
+
+class KvqSegment(ctypes.Structure):
+    _fields_ = [("k_q", c_void_p), ("k_s", c_void_p), ("v_q", c_void_p), ("v_s", c_void_p),
+                ("cap", c_int32), ("len", c_int32), ("pos0", c_int32), ("reserved", c_int32)]
+
+
+class KvqCache(ctypes.Structure):
+    _fields_ = [("n_seqs", c_int32), ("n_kv_heads", c_int32), ("head_dim", c_int32),
+                ("v_type", c_int32), ("max_segs", c_int32), ("n_segs", POINTER(c_int32)),
+                ("segs", POINTER(KvqSegment))]
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s failed: %s (%d)" % (what, status_string(status), status))
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load():
+    """Load libkvq.so (built by ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libkvq.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+            lib = ctypes.CDLL(LIB_PATH)
+            lib.kvq_status_string.restype = ctypes.c_char_p
+            lib.kvq_status_string.argtypes = [c_int32]
+            lib.kvq_append.restype = c_int32
+            lib.kvq_append.argtypes = [POINTER(KvqCache), c_int32, POINTER(c_int32), POINTER(c_int32),
+                                       c_void_p, c_void_p, c_void_p]
+            lib.kvq_decode_attn.restype = c_int32
+            lib.kvq_decode_attn.argtypes = [POINTER(KvqCache), c_void_p, c_int32, c_int32, c_int32, c_void_p,
+                                            c_int32, POINTER(c_int32), c_float, c_void_p, c_void_p, c_void_p,
+                                            c_size_t, c_void_p]
+            lib.kvq_decode_workspace_size.restype = c_int32
+            lib.kvq_decode_workspace_size.argtypes = [POINTER(KvqCache), c_int32, c_int32, c_int32,
+                                                      POINTER(c_int32), POINTER(c_size_t)]
+            lib.kvq_debug_qk.restype = c_int32
+            lib.kvq_debug_qk.argtypes = [POINTER(KvqCache), c_void_p, c_int32, c_int32, c_void_p, c_int32,
+                                         POINTER(c_int32), c_void_p, c_void_p, c_void_p, c_void_p]
+            _lib = lib
+    return _lib
+
+
+def status_string(s: int) -> str:
+    return load().kvq_status_string(int(s)).decode()
+
+
+def _ptr(t):
+    return None if t is None else c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _i32(vals):
+    vals = [int(v) for v in vals]
+    return (c_int32 * max(1, len(vals)))(*vals)
+
+
+class Cache:
+    """A batch of append-only segmented caches (device memory from torch).
+
+    Holds the host descriptor of include/kvq.h and keeps the segment tensors
+    alive.  Segment arrays are allocated with the byte layout of kvq_segment.
+    """
+
+    def __init__(self, n_seqs: int, n_kv_heads: int, v_type: int, max_segs: int = 8,
+                 head_dim: int = HEAD_DIM, device=None):
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.n_seqs, self.n_kv_heads, self.v_type, self.head_dim = n_seqs, n_kv_heads, v_type, head_dim
+        self.max_segs = max_segs
+        self._segs = (KvqSegment * max(1, n_seqs * max_segs))()
+        self._nsegs = (c_int32 * max(1, n_seqs))()
+        self.desc = KvqCache(n_seqs, n_kv_heads, head_dim, v_type, max_segs,
+                             ctypes.cast(self._nsegs, POINTER(c_int32)),
+                             ctypes.cast(self._segs, POINTER(KvqSegment)))
+        self.tensors = [[] for _ in range(n_seqs)]
+
+    def seg(self, b: int, k: int) -> KvqSegment:
+        return self._segs[b * self.max_segs + k]
+
+    def n_segs(self, b: int) -> int:
+        return self._nsegs[b]
+
+    def add_segment(self, b: int, cap: int):
+        """Open a new segment of `cap` tokens (rounded up to 64) for sequence b."""
+        ns = self._nsegs[b]
+        if ns >= self.max_segs:
+            raise ValueError("sequence %d already has max_segs segments" % b)
+        cap = max(SEG_ALIGN, (int(cap) + SEG_ALIGN - 1) // SEG_ALIGN * SEG_ALIGN)
+        H, D = self.n_kv_heads, self.head_dim
+        vb = D // 2 if self.v_type == V_Q4_0 else D
+        t = dict(k_q=torch.empty((H, cap, D), dtype=torch.int8, device=self.device),
+                 k_s=torch.empty((H, cap, D // QBLOCK), dtype=torch.int16, device=self.device),
+                 v_q=torch.empty((H, cap, vb), dtype=torch.uint8, device=self.device),
+                 v_s=torch.empty((H, cap, D // QBLOCK), dtype=torch.int16, device=self.device))
+        pos0 = 0
+        if ns:
+            prev = self.seg(b, ns - 1)
+            pos0 = prev.pos0 + prev.len
+        s = self.seg(b, ns)
+        s.k_q, s.k_s, s.v_q, s.v_s = (t[n].data_ptr() for n in ("k_q", "k_s", "v_q", "v_s"))
+        s.cap, s.len, s.pos0 = cap, 0, pos0
+        self.tensors[b].append(t)
+        self._nsegs[b] = ns + 1
+        return t
+
+    def length(self, b: int) -> int:
+        ns = self._nsegs[b]
+        if not ns:
+            return 0
+        s = self.seg(b, ns - 1)
+        return s.pos0 + s.len
+
+    def lengths(self):
+        return [self.length(b) for b in range(self.n_seqs)]
+
+    def export(self, b: int):
+        """Test helper: the filled positions of sequence b gathered to host
+        numpy arrays in logical order ([H][L][...] per array)."""
+        import numpy as np
+        parts = {n: [] for n in ("kq", "ks", "vq", "vs")}
+        for k in range(self._nsegs[b]):
+            s, t = self.seg(b, k), self.tensors[b][k]
+            parts["kq"].append(t["k_q"][:, :s.len].cpu().numpy())
+            parts["ks"].append(t["k_s"][:, :s.len].cpu().numpy().view(np.uint16))
+            parts["vq"].append(t["v_q"][:, :s.len].cpu().numpy())
+            parts["vs"].append(t["v_s"][:, :s.len].cpu().numpy().view(np.uint16))
+        return {n: np.concatenate(v, axis=1) for n, v in parts.items()}
+
+
+def kvq_append(cache: Cache, seq_ids, n_new, k16: torch.Tensor, v16: torch.Tensor, stream=None) -> None:
+    """kvq_append of include/kvq.h.  k16/v16: fp16 [sum(n_new)][Hkv][D] on the device."""
+    ids, nn = list(seq_ids), list(n_new)
+    st = load().kvq_append(ctypes.byref(cache.desc), len(ids), _i32(ids), _i32(nn), _ptr(k16), _ptr(v16),
+                           _stream(stream))
+    if st:
+        raise KvqError(st, "kvq_append")
+
+
+def kvq_decode_workspace_size(cache: Cache, n_q_heads: int, t_q: int, max_len: int, head_map=None) -> int:
+    """Bytes of workspace kvq_decode_attn needs for these arguments."""
+    size = c_size_t(0)
+    hm = None if head_map is None else _i32(head_map)
+    st = load().kvq_decode_workspace_size(ctypes.byref(cache.desc), n_q_heads, t_q, max_len, hm,
+                                          ctypes.byref(size))
+    if st:
+        raise KvqError(st, "kvq_decode_workspace_size")
+    return size.value
+
+
+def kvq_decode_attn(cache: Cache, q16: torch.Tensor, n_q_heads: int, t_q: int, causal_tail: bool,
+                    seq_lens: torch.Tensor, max_len: int, head_map, sm_scale: float, out: torch.Tensor,
+                    lse: torch.Tensor, workspace: torch.Tensor | None, stream=None) -> None:
+    """kvq_decode_attn of include/kvq.h (workspace: a uint8 device tensor of at
+    least kvq_decode_workspace_size() bytes, or None when that size is 0)."""
+    hm = None if head_map is None else _i32(head_map)
+    st = load().kvq_decode_attn(ctypes.byref(cache.desc), _ptr(q16), n_q_heads, t_q, int(causal_tail),
+                                _ptr(seq_lens), max_len, hm, float(sm_scale), _ptr(out), _ptr(lse),
+                                _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                                _stream(stream))
+    if st:
+        raise KvqError(st, "kvq_decode_attn")
+
+
+def kvq_debug_qk(cache: Cache, q16, n_q_heads, t_q, seq_lens, max_len, head_map, q_codes, q_scales, scores,
+                 stream=None) -> None:
+    """kvq_debug_qk test hook of include/kvq.h."""
+    hm = None if head_map is None else _i32(head_map)
+    st = load().kvq_debug_qk(ctypes.byref(cache.desc), _ptr(q16), n_q_heads, t_q, _ptr(seq_lens), max_len, hm,
+                             _ptr(q_codes), _ptr(q_scales), _ptr(scores), _stream(stream))
+    if st:
+        raise KvqError(st, "kvq_debug_qk")

@@ -1,0 +1,70 @@
+"""Parity at the workloads' full sizes, in the launch configuration the
+benchmark times (default split policy): cache bytes of sampled positions,
+sampled query rows' out/lse, and sampled int32 block scores, each against the
+oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+
+import oracle
+from quantized_kv_cache_03_gb300 import workloads as W
+
+from kvq_cases import Case, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _sample_check(case, seqs, n_rows=6, seed=0):
+    rng = np.random.default_rng(seed)
+    out, lse = case.decode()
+    qc, qs, sc = case.debug_qk()
+    for b in seqs:
+        L = case.lens[b]
+        oc = case.oracle_cache(b)
+        got = case.cache.export(b)
+        pos = np.unique(np.concatenate([np.arange(min(L, 300)), np.arange(max(0, L - 300), L),
+                                        rng.integers(0, L, 2000)]))
+        for name in ("kq", "ks", "vq", "vs"):
+            assert np.array_equal(got[name].view(np.uint8)[:, pos], oc[name].view(np.uint8)[:, pos]), name
+        nr = case.tq * case.Hq
+        rows = np.unique(np.concatenate([[0, nr - 1], rng.integers(0, nr, n_rows)]))
+        mask = np.zeros(nr, np.uint8)
+        mask[rows] = 1
+        ref = case.oracle_decode(b, row_mask=mask, want_scores=True)
+        assert_close(out[b], lse[b], ref, rows=rows, what="seq %d" % b)
+        for r in rows:
+            i, h = divmod(int(r), case.Hq)
+            vis = L - case.tq + i + 1 if case.spec.causal else L
+            assert np.array_equal(sc[b, i, h, :vis], ref["scores"][i, h, :vis]), "scores row %d" % r
+            assert np.array_equal(qc[b, i, h], ref["q_codes"][i, h])
+
+
+def test_long_context_main_and_draft_full_size():
+    for spec in W.make_spec("long"):
+        case = Case(spec).build()
+        _sample_check(case, [0])
+
+
+def test_batched_full_size():
+    spec = W.make_spec("batched")[0]
+    case = Case(spec).build()
+    lens = np.array(case.lens)
+    _sample_check(case, [int(lens.argmax()), int(lens.argmin()), 17], n_rows=4)
+
+
+def test_verify_full_size():
+    spec = W.make_spec("verify")[0]
+    case = Case(spec).build()
+    _sample_check(case, [0, 15], n_rows=6)
+
+
+def test_single_full_size_all_rows():
+    spec = W.make_spec("single")[0]
+    case = Case(spec).build()
+    out, lse = case.decode()
+    assert_close(out[0], lse[0], case.oracle_decode(0))

@@ -1,0 +1,48 @@
+"""GPU vs oracle on the same seeded inputs, through the C ABI.
+
+Bar: cache bytes, query codes/scales and per-block int32 scores bit-exact;
+out within 2e-3 and lse within 1e-4 (max abs)."""
+import numpy as np
+import pytest
+
+import oracle
+from quantized_kv_cache_03_gb300 import workloads as W
+
+from kvq_cases import Case, assert_cache_bytes, assert_close
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    "tiny": dict(),                               # 256 positions, GQA 4, q8_0
+    "single": dict(),                             # 8192 positions, outliers, q4_0
+    "long": dict(ctx=5000),                       # 4 segments, GQA 5 main + GQA 4 draft
+    "batched": dict(ctx=4096, n_seqs=6),          # ragged lengths, q8_0, outliers
+    "verify": dict(ctx=3000, n_seqs=2),           # t_q = 4 causal, 32 rows per kv head
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_config_parity(name):
+    for spec in W.make_spec(name, **SMALL[name]):
+        case = Case(spec).build()
+        out, lse = case.decode()
+        for b in range(case.B):
+            oc = case.oracle_cache(b)
+            assert_cache_bytes(case, b, oc)
+            ref = case.oracle_decode(b, want_scores=True)
+            assert_close(out[b], lse[b], ref, what="%s seq %d" % (spec.name, b))
+        qc, qs, sc = case.debug_qk()
+        for b in range(case.B):
+            ref = case.oracle_decode(b, want_scores=True)
+            assert np.array_equal(qc[b], ref["q_codes"]), "query codes"
+            assert np.array_equal(qs[b], ref["q_scales"]), "query scales"
+            L = case.lens[b]
+            for i in range(case.tq):
+                vis = L - case.tq + i + 1 if spec.causal else L
+                assert np.array_equal(sc[b, i, :, :vis], ref["scores"][i, :, :vis]), "int32 block scores"
