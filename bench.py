@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", default="bench", choices=["bench", "profile"],
+                    help="profile: one cache copy, a few directly launched steps, no timing (for ncu)")
+    ap.add_argument("--ctx", type=int, default=None, help="shrink the workload's context (profile mode)")
     return ap.parse_args()
 
 
@@ -190,7 +193,7 @@ def main():
     rank, world, local = dist_env()
     from quantized_kv_cache_03_gb300 import workloads as W
 
-    specs = W.make_spec(args.workload)
+    specs = W.make_spec(args.workload, ctx=args.ctx)
     kv_bytes = W.step_kv_bytes(specs)
     tokens_per_step = sum(s.n_seqs * s.t_q for s in specs)
     threads = os.cpu_count() or 1
@@ -227,6 +230,23 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     data = [HostData(s) for s in specs]
+    if args.mode == "profile":
+        grp = [DecodeSet(d, dev) for d in data]
+        for ds in grp:
+            ds.staging = None
+        for _ in range(max(1, args.warmup) + max(1, args.steps)):
+            for ds in grp:
+                ds.append_step()
+            for ds in grp:
+                ds.decode()
+            for ds in grp:
+                ds.rewind()
+        torch.cuda.synchronize()
+        print(json.dumps({"mode": "profile", "workload": args.workload, "ctx": args.ctx,
+                          "steps": max(1, args.warmup) + max(1, args.steps),
+                          "launches_per_step": sum(ds.launches_per_step() for ds in grp),
+                          "kv_bytes_per_step": kv_bytes}), flush=True)
+        return
     n_rot = max(3, -(-3 * L2_BYTES // max(1, kv_bytes)))
     n_rot = min(n_rot, 64)
     first = [DecodeSet(d, dev) for d in data]
@@ -261,7 +281,9 @@ def main():
             step(grp)
     # per-cache timing graphs: events around each decode call (separate pass)
     g_ev = torch.cuda.CUDAGraph()
-    ev_pairs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    # external event nodes: their timestamps can be read after each replay
+    ev_pairs = [[(torch.cuda.Event(enable_timing=True, external=True),
+                  torch.cuda.Event(enable_timing=True, external=True))
                  for _ in sets[0]] for _ in sets]
     with torch.cuda.graph(g_ev, stream=stream):
         for grp, evs in zip(sets, ev_pairs):

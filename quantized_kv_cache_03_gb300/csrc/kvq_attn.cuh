@@ -479,26 +479,33 @@ __global__ void __launch_bounds__(kThreads) split_attn_kernel(const __grid_const
             sm_m[warp * 8 * NT + 8 * nt + g] = m[nt];
             sm_l[warp * 8 * NT + 8 * nt + g] = l[nt];
         }
-    for (int i = tid; i < 8 * NT * kD; i += kThreads) sm_o[i] = 0.f;
     __syncthreads();
+    // Fixed merge order (warp 0 stores, warps 1..3 add in turn) so results do
+    // not depend on scheduling; each (row, dim) belongs to one lane per warp.
+    for (int w = 0; w < kWarps; ++w) {
+        if (warp == w) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int row = 8 * nt + 2 * c + e;
-            if (row >= R) continue;
-            float M = -INFINITY;
+                for (int e = 0; e < 2; ++e) {
+                    const int row = 8 * nt + 2 * c + e;
+                    if (row >= R) continue;
+                    float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * 8 * NT + row]);
-            const float mw = sm_m[warp * 8 * NT + row];
-            const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+                    for (int v = 0; v < kWarps; ++v) M = fmaxf(M, sm_m[v * 8 * NT + row]);
+                    const float mw = sm_m[w * 8 * NT + row];
+                    const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                atomicAdd(&sm_o[row * kD + pv_dim<VT>(mt, g)], acc[mt][nt][e] * f);
-                atomicAdd(&sm_o[row * kD + pv_dim<VT>(mt, g + 8)], acc[mt][nt][2 + e] * f);
-            }
+                    for (int mt = 0; mt < 8; ++mt) {
+                        float *o0 = &sm_o[row * kD + pv_dim<VT>(mt, g)];
+                        float *o1 = &sm_o[row * kD + pv_dim<VT>(mt, g + 8)];
+                        *o0 = (w == 0 ? 0.f : *o0) + acc[mt][nt][e] * f;
+                        *o1 = (w == 0 ? 0.f : *o1) + acc[mt][nt][2 + e] * f;
+                    }
+                }
         }
-    __syncthreads();
+        __syncthreads();
+    }
     for (int row = 0; row < R; ++row) {
         float M = -INFINITY;
 #pragma unroll
