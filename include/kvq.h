@@ -153,7 +153,8 @@ kvq_status kvq_append(kvq_cache *c, int32_t n_seqs_in, const int32_t *seq_ids,
  *            h / (n_q_heads/n_kv_heads)).  t_q times the largest group must
  *            not exceed KVQ_MAX_ROWS.
  *  sm_scale  softmax scale applied to q.k (e.g. 1/sqrt(head_dim)).
- *  out       device fp32 [n_seqs][t_q][n_q_heads][head_dim]: softmax(q.k*sm_scale).v
+ *  out       device fp32 [n_seqs][t_q][n_q_heads][head_dim], 16-byte aligned:
+ *            softmax(q.k*sm_scale).v
  *  lse       device fp32 [n_seqs][t_q][n_q_heads]: natural log of
  *            sum_t exp(sm_scale*q.k_t).  A row that sees no position gets
  *            out = 0 and lse = -inf.

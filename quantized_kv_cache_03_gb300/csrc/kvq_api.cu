@@ -171,6 +171,7 @@ void choose_split(const kvq_cache *c, const Group &g, int max_len, int slots, in
         if (lmin * 2 >= lmax || total == 0) {
             const int n_min = std::max(1, (slots + pairs - 1) / pairs);
             double best = -1.0;
+            n = std::min(n_min, max_n);   // short contexts: as many splits as the 256-position floor allows
             for (int k = n_min; k <= 4 * n_min && k <= max_n; ++k) {
                 const double waves = (double)pairs * k / slots;
                 const double eff = waves / std::ceil(waves);
@@ -267,6 +268,7 @@ kvq_status run_decode(const DecodeArgs &a)
     if (!a.size_out) {
         if (!a.q16 || !aligned16(a.q16) || !a.seq_lens) return KVQ_ERR_INVALID_ARG;
         if (a.dump ? (!a.dbg_qc || !a.dbg_qs || !a.dbg_scores) : (!a.out || !a.lse)) return KVQ_ERR_INVALID_ARG;
+        if (!a.dump && (!aligned16(a.out) || (reinterpret_cast<uintptr_t>(a.lse) & 3u))) return KVQ_ERR_INVALID_ARG;
     }
 
     DeviceInfo *dev = nullptr;

@@ -7,11 +7,14 @@
 //
 // Data path per 64-token stage (cp.async 16-byte copies into a 4-deep shared
 // ring, XOR-swizzled so every fragment read below is bank-conflict free):
-//   * QK^T: int8 tensor-core MMA m16n8k32 -- A = the query codes (rows), B = the
-//     packed K words of 8 positions, one MMA per 32-block, so each accumulator
-//     is the exact integer block dot I_b (never summed across blocks before
-//     scaling).  The accumulator starts at the bit pattern of 1.5*2^23 so that
-//     reinterpreting it as fp32 and subtracting 1.5*2^23 yields I_b exactly.
+//   * QK^T: fp16 tensor-core MMA m16n8k16 on exact integers -- A = the query
+//     codes (rows), B = the K codes of 8 positions entered as 1152 + code (one
+//     xor and two byte-permutes per packed word), two MMAs per 32-block into
+//     one accumulator that starts at -1152 * (sum of the row's codes in the
+//     block).  Every partial sum is an integer below 2^24, so the fp32
+//     accumulator ends exactly at the integer block dot I_b (never summed
+//     across blocks before scaling).  (GB300's int8 mma.sync issues ~8x slower
+//     than the fp16 one, which is why the integer dot runs on the fp16 path.)
 //   * score = sum_b I_b * (sq_b * sk_b) * sm_scale*log2(e), masked to -inf
 //     outside the sequence / causal range; online softmax in base 2 with the
 //     running max only raised when some row's maximum grows.
@@ -25,6 +28,8 @@
 // Warps: 4, each owns 16 positions of every stage and keeps its own (m, l, acc);
 // the four states are merged through shared memory at the end.
 #pragma once
+
+#include <type_traits>
 
 #include "kvq_internal.cuh"
 
@@ -42,7 +47,8 @@ struct SplitCfg {
     static constexpr int STAGE = VS_OFF + kTile * kNB * 2;
     static constexpr int Q_OFF = kStages * STAGE;            // int8 [QROWS][kD]
     static constexpr int QS_OFF = Q_OFF + QROWS * kD;        // fp32 [QROWS][kNB]
-    static constexpr int ML_OFF = QS_OFF + QROWS * kNB * 4;  // fp32 m, l [kWarps][8*NT]
+    static constexpr int QSUM_OFF = QS_OFF + QROWS * kNB * 4; // int32 [QROWS][kNB]
+    static constexpr int ML_OFF = QSUM_OFF + QROWS * kNB * 4; // fp32 m, l [kWarps][8*NT]
     static constexpr int SMEM = ML_OFF + 2 * kWarps * 8 * NT * 4;
     static_assert(8 * NT * kD * 4 <= kStages * STAGE, "merge buffer must fit in the stage ring");
 };
@@ -182,13 +188,37 @@ __device__ __forceinline__ void unpack4h(uint2 raw, float (&x)[4])
     x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
 }
 
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Four signed int8 K codes -> two fp16 pairs holding 1152 + code (exact): the
+// byte is biased by 128 (xor 0x80) and placed under the binary16 exponent of
+// 1024 (0x64XX = 1024 + XX).
+__device__ __forceinline__ void k_word_biased(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t x = w ^ 0x80808080u;
+    lo = __byte_perm(x, 0x64646464u, 0x4140);
+    hi = __byte_perm(x, 0x64646464u, 0x4342);
+}
+
+// Two signed int8 codes (bytes k0, k1 of w) -> exact fp16 pair.
+__device__ __forceinline__ uint32_t q_pair(uint32_t w, int k0)
+{
+    const __half2 h = __halves2half2(__int2half_rn((int)(int8_t)(w >> (8 * k0))),
+                                     __int2half_rn((int)(int8_t)(w >> (8 * k0 + 8))));
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
 template <int NT, int VT, bool DUMP>
 __global__ void __launch_bounds__(kThreads) split_attn_kernel(const __grid_constant__ AttnParams p)
 {
     using C = SplitCfg<NT, VT>;
     constexpr int MTQ = C::MTQ;
-    constexpr float kMagic = 12582912.0f;            // 1.5 * 2^23
-    constexpr int kMagicBits = 0x4B400000;
+    constexpr float kBias = 1152.0f;                 // K codes enter the MMA as 1152 + code
     extern __shared__ __align__(128) uint8_t smem[];
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -219,35 +249,7 @@ __global__ void __launch_bounds__(kThreads) split_attn_kernel(const __grid_const
         return;
     }
 
-    // ---- quantize the query rows of this kv head (int8 rule, fp16 scale) ----
-    uint32_t *qw = reinterpret_cast<uint32_t *>(smem + C::Q_OFF);
-    float *qs = reinterpret_cast<float *>(smem + C::QS_OFF);
-    for (int r = warp; r < C::QROWS; r += kWarps) {
-        uint32_t word = 0;
-        float s = 0.f;
-        if (r < R) {
-            const int i = r / gsz, hq = p.grp_q[gb + r % gsz];
-            const size_t qrow = ((size_t)b * p.t_q + i) * p.n_q_heads + hq;
-            float x[4];
-            unpack4h(*reinterpret_cast<const uint2 *>(p.q + qrow * kD + lane * 4), x);
-            float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-            const __half sh = __float2half_rn(__fdiv_rn(a, 127.f));
-            s = __half2float(sh);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) word |= (uint32_t)(quant_i8(x[k], s) & 0xff) << (8 * k);
-            if (DUMP && split == 0) {
-                reinterpret_cast<uint32_t *>(p.dbg_qc)[qrow * (kD / 4) + lane] = word;
-                if ((lane & 7) == 0) p.dbg_qs[qrow * kNB + (lane >> 3)] = __half_as_ushort(sh);
-            }
-        }
-        qw[r * (kD / 4) + lane] = word;
-        if ((lane & 7) == 0) qs[r * kNB + (lane >> 3)] = s * p.qk_scale_log2;
-    }
-
-    // ---- tile schedule ----
+    // ---- tile schedule; start the copies before the query prologue ----
     int n_tiles = 0;
     for (int k = 0; k < nseg; ++k) {
         int la, le;
@@ -265,20 +267,74 @@ __global__ void __launch_bounds__(kThreads) split_attn_kernel(const __grid_const
         cp_async_commit();
     }
 
+    // ---- quantize the query rows of this kv head (int8 rule, fp16 scale) ----
+    uint32_t *qw = reinterpret_cast<uint32_t *>(smem + C::Q_OFF);
+    float *qs = reinterpret_cast<float *>(smem + C::QS_OFF);
+    int *qsum = reinterpret_cast<int *>(smem + C::QSUM_OFF);
+    for (int r = warp; r < C::QROWS; r += kWarps) {
+        uint32_t word = 0;
+        float s = 0.f;
+        int sum = 0;
+        if (r < R) {
+            const int i = r / gsz, hq = p.grp_q[gb + r % gsz];
+            const size_t qrow = ((size_t)b * p.t_q + i) * p.n_q_heads + hq;
+            float x[4];
+            unpack4h(*reinterpret_cast<const uint2 *>(p.q + qrow * kD + lane * 4), x);
+            float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+            const __half sh = __float2half_rn(__fdiv_rn(a, 127.f));
+            s = __half2float(sh);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int code = quant_i8(x[k], s);
+                word |= (uint32_t)(code & 0xff) << (8 * k);
+                sum += code;
+            }
+            if (DUMP && split == 0) {
+                reinterpret_cast<uint32_t *>(p.dbg_qc)[qrow * (kD / 4) + lane] = word;
+                if ((lane & 7) == 0) p.dbg_qs[qrow * kNB + (lane >> 3)] = __half_as_ushort(sh);
+            }
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        qw[r * (kD / 4) + lane] = word;
+        if ((lane & 7) == 0) {
+            qs[r * kNB + (lane >> 3)] = s * p.qk_scale_log2;
+            qsum[r * kNB + (lane >> 3)] = sum;
+        }
+    }
     __syncthreads();   // query codes visible
 
-    // query A fragments (rows 16*mq + g / + 8) and per-lane row state
-    uint32_t qa[MTQ][kNB][4];
+    // Query A fragments (fp16, exact codes).  Within block bb, k16 step ks, this
+    // lane's k slots (2c, 2c+1 | 2c+8, 2c+9) carry head dims
+    // 32bb + 8c + 4ks + (0, 1 | 2, 3): the bytes of word 8bb + 2c + ks, the same
+    // word the lane reads from K, so q.k is unchanged.
+    uint32_t qa[MTQ][kNB][2][4];
+    float cinit[MTQ][kNB][2];   // -1152 * sum of the row's codes in the block
 #pragma unroll
     for (int mq = 0; mq < MTQ; ++mq)
 #pragma unroll
         for (int bb = 0; bb < kNB; ++bb) {
-            const uint2 lo = *reinterpret_cast<const uint2 *>(qw + (16 * mq + g) * (kD / 4) + 8 * bb + 2 * c);
-            const uint2 hi = *reinterpret_cast<const uint2 *>(qw + (16 * mq + g + 8) * (kD / 4) + 8 * bb + 2 * c);
-            qa[mq][bb][0] = lo.x; qa[mq][bb][1] = hi.x; qa[mq][bb][2] = lo.y; qa[mq][bb][3] = hi.y;
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const uint32_t w0 = qw[(16 * mq + g) * (kD / 4) + 8 * bb + 2 * c + ks];
+                const uint32_t w1 = qw[(16 * mq + g + 8) * (kD / 4) + 8 * bb + 2 * c + ks];
+                qa[mq][bb][ks][0] = q_pair(w0, 0);
+                qa[mq][bb][ks][2] = q_pair(w0, 2);
+                // with at most 8 rows, rows 8..15 of the tile are padding: keep them
+                // compile-time zeros so they occupy no registers
+                qa[mq][bb][ks][1] = NT == 1 ? 0u : q_pair(w1, 0);
+                qa[mq][bb][ks][3] = NT == 1 ? 0u : q_pair(w1, 2);
+            }
+            cinit[mq][bb][0] = -kBias * (float)qsum[(16 * mq + g) * kNB + bb];
+            cinit[mq][bb][1] = NT == 1 ? 0.f : -kBias * (float)qsum[(16 * mq + g + 8) * kNB + bb];
         }
     float sqf[NT][kNB], m[NT], l[NT];
     int lim[NT];
+    int lim_min = 0x7fffffff;   // smallest visible-position limit over live rows
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int row = 8 * nt + g;
@@ -288,6 +344,7 @@ __global__ void __launch_bounds__(kThreads) split_attn_kernel(const __grid_const
         m[nt] = -INFINITY;
         l[nt] = 0.f;
     }
+    lim_min = p.causal ? L - p.t_q : L - 1;
     float acc[8][NT][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
@@ -313,155 +370,179 @@ __global__ void __launch_bounds__(kThreads) split_attn_kernel(const __grid_const
         const int pos_base = p.seg[seg0 + cc.k].pos0 + tb;
         cursor_next(p, seg0, nseg, r0, r1, cc);
         if (tb + u0w >= le || tb + u0w + 16 <= la) continue;   // no valid token for this warp
+        // every token of this warp's 16 valid and visible to every live row?
+        const bool full = tb + u0w >= la && tb + u0w + 16 <= le && pos_base + u0w + 15 <= lim_min;
 
-        // ---- S = Q K^T per 32-block (exact int32), then scaled scores ----
-        float s[2][NT][2];
+        auto chunk = [&](auto full_tag) {
+            constexpr bool FULL = decltype(full_tag)::value;
+            // ---- S = Q K^T per 32-block (exact integers in fp32), scaled scores ----
+            float s[2][NT][2];
 #pragma unroll
-        for (int sub = 0; sub < 2; ++sub) {
-            const int u = u0w + 8 * sub + g;                  // K column this lane supplies
-            int sc[MTQ][kNB][4];
+            for (int sub = 0; sub < 2; ++sub) {
+                const int u = u0w + 8 * sub + g;              // K column this lane supplies
+                float sc[MTQ][kNB][4];
 #pragma unroll
-            for (int bb = 0; bb < kNB; ++bb) {
-                const uint2 kb = *reinterpret_cast<const uint2 *>(st + C::K_OFF + u * kD +
-                                                                  (((2 * bb + (c >> 1)) ^ g) << 4) + ((c & 1) << 3));
+                for (int bb = 0; bb < kNB; ++bb) {
+                    const uint2 kb = *reinterpret_cast<const uint2 *>(st + C::K_OFF + u * kD +
+                                                                      (((2 * bb + (c >> 1)) ^ g) << 4) + ((c & 1) << 3));
+                    uint32_t b00, b01, b10, b11;
+                    k_word_biased(kb.x, b00, b01);
+                    k_word_biased(kb.y, b10, b11);
 #pragma unroll
-                for (int mq = 0; mq < MTQ; ++mq) mma_s8_16832(sc[mq][bb], qa[mq][bb], kb.x, kb.y, kMagicBits);
-            }
-            // K scales of this lane's two score columns (tokens u0w + 8sub + 2c + e)
-            const int ut = u0w + 8 * sub + 2 * c;
-            const uint4 ksr = *reinterpret_cast<const uint4 *>(st + C::KS_OFF + ut * kNB * 2);
-            float sk[2][kNB];
-            {
-                const float2 a0 = __half22float2(*reinterpret_cast<const __half2 *>(&ksr.x));
-                const float2 a1 = __half22float2(*reinterpret_cast<const __half2 *>(&ksr.y));
-                const float2 a2 = __half22float2(*reinterpret_cast<const __half2 *>(&ksr.z));
-                const float2 a3 = __half22float2(*reinterpret_cast<const __half2 *>(&ksr.w));
-                sk[0][0] = a0.x; sk[0][1] = a0.y; sk[0][2] = a1.x; sk[0][3] = a1.y;
-                sk[1][0] = a2.x; sk[1][1] = a2.y; sk[1][2] = a3.x; sk[1][3] = a3.y;
-            }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int mq = nt >> 1, idx = 2 * (nt & 1) + e;
-                    float a = 0.f;
-#pragma unroll
-                    for (int bb = 0; bb < kNB; ++bb)
-                        a = fmaf(__int_as_float(sc[mq][bb][idx]) - kMagic, sqf[nt][bb] * sk[e][bb], a);
-                    const int tok = tb + ut + e;
-                    const bool ok = tok >= la && tok < le && pos_base + ut + e <= lim[nt];
-                    s[sub][nt][e] = ok ? a : -INFINITY;
+                    for (int mq = 0; mq < MTQ; ++mq) {
+                        sc[mq][bb][0] = sc[mq][bb][1] = cinit[mq][bb][0];
+                        sc[mq][bb][2] = sc[mq][bb][3] = cinit[mq][bb][1];
+                        mma_f16_16816(sc[mq][bb], qa[mq][bb][0], b00, b01);
+                        mma_f16_16816(sc[mq][bb], qa[mq][bb][1], b10, b11);
+                    }
                 }
-            if (DUMP) {
+                // K scales of this lane's two score columns (tokens u0w + 8sub + 2c + e)
+                const int ut = u0w + 8 * sub + 2 * c;
+                const uint4 ksr = *reinterpret_cast<const uint4 *>(st + C::KS_OFF + ut * kNB * 2);
+                float sk[2][kNB];
+                {
+                    const float2 a0 = __half22float2(*reinterpret_cast<const __half2 *>(&ksr.x));
+                    const float2 a1 = __half22float2(*reinterpret_cast<const __half2 *>(&ksr.y));
+                    const float2 a2 = __half22float2(*reinterpret_cast<const __half2 *>(&ksr.z));
+                    const float2 a3 = __half22float2(*reinterpret_cast<const __half2 *>(&ksr.w));
+                    sk[0][0] = a0.x; sk[0][1] = a0.y; sk[0][2] = a1.x; sk[0][3] = a1.y;
+                    sk[1][0] = a2.x; sk[1][1] = a2.y; sk[1][2] = a3.x; sk[1][3] = a3.y;
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int row = 8 * nt + g, tok = tb + ut + e, pos = pos_base + ut + e;
-                        if (row < R && tok >= la && tok < le && pos < L) {
-                            const int mq = nt >> 1, idx = 2 * (nt & 1) + e;
-                            const int i = row / gsz, hq = p.grp_q[gb + row % gsz];
-                            const size_t o = ((((size_t)b * p.t_q + i) * p.n_q_heads + hq) * p.max_len + pos) * kNB;
-                            int4 v;
-                            v.x = sc[mq][0][idx] - kMagicBits; v.y = sc[mq][1][idx] - kMagicBits;
-                            v.z = sc[mq][2][idx] - kMagicBits; v.w = sc[mq][3][idx] - kMagicBits;
-                            *reinterpret_cast<int4 *>(p.dbg_scores + o) = v;
+                        const int mq = nt >> 1, idx = 2 * (nt & 1) + e;
+                        float a = 0.f;
+#pragma unroll
+                        for (int bb = 0; bb < kNB; ++bb) a = fmaf(sc[mq][bb][idx], sqf[nt][bb] * sk[e][bb], a);
+                        if (FULL) {
+                            s[sub][nt][e] = a;
+                        } else {
+                            const int tok = tb + ut + e;
+                            const bool ok = tok >= la && tok < le && pos_base + ut + e <= lim[nt];
+                            s[sub][nt][e] = ok ? a : -INFINITY;
                         }
                     }
-            }
-        }
-        if (DUMP) continue;
-
-        // ---- online softmax (base 2) ----
-        bool grow = false;
-        float mnew[NT];
+                if (DUMP) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            float mx = fmaxf(fmaxf(s[0][nt][0], s[0][nt][1]), fmaxf(s[1][nt][0], s[1][nt][1]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            mnew[nt] = fmaxf(m[nt], mx);
-            grow |= mnew[nt] > m[nt];
-        }
-        if (__any_sync(0xffffffffu, grow)) {
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int row = 8 * nt + g, tok = tb + ut + e, pos = pos_base + ut + e;
+                            if (row < R && tok >= la && tok < le && pos < L) {
+                                const int mq = nt >> 1, idx = 2 * (nt & 1) + e;
+                                const int i = row / gsz, hq = p.grp_q[gb + row % gsz];
+                                const size_t o = ((((size_t)b * p.t_q + i) * p.n_q_heads + hq) * p.max_len + pos) * kNB;
+                                int4 v;
+                                v.x = (int)sc[mq][0][idx]; v.y = (int)sc[mq][1][idx];
+                                v.z = (int)sc[mq][2][idx]; v.w = (int)sc[mq][3][idx];
+                                *reinterpret_cast<int4 *>(p.dbg_scores + o) = v;
+                            }
+                        }
+                }
+            }
+            if (DUMP) return;
+
+            // ---- online softmax (base 2) ----
+            bool grow = false;
+            float mnew[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const float al = (mnew[nt] == -INFINITY) ? 1.f : exp2f(m[nt] - mnew[nt]);
-                l[nt] *= al;
-                m[nt] = mnew[nt];
-                const float a0 = __shfl_sync(0xffffffffu, al, 8 * c);       // row 8nt + 2c
-                const float a1 = __shfl_sync(0xffffffffu, al, 8 * c + 4);   // row 8nt + 2c + 1
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    acc[mt][nt][0] *= a0; acc[mt][nt][1] *= a1;
-                    acc[mt][nt][2] *= a0; acc[mt][nt][3] *= a1;
-                }
+                float mx = fmaxf(fmaxf(s[0][nt][0], s[0][nt][1]), fmaxf(s[1][nt][0], s[1][nt][1]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                mnew[nt] = fmaxf(m[nt], mx);
+                grow |= mnew[nt] > m[nt];
             }
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const float mu = (m[nt] == -INFINITY) ? 0.f : m[nt];
-#pragma unroll
-            for (int sub = 0; sub < 2; ++sub)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    s[sub][nt][e] = exp2f(s[sub][nt][e] - mu);
-                    l[nt] += s[sub][nt][e];
-                }
-        }
-
-        // ---- O += P . V  (per 32-block: B = p*d as fp16 hi + lo, A = V codes) ----
-        float dv[2][2][kNB];   // [sub][e][block] V scales of this lane's B columns, 0 if invalid
-#pragma unroll
-        for (int sub = 0; sub < 2; ++sub) {
-            const int ut = u0w + 8 * sub + 2 * c;
-            const uint4 vsr = *reinterpret_cast<const uint4 *>(st + C::VS_OFF + ut * kNB * 2);
-            const float2 a0 = __half22float2(*reinterpret_cast<const __half2 *>(&vsr.x));
-            const float2 a1 = __half22float2(*reinterpret_cast<const __half2 *>(&vsr.y));
-            const float2 a2 = __half22float2(*reinterpret_cast<const __half2 *>(&vsr.z));
-            const float2 a3 = __half22float2(*reinterpret_cast<const __half2 *>(&vsr.w));
-            const bool ok0 = tb + ut >= la && tb + ut < le, ok1 = tb + ut + 1 >= la && tb + ut + 1 < le;
-            dv[sub][0][0] = ok0 ? a0.x : 0.f; dv[sub][0][1] = ok0 ? a0.y : 0.f;
-            dv[sub][0][2] = ok0 ? a1.x : 0.f; dv[sub][0][3] = ok0 ? a1.y : 0.f;
-            dv[sub][1][0] = ok1 ? a2.x : 0.f; dv[sub][1][1] = ok1 ? a2.y : 0.f;
-            dv[sub][1][2] = ok1 ? a3.x : 0.f; dv[sub][1][3] = ok1 ? a3.y : 0.f;
-        }
-#pragma unroll
-        for (int bb = 0; bb < kNB; ++bb) {
-            uint32_t bhi[NT][2], blo[NT][2];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int sub = 0; sub < 2; ++sub) {
-                    const float x0 = s[sub][nt][0] * dv[sub][0][bb];
-                    const float x1 = s[sub][nt][1] * dv[sub][1][bb];
-                    const uint32_t hv = pack_half2(x0, x1);
-                    const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hv));
-                    bhi[nt][sub] = hv;
-                    blo[nt][sub] = pack_half2(x0 - hf.x, x1 - hf.y);
-                }
-            uint32_t t[2][4];
-#pragma unroll
-            for (int sub = 0; sub < 2; ++sub) {
-                uint32_t P[4];
-                v_codes_to_half2<VT>(st + C::V_OFF, u0w + 8 * sub + g, bb, c, P);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) t[sub][i] = movmatrix_t(P[i]);
-            }
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const uint32_t a[4] = {t[0][2 * h2], t[0][2 * h2 + 1], t[1][2 * h2], t[1][2 * h2 + 1]};
+            if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    mma_f16_16816(acc[2 * bb + h2][nt], a, bhi[nt][0], bhi[nt][1]);
-                    mma_f16_16816(acc[2 * bb + h2][nt], a, blo[nt][0], blo[nt][1]);
+                    const float al = (mnew[nt] == -INFINITY) ? 1.f : fast_exp2(m[nt] - mnew[nt]);
+                    l[nt] *= al;
+                    m[nt] = mnew[nt];
+                    const float a0 = __shfl_sync(0xffffffffu, al, 8 * c);       // row 8nt + 2c
+                    const float a1 = __shfl_sync(0xffffffffu, al, 8 * c + 4);   // row 8nt + 2c + 1
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        acc[mt][nt][0] *= a0; acc[mt][nt][1] *= a1;
+                        acc[mt][nt][2] *= a0; acc[mt][nt][3] *= a1;
+                    }
                 }
             }
-        }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float mu = (m[nt] == -INFINITY) ? 0.f : m[nt];
+#pragma unroll
+                for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        s[sub][nt][e] = fast_exp2(s[sub][nt][e] - mu);
+                        l[nt] += s[sub][nt][e];
+                    }
+            }
+
+            // ---- O += P . V  (per 32-block: B = p*d as fp16 hi + lo, A = V codes) ----
+            float dv[2][2][kNB];   // [sub][e][block] V scales of this lane's B columns, 0 if invalid
+#pragma unroll
+            for (int sub = 0; sub < 2; ++sub) {
+                const int ut = u0w + 8 * sub + 2 * c;
+                const uint4 vsr = *reinterpret_cast<const uint4 *>(st + C::VS_OFF + ut * kNB * 2);
+                const float2 a0 = __half22float2(*reinterpret_cast<const __half2 *>(&vsr.x));
+                const float2 a1 = __half22float2(*reinterpret_cast<const __half2 *>(&vsr.y));
+                const float2 a2 = __half22float2(*reinterpret_cast<const __half2 *>(&vsr.z));
+                const float2 a3 = __half22float2(*reinterpret_cast<const __half2 *>(&vsr.w));
+                bool ok0 = true, ok1 = true;
+                if (!FULL) {
+                    ok0 = tb + ut >= la && tb + ut < le;
+                    ok1 = tb + ut + 1 >= la && tb + ut + 1 < le;
+                }
+                dv[sub][0][0] = ok0 ? a0.x : 0.f; dv[sub][0][1] = ok0 ? a0.y : 0.f;
+                dv[sub][0][2] = ok0 ? a1.x : 0.f; dv[sub][0][3] = ok0 ? a1.y : 0.f;
+                dv[sub][1][0] = ok1 ? a2.x : 0.f; dv[sub][1][1] = ok1 ? a2.y : 0.f;
+                dv[sub][1][2] = ok1 ? a3.x : 0.f; dv[sub][1][3] = ok1 ? a3.y : 0.f;
+            }
+#pragma unroll
+            for (int bb = 0; bb < kNB; ++bb) {
+                uint32_t bhi[NT][2], blo[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int sub = 0; sub < 2; ++sub) {
+                        const float x0 = s[sub][nt][0] * dv[sub][0][bb];
+                        const float x1 = s[sub][nt][1] * dv[sub][1][bb];
+                        const uint32_t hv = pack_half2(x0, x1);
+                        const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hv));
+                        bhi[nt][sub] = hv;
+                        blo[nt][sub] = pack_half2(x0 - hf.x, x1 - hf.y);
+                    }
+                uint32_t t[2][4];
+#pragma unroll
+                for (int sub = 0; sub < 2; ++sub) {
+                    uint32_t P[4];
+                    v_codes_to_half2<VT>(st + C::V_OFF, u0w + 8 * sub + g, bb, c, P);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) t[sub][i] = movmatrix_t(P[i]);
+                }
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const uint32_t a[4] = {t[0][2 * h2], t[0][2 * h2 + 1], t[1][2 * h2], t[1][2 * h2 + 1]};
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_f16_16816(acc[2 * bb + h2][nt], a, bhi[nt][0], bhi[nt][1]);
+                        mma_f16_16816(acc[2 * bb + h2][nt], a, blo[nt][0], blo[nt][1]);
+                    }
+                }
+            }
+        };
+        if (full)
+            chunk(std::integral_constant<bool, true>());
+        else
+            chunk(std::integral_constant<bool, false>());
     }
 
     cp_async_wait<0>();
-    if (DUMP) return;
+    if constexpr (!DUMP) {
 
     // ---- merge the four warps' (m, l, acc) and write ----
 #pragma unroll
@@ -528,6 +609,7 @@ __global__ void __launch_bounds__(kThreads) split_attn_kernel(const __grid_const
             p.ws_o[(orow * p.n_split + split) * kD + tid] = o;
             if (tid == 0) p.ws_lse[orow * p.n_split + split] = ls;
         }
+    }
     }
 }
 

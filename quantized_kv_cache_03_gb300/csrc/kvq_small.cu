@@ -98,61 +98,86 @@ cudaError_t launch_append(const AppendParams &p, int v_type, int max_rows, cudaS
 
 // ---------------------------------------------------------------------------
 // Split combine: per query row, M = max_s lse_s, w_s = exp(lse_s - M),
-// out = sum_s w_s o_s / sum_s w_s, lse = M + log(sum_s w_s).  One CTA per row,
-// thread = head dim; splits with lse = -inf (no visible position) weigh 0 and
-// their o is never read.
+// out = sum_s w_s o_s / sum_s w_s, lse = M + log(sum_s w_s).  One CTA per row;
+// 8 warps take every 8th split and each lane four head dims (float4), with four
+// partials in flight per warp, then the warps' sums are added in a fixed
+// order.  Splits with lse = -inf (no visible position) weigh 0 and their o is
+// never read.
 // ---------------------------------------------------------------------------
 constexpr int kMaxSplit = 1024;
+constexpr int kCombineWarps = 8;
 
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float *red)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float t = __shfl_xor_sync(0xffffffffu, v, o);
-        v = is_max ? fmaxf(v, t) : v + t;
-    }
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    v = red[0];
-#pragma unroll
-    for (int w = 1; w < 4; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
-    return v;
-}
-
-__global__ void __launch_bounds__(128) combine_kernel(const __grid_constant__ CombineParams p)
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __grid_constant__ CombineParams p)
 {
     __shared__ float w_s[kMaxSplit];
-    __shared__ float red[4];
+    __shared__ float red[kCombineWarps];
+    __shared__ float4 part[kCombineWarps][32];
     pdl_wait();
     pdl_trigger();
-    const int row = blockIdx.x, tid = threadIdx.x, n = p.n_split;
+    const int row = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, n = p.n_split;
     const float *ls = p.ws_lse + (size_t)row * n;
     float M = -INFINITY;
-    for (int s = tid; s < n; s += 128) {
+    for (int s = tid; s < n; s += kCombineWarps * 32) {
         const float v = ls[s];
         w_s[s] = v;
         M = fmaxf(M, v);
     }
-    M = block_reduce(M, true, red);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (lane == 0) red[warp] = M;
+    __syncthreads();
+    M = red[0];
+#pragma unroll
+    for (int w = 1; w < kCombineWarps; ++w) M = fmaxf(M, red[w]);
     float W = 0.f;
-    for (int s = tid; s < n; s += 128) {
+    for (int s = tid; s < n; s += kCombineWarps * 32) {
         const float v = w_s[s];
-        const float w = (v == -INFINITY) ? 0.f : expf(v - M);
-        w_s[s] = w;
-        W += w;
+        const float wv = (v == -INFINITY) ? 0.f : expf(v - M);
+        w_s[s] = wv;
+        W += wv;
     }
-    W = block_reduce(W, false, red);   // the reduce's barriers also publish w_s
-    float acc = 0.f;
-    const float *o = p.ws_o + (size_t)row * n * kD + tid;
-    for (int s = 0; s < n; ++s) {
-        const float w = w_s[s];
-        if (w != 0.f) acc = fmaf(w, o[(size_t)s * kD], acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+    __syncthreads();   // all reads of red[] above are done; w_s complete
+    if (lane == 0) red[warp] = W;
+    __syncthreads();
+    W = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) W += red[w];
+
+    const float4 *o = reinterpret_cast<const float4 *>(p.ws_o + (size_t)row * n * kD) + lane;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = warp; s0 < n; s0 += 4 * kCombineWarps) {
+        float4 v[4];
+        float wv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int s = s0 + k * kCombineWarps;
+            wv[k] = (s < n) ? w_s[s] : 0.f;
+            v[k] = wv[k] != 0.f ? o[(size_t)s * (kD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            acc.x = fmaf(wv[k], v[k].x, acc.x);
+            acc.y = fmaf(wv[k], v[k].y, acc.y);
+            acc.z = fmaf(wv[k], v[k].z, acc.z);
+            acc.w = fmaf(wv[k], v[k].w, acc.w);
+        }
     }
-    const bool any = W > 0.f;
-    p.out[(size_t)row * kD + tid] = any ? acc / W : 0.f;
-    if (tid == 0) p.lse[row] = any ? M + logf(W) : -INFINITY;
+    part[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0) {
+        float4 t = part[0][lane];
+#pragma unroll
+        for (int w = 1; w < kCombineWarps; ++w) {
+            t.x += part[w][lane].x; t.y += part[w][lane].y; t.z += part[w][lane].z; t.w += part[w][lane].w;
+        }
+        const bool any = W > 0.f;
+        const float inv = any ? 1.f / W : 0.f;
+        float4 r = make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
+        reinterpret_cast<float4 *>(p.out + (size_t)row * kD)[lane] = r;
+        if (lane == 0) p.lse[row] = any ? M + logf(W) : -INFINITY;
+    }
 }
 
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s, bool pdl)
@@ -160,7 +185,7 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t s, bool pdl)
     if (p.n_split > kMaxSplit) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_rows);
-    cfg.blockDim = dim3(kD);
+    cfg.blockDim = dim3(kCombineWarps * 32);
     cfg.stream = s;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
