@@ -181,6 +181,36 @@ kvq_status kvq_decode_attn(const kvq_cache *c, const void *q16, int32_t n_q_head
 kvq_status kvq_decode_workspace_size(const kvq_cache *c, int32_t n_q_heads, int32_t t_q,
                                      int32_t max_len, const int32_t *head_map, size_t *bytes);
 
+/*
+ * kvq_decode_attn_noalloc -- kvq_decode_attn for callers that cannot allocate
+ * device memory.  (The pages have no counterpart: this is a library-usage
+ * variant, not a step of the method.)  Typical callers: code recorded into a
+ * CUDA graph or running inside a latency-critical decode loop, where a
+ * cudaMalloc (which may synchronize the device) is not allowed, and runtimes
+ * whose memory manager owns all device memory and has no way to hand over a
+ * temporary buffer.  Inputs and outputs are still passed by the caller; only
+ * the split partials go to a scratch array inside the library.
+ *
+ *  The scratch is one file-scope device array of KVQ_NOALLOC_SCRATCH_BYTES
+ *  (32 MiB) that every GPU loading the library holds until the process exits.
+ *  The call allocates nothing and calls no allocating routine.  If this call's
+ *  partials would need more than KVQ_NOALLOC_SCRATCH_BYTES it returns
+ *  KVQ_ERR_WORKSPACE and enqueues nothing (kvq_decode_workspace_size gives the
+ *  need; roughly rows x splits x 516 bytes).
+ *  The first call on a device looks up the array's device address (once per
+ *  device, with that device current); make that first call before any stream
+ *  capture.  All calls share the array and it keeps the last call's contents;
+ *  nothing in it has to start at zero, because every partial a call reads was
+ *  written earlier in the same call.  Calls whose work overlaps on the GPU
+ *  (other streams, or other host threads) race on the array: serialize them.
+ * Other arguments and results as kvq_decode_attn.
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (32u << 20)
+kvq_status kvq_decode_attn_noalloc(const kvq_cache *c, const void *q16, int32_t n_q_heads,
+                                   int32_t t_q, int32_t causal_tail, const int32_t *seq_lens,
+                                   int32_t max_len, const int32_t *head_map, float sm_scale,
+                                   float *out, float *lse, void *stream);
+
 /* Short English text of a status code (static storage). */
 const char *kvq_status_string(kvq_status s);
 

@@ -505,3 +505,52 @@ kvq_status kvq_debug_qk(const kvq_cache *c, const void *q16, int32_t n_q_heads, 
 }
 
 }  // extern "C"
+
+// Scratch of kvq_decode_attn_noalloc: a file-scope device array, so callers
+// that cannot allocate never need to pass a workspace.  Host code must not use
+// the symbol itself as a pointer; its device address is looked up once per
+// device below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices];
+
+// Device address of g_noalloc_scratch on the current device (looked up once).
+kvq_status noalloc_scratch(void **ptr)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return KVQ_ERR_UNSUPPORTED;
+    }
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return KVQ_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return KVQ_OK;
+}
+}  // namespace
+
+extern "C" kvq_status kvq_decode_attn_noalloc(const kvq_cache *c, const void *q16, int32_t n_q_heads, int32_t t_q,
+                                              int32_t causal_tail, const int32_t *seq_lens, int32_t max_len,
+                                              const int32_t *head_map, float sm_scale, float *out, float *lse,
+                                              void *stream)
+{
+    kvq_status st = check_cache(c);   // reject bad descriptors before touching the device
+    if (st != KVQ_OK) return st;
+    DeviceInfo *dev = nullptr;
+    st = device_setup(&dev);
+    if (st != KVQ_OK) return st;
+    void *scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != KVQ_OK) return st;
+    return kvq_decode_attn(c, q16, n_q_heads, t_q, causal_tail, seq_lens, max_len, head_map, sm_scale, out, lse,
+                           scratch, KVQ_NOALLOC_SCRATCH_BYTES, stream);
+}

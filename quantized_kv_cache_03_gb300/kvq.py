@@ -28,7 +28,9 @@ HEAD_DIM = 128
 SEG_ALIGN = 64
 QBLOCK = 32
 
-EXPORTED = ("kvq_append", "kvq_decode_attn", "kvq_decode_workspace_size", "kvq_status_string", "kvq_debug_qk")
+EXPORTED = ("kvq_append", "kvq_decode_attn", "kvq_decode_workspace_size", "kvq_decode_attn_noalloc",
+            "kvq_status_string", "kvq_debug_qk")
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class KvqSegment(ctypes.Structure):
@@ -72,6 +74,10 @@ def load():
             lib.kvq_decode_workspace_size.restype = c_int32
             lib.kvq_decode_workspace_size.argtypes = [POINTER(KvqCache), c_int32, c_int32, c_int32,
                                                       POINTER(c_int32), POINTER(c_size_t)]
+            lib.kvq_decode_attn_noalloc.restype = c_int32
+            lib.kvq_decode_attn_noalloc.argtypes = [POINTER(KvqCache), c_void_p, c_int32, c_int32, c_int32,
+                                                    c_void_p, c_int32, POINTER(c_int32), c_float, c_void_p,
+                                                    c_void_p, c_void_p]
             lib.kvq_debug_qk.restype = c_int32
             lib.kvq_debug_qk.argtypes = [POINTER(KvqCache), c_void_p, c_int32, c_int32, c_void_p, c_int32,
                                          POINTER(c_int32), c_void_p, c_void_p, c_void_p, c_void_p]
@@ -202,6 +208,20 @@ def kvq_decode_attn(cache: Cache, q16: torch.Tensor, n_q_heads: int, t_q: int, c
                                 _stream(stream))
     if st:
         raise KvqError(st, "kvq_decode_attn")
+
+
+def kvq_decode_attn_noalloc(cache: Cache, q16: torch.Tensor, n_q_heads: int, t_q: int, causal_tail: bool,
+                            seq_lens: torch.Tensor, max_len: int, head_map, sm_scale: float, out: torch.Tensor,
+                            lse: torch.Tensor, stream=None) -> None:
+    """kvq_decode_attn_noalloc of include/kvq.h: no workspace argument; the split
+    partials use the library's fixed device scratch (see the header for the
+    size limit, the first-call set-up and the no-overlap rule)."""
+    hm = None if head_map is None else _i32(head_map)
+    st = load().kvq_decode_attn_noalloc(ctypes.byref(cache.desc), _ptr(q16), n_q_heads, t_q, int(causal_tail),
+                                        _ptr(seq_lens), max_len, hm, float(sm_scale), _ptr(out), _ptr(lse),
+                                        _stream(stream))
+    if st:
+        raise KvqError(st, "kvq_decode_attn_noalloc")
 
 
 def kvq_debug_qk(cache: Cache, q16, n_q_heads, t_q, seq_lens, max_len, head_map, q_codes, q_scales, scores,

@@ -1,0 +1,64 @@
+"""kvq_decode_attn_noalloc: the decode entry point for callers that cannot
+allocate device memory (graph-recorded or latency-critical loops where
+cudaMalloc is not allowed, runtimes whose allocator owns all device memory).
+
+It must give the same results as kvq_decode_attn with a caller workspace, on
+two calls in a row (the second call runs over whatever the first left in the
+shared scratch), and reject a call whose partials would not fit the scratch.
+This file is collected last on purpose."""
+import numpy as np
+import pytest
+import torch
+
+from quantized_kv_cache_03_gb300 import kvq
+from quantized_kv_cache_03_gb300 import workloads as W
+
+from kvq_cases import SM_SCALE, Case, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _noalloc(case):
+    s = case.spec
+    dev = torch.device("cuda", 0)
+    q16 = torch.from_numpy(case.q).to(dev)
+    lens = torch.tensor(case.lens, dtype=torch.int32, device=dev)
+    out = torch.full((case.B, case.tq, case.Hq, 128), float("nan"), dtype=torch.float32, device=dev)
+    lse = torch.full((case.B, case.tq, case.Hq), float("nan"), dtype=torch.float32, device=dev)
+    kvq.kvq_decode_attn_noalloc(case.cache, q16, case.Hq, case.tq, s.causal, lens, case.max_len, None, SM_SCALE,
+                                out, lse)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), lse.cpu().numpy()
+
+
+def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row():
+    # two different caches back to back: the second call reuses the scratch
+    # the first one filled
+    cases = [Case(W.make_spec("long", ctx=6000)[0]).build(),
+             Case(W.make_spec("batched", ctx=3000, n_seqs=5)[0]).build()]
+    for case in cases:
+        assert kvq.kvq_decode_workspace_size(case.cache, case.Hq, case.tq, case.max_len) > 0  # uses scratch
+        o_ref, l_ref = case.decode()
+        o, l = _noalloc(case)
+        for b in range(case.B):
+            assert_close(o[b], l[b], {"out": o_ref[b].astype(np.float64), "lse": l_ref[b].astype(np.float64)},
+                         what="noalloc vs workspace, seq %d" % b)
+        ref = case.oracle_decode(0)
+        assert_close(o[0], l[0], ref, what="noalloc vs oracle")
+
+
+def test_noalloc_rejects_partials_beyond_the_scratch(monkeypatch):
+    monkeypatch.setenv("KVQ_SPLIT", "64")    # many splits -> partials above 32 MiB
+    spec = W.make_spec("verify", ctx=8192, n_seqs=4)[0]
+    case = Case(spec).build()
+    need = kvq.kvq_decode_workspace_size(case.cache, case.Hq, case.tq, case.max_len)
+    assert need > kvq.NOALLOC_SCRATCH_BYTES
+    with pytest.raises(kvq.KvqError) as e:
+        _noalloc(case)
+    assert e.value.status == kvq.KVQ_ERR_WORKSPACE
