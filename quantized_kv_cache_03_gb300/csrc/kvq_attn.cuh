@@ -5,8 +5,14 @@
 // the positions [s*chunk, (s+1)*chunk) of sequence b and writes either the
 // final output (one split) or a partial (normalised o, lse) for the combine.
 //
-// Data path per 64-token stage (cp.async 16-byte copies into a 4-deep shared
-// ring, XOR-swizzled so every fragment read below is bank-conflict free):
+// Data path: every warp streams its own contiguous quarter of the CTA's
+// positions through a private ring of 16-position stages in shared memory
+// (16-byte cp.async copies issued by the warp itself).  Rows are padded
+// (K 160 B, q4_0 V 80 B, q8_0 V 144 B) so that every fragment read below is
+// bank-conflict free and every address is a per-lane constant plus an
+// immediate.  Only __syncwarp runs in the main loop; the block synchronizes
+// once for the query prologue and once to merge the four warps at the end.
+//
 //   * QK^T: fp16 tensor-core MMA m16n8k16 on exact integers -- A = the query
 //     codes (rows), B = the K codes of 8 positions entered as 1152 + code (one
 //     xor and two byte-permutes per packed word), two MMAs per 32-block into
@@ -19,14 +25,16 @@
 //     outside the sequence / causal range; online softmax in base 2 with the
 //     running max only raised when some row's maximum grows.
 //   * P.V: fp16 tensor-core MMA m16n8k16 with fp32 accumulation.  The V codes
-//     enter as exact small integers in fp16 (built from the nibbles/bytes with
-//     the binary16 exponent trick: 0x6400|n is 1024+n), turned token-paired by
-//     an in-register 8x8 transpose (movmatrix).  The per-(position, block)
-//     scale d rides on the P side: B = p*d split into an fp16 high part and an
-//     fp16 low part (two MMAs), so P.V keeps ~22 bits of the fp32 product.
+//     enter as exact small integers in fp16 (binary16 exponent trick: 0x6400|n
+//     is 1024+n).  Each lane reads the same head dims of two adjacent positions
+//     and interleaves them with byte permutes, which yields the
+//     (position, position) pairs the MMA's k dimension needs without a
+//     transpose.  The per-(position, block) scale d rides on the P side:
+//     B = p*d split into an fp16 high part and an fp16 low part (two MMAs), so
+//     P.V keeps ~22 bits of the fp32 product.
 //
-// Warps: 4, each owns 16 positions of every stage and keeps its own (m, l, acc);
-// the four states are merged through shared memory at the end.
+// Each warp keeps its own (m, l, acc); the four states are merged through
+// shared memory at the end in a fixed order.
 #pragma once
 
 #include <type_traits>
@@ -35,100 +43,141 @@
 
 namespace kvq {
 
+#ifndef KVQ_STAGES_Q4
+#define KVQ_STAGES_Q4 3   // 16-position stages per warp ring (q4_0 V): 4 CTAs per SM fit
+#endif
+#ifndef KVQ_STAGES_Q8
+#define KVQ_STAGES_Q8 2   // (q8_0 V)
+#endif
+
 template <int NT, int VT>
 struct SplitCfg {
-    static constexpr int MTQ = (NT + 1) / 2;                 // 16-row QK m-tiles
-    static constexpr int QROWS = 16 * MTQ;                   // query rows kept in smem
-    static constexpr int VROW = (VT == KVQ_V_Q4_0) ? kD / 2 : kD;
+    static constexpr int MTQ = (NT + 1) / 2;                  // 16-row QK m-tiles
+    static constexpr int QROWS = 16 * MTQ;                    // query rows kept in smem
+    static constexpr int STAGES = (VT == KVQ_V_Q4_0) ? KVQ_STAGES_Q4 : KVQ_STAGES_Q8;   // ring depth per warp
+    static constexpr int KROW = kD + 32;                      // padded K row (160 B)
+    static constexpr int VCODE = (VT == KVQ_V_Q4_0) ? kD / 2 : kD;            // V code bytes per position
+    static constexpr int VROW = (VT == KVQ_V_Q4_0) ? kD / 2 + 16 : kD + 16;   // padded (80 / 144 B)
+    // one warp stage: kWTile positions of K codes, K scales, V codes, V scales
     static constexpr int K_OFF = 0;
-    static constexpr int KS_OFF = K_OFF + kTile * kD;
-    static constexpr int V_OFF = KS_OFF + kTile * kNB * 2;
-    static constexpr int VS_OFF = V_OFF + kTile * VROW;
-    static constexpr int STAGE = VS_OFF + kTile * kNB * 2;
-    static constexpr int Q_OFF = kStages * STAGE;            // int8 [QROWS][kD]
-    static constexpr int QS_OFF = Q_OFF + QROWS * kD;        // fp32 [QROWS][kNB]
+    static constexpr int KS_OFF = K_OFF + kWTile * KROW;
+    static constexpr int V_OFF = KS_OFF + kWTile * kNB * 2;
+    static constexpr int VS_OFF = V_OFF + kWTile * VROW;
+    static constexpr int STAGE = VS_OFF + kWTile * kNB * 2;
+    static constexpr int RING = STAGES * STAGE;               // per warp
+    static constexpr int Q_OFF = kWarps * RING;               // int8 [QROWS][kD]
+    static constexpr int QS_OFF = Q_OFF + QROWS * kD;         // fp32 [QROWS][kNB]
     static constexpr int QSUM_OFF = QS_OFF + QROWS * kNB * 4; // int32 [QROWS][kNB]
     static constexpr int ML_OFF = QSUM_OFF + QROWS * kNB * 4; // fp32 m, l [kWarps][8*NT]
-    static constexpr int SMEM = ML_OFF + 2 * kWarps * 8 * NT * 4;
-    static_assert(8 * NT * kD * 4 <= kStages * STAGE, "merge buffer must fit in the stage ring");
+    // Per-lane query table, [chunk][lane][4 words] (16-byte chunks, lane-major
+    // so a warp's LDS.128 of one chunk is conflict free): the query MMA
+    // fragments (for NT == 1 only the a0/a2 words of rows 0..7), the lane's
+    // query-row scales [NT][kNB] and the QK accumulator seeds.
+    static constexpr int QA_CHUNKS = (NT == 1) ? kNB : MTQ * kNB * 2;
+    static constexpr int SQ_CHUNKS = NT;
+    static constexpr int CI_CHUNKS = (NT == 1) ? 1 : MTQ * 2;
+    static constexpr int QF_CHUNKS = QA_CHUNKS + SQ_CHUNKS + CI_CHUNKS;
+    static constexpr int QF_OFF = ML_OFF + 2 * kWarps * 8 * NT * 4;
+    static constexpr int TI_OFF = QF_OFF + QF_CHUNKS * 32 * 16;  // int4 tile record [kWarps][STAGES]
+    static constexpr int SMEM = TI_OFF + kWarps * STAGES * 16;
+    static_assert(8 * NT * kD * 4 <= kWarps * RING, "merge buffer must fit in the stage rings");
+    static_assert(STAGE % 16 == 0 && KS_OFF % 16 == 0 && V_OFF % 16 == 0 && VS_OFF % 16 == 0, "16-byte granules");
 };
 
-// Range of segment k of the sequence intersected with [r0, r1): local token
-// indices [la, le).  Returns false when empty.
-__device__ __forceinline__ bool seg_range(const AttnParams &p, int seg0, int nseg, int k, int r0, int r1,
-                                          int &la, int &le)
+// 16-byte async copy issued only when pred is nonzero (no branch).
+__device__ __forceinline__ void cp_async16_if(uint32_t dst, const void *src, int src_bytes, int pred)
 {
-    const SegDesc &s = p.seg[seg0 + k];
-    const int end = (k + 1 < nseg) ? p.seg[seg0 + k + 1].pos0 : s.pos0 + s.cap;
-    const int a = max(r0, s.pos0);
-    const int e = min(min(r1, end), s.pos0 + s.cap);
-    la = a - s.pos0;
-    le = e - s.pos0;
-    return a < e;
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %3, 0;\n @p cp.async.cg.shared.global [%0], [%1], 16, %2;\n}\n" ::"r"(dst),
+        "l"(src), "r"(src_bytes), "r"(pred)
+        : "memory");
 }
 
-struct TileCursor {
-    int k, T, la, le;
+// The pieces of a sequence's segments that fall in [r0, r1), walked in order
+// in tiles of kWTile positions (local token index T * kWTile of segment k).
+struct Walk {
+    int k;            // segment table entry (relative to the sequence's first)
+    int T;            // tile index inside the segment
+    int la, le;       // local range [la, le) of the current piece
+    int pos0;
+    const uint8_t *kq, *ks, *vq, *vs;   // kv head h's rows of the current segment
 };
 
-__device__ __forceinline__ void cursor_seek(const AttnParams &p, int seg0, int nseg, int r0, int r1,
-                                            TileCursor &cur, int from_k)
+__device__ __forceinline__ void walk_seek(const AttnParams &p, int seg0, int nseg, int h, int r0, int r1, int k,
+                                          int vcode, Walk &w)
 {
-    for (cur.k = from_k; cur.k < nseg; ++cur.k)
-        if (seg_range(p, seg0, nseg, cur.k, r0, r1, cur.la, cur.le)) {
-            cur.T = cur.la / kTile;
+    for (w.k = k; w.k < nseg; ++w.k) {
+        const SegDesc &s = p.seg[seg0 + w.k];
+        const int end = (w.k + 1 < nseg) ? p.seg[seg0 + w.k + 1].pos0 : s.pos0 + s.cap;
+        const int a = max(r0, s.pos0), e = min(min(r1, end), s.pos0 + s.cap);
+        if (a < e) {
+            w.la = a - s.pos0;
+            w.le = e - s.pos0;
+            w.T = w.la / kWTile;
+            w.pos0 = s.pos0;
+            const size_t row = (size_t)h * s.cap;
+            w.kq = reinterpret_cast<const uint8_t *>(s.kq) + row * kD;
+            w.ks = reinterpret_cast<const uint8_t *>(s.ks) + row * kNB * 2;
+            w.vq = s.vq + row * vcode;
+            w.vs = reinterpret_cast<const uint8_t *>(s.vs) + row * kNB * 2;
             return;
         }
+    }
 }
 
-__device__ __forceinline__ void cursor_next(const AttnParams &p, int seg0, int nseg, int r0, int r1,
-                                            TileCursor &cur)
+__device__ __forceinline__ void walk_next(const AttnParams &p, int seg0, int nseg, int h, int r0, int r1, int vcode,
+                                          Walk &w)
 {
-    ++cur.T;
-    if (cur.T * kTile >= cur.le) cursor_seek(p, seg0, nseg, r0, r1, cur, cur.k + 1);
+    ++w.T;
+    if (w.T * kWTile >= w.le) walk_seek(p, seg0, nseg, h, r0, r1, w.k + 1, vcode, w);
 }
 
-// Copy one 64-token stage (K codes, K scales, V codes, V scales of kv head h)
-// into shared memory.  Tokens outside [la, le) are zero-filled without a read.
-template <int NT, int VT>
-__device__ __forceinline__ void issue_stage(const AttnParams &p, const SegDesc &s, int h, const TileCursor &cur,
-                                            uint8_t *st, int tid)
+// Copy the stage at the walk's current tile into ring slot st.  Lane l copies K
+// granules (position l/8 + 4i, part l%8), V granules (q4_0: position
+// l/4 + 8i, part l%4; q8_0 as K) and, for lanes 0..15, one 16-byte granule of K
+// (lanes 0..7) or V (8..15) scales covering positions 2(l%8), 2(l%8)+1.  With
+// FULL every position lies in [la, le); otherwise positions outside are
+// zero-filled without a read.
+template <int NT, int VT, bool FULL>
+__device__ __forceinline__ void warp_issue(const Walk &w, uint8_t *st, int lane)
 {
     using C = SplitCfg<NT, VT>;
-    const int tb = cur.T * kTile;
-    const size_t hb = (size_t)h * s.cap + tb;   // row of the stage's token 0
+    const int tb = w.T * kWTile;
+    const uint32_t sb = smem_u32(st);
+    {
+        const int u0 = lane >> 3, part = lane & 7;
+        const uint8_t *src = w.kq + (size_t)(tb + u0) * kD + part * 16;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {               // K: 64 tokens x 8 granules
-        const int gi = tid + i * kThreads, u = gi >> 3, part = gi & 7;
-        const bool ok = tb + u >= cur.la && tb + u < cur.le;
-        const uint32_t *src = s.kq + (hb + u) * (kD / 4) + part * 4;
-        cp_async16(smem_u32(st + C::K_OFF + u * kD + ((part ^ (u & 7)) << 4)), ok ? src : s.kq, ok ? 16 : 0);
+        for (int i = 0; i < 4; ++i) {
+            const int u = u0 + 4 * i;
+            const bool ok = FULL || (tb + u >= w.la && tb + u < w.le);
+            cp_async16(sb + C::K_OFF + u * C::KROW + part * 16, ok ? src + i * 4 * kD : src, ok ? 16 : 0);
+        }
     }
     if (VT == KVQ_V_Q4_0) {
+        const int u0 = lane >> 2, part = lane & 3;
+        const uint8_t *src = w.vq + (size_t)(tb + u0) * C::VCODE + part * 16;
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {           // V q4_0: 64 tokens x 4 granules
-            const int gi = tid + i * kThreads, u = gi >> 2, part = gi & 3;
-            const bool ok = tb + u >= cur.la && tb + u < cur.le;
-            const uint8_t *src = s.vq + (hb + u) * (kD / 2) + part * 16;
-            cp_async16(smem_u32(st + C::V_OFF + u * (kD / 2) + ((part ^ ((u >> 1) & 3)) << 4)),
-                       ok ? src : s.vq, ok ? 16 : 0);
+        for (int i = 0; i < 2; ++i) {
+            const int u = u0 + 8 * i;
+            const bool ok = FULL || (tb + u >= w.la && tb + u < w.le);
+            cp_async16(sb + C::V_OFF + u * C::VROW + part * 16, ok ? src + i * 8 * C::VCODE : src, ok ? 16 : 0);
         }
     } else {
+        const int u0 = lane >> 3, part = lane & 7;
+        const uint8_t *src = w.vq + (size_t)(tb + u0) * C::VCODE + part * 16;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {           // V q8_0: 64 tokens x 8 granules
-            const int gi = tid + i * kThreads, u = gi >> 3, part = gi & 7;
-            const bool ok = tb + u >= cur.la && tb + u < cur.le;
-            const uint8_t *src = s.vq + (hb + u) * kD + part * 16;
-            cp_async16(smem_u32(st + C::V_OFF + u * kD + ((part ^ (u & 7)) << 4)), ok ? src : s.vq,
-                       ok ? 16 : 0);
+        for (int i = 0; i < 4; ++i) {
+            const int u = u0 + 4 * i;
+            const bool ok = FULL || (tb + u >= w.la && tb + u < w.le);
+            cp_async16(sb + C::V_OFF + u * C::VROW + part * 16, ok ? src + i * 4 * C::VCODE : src, ok ? 16 : 0);
         }
     }
-    if (tid < 64) {                             // scales: 16 B = 2 tokens x 4 blocks
-        const int u = 2 * (tid & 31);
-        const bool ok = tb + u + 1 >= cur.la && tb + u < cur.le;
-        const uint16_t *base = (tid < 32) ? s.ks : s.vs;
-        const int off = ((tid < 32) ? C::KS_OFF : C::VS_OFF) + u * kNB * 2;
-        cp_async16(smem_u32(st + off), ok ? base + (hb + u) * kNB : base, ok ? 16 : 0);
+    {
+        const int q = lane & 7;
+        const uint8_t *b = ((lane < 8) ? w.ks : w.vs) + (size_t)(tb + 2 * q) * kNB * 2;
+        const bool ok = FULL || (tb + 2 * q + 1 >= w.la && tb + 2 * q < w.le);
+        cp_async16_if(sb + ((lane < 8) ? C::KS_OFF : C::VS_OFF) + 2 * q * kNB * 2, b, ok ? 16 : 0, lane < 16);
     }
 }
 
@@ -136,48 +185,51 @@ __device__ __forceinline__ void issue_stage(const AttnParams &p, const SegDesc &
 template <int VT>
 __device__ __forceinline__ int pv_dim(int mt, int rho)
 {
-    const int bb = mt >> 1, h2 = mt & 1, gg = rho & 7, half = rho >> 3;
-    if (VT == KVQ_V_Q4_0) return 32 * bb + 16 * h2 + 4 * (gg >> 1) + 2 * half + (gg & 1);
-    return 32 * bb + 8 * (gg >> 1) + 4 * h2 + 2 * half + (gg & 1);
+    const int bb = mt >> 1, h2 = mt & 1, g = rho & 7, half = rho >> 3;
+    if (VT == KVQ_V_Q4_0) return 32 * bb + 16 * h2 + 2 * g + half;
+    return 32 * bb + 4 * g + 2 * h2 + half;
 }
 
-// fp16 pair (elements of two adjacent head dims) -> exact integer values.
+// PV A-fragment registers of one 32-block for the position pair (t, t+1):
+// reg[h2][half] = fp16 pair (value at t, value at t+1) of the exact V code
+// (q - 8 for q4_0, the int8 code for q8_0) of head dim pv_dim(2*bb + h2, g + 8*half).
 template <int VT>
-__device__ __forceinline__ void v_codes_to_half2(const uint8_t *st_v, int u, int bb, int c, uint32_t (&P)[4])
+__device__ __forceinline__ void v_pair_codes(const uint8_t *st_v, int t, int bb, int g, uint32_t (&reg)[2][2])
 {
     if (VT == KVQ_V_Q4_0) {
-        // word c of block bb: bytes 4c..4c+3; low nibbles are dims 4c..4c+3,
-        // high nibbles dims 16+4c..16+4c+3
-        const uint32_t w = *reinterpret_cast<const uint32_t *>(st_v + u * (kD / 2) + ((bb ^ ((u >> 1) & 3)) << 4) +
-                                                                4 * c);
-        const uint32_t t01 = __byte_perm(w, 0, 0x4140), t23 = __byte_perm(w, 0, 0x4342);
+        // bytes 2g, 2g+1 of the block: low nibbles = dims 2g, 2g+1, high = 2g+16, 2g+17
+        constexpr int VROW = kD / 2 + 16;
+        const uint32_t h0 = *reinterpret_cast<const uint16_t *>(st_v + t * VROW + 16 * bb + 2 * g);
+        const uint32_t h1 = *reinterpret_cast<const uint16_t *>(st_v + (t + 1) * VROW + 16 * bb + 2 * g);
+        const uint32_t x01 = __byte_perm(h0, h1, 0x2420);   // [byte 2g of t, 0, byte 2g of t+1, 0]
+        const uint32_t x23 = __byte_perm(h0, h1, 0x2521);   // byte 2g+1
         const __half2 k1032 = __half2half2(__ushort_as_half(0x6408));   // 1032
         const __half2 k16th = __half2half2(__ushort_as_half(0x2c00));   // 1/16
         const __half2 km72 = __half2half2(__ushort_as_half(0xd480));    // -72
         uint32_t x;
-        x = (t01 & 0x000F000Fu) | 0x64006400u;
-        *reinterpret_cast<__half2 *>(&P[0]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1032);
-        x = (t23 & 0x000F000Fu) | 0x64006400u;
-        *reinterpret_cast<__half2 *>(&P[1]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1032);
-        x = (t01 & 0x00F000F0u) | 0x64006400u;
-        *reinterpret_cast<__half2 *>(&P[2]) = __hfma2(*reinterpret_cast<__half2 *>(&x), k16th, km72);
-        x = (t23 & 0x00F000F0u) | 0x64006400u;
-        *reinterpret_cast<__half2 *>(&P[3]) = __hfma2(*reinterpret_cast<__half2 *>(&x), k16th, km72);
+        x = (x01 & 0x000F000Fu) | 0x64006400u;
+        *reinterpret_cast<__half2 *>(&reg[0][0]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1032);
+        x = (x23 & 0x000F000Fu) | 0x64006400u;
+        *reinterpret_cast<__half2 *>(&reg[0][1]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1032);
+        x = (x01 & 0x00F000F0u) | 0x64006400u;
+        *reinterpret_cast<__half2 *>(&reg[1][0]) = __hfma2(*reinterpret_cast<__half2 *>(&x), k16th, km72);
+        x = (x23 & 0x00F000F0u) | 0x64006400u;
+        *reinterpret_cast<__half2 *>(&reg[1][1]) = __hfma2(*reinterpret_cast<__half2 *>(&x), k16th, km72);
     } else {
-        // words 2c, 2c+1 of block bb: dims 8c..8c+7 as signed bytes
-        const uint2 w = *reinterpret_cast<const uint2 *>(st_v + u * kD + (((2 * bb + (c >> 1)) ^ (u & 7)) << 4) +
-                                                         ((c & 1) << 3));
-        const uint32_t x0 = w.x ^ 0x80808080u, x1 = w.y ^ 0x80808080u;   // biased: code + 128
-        const __half2 k1152 = __half2half2(__ushort_as_half(0x6480));     // 1152
+        // word g of the block: dims 4g..4g+3 as signed bytes, biased by 128
+        constexpr int VROW = kD + 16;
+        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(st_v + t * VROW + 32 * bb + 4 * g) ^ 0x80808080u;
+        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(st_v + (t + 1) * VROW + 32 * bb + 4 * g) ^ 0x80808080u;
+        const __half2 k1152 = __half2half2(__ushort_as_half(0x6480));   // 1152
         uint32_t x;
-        x = __byte_perm(x0, 0x64646464u, 0x4140);
-        *reinterpret_cast<__half2 *>(&P[0]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1152);
-        x = __byte_perm(x0, 0x64646464u, 0x4342);
-        *reinterpret_cast<__half2 *>(&P[1]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1152);
-        x = __byte_perm(x1, 0x64646464u, 0x4140);
-        *reinterpret_cast<__half2 *>(&P[2]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1152);
-        x = __byte_perm(x1, 0x64646464u, 0x4342);
-        *reinterpret_cast<__half2 *>(&P[3]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1152);
+        x = (__byte_perm(w0, w1, 0x4440) & 0x00FF00FFu) | 0x64006400u;   // dim 4g
+        *reinterpret_cast<__half2 *>(&reg[0][0]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1152);
+        x = (__byte_perm(w0, w1, 0x5551) & 0x00FF00FFu) | 0x64006400u;   // dim 4g+1
+        *reinterpret_cast<__half2 *>(&reg[0][1]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1152);
+        x = (__byte_perm(w0, w1, 0x6662) & 0x00FF00FFu) | 0x64006400u;   // dim 4g+2
+        *reinterpret_cast<__half2 *>(&reg[1][0]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1152);
+        x = (__byte_perm(w0, w1, 0x7773) & 0x00FF00FFu) | 0x64006400u;   // dim 4g+3
+        *reinterpret_cast<__half2 *>(&reg[1][1]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1152);
     }
 }
 
@@ -205,7 +257,7 @@ __device__ __forceinline__ void k_word_biased(uint32_t w, uint32_t &lo, uint32_t
     hi = __byte_perm(x, 0x64646464u, 0x4342);
 }
 
-// Two signed int8 codes (bytes k0, k1 of w) -> exact fp16 pair.
+// Two signed int8 codes (bytes k0, k0+1 of w) -> exact fp16 pair.
 __device__ __forceinline__ uint32_t q_pair(uint32_t w, int k0)
 {
     const __half2 h = __halves2half2(__int2half_rn((int)(int8_t)(w >> (8 * k0))),
@@ -213,11 +265,17 @@ __device__ __forceinline__ uint32_t q_pair(uint32_t w, int k0)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+#ifndef KVQ_SPLIT_MIN_CTAS
+#define KVQ_SPLIT_MIN_CTAS 4   // resident CTAs per SM the kernels are compiled for
+#endif
+
 template <int NT, int VT, bool DUMP>
-__global__ void __launch_bounds__(kThreads) split_attn_kernel(const __grid_constant__ AttnParams p)
+__global__ void __launch_bounds__(kThreads, NT == 1 ? KVQ_SPLIT_MIN_CTAS : 1)
+    split_attn_kernel(const __grid_constant__ AttnParams p)
 {
     using C = SplitCfg<NT, VT>;
     constexpr int MTQ = C::MTQ;
+    constexpr int S = C::STAGES;
     constexpr float kBias = 1152.0f;                 // K codes enter the MMA as 1152 + code
     extern __shared__ __align__(128) uint8_t smem[];
 
@@ -249,21 +307,46 @@ __global__ void __launch_bounds__(kThreads) split_attn_kernel(const __grid_const
         return;
     }
 
-    // ---- tile schedule; start the copies before the query prologue ----
-    int n_tiles = 0;
-    for (int k = 0; k < nseg; ++k) {
-        int la, le;
-        if (seg_range(p, seg0, nseg, k, r0, r1, la, le)) n_tiles += (le - 1) / kTile - la / kTile + 1;
-    }
-    TileCursor pc, cc;
-    cursor_seek(p, seg0, nseg, r0, r1, pc, 0);
-    cc = pc;
+    // ---- the query rows' loads go out first: they are tiny, and issued after the
+    // K/V prefetch below they would queue behind it ----
+    constexpr int QPW = C::QROWS / kWarps;   // query rows per warp
+    uint2 qraw[QPW];                          // all of this warp's row loads in flight at once
 #pragma unroll
-    for (int st = 0; st < kStages - 1; ++st) {
-        if (st < n_tiles) {
-            issue_stage<NT, VT>(p, p.seg[seg0 + pc.k], h, pc, smem + st * C::STAGE, tid);
-            cursor_next(p, seg0, nseg, r0, r1, pc);
+    for (int k = 0; k < QPW; ++k) {
+        const int r = warp + kWarps * k;
+        qraw[k] = make_uint2(0u, 0u);
+        if (r < R) {
+            const int i = r / gsz, hq = p.grp_q[gb + r % gsz];
+            qraw[k] = *reinterpret_cast<const uint2 *>(p.q + (((size_t)b * p.t_q + i) * p.n_q_heads + hq) * kD + lane * 4);
         }
+    }
+    // ---- this warp's sub-range and its first copies (before the query prologue) ----
+    const int span = (r1 - r0 + kWarps * kWTile - 1) / (kWarps * kWTile) * kWTile;
+    const int w0 = min(r1, r0 + warp * span), w1 = min(r1, w0 + span);
+    int n_tiles = 0;
+    if (w0 < w1)
+        for (int k = 0; k < nseg; ++k) {
+            const SegDesc &s = p.seg[seg0 + k];
+            const int end = (k + 1 < nseg) ? p.seg[seg0 + k + 1].pos0 : s.pos0 + s.cap;
+            const int a = max(w0, s.pos0) - s.pos0, e = min(min(w1, end), s.pos0 + s.cap) - s.pos0;
+            if (a < e) n_tiles += (e - 1) / kWTile - a / kWTile + 1;
+        }
+    uint8_t *ring = smem + warp * C::RING;
+    int4 *tile_rec = reinterpret_cast<int4 *>(smem + C::TI_OFF) + warp * S;
+    Walk pw;
+    walk_seek(p, seg0, nseg, h, w0, w1, 0, C::VCODE, pw);
+    auto issue = [&](int slot) {
+        const int tb = pw.T * kWTile;
+        if (tb >= pw.la && tb + kWTile <= pw.le)
+            warp_issue<NT, VT, true>(pw, ring + slot * C::STAGE, lane);
+        else
+            warp_issue<NT, VT, false>(pw, ring + slot * C::STAGE, lane);
+        if (lane == 0) tile_rec[slot] = make_int4(tb, pw.la, pw.le, pw.pos0 + tb);
+        walk_next(p, seg0, nseg, h, w0, w1, C::VCODE, pw);
+    };
+#pragma unroll
+    for (int st = 0; st < S - 1; ++st) {
+        if (st < n_tiles) issue(st);
         cp_async_commit();
     }
 
@@ -271,7 +354,9 @@ __global__ void __launch_bounds__(kThreads) split_attn_kernel(const __grid_const
     uint32_t *qw = reinterpret_cast<uint32_t *>(smem + C::Q_OFF);
     float *qs = reinterpret_cast<float *>(smem + C::QS_OFF);
     int *qsum = reinterpret_cast<int *>(smem + C::QSUM_OFF);
-    for (int r = warp; r < C::QROWS; r += kWarps) {
+#pragma unroll
+    for (int k = 0; k < QPW; ++k) {
+        const int r = warp + kWarps * k;
         uint32_t word = 0;
         float s = 0.f;
         int sum = 0;
@@ -279,7 +364,7 @@ __global__ void __launch_bounds__(kThreads) split_attn_kernel(const __grid_const
             const int i = r / gsz, hq = p.grp_q[gb + r % gsz];
             const size_t qrow = ((size_t)b * p.t_q + i) * p.n_q_heads + hq;
             float x[4];
-            unpack4h(*reinterpret_cast<const uint2 *>(p.q + qrow * kD + lane * 4), x);
+            unpack4h(qraw[k], x);
             float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
@@ -311,40 +396,62 @@ __global__ void __launch_bounds__(kThreads) split_attn_kernel(const __grid_const
     // Query A fragments (fp16, exact codes).  Within block bb, k16 step ks, this
     // lane's k slots (2c, 2c+1 | 2c+8, 2c+9) carry head dims
     // 32bb + 8c + 4ks + (0, 1 | 2, 3): the bytes of word 8bb + 2c + ks, the same
-    // word the lane reads from K, so q.k is unchanged.
-    uint32_t qa[MTQ][kNB][2][4];
-    float cinit[MTQ][kNB][2];   // -1152 * sum of the row's codes in the block
+    // word the lane reads from K, so q.k is unchanged.  Warp 0 writes them, with
+    // the row scales and the accumulator seeds (-1152 * sum of the row's codes
+    // in the block), to the per-lane table that every stage reads back.
+    uint4 *qf = reinterpret_cast<uint4 *>(smem + C::QF_OFF) + lane;   // chunk k at qf[32 * k]
+    if (warp == 0) {
 #pragma unroll
-    for (int mq = 0; mq < MTQ; ++mq)
+        for (int mq = 0; mq < MTQ; ++mq)
 #pragma unroll
-        for (int bb = 0; bb < kNB; ++bb) {
+            for (int bb = 0; bb < kNB; ++bb) {
+                uint32_t f[2][4];
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const uint32_t w0 = qw[(16 * mq + g) * (kD / 4) + 8 * bb + 2 * c + ks];
-                const uint32_t w1 = qw[(16 * mq + g + 8) * (kD / 4) + 8 * bb + 2 * c + ks];
-                qa[mq][bb][ks][0] = q_pair(w0, 0);
-                qa[mq][bb][ks][2] = q_pair(w0, 2);
-                // with at most 8 rows, rows 8..15 of the tile are padding: keep them
-                // compile-time zeros so they occupy no registers
-                qa[mq][bb][ks][1] = NT == 1 ? 0u : q_pair(w1, 0);
-                qa[mq][bb][ks][3] = NT == 1 ? 0u : q_pair(w1, 2);
+                for (int ks = 0; ks < 2; ++ks) {
+                    const uint32_t wa = qw[(16 * mq + g) * (kD / 4) + 8 * bb + 2 * c + ks];
+                    const uint32_t wb = qw[(16 * mq + g + 8) * (kD / 4) + 8 * bb + 2 * c + ks];
+                    f[ks][0] = q_pair(wa, 0);
+                    f[ks][1] = q_pair(wb, 0);
+                    f[ks][2] = q_pair(wa, 2);
+                    f[ks][3] = q_pair(wb, 2);
+                }
+                if (NT == 1) {
+                    qf[32 * bb] = make_uint4(f[0][0], f[0][2], f[1][0], f[1][2]);
+                } else {
+                    qf[32 * ((mq * kNB + bb) * 2 + 0)] = make_uint4(f[0][0], f[0][1], f[0][2], f[0][3]);
+                    qf[32 * ((mq * kNB + bb) * 2 + 1)] = make_uint4(f[1][0], f[1][1], f[1][2], f[1][3]);
+                }
             }
-            cinit[mq][bb][0] = -kBias * (float)qsum[(16 * mq + g) * kNB + bb];
-            cinit[mq][bb][1] = NT == 1 ? 0.f : -kBias * (float)qsum[(16 * mq + g + 8) * kNB + bb];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int row = 8 * nt + g;
+            qf[32 * (C::QA_CHUNKS + nt)] =
+                make_uint4(__float_as_uint(qs[row * kNB + 0]), __float_as_uint(qs[row * kNB + 1]),
+                           __float_as_uint(qs[row * kNB + 2]), __float_as_uint(qs[row * kNB + 3]));
         }
-    float sqf[NT][kNB], m[NT], l[NT];
+#pragma unroll
+        for (int mq = 0; mq < MTQ; ++mq)
+#pragma unroll
+            for (int hf = 0; hf < (NT == 1 ? 1 : 2); ++hf) {
+                const int row = 16 * mq + 8 * hf + g;
+                qf[32 * (C::QA_CHUNKS + C::SQ_CHUNKS + mq * 2 + hf)] =
+                    make_uint4(__float_as_uint(-kBias * (float)qsum[row * kNB + 0]),
+                               __float_as_uint(-kBias * (float)qsum[row * kNB + 1]),
+                               __float_as_uint(-kBias * (float)qsum[row * kNB + 2]),
+                               __float_as_uint(-kBias * (float)qsum[row * kNB + 3]));
+            }
+    }
+    __syncthreads();   // query table visible
+    float m[NT], l[NT];
     int lim[NT];
-    int lim_min = 0x7fffffff;   // smallest visible-position limit over live rows
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int row = 8 * nt + g;
-#pragma unroll
-        for (int bb = 0; bb < kNB; ++bb) sqf[nt][bb] = qs[row * kNB + bb];
         lim[nt] = (row < R) ? (p.causal ? L - p.t_q + row / gsz : L - 1) : -1;
         m[nt] = -INFINITY;
         l[nt] = 0.f;
     }
-    lim_min = p.causal ? L - p.t_q : L - 1;
+    const int lim_min = p.causal ? L - p.t_q : L - 1;   // smallest limit over live rows
     float acc[8][NT][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
@@ -353,51 +460,77 @@ __global__ void __launch_bounds__(kThreads) split_attn_kernel(const __grid_const
 #pragma unroll
             for (int k = 0; k < 4; ++k) acc[mt][nt][k] = 0.f;
 
-    const int u0w = warp * 16;   // this warp's first token of every stage
-
     for (int j = 0; j < n_tiles; ++j) {
-        cp_async_wait<kStages - 2>();
-        __syncthreads();
-        if (j + kStages - 1 < n_tiles) {
-            issue_stage<NT, VT>(p, p.seg[seg0 + pc.k], h, pc, smem + ((j + kStages - 1) % kStages) * C::STAGE, tid);
-            cursor_next(p, seg0, nseg, r0, r1, pc);
-        }
+        cp_async_wait<S - 2>();
+        __syncwarp();   // stage j landed for every lane; every lane is done with stage j-1
+        if (j + S - 1 < n_tiles) issue((j + S - 1) % S);
         cp_async_commit();
 
-        const uint8_t *st = smem + (j % kStages) * C::STAGE;
-        const int tb = cc.T * kTile;
-        const int la = cc.la, le = cc.le;
-        const int pos_base = p.seg[seg0 + cc.k].pos0 + tb;
-        cursor_next(p, seg0, nseg, r0, r1, cc);
-        if (tb + u0w >= le || tb + u0w + 16 <= la) continue;   // no valid token for this warp
-        // every token of this warp's 16 valid and visible to every live row?
-        const bool full = tb + u0w >= la && tb + u0w + 16 <= le && pos_base + u0w + 15 <= lim_min;
+        const uint8_t *st = ring + (j % S) * C::STAGE;
+        const int4 rec = tile_rec[j % S];
+        const int tb = rec.x, la = rec.y, le = rec.z, pos_base = rec.w;
+        // every position of the stage valid and visible to every live row?
+        const bool full = tb >= la && tb + kWTile <= le && pos_base + kWTile - 1 <= lim_min;
 
         auto chunk = [&](auto full_tag) {
             constexpr bool FULL = decltype(full_tag)::value;
             // ---- S = Q K^T per 32-block (exact integers in fp32), scaled scores ----
+            uint32_t qa[MTQ][kNB][2][4];
+            float cinit[MTQ][kNB][2], sqf[NT][kNB];
+#pragma unroll
+            for (int mq = 0; mq < MTQ; ++mq)
+#pragma unroll
+                for (int bb = 0; bb < kNB; ++bb) {
+                    if (NT == 1) {
+                        const uint4 f = qf[32 * bb];
+                        qa[mq][bb][0][0] = f.x; qa[mq][bb][0][2] = f.y;
+                        qa[mq][bb][1][0] = f.z; qa[mq][bb][1][2] = f.w;
+                        qa[mq][bb][0][1] = qa[mq][bb][0][3] = qa[mq][bb][1][1] = qa[mq][bb][1][3] = 0u;
+                    } else {
+                        const uint4 f0 = qf[32 * ((mq * kNB + bb) * 2 + 0)];
+                        const uint4 f1 = qf[32 * ((mq * kNB + bb) * 2 + 1)];
+                        qa[mq][bb][0][0] = f0.x; qa[mq][bb][0][1] = f0.y; qa[mq][bb][0][2] = f0.z; qa[mq][bb][0][3] = f0.w;
+                        qa[mq][bb][1][0] = f1.x; qa[mq][bb][1][1] = f1.y; qa[mq][bb][1][2] = f1.z; qa[mq][bb][1][3] = f1.w;
+                    }
+                }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint4 f = qf[32 * (C::QA_CHUNKS + nt)];
+                sqf[nt][0] = __uint_as_float(f.x); sqf[nt][1] = __uint_as_float(f.y);
+                sqf[nt][2] = __uint_as_float(f.z); sqf[nt][3] = __uint_as_float(f.w);
+            }
+#pragma unroll
+            for (int mq = 0; mq < MTQ; ++mq)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    if (NT == 1 && hf == 1) {
+#pragma unroll
+                        for (int bb = 0; bb < kNB; ++bb) cinit[mq][bb][1] = 0.f;
+                    } else {
+                        const uint4 f = qf[32 * (C::QA_CHUNKS + C::SQ_CHUNKS + mq * 2 + hf)];
+                        cinit[mq][0][hf] = __uint_as_float(f.x); cinit[mq][1][hf] = __uint_as_float(f.y);
+                        cinit[mq][2][hf] = __uint_as_float(f.z); cinit[mq][3][hf] = __uint_as_float(f.w);
+                    }
+                }
             float s[2][NT][2];
 #pragma unroll
             for (int sub = 0; sub < 2; ++sub) {
-                const int u = u0w + 8 * sub + g;              // K column this lane supplies
+                const int u = 8 * sub + g;                    // K column this lane supplies
                 float sc[MTQ][kNB][4];
 #pragma unroll
                 for (int bb = 0; bb < kNB; ++bb) {
-                    const uint2 kb = *reinterpret_cast<const uint2 *>(st + C::K_OFF + u * kD +
-                                                                      (((2 * bb + (c >> 1)) ^ g) << 4) + ((c & 1) << 3));
+                    const uint2 kb = *reinterpret_cast<const uint2 *>(st + C::K_OFF + u * C::KROW + 32 * bb + 8 * c);
                     uint32_t b00, b01, b10, b11;
                     k_word_biased(kb.x, b00, b01);
                     k_word_biased(kb.y, b10, b11);
 #pragma unroll
                     for (int mq = 0; mq < MTQ; ++mq) {
-                        sc[mq][bb][0] = sc[mq][bb][1] = cinit[mq][bb][0];
-                        sc[mq][bb][2] = sc[mq][bb][3] = cinit[mq][bb][1];
-                        mma_f16_16816(sc[mq][bb], qa[mq][bb][0], b00, b01);
+                        mma_f16_16816_c(sc[mq][bb], qa[mq][bb][0], b00, b01, cinit[mq][bb][0], cinit[mq][bb][1]);
                         mma_f16_16816(sc[mq][bb], qa[mq][bb][1], b10, b11);
                     }
                 }
-                // K scales of this lane's two score columns (tokens u0w + 8sub + 2c + e)
-                const int ut = u0w + 8 * sub + 2 * c;
+                // K scales of this lane's two score columns (positions 8sub + 2c + e)
+                const int ut = 8 * sub + 2 * c;
                 const uint4 ksr = *reinterpret_cast<const uint4 *>(st + C::KS_OFF + ut * kNB * 2);
                 float sk[2][kNB];
                 {
@@ -483,56 +616,56 @@ __global__ void __launch_bounds__(kThreads) split_attn_kernel(const __grid_const
             }
 
             // ---- O += P . V  (per 32-block: B = p*d as fp16 hi + lo, A = V codes) ----
-            float dv[2][2][kNB];   // [sub][e][block] V scales of this lane's B columns, 0 if invalid
+            uint4 vsr[2];   // V scales of this lane's B columns (positions 8sub + 2c, +1)
+            bool okv[2][2];
 #pragma unroll
             for (int sub = 0; sub < 2; ++sub) {
-                const int ut = u0w + 8 * sub + 2 * c;
-                const uint4 vsr = *reinterpret_cast<const uint4 *>(st + C::VS_OFF + ut * kNB * 2);
-                const float2 a0 = __half22float2(*reinterpret_cast<const __half2 *>(&vsr.x));
-                const float2 a1 = __half22float2(*reinterpret_cast<const __half2 *>(&vsr.y));
-                const float2 a2 = __half22float2(*reinterpret_cast<const __half2 *>(&vsr.z));
-                const float2 a3 = __half22float2(*reinterpret_cast<const __half2 *>(&vsr.w));
-                bool ok0 = true, ok1 = true;
-                if (!FULL) {
-                    ok0 = tb + ut >= la && tb + ut < le;
-                    ok1 = tb + ut + 1 >= la && tb + ut + 1 < le;
-                }
-                dv[sub][0][0] = ok0 ? a0.x : 0.f; dv[sub][0][1] = ok0 ? a0.y : 0.f;
-                dv[sub][0][2] = ok0 ? a1.x : 0.f; dv[sub][0][3] = ok0 ? a1.y : 0.f;
-                dv[sub][1][0] = ok1 ? a2.x : 0.f; dv[sub][1][1] = ok1 ? a2.y : 0.f;
-                dv[sub][1][2] = ok1 ? a3.x : 0.f; dv[sub][1][3] = ok1 ? a3.y : 0.f;
+                const int ut = 8 * sub + 2 * c;
+                vsr[sub] = *reinterpret_cast<const uint4 *>(st + C::VS_OFF + ut * kNB * 2);
+                okv[sub][0] = FULL || (tb + ut >= la && tb + ut < le);
+                okv[sub][1] = FULL || (tb + ut + 1 >= la && tb + ut + 1 < le);
             }
 #pragma unroll
             for (int bb = 0; bb < kNB; ++bb) {
                 uint32_t bhi[NT][2], blo[NT][2];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int sub = 0; sub < 2; ++sub) {
-                        const float x0 = s[sub][nt][0] * dv[sub][0][bb];
-                        const float x1 = s[sub][nt][1] * dv[sub][1][bb];
-                        const uint32_t hv = pack_half2(x0, x1);
-                        const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hv));
-                        bhi[nt][sub] = hv;
-                        blo[nt][sub] = pack_half2(x0 - hf.x, x1 - hf.y);
-                    }
-                uint32_t t[2][4];
+                uint32_t a[2][4];   // [h2] A fragment of m-tile 2bb + h2
 #pragma unroll
                 for (int sub = 0; sub < 2; ++sub) {
-                    uint32_t P[4];
-                    v_codes_to_half2<VT>(st + C::V_OFF, u0w + 8 * sub + g, bb, c, P);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) t[sub][i] = movmatrix_t(P[i]);
-                }
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const uint32_t a[4] = {t[0][2 * h2], t[0][2 * h2 + 1], t[1][2 * h2], t[1][2 * h2 + 1]};
+                    // V scale of block bb for the two positions (fp16 -> fp32), 0 if invalid
+                    const uint32_t w0 = (bb < 2) ? vsr[sub].x : vsr[sub].y;
+                    const uint32_t w1 = (bb < 2) ? vsr[sub].z : vsr[sub].w;
+                    float d0 = __half2float(__ushort_as_half((uint16_t)((bb & 1) ? (w0 >> 16) : (w0 & 0xffffu))));
+                    float d1 = __half2float(__ushort_as_half((uint16_t)((bb & 1) ? (w1 >> 16) : (w1 & 0xffffu))));
+                    if (!FULL) {
+                        d0 = okv[sub][0] ? d0 : 0.f;
+                        d1 = okv[sub][1] ? d1 : 0.f;
+                    }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        mma_f16_16816(acc[2 * bb + h2][nt], a, bhi[nt][0], bhi[nt][1]);
-                        mma_f16_16816(acc[2 * bb + h2][nt], a, blo[nt][0], blo[nt][1]);
+                        // x = p*d split as hi (x with its low 13 mantissa bits cleared:
+                        // exact in fp16 when x is in fp16's normal range) + lo (x - hi,
+                        // exact in fp32, then rounded to fp16)
+                        const float x0 = s[sub][nt][0] * d0;
+                        const float x1 = s[sub][nt][1] * d1;
+                        const float h0 = __uint_as_float(__float_as_uint(x0) & 0xffffe000u);
+                        const float h1 = __uint_as_float(__float_as_uint(x1) & 0xffffe000u);
+                        bhi[nt][sub] = pack_half2(h0, h1);
+                        blo[nt][sub] = pack_half2(x0 - h0, x1 - h1);
                     }
+                    uint32_t r[2][2];
+                    v_pair_codes<VT>(st + C::V_OFF, 8 * sub + 2 * c, bb, g, r);
+                    a[0][2 * sub] = r[0][0];
+                    a[0][2 * sub + 1] = r[0][1];
+                    a[1][2 * sub] = r[1][0];
+                    a[1][2 * sub + 1] = r[1][1];
                 }
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_f16_16816(acc[2 * bb + h2][nt], a[h2], bhi[nt][0], bhi[nt][1]);
+                        mma_f16_16816(acc[2 * bb + h2][nt], a[h2], blo[nt][0], blo[nt][1]);
+                    }
             }
         };
         if (full)
@@ -543,28 +676,28 @@ __global__ void __launch_bounds__(kThreads) split_attn_kernel(const __grid_const
 
     cp_async_wait<0>();
     if constexpr (!DUMP) {
-
-    // ---- merge the four warps' (m, l, acc) and write ----
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        l[nt] += __shfl_xor_sync(0xffffffffu, l[nt], 1);
-        l[nt] += __shfl_xor_sync(0xffffffffu, l[nt], 2);
-    }
-    __syncthreads();   // every warp is done with the stage ring
-    float *sm_m = reinterpret_cast<float *>(smem + C::ML_OFF);
-    float *sm_l = sm_m + kWarps * 8 * NT;
-    float *sm_o = reinterpret_cast<float *>(smem);   // [8*NT][kD]
-    if (c == 0)
+        // ---- merge the four warps' (m, l, acc) and write ----
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            sm_m[warp * 8 * NT + 8 * nt + g] = m[nt];
-            sm_l[warp * 8 * NT + 8 * nt + g] = l[nt];
+            l[nt] += __shfl_xor_sync(0xffffffffu, l[nt], 1);
+            l[nt] += __shfl_xor_sync(0xffffffffu, l[nt], 2);
         }
-    __syncthreads();
-    // Fixed merge order (warp 0 stores, warps 1..3 add in turn) so results do
-    // not depend on scheduling; each (row, dim) belongs to one lane per warp.
-    for (int w = 0; w < kWarps; ++w) {
-        if (warp == w) {
+        __syncthreads();   // every warp is done with the stage rings
+        float *sm_m = reinterpret_cast<float *>(smem + C::ML_OFF);
+        float *sm_l = sm_m + kWarps * 8 * NT;
+        float *sm_o = reinterpret_cast<float *>(smem);   // [8*NT][kD]
+        if (c == 0)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                sm_m[warp * 8 * NT + 8 * nt + g] = m[nt];
+                sm_l[warp * 8 * NT + 8 * nt + g] = l[nt];
+            }
+        __syncthreads();
+        // Merge in a fixed order so results do not depend on scheduling.  Each
+        // (row, dim) belongs to one lane per warp; a warp's accumulator is
+        // scaled by exp2(m_warp - M) for the row's overall max M.
+        constexpr bool kSlices = kWarps * 8 * NT * kD * 4 <= kWarps * C::RING;
+        auto put = [&](float *dst, bool add) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -574,42 +707,61 @@ __global__ void __launch_bounds__(kThreads) split_attn_kernel(const __grid_const
                     float M = -INFINITY;
 #pragma unroll
                     for (int v = 0; v < kWarps; ++v) M = fmaxf(M, sm_m[v * 8 * NT + row]);
-                    const float mw = sm_m[w * 8 * NT + row];
-                    const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+                    const float mw = sm_m[warp * 8 * NT + row];
+                    const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
 #pragma unroll
                     for (int mt = 0; mt < 8; ++mt) {
-                        float *o0 = &sm_o[row * kD + pv_dim<VT>(mt, g)];
-                        float *o1 = &sm_o[row * kD + pv_dim<VT>(mt, g + 8)];
-                        *o0 = (w == 0 ? 0.f : *o0) + acc[mt][nt][e] * f;
-                        *o1 = (w == 0 ? 0.f : *o1) + acc[mt][nt][2 + e] * f;
+                        float *o0 = &dst[row * kD + pv_dim<VT>(mt, g)];
+                        float *o1 = &dst[row * kD + pv_dim<VT>(mt, g + 8)];
+                        *o0 = (add ? *o0 : 0.f) + acc[mt][nt][e] * f;
+                        *o1 = (add ? *o1 : 0.f) + acc[mt][nt][2 + e] * f;
                     }
                 }
-        }
-        __syncthreads();
-    }
-    for (int row = 0; row < R; ++row) {
-        float M = -INFINITY;
+        };
+        if (kSlices) {
+            // every warp writes its own slice, then the slices are added 0..3
+            put(sm_o + warp * 8 * NT * kD, false);
+            __syncthreads();
+            for (int i = tid; i < R * kD; i += kThreads) {
+                float t = sm_o[i];
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * 8 * NT + row]);
-        float Lsum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float mw = sm_m[w * 8 * NT + row];
-            if (mw != -INFINITY) Lsum += sm_l[w * 8 * NT + row] * exp2f(mw - M);
-        }
-        const int i = row / gsz, hq = p.grp_q[gb + row % gsz];
-        const size_t orow = ((size_t)b * p.t_q + i) * p.n_q_heads + hq;
-        const bool any = Lsum > 0.f;
-        const float o = any ? sm_o[row * kD + tid] / Lsum : 0.f;
-        const float ls = any ? (M + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
-        if (p.n_split == 1) {
-            p.out[orow * kD + tid] = o;
-            if (tid == 0) p.lse[orow] = ls;
+                for (int w = 1; w < kWarps; ++w) t += sm_o[w * 8 * NT * kD + i];
+                sm_o[i] = t;
+            }
+            __syncthreads();
         } else {
-            p.ws_o[(orow * p.n_split + split) * kD + tid] = o;
-            if (tid == 0) p.ws_lse[orow * p.n_split + split] = ls;
+            // warp 0 stores, warps 1..3 add in turn
+            for (int w = 0; w < kWarps; ++w) {
+                if (warp == w) put(sm_o, w > 0);
+                __syncthreads();
+            }
         }
-    }
+        for (int row = 0; row < R; ++row) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * 8 * NT + row]);
+            float Lsum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float mw = sm_m[w * 8 * NT + row];
+                if (mw != -INFINITY) Lsum += sm_l[w * 8 * NT + row] * fast_exp2(mw - M);
+            }
+            const int i = row / gsz, hq = p.grp_q[gb + row % gsz];
+            const size_t orow = ((size_t)b * p.t_q + i) * p.n_q_heads + hq;
+            const bool any = Lsum > 0.f;
+            float inv, lg;
+            asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(Lsum));
+            asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(Lsum));
+            const float o = any ? sm_o[row * kD + tid] * inv : 0.f;
+            const float ls = any ? (M + lg) * 0.69314718055994531f : -INFINITY;
+            if (p.n_split == 1) {
+                p.out[orow * kD + tid] = o;
+                if (tid == 0) p.lse[orow] = ls;
+            } else {
+                p.ws_o[(orow * p.n_split + split) * kD + tid] = o;
+                if (tid == 0) p.ws_lse[orow * p.n_split + split] = ls;
+            }
+        }
     }
 }
 

@@ -12,8 +12,9 @@ namespace kvq {
 
 constexpr int kD = KVQ_HEAD_DIM;        // head dim
 constexpr int kNB = kD / KVQ_QBLOCK;    // 32-blocks per head row (4)
-constexpr int kTile = 64;               // tokens per pipeline stage
-constexpr int kWarps = 4;               // warps per split CTA, 16 tokens each per stage
+constexpr int kTile = 64;               // split chunks are multiples of this (kWarps * kWTile)
+constexpr int kWTile = 16;              // positions per warp pipeline stage
+constexpr int kWarps = 4;               // warps per split CTA, each streams its own sub-range
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 4;              // cp.async ring depth
 constexpr int kMaxSegsLaunch = 64;      // segment-table entries per launch
@@ -121,6 +122,17 @@ __device__ __forceinline__ void mma_s8_16832(int (&d)[4], const uint32_t (&a)[4]
         "{%10,%10,%10,%10};\n"
         : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(c));
+}
+
+// D = A(16x16 f16, row) * B(16x8 f16, col) + C, fp32 accumulate (C separate).
+__device__ __forceinline__ void mma_f16_16816_c(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                                float c0, float c1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%11,%11};\n"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
 }
 
 // D += A(16x16 f16, row) * B(16x8 f16, col), fp32 accumulate.
