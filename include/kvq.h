@@ -59,7 +59,8 @@ typedef enum kvq_status {
     KVQ_ERR_UNSUPPORTED = 2,   /* no sm_103 device, or a size this build lacks    */
     KVQ_ERR_CAPACITY = 3,      /* kvq_append: the open segment is too small       */
     KVQ_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required      */
-    KVQ_ERR_CUDA = 5           /* a CUDA runtime call or kernel launch failed     */
+    KVQ_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed     */
+    KVQ_ERR_TIMEOUT = 6        /* a kernel gave up waiting for its own copies     */
 } kvq_status;
 
 typedef enum kvq_vtype {
@@ -69,15 +70,26 @@ typedef enum kvq_vtype {
 
 /*
  * One append-only segment of one sequence.  All four arrays are device memory,
- * 16-byte aligned, head-major, indexed [kv_head][token][...] with token in
- * [0, cap):
- *   k_q  int8  [n_kv_heads][cap][head_dim]      (little-endian words: byte i of
- *                                                word w is element 4w+i)
- *   k_s  fp16  [n_kv_heads][cap][head_dim/32]
- *   v_q  q4_0: uint8 [n_kv_heads][cap][head_dim/2], in each 32-block byte j holds
- *              element j (low nibble) and element j+16 (high nibble);
- *        q8_0: int8  [n_kv_heads][cap][head_dim]
- *   v_s  fp16  [n_kv_heads][cap][head_dim/32]
+ * 16-byte aligned and head-major: kv head h owns cap token rows starting at row
+ * h*cap, and token t of the segment is row t of its head.  Row sizes:
+ *   k_q  int8 codes, head_dim bytes per row
+ *   k_s  fp16 scales, head_dim/32 per row, plain [kv_head][token][block] order
+ *   v_q  q4_0: head_dim/2 bytes per row, in each 32-block byte j holds element j
+ *              (low nibble) and element j+16 (high nibble);
+ *        q8_0: int8 codes, head_dim bytes per row
+ *   v_s  fp16 scales, as k_s
+ * Tiles.  Tokens 16T..16T+15 of a head form tile T, one contiguous run of 16
+ * rows in every array.  Scales keep row order inside a tile; the code bytes of
+ * k_q and v_q are permuted inside the tile so that the attention kernel copies
+ * a tile with one bulk copy and reads it with conflict-free 16-byte loads.
+ * With u = token % 16 (sub = u/8, gu = u%8, cu = gu/2, e = u%2) and j the byte
+ * of the row in the logical order above, byte j of token u sits at tile offset
+ *   k_q       ((2*sub + j/64)*32 + 4*gu + (j%32)/8)*16 + 8*((j/32)%2) + j%8
+ *   v_q q4_0  (sub*32 + 4*((j%16)/2) + cu)*16 + 4*(j/16) + 2*e + j%2
+ *   v_q q8_0  ((2*sub + j/64)*32 + 4*((j%32)/4) + cu)*16 + 8*((j/32)%2)
+ *             + 4*((j%4)/2) + 2*(j%2) + e
+ * (head_dim 128).  Only kvq_append writes code bytes, so callers never see the
+ * permutation unless they read the arrays themselves.
  * cap  : capacity in tokens, a positive multiple of KVQ_SEG_ALIGN.
  * len  : tokens filled, 0..cap (host bookkeeping; kvq_append advances it).
  * pos0 : absolute position of the segment's token 0.  Segment k+1 of a sequence
@@ -210,6 +222,17 @@ kvq_status kvq_decode_attn_noalloc(const kvq_cache *c, const void *q16, int32_t 
                                    int32_t t_q, int32_t causal_tail, const int32_t *seq_lens,
                                    int32_t max_len, const int32_t *head_map, float sm_scale,
                                    float *out, float *lse, void *stream);
+
+/*
+ * kvq_wait_timeouts -- the attention kernel bounds every wait for a copy it
+ * issued; a wait that gives up (which no correct run does) makes the kernel
+ * drain its copies, write NaN for the CTA's rows and bump a per-device
+ * counter.  This call reads that counter for the current device into *count
+ * (host; synchronizes with the device) and returns KVQ_ERR_TIMEOUT when it is
+ * nonzero, KVQ_OK otherwise.  The pages have no counterpart: it is the
+ * library's own hang guard.
+ */
+kvq_status kvq_wait_timeouts(uint32_t *count);
 
 /* Short English text of a status code (static storage). */
 const char *kvq_status_string(kvq_status s);

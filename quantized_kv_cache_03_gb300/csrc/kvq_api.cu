@@ -1,5 +1,6 @@
 // kvq_api.cu -- the C ABI of libkvq.so: argument validation, segment-table
-// marshalling, split policy and kernel launches.  No allocation, no host sync.
+// marshalling, split policy and kernel launches.  No allocation, and no host
+// sync except in kvq_wait_timeouts.
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -18,10 +19,17 @@ struct DeviceInfo {
     bool ready = false;
     int n_sms = 0;
     int ctas[2][5] = {};   // [v_type][n_tiles8] resident split CTAs per SM
+    unsigned int *timeouts = nullptr;   // device address of g_wait_timeouts
 };
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
+}  // namespace
+
+// Waits in the attention kernel that gave up (see kvq_wait_timeouts).
+static __device__ unsigned int g_wait_timeouts;
+
+namespace {
 
 // Device attributes and kernel attributes, once per device.
 kvq_status device_setup(DeviceInfo **out)
@@ -53,6 +61,12 @@ kvq_status device_setup(DeviceInfo **out)
                 return KVQ_ERR_CUDA;
             }
         }
+        void *t = nullptr;
+        if (cudaGetSymbolAddress(&t, g_wait_timeouts) != cudaSuccess || !t) {
+            cudaGetLastError();
+            return KVQ_ERR_CUDA;
+        }
+        d.timeouts = static_cast<unsigned int *>(t);
         d.ready = true;
     }
     *out = &d;
@@ -139,7 +153,10 @@ int round_up(long long x, int m) { return (int)((x + m - 1) / m * m); }
 // Split policy: enough CTAs to fill every SM with whole waves.  Uniform lengths:
 // the smallest split count (>= one wave) whose last wave is >= 90% full.
 // Ragged lengths: a chunk of about a quarter wave's share of the positions.
-void choose_split(const kvq_cache *c, const Group &g, int max_len, int slots, int &n_split, int &chunk)
+// Chunks are multiples of gran (one stage per warp of the CTA) so that every
+// warp gets the same number of stages; a chunk forced through KVQ_SPLIT only
+// needs the 64-position segment alignment.
+void choose_split(const kvq_cache *c, const Group &g, int max_len, int slots, int gran, int &n_split, int &chunk)
 {
     const int H = c->n_kv_heads;
     long long total = 0;
@@ -163,7 +180,7 @@ void choose_split(const kvq_cache *c, const Group &g, int max_len, int slots, in
     }
     const char *env = std::getenv("KVQ_SPLIT");
     if (env && std::atoi(env) > 0) {
-        chunk = round_up(std::atoi(env), kTile);
+        chunk = round_up(std::atoi(env), KVQ_SEG_ALIGN);
     } else {
         const int pairs = g.nb * H;
         const int max_n = std::max(1, (lmax + 255) / 256);   // at least 256 positions per split
@@ -186,11 +203,11 @@ void choose_split(const kvq_cache *c, const Group &g, int max_len, int slots, in
             const long long per_cta = std::max<long long>(256, total / std::max(1, 4 * slots));
             n = (int)std::min<long long>(max_n, (lmax + per_cta - 1) / per_cta);
         }
-        chunk = round_up((lmax + n - 1) / n, kTile);
+        chunk = round_up((lmax + n - 1) / n, gran);
     }
     n_split = (lmax + chunk - 1) / chunk;
     if (n_split > 1024) {
-        chunk = round_up((lmax + 1023) / 1024, kTile);
+        chunk = round_up((lmax + 1023) / 1024, gran);
         n_split = (lmax + chunk - 1) / chunk;
     }
 }
@@ -200,7 +217,7 @@ void make_groups(const kvq_cache *c, std::vector<Group> &gs)
 {
     int b = 0;
     while (b < c->n_seqs) {
-        Group g{b, 0, 1, kTile, 0};
+        Group g{b, 0, 1, KVQ_SEG_ALIGN, 0};
         int segs = 0;
         while (b < c->n_seqs && g.nb < kMaxSeqsLaunch && segs + c->n_segs[b] <= kMaxSegsLaunch) {
             segs += c->n_segs[b];
@@ -220,7 +237,7 @@ void fill_segments(const kvq_cache *c, const Group &g, AttnParams &p)
         p.seq_nseg[i] = (uint8_t)c->n_segs[b];
         for (int k = 0; k < c->n_segs[b]; ++k, ++n) {
             const kvq_segment &s = seg_of(c, b, k);
-            p.seg[n].kq = static_cast<const uint32_t *>(s.k_q);
+            p.seg[n].kq = static_cast<const uint8_t *>(s.k_q);
             p.seg[n].ks = static_cast<const uint16_t *>(s.k_s);
             p.seg[n].vq = static_cast<const uint8_t *>(s.v_q);
             p.seg[n].vs = static_cast<const uint16_t *>(s.v_s);
@@ -282,7 +299,7 @@ kvq_status run_decode(const DecodeArgs &a)
     size_t ws = 0;
     const size_t rows_per_seq = (size_t)a.t_q * a.n_q_heads;
     for (Group &g : gs) {
-        choose_split(c, g, a.max_len, slots, g.n_split, g.chunk);
+        choose_split(c, g, a.max_len, slots, split_warps(nt) * kWTile, g.n_split, g.chunk);
         if (g.n_split > 1 && !a.dump) {
             g.ws_off = ws;
             const size_t bytes = (size_t)g.nb * rows_per_seq * g.n_split * (kD + 1) * sizeof(float);
@@ -314,6 +331,7 @@ kvq_status run_decode(const DecodeArgs &a)
         p.n_split = g.n_split;
         p.chunk = g.chunk;
         p.qk_scale_log2 = a.sm_scale * 1.4426950408889634f;
+        p.timeouts = dev->timeouts;
         if (a.dump) {
             p.dbg_qc = a.dbg_qc + r0 * kD;
             p.dbg_qs = a.dbg_qs + r0 * kNB;
@@ -372,6 +390,7 @@ const char *kvq_status_string(kvq_status s)
     case KVQ_ERR_CAPACITY: return "segment capacity exceeded";
     case KVQ_ERR_WORKSPACE: return "workspace missing or too small";
     case KVQ_ERR_CUDA: return "CUDA error";
+    case KVQ_ERR_TIMEOUT: return "a kernel wait gave up";
     }
     return "unknown status";
 }
@@ -419,7 +438,7 @@ kvq_status kvq_append(kvq_cache *c, int32_t n_seqs_in, const int32_t *seq_ids, c
             if (n_new[i] > 0) {
                 const kvq_segment &sg = seg_of(c, seq_ids[i], c->n_segs[seq_ids[i]] - 1);
                 AppendEntry &e = p.e[p.n_entries++];
-                e.kq = static_cast<uint32_t *>(sg.k_q);
+                e.kq = static_cast<uint8_t *>(sg.k_q);
                 e.ks = static_cast<uint16_t *>(sg.k_s);
                 e.vq = static_cast<uint8_t *>(sg.v_q);
                 e.vs = static_cast<uint16_t *>(sg.v_s);
@@ -553,4 +572,19 @@ extern "C" kvq_status kvq_decode_attn_noalloc(const kvq_cache *c, const void *q1
     if (st != KVQ_OK) return st;
     return kvq_decode_attn(c, q16, n_q_heads, t_q, causal_tail, seq_lens, max_len, head_map, sm_scale, out, lse,
                            scratch, KVQ_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" kvq_status kvq_wait_timeouts(uint32_t *count)
+{
+    if (!count) return KVQ_ERR_INVALID_ARG;
+    DeviceInfo *dev = nullptr;
+    kvq_status st = device_setup(&dev);
+    if (st != KVQ_OK) return st;
+    unsigned int n = 0;
+    if (cudaMemcpy(&n, dev->timeouts, sizeof(n), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return KVQ_ERR_CUDA;
+    }
+    *count = n;
+    return n ? KVQ_ERR_TIMEOUT : KVQ_OK;
 }

@@ -5,13 +5,15 @@
 // the positions [s*chunk, (s+1)*chunk) of sequence b and writes either the
 // final output (one split) or a partial (normalised o, lse) for the combine.
 //
-// Data path: every warp streams its own contiguous quarter of the CTA's
-// positions through a private ring of 16-position stages in shared memory
-// (16-byte cp.async copies issued by the warp itself).  Rows are padded
-// (K 160 B, q4_0 V 80 B, q8_0 V 144 B) so that every fragment read below is
-// bank-conflict free and every address is a per-lane constant plus an
-// immediate.  Only __syncwarp runs in the main loop; the block synchronizes
-// once for the query prologue and once to merge the four warps at the end.
+// Data path: every warp streams its own contiguous share of the CTA's
+// positions through a private ring of 16-position stages in shared memory.
+// The cache stores each 16-position tile of every array contiguously, with the
+// code bytes already in the order the MMA fragments read them (the tile layout
+// in kvq_internal.cuh), so one lane fills a stage with four bulk async copies
+// (cp.async.bulk, completion counted in bytes on the stage's mbarrier) and
+// every fragment read is one conflict-free 16-byte shared load.  Only
+// __syncwarp and the stage barriers run in the main loop; the block
+// synchronizes once for the query prologue and once to merge the warps.
 //
 //   * QK^T: fp16 tensor-core MMA m16n8k16 on exact integers -- A = the query
 //     codes (rows), B = the K codes of 8 positions entered as 1152 + code (one
@@ -26,10 +28,9 @@
 //     running max only raised when some row's maximum grows.
 //   * P.V: fp16 tensor-core MMA m16n8k16 with fp32 accumulation.  The V codes
 //     enter as exact small integers in fp16 (binary16 exponent trick: 0x6400|n
-//     is 1024+n).  Each lane reads the same head dims of two adjacent positions
-//     and interleaves them with byte permutes, which yields the
-//     (position, position) pairs the MMA's k dimension needs without a
-//     transpose.  The per-(position, block) scale d rides on the P side:
+//     is 1024+n).  The tile layout puts the same head dims of two adjacent
+//     positions side by side, which gives the (position, position) pairs the
+//     MMA's k dimension needs without a transpose.  The per-(position, block) scale d rides on the P side:
 //     B = p*d split into an fp16 high part and an fp16 low part (two MMAs), so
 //     P.V keeps ~22 bits of the fp32 product.
 //
@@ -44,31 +45,37 @@
 namespace kvq {
 
 #ifndef KVQ_STAGES_Q4
-#define KVQ_STAGES_Q4 3   // 16-position stages per warp ring (q4_0 V): 4 CTAs per SM fit
+#define KVQ_STAGES_Q4 3   // 16-position stages per warp ring (q4_0 V)
 #endif
 #ifndef KVQ_STAGES_Q8
-#define KVQ_STAGES_Q8 2   // (q8_0 V)
+#define KVQ_STAGES_Q8 3   // (q8_0 V)
 #endif
+
+
 
 template <int NT, int VT>
 struct SplitCfg {
+    static constexpr int WARPS = split_warps(NT);
+    static constexpr int THREADS = WARPS * 32;
+    // the <= 8-row kernels are held to 128 registers per thread (512 threads per SM x 4 CTAs of 4 warps,
+    // or one CTA of 16 warps); the others take what they need
+    static constexpr int MIN_CTAS = (NT == 1) ? (16 / WARPS > 0 ? 16 / WARPS : 1) : 1;
     static constexpr int MTQ = (NT + 1) / 2;                  // 16-row QK m-tiles
     static constexpr int QROWS = 16 * MTQ;                    // query rows kept in smem
+    static_assert(QROWS % WARPS == 0, "every warp quantizes the same number of query rows");
     static constexpr int STAGES = (VT == KVQ_V_Q4_0) ? KVQ_STAGES_Q4 : KVQ_STAGES_Q8;   // ring depth per warp
-    static constexpr int KROW = kD + 32;                      // padded K row (160 B)
     static constexpr int VCODE = (VT == KVQ_V_Q4_0) ? kD / 2 : kD;            // V code bytes per position
-    static constexpr int VROW = (VT == KVQ_V_Q4_0) ? kD / 2 + 16 : kD + 16;   // padded (80 / 144 B)
-    // one warp stage: kWTile positions of K codes, K scales, V codes, V scales
+    // one warp stage: one tile of K codes, K scales, V codes, V scales (cache order)
     static constexpr int K_OFF = 0;
-    static constexpr int KS_OFF = K_OFF + kWTile * KROW;
+    static constexpr int KS_OFF = K_OFF + kWTile * kD;
     static constexpr int V_OFF = KS_OFF + kWTile * kNB * 2;
-    static constexpr int VS_OFF = V_OFF + kWTile * VROW;
-    static constexpr int STAGE = VS_OFF + kWTile * kNB * 2;
+    static constexpr int VS_OFF = V_OFF + kWTile * VCODE;
+    static constexpr int STAGE = VS_OFF + kWTile * kNB * 2;   // = bytes the four copies land
     static constexpr int RING = STAGES * STAGE;               // per warp
-    static constexpr int Q_OFF = kWarps * RING;               // int8 [QROWS][kD]
+    static constexpr int Q_OFF = WARPS * RING;                // int8 [QROWS][kD]
     static constexpr int QS_OFF = Q_OFF + QROWS * kD;         // fp32 [QROWS][kNB]
     static constexpr int QSUM_OFF = QS_OFF + QROWS * kNB * 4; // int32 [QROWS][kNB]
-    static constexpr int ML_OFF = QSUM_OFF + QROWS * kNB * 4; // fp32 m, l [kWarps][8*NT]
+    static constexpr int ML_OFF = QSUM_OFF + QROWS * kNB * 4; // fp32 m, l [WARPS][8*NT]
     // Per-lane query table, [chunk][lane][4 words] (16-byte chunks, lane-major
     // so a warp's LDS.128 of one chunk is conflict free): the query MMA
     // fragments (for NT == 1 only the a0/a2 words of rows 0..7), the lane's
@@ -77,21 +84,14 @@ struct SplitCfg {
     static constexpr int SQ_CHUNKS = NT;
     static constexpr int CI_CHUNKS = (NT == 1) ? 1 : MTQ * 2;
     static constexpr int QF_CHUNKS = QA_CHUNKS + SQ_CHUNKS + CI_CHUNKS;
-    static constexpr int QF_OFF = ML_OFF + 2 * kWarps * 8 * NT * 4;
-    static constexpr int TI_OFF = QF_OFF + QF_CHUNKS * 32 * 16;  // int4 tile record [kWarps][STAGES]
-    static constexpr int SMEM = TI_OFF + kWarps * STAGES * 16;
-    static_assert(8 * NT * kD * 4 <= kWarps * RING, "merge buffer must fit in the stage rings");
+    static constexpr int QF_OFF = ML_OFF + 2 * WARPS * 8 * NT * 4;
+    static constexpr int TI_OFF = QF_OFF + QF_CHUNKS * 32 * 16;  // int4 tile record [WARPS][STAGES]
+    static constexpr int BAR_OFF = TI_OFF + WARPS * STAGES * 16; // uint64 mbarrier [WARPS][STAGES]
+    static constexpr int FLAG_OFF = BAR_OFF + WARPS * STAGES * 8;
+    static constexpr int SMEM = FLAG_OFF + 16;
+    static_assert(8 * NT * kD * 4 <= WARPS * RING, "merge buffer must fit in the stage rings");
     static_assert(STAGE % 16 == 0 && KS_OFF % 16 == 0 && V_OFF % 16 == 0 && VS_OFF % 16 == 0, "16-byte granules");
 };
-
-// 16-byte async copy issued only when pred is nonzero (no branch).
-__device__ __forceinline__ void cp_async16_if(uint32_t dst, const void *src, int src_bytes, int pred)
-{
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %3, 0;\n @p cp.async.cg.shared.global [%0], [%1], 16, %2;\n}\n" ::"r"(dst),
-        "l"(src), "r"(src_bytes), "r"(pred)
-        : "memory");
-}
 
 // The pieces of a sequence's segments that fall in [r0, r1), walked in order
 // in tiles of kWTile positions (local token index T * kWTile of segment k).
@@ -132,53 +132,20 @@ __device__ __forceinline__ void walk_next(const AttnParams &p, int seg0, int nse
     if (w.T * kWTile >= w.le) walk_seek(p, seg0, nseg, h, r0, r1, w.k + 1, vcode, w);
 }
 
-// Copy the stage at the walk's current tile into ring slot st.  Lane l copies K
-// granules (position l/8 + 4i, part l%8), V granules (q4_0: position
-// l/4 + 8i, part l%4; q8_0 as K) and, for lanes 0..15, one 16-byte granule of K
-// (lanes 0..7) or V (8..15) scales covering positions 2(l%8), 2(l%8)+1.  With
-// FULL every position lies in [la, le); otherwise positions outside are
-// zero-filled without a read.
-template <int NT, int VT, bool FULL>
-__device__ __forceinline__ void warp_issue(const Walk &w, uint8_t *st, int lane)
+// Lane 0 fills ring slot `dst` (shared address) with the walk's current tile:
+// four contiguous bulk copies whose bytes complete on the slot's barrier.
+// Positions of the tile outside [la, le) are copied too (they are cache rows
+// of the same segment, possibly never written) and masked where they are used.
+template <int NT, int VT>
+__device__ __forceinline__ void tile_issue(const Walk &w, uint32_t dst, uint32_t bar)
 {
     using C = SplitCfg<NT, VT>;
-    const int tb = w.T * kWTile;
-    const uint32_t sb = smem_u32(st);
-    {
-        const int u0 = lane >> 3, part = lane & 7;
-        const uint8_t *src = w.kq + (size_t)(tb + u0) * kD + part * 16;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int u = u0 + 4 * i;
-            const bool ok = FULL || (tb + u >= w.la && tb + u < w.le);
-            cp_async16(sb + C::K_OFF + u * C::KROW + part * 16, ok ? src + i * 4 * kD : src, ok ? 16 : 0);
-        }
-    }
-    if (VT == KVQ_V_Q4_0) {
-        const int u0 = lane >> 2, part = lane & 3;
-        const uint8_t *src = w.vq + (size_t)(tb + u0) * C::VCODE + part * 16;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int u = u0 + 8 * i;
-            const bool ok = FULL || (tb + u >= w.la && tb + u < w.le);
-            cp_async16(sb + C::V_OFF + u * C::VROW + part * 16, ok ? src + i * 8 * C::VCODE : src, ok ? 16 : 0);
-        }
-    } else {
-        const int u0 = lane >> 3, part = lane & 7;
-        const uint8_t *src = w.vq + (size_t)(tb + u0) * C::VCODE + part * 16;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int u = u0 + 4 * i;
-            const bool ok = FULL || (tb + u >= w.la && tb + u < w.le);
-            cp_async16(sb + C::V_OFF + u * C::VROW + part * 16, ok ? src + i * 4 * C::VCODE : src, ok ? 16 : 0);
-        }
-    }
-    {
-        const int q = lane & 7;
-        const uint8_t *b = ((lane < 8) ? w.ks : w.vs) + (size_t)(tb + 2 * q) * kNB * 2;
-        const bool ok = FULL || (tb + 2 * q + 1 >= w.la && tb + 2 * q < w.le);
-        cp_async16_if(sb + ((lane < 8) ? C::KS_OFF : C::VS_OFF) + 2 * q * kNB * 2, b, ok ? 16 : 0, lane < 16);
-    }
+    const size_t tb = (size_t)w.T * kWTile;
+    mbar_arrive_expect_tx(bar, C::STAGE);
+    bulk_g2s(dst + C::K_OFF, w.kq + tb * kD, kWTile * kD, bar);
+    bulk_g2s(dst + C::KS_OFF, w.ks + tb * kNB * 2, kWTile * kNB * 2, bar);
+    bulk_g2s(dst + C::V_OFF, w.vq + tb * C::VCODE, kWTile * C::VCODE, bar);
+    bulk_g2s(dst + C::VS_OFF, w.vs + tb * kNB * 2, kWTile * kNB * 2, bar);
 }
 
 // Head-dim index of accumulator row rho (0..15) of PV m-tile mt = 2*block + h2.
@@ -193,42 +160,38 @@ __device__ __forceinline__ int pv_dim(int mt, int rho)
 // PV A-fragment registers of one 32-block for the position pair (t, t+1):
 // reg[h2][half] = fp16 pair (value at t, value at t+1) of the exact V code
 // (q - 8 for q4_0, the int8 code for q8_0) of head dim pv_dim(2*bb + h2, g + 8*half).
+// q4_0: w0 = [byte 2g of t, byte 2g+1 of t, byte 2g of t+1, byte 2g+1 of t+1]
+// of the block (low nibbles = dims 2g, 2g+1, high = 2g+16, 2g+17).  q8_0:
+// w0 = codes of dims 4g, 4g+1 and w1 of dims 4g+2, 4g+3, each as
+// [t, t+1, t, t+1].
 template <int VT>
-__device__ __forceinline__ void v_pair_codes(const uint8_t *st_v, int t, int bb, int g, uint32_t (&reg)[2][2])
+__device__ __forceinline__ void v_pair_codes(uint32_t w0, uint32_t w1, uint32_t (&reg)[2][2])
 {
     if (VT == KVQ_V_Q4_0) {
-        // bytes 2g, 2g+1 of the block: low nibbles = dims 2g, 2g+1, high = 2g+16, 2g+17
-        constexpr int VROW = kD / 2 + 16;
-        const uint32_t h0 = *reinterpret_cast<const uint16_t *>(st_v + t * VROW + 16 * bb + 2 * g);
-        const uint32_t h1 = *reinterpret_cast<const uint16_t *>(st_v + (t + 1) * VROW + 16 * bb + 2 * g);
-        const uint32_t x01 = __byte_perm(h0, h1, 0x2420);   // [byte 2g of t, 0, byte 2g of t+1, 0]
-        const uint32_t x23 = __byte_perm(h0, h1, 0x2521);   // byte 2g+1
         const __half2 k1032 = __half2half2(__ushort_as_half(0x6408));   // 1032
         const __half2 k16th = __half2half2(__ushort_as_half(0x2c00));   // 1/16
         const __half2 km72 = __half2half2(__ushort_as_half(0xd480));    // -72
+        const uint32_t w23 = w0 >> 8;                                   // bytes 2g+1 at 0 and 2
         uint32_t x;
-        x = (x01 & 0x000F000Fu) | 0x64006400u;
+        x = (w0 & 0x000F000Fu) | 0x64006400u;
         *reinterpret_cast<__half2 *>(&reg[0][0]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1032);
-        x = (x23 & 0x000F000Fu) | 0x64006400u;
+        x = (w23 & 0x000F000Fu) | 0x64006400u;
         *reinterpret_cast<__half2 *>(&reg[0][1]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1032);
-        x = (x01 & 0x00F000F0u) | 0x64006400u;
+        x = (w0 & 0x00F000F0u) | 0x64006400u;
         *reinterpret_cast<__half2 *>(&reg[1][0]) = __hfma2(*reinterpret_cast<__half2 *>(&x), k16th, km72);
-        x = (x23 & 0x00F000F0u) | 0x64006400u;
+        x = (w23 & 0x00F000F0u) | 0x64006400u;
         *reinterpret_cast<__half2 *>(&reg[1][1]) = __hfma2(*reinterpret_cast<__half2 *>(&x), k16th, km72);
     } else {
-        // word g of the block: dims 4g..4g+3 as signed bytes, biased by 128
-        constexpr int VROW = kD + 16;
-        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(st_v + t * VROW + 32 * bb + 4 * g) ^ 0x80808080u;
-        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(st_v + (t + 1) * VROW + 32 * bb + 4 * g) ^ 0x80808080u;
         const __half2 k1152 = __half2half2(__ushort_as_half(0x6480));   // 1152
+        const uint32_t x0 = w0 ^ 0x80808080u, x1 = w1 ^ 0x80808080u;   // biased by 128
         uint32_t x;
-        x = (__byte_perm(w0, w1, 0x4440) & 0x00FF00FFu) | 0x64006400u;   // dim 4g
+        x = __byte_perm(x0, 0x64646464u, 0x4140);   // dim 4g
         *reinterpret_cast<__half2 *>(&reg[0][0]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1152);
-        x = (__byte_perm(w0, w1, 0x5551) & 0x00FF00FFu) | 0x64006400u;   // dim 4g+1
+        x = __byte_perm(x0, 0x64646464u, 0x4342);   // dim 4g+1
         *reinterpret_cast<__half2 *>(&reg[0][1]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1152);
-        x = (__byte_perm(w0, w1, 0x6662) & 0x00FF00FFu) | 0x64006400u;   // dim 4g+2
+        x = __byte_perm(x1, 0x64646464u, 0x4140);   // dim 4g+2
         *reinterpret_cast<__half2 *>(&reg[1][0]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1152);
-        x = (__byte_perm(w0, w1, 0x7773) & 0x00FF00FFu) | 0x64006400u;   // dim 4g+3
+        x = __byte_perm(x1, 0x64646464u, 0x4342);   // dim 4g+3
         *reinterpret_cast<__half2 *>(&reg[1][1]) = __hsub2(*reinterpret_cast<__half2 *>(&x), k1152);
     }
 }
@@ -265,15 +228,13 @@ __device__ __forceinline__ uint32_t q_pair(uint32_t w, int k0)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-#ifndef KVQ_SPLIT_MIN_CTAS
-#define KVQ_SPLIT_MIN_CTAS 4   // resident CTAs per SM the kernels are compiled for
-#endif
-
 template <int NT, int VT, bool DUMP>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? KVQ_SPLIT_MIN_CTAS : 1)
+__global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::MIN_CTAS)
     split_attn_kernel(const __grid_constant__ AttnParams p)
 {
     using C = SplitCfg<NT, VT>;
+    constexpr int kWarps = C::WARPS;
+    constexpr int kThreads = C::THREADS;
     constexpr int MTQ = C::MTQ;
     constexpr int S = C::STAGES;
     constexpr float kBias = 1152.0f;                 // K codes enter the MMA as 1152 + code
@@ -332,23 +293,32 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? KVQ_SPLIT_MIN_CTAS : 1)
             if (a < e) n_tiles += (e - 1) / kWTile - a / kWTile + 1;
         }
     uint8_t *ring = smem + warp * C::RING;
+    const uint32_t ring_s = smem_u32(ring);
+    const uint32_t bar_s = smem_u32(smem + C::BAR_OFF) + warp * S * 8;
     int4 *tile_rec = reinterpret_cast<int4 *>(smem + C::TI_OFF) + warp * S;
+    int *bad_flag = reinterpret_cast<int *>(smem + C::FLAG_OFF);
+    if (tid == 0) *bad_flag = 0;
+    if (lane == 0) {
+#pragma unroll
+        for (int st = 0; st < S; ++st) mbar_init(bar_s + st * 8, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
     Walk pw;
     walk_seek(p, seg0, nseg, h, w0, w1, 0, C::VCODE, pw);
+    int issued = 0;   // tiles handed to the copy engine
     auto issue = [&](int slot) {
-        const int tb = pw.T * kWTile;
-        if (tb >= pw.la && tb + kWTile <= pw.le)
-            warp_issue<NT, VT, true>(pw, ring + slot * C::STAGE, lane);
-        else
-            warp_issue<NT, VT, false>(pw, ring + slot * C::STAGE, lane);
-        if (lane == 0) tile_rec[slot] = make_int4(tb, pw.la, pw.le, pw.pos0 + tb);
+        if (lane == 0) {
+            const int tb = pw.T * kWTile;
+            tile_rec[slot] = make_int4(tb, pw.la, pw.le, pw.pos0 + tb);
+            tile_issue<NT, VT>(pw, ring_s + slot * C::STAGE, bar_s + slot * 8);
+        }
         walk_next(p, seg0, nseg, h, w0, w1, C::VCODE, pw);
+        ++issued;
     };
 #pragma unroll
-    for (int st = 0; st < S - 1; ++st) {
+    for (int st = 0; st < S - 1; ++st)
         if (st < n_tiles) issue(st);
-        cp_async_commit();
-    }
 
     // ---- quantize the query rows of this kv head (int8 rule, fp16 scale) ----
     uint32_t *qw = reinterpret_cast<uint32_t *>(smem + C::Q_OFF);
@@ -460,11 +430,18 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? KVQ_SPLIT_MIN_CTAS : 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k) acc[mt][nt][k] = 0.f;
 
+    bool bad = false;   // a stage never arrived (the warp then stops and drains)
     for (int j = 0; j < n_tiles; ++j) {
-        cp_async_wait<S - 2>();
-        __syncwarp();   // stage j landed for every lane; every lane is done with stage j-1
-        if (j + S - 1 < n_tiles) issue((j + S - 1) % S);
-        cp_async_commit();
+        const bool landed = mbar_wait(bar_s + (j % S) * 8, (j / S) & 1);
+        if (!__all_sync(0xffffffffu, landed)) {
+            bad = true;
+            break;
+        }
+        __syncwarp();   // every lane is done with stage j-1, whose slot is refilled next
+        if (j + S - 1 < n_tiles) {
+            if (lane == 0) fence_proxy_async_smem();
+            issue((j + S - 1) % S);
+        }
 
         const uint8_t *st = ring + (j % S) * C::STAGE;
         const int4 rec = tile_rec[j % S];
@@ -515,14 +492,20 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? KVQ_SPLIT_MIN_CTAS : 1)
             float s[2][NT][2];
 #pragma unroll
             for (int sub = 0; sub < 2; ++sub) {
-                const int u = 8 * sub + g;                    // K column this lane supplies
+                // K column 8sub + g: load 2sub + hb holds its codes 8c..8c+7 of
+                // blocks 2hb and 2hb + 1
+                uint4 kk[2];
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb)
+                    kk[hb] = *reinterpret_cast<const uint4 *>(st + C::K_OFF + (2 * sub + hb) * 512 + lane * 16);
                 float sc[MTQ][kNB][4];
 #pragma unroll
                 for (int bb = 0; bb < kNB; ++bb) {
-                    const uint2 kb = *reinterpret_cast<const uint2 *>(st + C::K_OFF + u * C::KROW + 32 * bb + 8 * c);
+                    const uint32_t kx = (bb & 1) ? kk[bb >> 1].z : kk[bb >> 1].x;
+                    const uint32_t ky = (bb & 1) ? kk[bb >> 1].w : kk[bb >> 1].y;
                     uint32_t b00, b01, b10, b11;
-                    k_word_biased(kb.x, b00, b01);
-                    k_word_biased(kb.y, b10, b11);
+                    k_word_biased(kx, b00, b01);
+                    k_word_biased(ky, b10, b11);
 #pragma unroll
                     for (int mq = 0; mq < MTQ; ++mq) {
                         mma_f16_16816_c(sc[mq][bb], qa[mq][bb][0], b00, b01, cinit[mq][bb][0], cinit[mq][bb][1]);
@@ -618,12 +601,19 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? KVQ_SPLIT_MIN_CTAS : 1)
             // ---- O += P . V  (per 32-block: B = p*d as fp16 hi + lo, A = V codes) ----
             uint4 vsr[2];   // V scales of this lane's B columns (positions 8sub + 2c, +1)
             bool okv[2][2];
+            // V code words of positions (8sub + 2c, +1): q4_0 one load per sub
+            // (word bb = block bb), q8_0 two (load 2sub + hb: blocks 2hb, 2hb + 1)
+            constexpr int NVL = (VT == KVQ_V_Q4_0) ? 1 : 2;
+            uint4 vv[2][NVL];
 #pragma unroll
             for (int sub = 0; sub < 2; ++sub) {
                 const int ut = 8 * sub + 2 * c;
                 vsr[sub] = *reinterpret_cast<const uint4 *>(st + C::VS_OFF + ut * kNB * 2);
                 okv[sub][0] = FULL || (tb + ut >= la && tb + ut < le);
                 okv[sub][1] = FULL || (tb + ut + 1 >= la && tb + ut + 1 < le);
+#pragma unroll
+                for (int hb = 0; hb < NVL; ++hb)
+                    vv[sub][hb] = *reinterpret_cast<const uint4 *>(st + C::V_OFF + (NVL * sub + hb) * 512 + lane * 16);
             }
 #pragma unroll
             for (int bb = 0; bb < kNB; ++bb) {
@@ -653,7 +643,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? KVQ_SPLIT_MIN_CTAS : 1)
                         blo[nt][sub] = pack_half2(x0 - h0, x1 - h1);
                     }
                     uint32_t r[2][2];
-                    v_pair_codes<VT>(st + C::V_OFF, 8 * sub + 2 * c, bb, g, r);
+                    if (VT == KVQ_V_Q4_0) {
+                        const uint4 &v = vv[sub][0];
+                        v_pair_codes<VT>(bb == 0 ? v.x : bb == 1 ? v.y : bb == 2 ? v.z : v.w, 0u, r);
+                    } else {
+                        const uint4 &v = vv[sub][NVL - 1 == 0 ? 0 : (bb >> 1)];
+                        v_pair_codes<VT>((bb & 1) ? v.z : v.x, (bb & 1) ? v.w : v.y, r);
+                    }
                     a[0][2 * sub] = r[0][0];
                     a[0][2 * sub + 1] = r[0][1];
                     a[1][2 * sub] = r[1][0];
@@ -674,7 +670,16 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? KVQ_SPLIT_MIN_CTAS : 1)
             chunk(std::integral_constant<bool, false>());
     }
 
-    cp_async_wait<0>();
+    if (bad) {
+        // a wait gave up: wait (bounded) for this warp's copies still in flight,
+        // then poison the CTA's results
+        for (int j = issued - (S - 1) > 0 ? issued - (S - 1) : 0; j < issued; ++j)
+            mbar_wait(bar_s + (j % S) * 8, (j / S) & 1);
+        if (lane == 0) {
+            atomicOr(bad_flag, 1);
+            atomicAdd(p.timeouts, 1u);
+        }
+    }
     if constexpr (!DUMP) {
         // ---- merge the four warps' (m, l, acc) and write ----
 #pragma unroll
@@ -736,7 +741,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? KVQ_SPLIT_MIN_CTAS : 1)
                 __syncthreads();
             }
         }
-        for (int row = 0; row < R; ++row) {
+        const bool poisoned = *bad_flag != 0;   // set before the merge's first barrier
+        for (int i0 = tid; i0 < R * kD; i0 += kThreads) {
+            const int row = i0 / kD, d = i0 % kD;
             float M = -INFINITY;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * 8 * NT + row]);
@@ -752,14 +759,15 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? KVQ_SPLIT_MIN_CTAS : 1)
             float inv, lg;
             asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(Lsum));
             asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(Lsum));
-            const float o = any ? sm_o[row * kD + tid] * inv : 0.f;
-            const float ls = any ? (M + lg) * 0.69314718055994531f : -INFINITY;
+            float o = any ? sm_o[row * kD + d] * inv : 0.f;
+            float ls = any ? (M + lg) * 0.69314718055994531f : -INFINITY;
+            if (poisoned) o = ls = __int_as_float(0x7fc00000);   // NaN: the CTA lost a stage
             if (p.n_split == 1) {
-                p.out[orow * kD + tid] = o;
-                if (tid == 0) p.lse[orow] = ls;
+                p.out[orow * kD + d] = o;
+                if (d == 0) p.lse[orow] = ls;
             } else {
-                p.ws_o[(orow * p.n_split + split) * kD + tid] = o;
-                if (tid == 0) p.ws_lse[orow * p.n_split + split] = ls;
+                p.ws_o[(orow * p.n_split + split) * kD + d] = o;
+                if (d == 0) p.ws_lse[orow * p.n_split + split] = ls;
             }
         }
     }
@@ -770,7 +778,7 @@ cudaError_t launch_split_t(const AttnParams &p, bool dump, cudaStream_t s, bool 
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_split, p.n_kv_heads, p.n_seqs);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(SplitCfg<NT, VT>::THREADS);
     cfg.dynamicSmemBytes = SplitCfg<NT, VT>::SMEM;
     cfg.stream = s;
     cudaLaunchAttribute at[1];
@@ -789,7 +797,8 @@ cudaError_t prepare_split_t(bool dump, int *ctas_per_sm)
     const void *fn = dump ? (const void *)split_attn_kernel<NT, VT, true> : (const void *)split_attn_kernel<NT, VT, false>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    if (ctas_per_sm) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, kThreads, smem);
+    if (ctas_per_sm)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, SplitCfg<NT, VT>::THREADS, smem);
     return cudaSuccess;
 }
 

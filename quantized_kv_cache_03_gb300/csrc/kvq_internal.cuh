@@ -12,23 +12,64 @@ namespace kvq {
 
 constexpr int kD = KVQ_HEAD_DIM;        // head dim
 constexpr int kNB = kD / KVQ_QBLOCK;    // 32-blocks per head row (4)
-constexpr int kTile = 64;               // split chunks are multiples of this (kWarps * kWTile)
 constexpr int kWTile = 16;              // positions per warp pipeline stage
-constexpr int kWarps = 4;               // warps per split CTA, each streams its own sub-range
-constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 4;              // cp.async ring depth
+
+#ifndef KVQ_WARPS_NT1
+#define KVQ_WARPS_NT1 16   // warps per CTA of the <= 8-row kernels (128 registers: one CTA per SM)
+#endif
+#ifndef KVQ_WARPS_NTX
+#define KVQ_WARPS_NTX 4    // warps per CTA of the 16- and 32-row kernels (more registers per thread)
+#endif
+// Warps per split CTA for nt 8-row query tiles; each warp streams its own
+// contiguous sub-range of the split, so split chunks are rounded to a multiple
+// of split_warps(nt) * kWTile positions.
+constexpr int split_warps(int nt) { return nt == 1 ? KVQ_WARPS_NT1 : KVQ_WARPS_NTX; }
 constexpr int kMaxSegsLaunch = 64;      // segment-table entries per launch
 constexpr int kMaxSeqsLaunch = 64;      // sequences per launch
+
+// ------------------------------------------------------------ tile layout --
+// A segment stores each kv head's positions in tiles of kWTile = 16: tile T of
+// head h holds positions 16T..16T+15 and starts (h*cap + 16T) rows into each
+// array, so a tile of every array is one contiguous run of bytes (K codes 2048,
+// V codes 1024 (q4_0) or 2048 (q8_0), K and V scales 128 each) that a single
+// bulk copy moves.  Scales keep the plain [position][block] fp16 order.  The
+// code bytes of a tile are permuted so that the 16-byte word at
+// i*512 + lane*16 is the lane's i-th shared-memory load (lane = 4g + c of the
+// attention kernel's mma fragments); the bytes themselves are unchanged.
+// With u the position in the tile (sub = u/8, gu = u%8, cu = (u%8)/2, e = u%2)
+// and j the byte of the logical row:
+//   K      (j < 128, block bb = j/32):
+//          ((2 sub + bb/2) * 32 + 4 gu + (j%32)/8) * 16 + 8 (bb%2) + j%8
+//   V q4_0 (j < 64, bb = j/16, jj = j%16):
+//          (sub * 32 + 4 (jj/2) + cu) * 16 + 4 bb + 2 e + jj%2
+//   V q8_0 (j < 128, bb = j/32, jj = j%32):
+//          ((2 sub + bb/2) * 32 + 4 (jj/4) + cu) * 16 + 8 (bb%2) + 4 ((jj%4)/2) + 2 (jj%2) + e
+// so a K load gives one position's 8 codes of two blocks, a q4_0 load the code
+// bytes 2g, 2g+1 of positions (t, t+1) of all four blocks, and a q8_0 load
+// codes 4g..4g+3 of positions (t, t+1) of two blocks, (t, t+1) interleaved.
+__host__ __device__ constexpr int k_tile_off(int u, int j)
+{
+    return ((2 * (u / 8) + j / 64) * 32 + 4 * (u % 8) + (j % 32) / 8) * 16 + 8 * ((j / 32) % 2) + j % 8;
+}
+__host__ __device__ constexpr int v4_tile_off(int u, int j)
+{
+    return ((u / 8) * 32 + 4 * ((j % 16) / 2) + (u % 8) / 2) * 16 + 4 * (j / 16) + 2 * (u % 2) + j % 2;
+}
+__host__ __device__ constexpr int v8_tile_off(int u, int j)
+{
+    return ((2 * (u / 8) + j / 64) * 32 + 4 * ((j % 32) / 4) + (u % 8) / 2) * 16 + 8 * ((j / 32) % 2) +
+           4 * ((j % 4) / 2) + 2 * (j % 2) + u % 2;
+}
 
 // One segment as the attention kernel sees it (device pointers of kv head 0;
 // head h starts h*cap tokens further).
 struct SegDesc {
-    const uint32_t *kq;   // [Hkv][cap][kD/4] words
+    const uint8_t *kq;    // [Hkv][cap/16] tiles of 2048 code bytes
     const uint16_t *ks;   // [Hkv][cap][kNB] fp16 bits
-    const uint8_t *vq;    // [Hkv][cap][kD/2 or kD]
+    const uint8_t *vq;    // [Hkv][cap/16] tiles of 1024 (q4_0) or 2048 (q8_0) code bytes
     const uint16_t *vs;   // [Hkv][cap][kNB]
     int pos0;             // absolute position of token 0
-    int cap;              // tokens, multiple of kTile
+    int cap;              // tokens, multiple of KVQ_SEG_ALIGN
 };
 
 struct AttnParams {
@@ -50,6 +91,7 @@ struct AttnParams {
     int max_len;                           // positions >= max_len are ignored
     int n_split, chunk;                    // split s covers [s*chunk, (s+1)*chunk)
     float qk_scale_log2;                   // sm_scale * log2(e)
+    unsigned int *timeouts;                // bumped when a copy wait gives up (never in a correct run)
 };
 
 struct CombineParams {
@@ -62,7 +104,7 @@ struct CombineParams {
 };
 
 struct AppendEntry {
-    uint32_t *kq;
+    uint8_t *kq;
     uint16_t *ks;
     uint8_t *vq;
     uint16_t *vs;
@@ -81,7 +123,7 @@ struct AppendParams {
 };
 
 // ------------------------------------------------------------ host launchers --
-// Implemented in kvq_append.cu / kvq_attn_q4.cu / kvq_attn_q8.cu.
+// Implemented in kvq_small.cu / kvq_attn_q4.cu / kvq_attn_q8.cu.
 // n_tiles8 = query rows per kv head rounded up to 1, 2 or 4 tiles of 8.
 cudaError_t launch_append(const AppendParams &p, int v_type, int max_rows, cudaStream_t s, bool pdl);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t s, bool pdl);
@@ -103,15 +145,48 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// 16-byte global->shared async copy; src_bytes 0 zero-fills without reading.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes)
+// ---- mbarrier + bulk async copy (one elected lane issues, the warp waits) ----
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+// Make barrier initialisation visible to the async proxy (bulk copies).
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;\n fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Order this thread's earlier generic-proxy shared accesses before later
+// async-proxy ones (a bulk copy into a stage the warp has just read).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// One arrival that also announces tx bytes still to land on the barrier.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t tx)
+{
+    asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(bar), "r"(tx)
                  : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+// Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses
+// 16-byte aligned) that completes its bytes on barrier `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+// Wait for phase `parity` of the barrier to complete, giving up after
+// kMbarSpins polls (each poll may suspend the thread for a short while).
+constexpr uint32_t kMbarSpins = 1u << 22;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < kMbarSpins; ++i) {
+        uint32_t done;
+        asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+                     : "=r"(done)
+                     : "r"(bar), "r"(parity)
+                     : "memory");
+        if (done) return true;
+    }
+    return false;
+}
 
 // D = A(16x32 s8, row) * B(32x8 s8, col) + C, int32 accumulate.
 __device__ __forceinline__ void mma_s8_16832(int (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,

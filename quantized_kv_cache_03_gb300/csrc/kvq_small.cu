@@ -6,10 +6,12 @@ namespace kvq {
 // ---------------------------------------------------------------------------
 // Append-quantize.  One warp per (token, kv head) row of 128 fp16 values: lane
 // l holds elements 4l..4l+3 (one 8-byte load), so lanes 8b..8b+7 hold 32-block
-// b and a 3-step xor shuffle gives the block absmax.  K (and q8_0 V) codes are
-// packed four per word and stored as one coalesced 128-byte row; q4_0 lanes
-// 0..3 of each block pull the codes of elements 16.. from lanes 4..7 and store
-// byte j = q[j] | q[j+16] << 4.
+// b and a 3-step xor shuffle gives the block absmax.  Codes go to their place
+// in the position's 16-position tile (k_tile_off / v4_tile_off / v8_tile_off):
+// a K lane's four codes stay one word; q4_0 lanes 0..3 of each block pull the
+// codes of elements 16.. from lanes 4..7, form bytes j = q[j] | q[j+16] << 4 and
+// store them as two byte pairs; q8_0 codes are stored byte by byte (the tile
+// interleaves neighbouring positions).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float block_absmax(const float (&x)[4])
 {
@@ -55,17 +57,22 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
     const size_t src = ((size_t)(e.src + tok) * H + h) * kD + lane * 4;
     const size_t dst = (size_t)h * e.cap + e.dst + tok;   // token row in the segment
 
+    const int u = (e.dst + tok) % kWTile;                      // position in its tile
+    const size_t tile = (size_t)h * e.cap + e.dst + tok - u;    // first row of the tile
+
     float x[4];
     uint16_t s16;
     load4h(p.k16 + src, x);
     const uint32_t kw = quant_row_i8(x, s16);
-    e.kq[dst * (kD / 4) + lane] = kw;
+    *reinterpret_cast<uint32_t *>(e.kq + tile * kD + k_tile_off(u, 4 * lane)) = kw;
     if ((lane & 7) == 0) e.ks[dst * kNB + (lane >> 3)] = s16;
 
     load4h(p.v16 + src, x);
     if (VT == KVQ_V_Q8_0) {
         const uint32_t vw = quant_row_i8(x, s16);
-        reinterpret_cast<uint32_t *>(e.vq)[dst * (kD / 4) + lane] = vw;
+        uint8_t *t = e.vq + tile * kD;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) t[v8_tile_off(u, 4 * lane + k)] = (uint8_t)(vw >> (8 * k));
         if ((lane & 7) == 0) e.vs[dst * kNB + (lane >> 3)] = s16;
     } else {
         const float a = block_absmax(x);
@@ -75,8 +82,13 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
 #pragma unroll
         for (int k = 0; k < 4; ++k) q |= (uint32_t)quant_q4(x[k], d) << (8 * k);
         const uint32_t qhi = __shfl_down_sync(0xffffffffu, q, 4);   // elements 16.. of the block
-        if ((lane & 7) < 4)
-            reinterpret_cast<uint32_t *>(e.vq)[dst * (kD / 8) + (lane >> 3) * 4 + (lane & 3)] = q | (qhi << 4);
+        if ((lane & 7) < 4) {
+            const uint32_t w = q | (qhi << 4);                       // bytes 4(l%4)..+3 of block l/8
+            const int j = 16 * (lane >> 3) + 4 * (lane & 3);
+            uint8_t *t = e.vq + tile * (kD / 2);
+            *reinterpret_cast<uint16_t *>(t + v4_tile_off(u, j)) = (uint16_t)w;
+            *reinterpret_cast<uint16_t *>(t + v4_tile_off(u, j + 2)) = (uint16_t)(w >> 16);
+        }
         if ((lane & 7) == 0) e.vs[dst * kNB + (lane >> 3)] = __half_as_ushort(dh);
     }
 }

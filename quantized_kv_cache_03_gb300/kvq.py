@@ -22,6 +22,7 @@ KVQ_ERR_UNSUPPORTED = 2
 KVQ_ERR_CAPACITY = 3
 KVQ_ERR_WORKSPACE = 4
 KVQ_ERR_CUDA = 5
+KVQ_ERR_TIMEOUT = 6
 V_Q4_0 = 0
 V_Q8_0 = 1
 HEAD_DIM = 128
@@ -29,7 +30,7 @@ SEG_ALIGN = 64
 QBLOCK = 32
 
 EXPORTED = ("kvq_append", "kvq_decode_attn", "kvq_decode_workspace_size", "kvq_decode_attn_noalloc",
-            "kvq_status_string", "kvq_debug_qk")
+            "kvq_wait_timeouts", "kvq_status_string", "kvq_debug_qk")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -78,6 +79,8 @@ def load():
             lib.kvq_decode_attn_noalloc.argtypes = [POINTER(KvqCache), c_void_p, c_int32, c_int32, c_int32,
                                                     c_void_p, c_int32, POINTER(c_int32), c_float, c_void_p,
                                                     c_void_p, c_void_p]
+            lib.kvq_wait_timeouts.restype = c_int32
+            lib.kvq_wait_timeouts.argtypes = [POINTER(ctypes.c_uint32)]
             lib.kvq_debug_qk.restype = c_int32
             lib.kvq_debug_qk.argtypes = [POINTER(KvqCache), c_void_p, c_int32, c_int32, c_void_p, c_int32,
                                          POINTER(c_int32), c_void_p, c_void_p, c_void_p, c_void_p]
@@ -162,18 +165,54 @@ class Cache:
     def lengths(self):
         return [self.length(b) for b in range(self.n_seqs)]
 
-    def export(self, b: int):
-        """Test helper: the filled positions of sequence b gathered to host
-        numpy arrays in logical order ([H][L][...] per array)."""
+    def export(self, b: int, raw: bool = False):
+        """Sequence b copied to host numpy arrays.  raw=False: the filled
+        positions, [H][L][row] per array in logical row order.  raw=True: one
+        dict per segment with the whole arrays as stored ([H][cap][row], code
+        bytes in their in-tile order) plus its "len"."""
         import numpy as np
         parts = {n: [] for n in ("kq", "ks", "vq", "vs")}
+        segs = []
         for k in range(self._nsegs[b]):
             s, t = self.seg(b, k), self.tensors[b][k]
-            parts["kq"].append(t["k_q"][:, :s.len].cpu().numpy())
-            parts["ks"].append(t["k_s"][:, :s.len].cpu().numpy().view(np.uint16))
-            parts["vq"].append(t["v_q"][:, :s.len].cpu().numpy())
-            parts["vs"].append(t["v_s"][:, :s.len].cpu().numpy().view(np.uint16))
+            seg = {"len": s.len}
+            for name, key, view in (("kq", "k_q", np.uint8), ("ks", "k_s", np.uint16),
+                                    ("vq", "v_q", np.uint8), ("vs", "v_s", np.uint16)):
+                a = t[key].cpu().numpy().view(view)
+                seg[name] = a
+                if not raw and name in ("kq", "vq"):
+                    a = untile_codes(a, name, self.v_type)
+                parts[name].append(a[:, :s.len])
+            segs.append(seg)
+        if raw:
+            return segs
         return {n: np.concatenate(v, axis=1) for n, v in parts.items()}
+
+
+def _tile_index(name: str, v_type: int):
+    """idx[u, j] = in-tile offset of byte j of the tile's token u (the tile
+    layout of include/kvq.h, head_dim 128)."""
+    import numpy as np
+    u = np.arange(16)[:, None]
+    sub, gu, e = u // 8, u % 8, u % 2
+    cu = gu // 2
+    if name == "kq":
+        j = np.arange(128)[None, :]
+        return ((2 * sub + j // 64) * 32 + 4 * gu + (j % 32) // 8) * 16 + 8 * ((j // 32) % 2) + j % 8
+    if v_type == V_Q4_0:
+        j = np.arange(64)[None, :]
+        return (sub * 32 + 4 * ((j % 16) // 2) + cu) * 16 + 4 * (j // 16) + 2 * e + j % 2
+    j = np.arange(128)[None, :]
+    return (((2 * sub + j // 64) * 32 + 4 * ((j % 32) // 4) + cu) * 16 + 8 * ((j // 32) % 2)
+            + 4 * ((j % 4) // 2) + 2 * (j % 2) + e)
+
+
+def untile_codes(a, name: str, v_type: int):
+    """Stored code bytes [H][cap][row] -> logical row order (cap % 16 == 0)."""
+    H, cap, row = a.shape
+    idx = _tile_index(name, v_type)
+    tiles = a.reshape(H, cap // 16, 16 * row)
+    return tiles[:, :, idx].reshape(H, cap, row)
 
 
 def kvq_append(cache: Cache, seq_ids, n_new, k16: torch.Tensor, v16: torch.Tensor, stream=None) -> None:
@@ -232,3 +271,13 @@ def kvq_debug_qk(cache: Cache, q16, n_q_heads, t_q, seq_lens, max_len, head_map,
                              _ptr(q_codes), _ptr(q_scales), _ptr(scores), _stream(stream))
     if st:
         raise KvqError(st, "kvq_debug_qk")
+
+
+def kvq_wait_timeouts() -> int:
+    """kvq_wait_timeouts of include/kvq.h: the device's count of attention-kernel
+    copy waits that gave up (0 in every correct run)."""
+    n = ctypes.c_uint32(0)
+    st = load().kvq_wait_timeouts(ctypes.byref(n))
+    if st not in (0, KVQ_ERR_TIMEOUT):
+        raise KvqError(st, "kvq_wait_timeouts")
+    return int(n.value)

@@ -95,9 +95,67 @@ class Case:
                                  n_threads=threads)
 
 
+def lane_view_index(name, v_type):
+    """(stored offset, token u, logical byte j) of every code byte of a 16-token
+    tile, enumerated the way the attention kernel reads a stage: 16-byte load i
+    of lane = 4g + c, byte q of that load.
+      K:    load i = 2 sub + hb: token 8 sub + g, codes 8c..8c+7 of block 2hb
+            (bytes 0..7) and of block 2hb + 1 (bytes 8..15).
+      q4_0: load i = sub, word bb = block bb: bytes 2g, 2g+1 of token t, then of
+            token t + 1, t = 8 sub + 2c.
+      q8_0: load i = 2 sub + hb, bytes 0..7 block 2hb, 8..15 block 2hb + 1; in
+            each half word 0 holds dims 4g, 4g+1 and word 1 dims 4g+2, 4g+3,
+            each as (t, t+1, t, t+1)."""
+    rows = []
+    for lane in range(32):
+        g, c = lane // 4, lane % 4
+        for q in range(16):
+            if name == "kq":
+                for i in range(4):
+                    sub, hb = i // 2, i % 2
+                    bb = 2 * hb + q // 8
+                    rows.append((i * 512 + lane * 16 + q, 8 * sub + g, 32 * bb + 8 * c + q % 8))
+            elif v_type == kvq.V_Q4_0:
+                for i in range(2):
+                    bb, w = q // 4, q % 4
+                    rows.append((i * 512 + lane * 16 + q, 8 * i + 2 * c + w // 2, 16 * bb + 2 * g + w % 2))
+            else:
+                for i in range(4):
+                    sub, hb = i // 2, i % 2
+                    bb, r = 2 * hb + q // 8, q % 8
+                    wd, y = r // 4, r % 4
+                    rows.append((i * 512 + lane * 16 + q, 8 * sub + 2 * c + y % 2, 32 * bb + 4 * g + 2 * wd + y // 2))
+    return np.array(rows, dtype=np.int64)
+
+
+def logical_codes(stored, name, v_type):
+    """Stored code bytes [H][cap][row] (tile order) -> logical [H][cap][row]."""
+    H, cap, row = stored.shape
+    idx = lane_view_index(name, v_type)
+    assert len(idx) == 16 * row and len(np.unique(idx[:, 0])) == 16 * row
+    tiles = stored.reshape(H, cap // 16, 16 * row)
+    out = np.empty((H, cap // 16, 16, row), dtype=np.uint8)
+    out[:, :, idx[:, 1], idx[:, 2]] = tiles[:, :, idx[:, 0]]
+    return out.reshape(H, cap, row)
+
+
+def export_logical(cache, b):
+    """Sequence b's filled positions in logical order, un-tiled by the lane view
+    above (independently of the library's own untile helper)."""
+    parts = {n: [] for n in ("kq", "ks", "vq", "vs")}
+    for seg in cache.export(b, raw=True):
+        n = seg["len"]
+        for name in parts:
+            a = seg[name]
+            if name in ("kq", "vq"):
+                a = logical_codes(a.view(np.uint8), name, cache.v_type)
+            parts[name].append(a[:, :n])
+    return {k: np.concatenate(v, axis=1) for k, v in parts.items()}
+
+
 def assert_cache_bytes(case, b, oc=None):
     oc = case.oracle_cache(b) if oc is None else oc
-    got = case.cache.export(b)
+    got = export_logical(case.cache, b)
     for name in ("kq", "ks", "vq", "vs"):
         g, o = got[name].view(np.uint8), oc[name].view(np.uint8)
         assert g.shape == o.shape, (name, g.shape, o.shape)

@@ -8,7 +8,7 @@ import pytest
 import oracle
 from quantized_kv_cache_03_gb300 import workloads as W
 
-from kvq_cases import Case, assert_close
+from kvq_cases import Case, assert_close, export_logical
 
 pytestmark = pytest.mark.gpu
 
@@ -26,7 +26,7 @@ def _sample_check(case, seqs, n_rows=6, seed=0):
     for b in seqs:
         L = case.lens[b]
         oc = case.oracle_cache(b)
-        got = case.cache.export(b)
+        got = export_logical(case.cache, b)
         pos = np.unique(np.concatenate([np.arange(min(L, 300)), np.arange(max(0, L - 300), L),
                                         rng.integers(0, L, 2000)]))
         for name in ("kq", "ks", "vq", "vs"):
