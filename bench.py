@@ -89,6 +89,16 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+def launches_of(grp, fused):
+    """Kernels one step launches: one append per cache, then the fused decode's
+    split kernel (one per launch group of <= 64 sequences / 64 segments / 8
+    work groups) and, when any sequence is split, its combine."""
+    seqs = sum(ds.B for ds in grp)
+    segs = sum(len(x) for ds in grp for x in ds.spec.segments)
+    groups = max(-(-seqs // 64), -(-segs // 64), -(-len(grp) // 8))
+    return len(grp) + groups * (2 if fused.call.ws is not None else 1)
+
+
 def profiled_traffic(workload):
     """DRAM bytes per split-kernel launch from the committed ncu summary, if it
     was taken on the current kernel sources (else None)."""
@@ -221,7 +231,7 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     from quantized_kv_cache_03_gb300 import kvq
-    from quantized_kv_cache_03_gb300.harness import DecodeSet, HostData
+    from quantized_kv_cache_03_gb300.harness import DecodeSet, HostData, StepSet
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -234,17 +244,17 @@ def main():
         grp = [DecodeSet(d, dev) for d in data]
         for ds in grp:
             ds.staging = None
+        fused = StepSet(grp)
         for _ in range(max(1, args.warmup) + max(1, args.steps)):
             for ds in grp:
                 ds.append_step()
-            for ds in grp:
-                ds.decode()
+            fused.decode()
             for ds in grp:
                 ds.rewind()
         torch.cuda.synchronize()
         print(json.dumps({"mode": "profile", "workload": args.workload, "ctx": args.ctx,
                           "steps": max(1, args.warmup) + max(1, args.steps),
-                          "launches_per_step": sum(ds.launches_per_step() for ds in grp),
+                          "launches_per_step": launches_of(grp, fused),
                           "kv_bytes_per_step": kv_bytes}), flush=True)
         return
     n_rot = max(3, -(-3 * L2_BYTES // max(1, kv_bytes)))
@@ -258,41 +268,51 @@ def main():
         for ds in grp:
             ds.staging = None
     torch.cuda.synchronize()
-    launches_per_step = sum(ds.launches_per_step() for ds in sets[0])
+    fused = [StepSet(grp) for grp in sets]
+    launches_per_step = launches_of(sets[0], fused[0])
 
     stream = torch.cuda.Stream(device=dev)
 
-    def step(grp):
+    def step(grp, fz=None):
+        """One step: append every cache's new tokens, decode all caches (one
+        fused call, or one call per cache when fz is None), rewind."""
         for ds in grp:
             ds.append_step(stream=stream)
-        for ds in grp:
-            ds.decode(stream=stream)
+        if fz is not None:
+            fz.decode(stream=stream)
+        else:
+            for ds in grp:
+                ds.decode(stream=stream)
         for ds in grp:
             ds.rewind()
 
     # ---- capture one graph that runs one step on every rotation copy ----
     with torch.cuda.stream(stream):
-        for grp in sets:          # warm-up outside capture (first call sets device attributes)
+        for grp, fz in zip(sets, fused):   # warm-up outside capture (first call sets device attributes)
+            step(grp, fz)
             step(grp)
     stream.synchronize()
     g_all = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_all, stream=stream):
+        for grp, fz in zip(sets, fused):
+            step(grp, fz)
+    # the same steps with one decode call per cache (reported beside the fused number)
+    g_sep = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_sep, stream=stream):
         for grp in sets:
             step(grp)
-    # per-cache timing graphs: events around each decode call (separate pass)
+    # decode timing graph: events around each step's fused decode call (separate pass);
+    # external event nodes, so their timestamps can be read after each replay
     g_ev = torch.cuda.CUDAGraph()
-    # external event nodes: their timestamps can be read after each replay
-    ev_pairs = [[(torch.cuda.Event(enable_timing=True, external=True),
-                  torch.cuda.Event(enable_timing=True, external=True))
-                 for _ in sets[0]] for _ in sets]
+    ev_pairs = [(torch.cuda.Event(enable_timing=True, external=True),
+                 torch.cuda.Event(enable_timing=True, external=True)) for _ in sets]
     with torch.cuda.graph(g_ev, stream=stream):
-        for grp, evs in zip(sets, ev_pairs):
+        for grp, fz, (a, b) in zip(sets, fused, ev_pairs):
             for ds in grp:
                 ds.append_step(stream=stream)
-            for ds, (a, b) in zip(grp, evs):
-                a.record(stream)
-                ds.decode(stream=stream)
-                b.record(stream)
+            a.record(stream)
+            fz.decode(stream=stream)
+            b.record(stream)
             for ds in grp:
                 ds.rewind()
 
@@ -324,19 +344,29 @@ def main():
         ms = float(t.item())
     ms_per_step = ms / steps
 
-    # ---- kernel-level timing pass (decode = split kernel + its combine) ----
+    # ---- one decode call per cache instead of the fused call (same steps) ----
+    sreps = max(1, min(reps, 2000 // n_rot))
+    with torch.cuda.stream(stream):
+        g_sep.replay()
+        e0.record(stream)
+        for _ in range(sreps):
+            g_sep.replay()
+        e1.record(stream)
+    stream.synchronize()
+    sep_ms_per_step = e0.elapsed_time(e1) / (sreps * n_rot)
+
+    # ---- kernel-level timing pass (decode = the split kernel + its combine) ----
     kreps = max(1, min(reps, 2000 // n_rot))
-    tot = np.zeros(len(sets[0]))
+    tot = 0.0
     with torch.cuda.stream(stream):
         for _ in range(kreps):
             g_ev.replay()
             stream.synchronize()
-            for evs in ev_pairs:
-                for j, (a, b) in enumerate(evs):
-                    tot[j] += a.elapsed_time(b)
-    dec_ms = tot / (kreps * n_rot)                     # per cache, per step
-    dec_bytes = np.array([W.step_kv_bytes([ds.spec]) for ds in sets[0]], dtype=np.float64)
-    achieved = float(dec_bytes.sum() / (dec_ms.sum() * 1e-3) / 1e9)
+            for a, b in ev_pairs:
+                tot += a.elapsed_time(b)
+    dec_ms = tot / (kreps * n_rot)                     # per step (all caches)
+    dec_bytes = float(kv_bytes)
+    achieved = float(dec_bytes / (dec_ms * 1e-3) / 1e9)
     peak, peak_kind = measured_peaks()
 
     # ---- end to end through the public API with host buffers ----
@@ -350,6 +380,8 @@ def main():
               for a, b, c in h_in)
     d2h = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in h_out)
 
+    e2e_call = StepSet(grp, q16=[dq for dq, _, _ in d_in])
+
     def e2e_step():
         for (hq, hk, hv), (dq, dk, dv) in zip(h_in, d_in):
             dq.copy_(hq, non_blocking=True)
@@ -357,8 +389,7 @@ def main():
             dv.copy_(hv, non_blocking=True)
         for ds, (dq, dk, dv) in zip(grp, d_in):
             ds.append_step(dk, dv, stream=stream)
-        for ds, (dq, dk, dv) in zip(grp, d_in):
-            ds.decode(dq, stream=stream)
+        e2e_call.decode(stream=stream)
         for ds, (ho, hl) in zip(grp, h_out):
             ho.copy_(ds.out, non_blocking=True)
             hl.copy_(ds.lse, non_blocking=True)
@@ -401,12 +432,12 @@ def main():
                    "kv_bytes_per_step": kv_bytes, "tokens_per_step": tokens_per_step},
         "kv_gbs": kv_gbs, "kv_frac_of_8tbs": kv_gbs / NOMINAL_HBM_GBS,
         "kv_frac_of_measured_copy": kv_gbs / peak,
-        "roofline": {"bound": "hbm", "kernel": "split_attn (+ its combine)", "achieved": achieved,
-                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
+        "roofline": {"bound": "hbm", "kernel": "split_attn (+ its combine), all caches in one launch",
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
                      "traffic": profiled_traffic(args.workload),
-                     "decode_us_per_cache": [1e3 * x for x in dec_ms],
-                     "algorithmic_bytes_per_cache": [int(x) for x in dec_bytes]},
+                     "decode_us": 1e3 * dec_ms, "algorithmic_bytes": int(dec_bytes)},
+        "per_cache_calls_ms_per_step": sep_ms_per_step,
         "e2e": {"value": tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * steps,

@@ -52,6 +52,7 @@ extern "C" {
 #define KVQ_MAX_ROWS 32        /* query rows per kv head: t_q * (q heads of it)   */
 #define KVQ_MAX_T_Q 8          /* query tokens per sequence per call              */
 #define KVQ_MAX_HEADS 256      /* n_q_heads and n_kv_heads limit                  */
+#define KVQ_MAX_CALLS 16       /* decode calls fused by kvq_decode_attn_multi     */
 
 typedef enum kvq_status {
     KVQ_OK = 0,
@@ -175,7 +176,8 @@ kvq_status kvq_append(kvq_cache *c, int32_t n_seqs_in, const int32_t *seq_ids,
  *            that size is 0.
  *  workspace_bytes size of workspace; KVQ_ERR_WORKSPACE if it is too small.
  * Launches (per group of at most 64 sequences): the split-KV attention kernel
- * and, when a sequence is split, the log-sum-exp combine kernel.
+ * and, when a sequence is split, the log-sum-exp combine kernel.  It is
+ * kvq_decode_attn_multi with one call.
  */
 kvq_status kvq_decode_attn(const kvq_cache *c, const void *q16, int32_t n_q_heads,
                            int32_t t_q, int32_t causal_tail, const int32_t *seq_lens,
@@ -192,6 +194,48 @@ kvq_status kvq_decode_attn(const kvq_cache *c, const void *q16, int32_t n_q_head
  */
 kvq_status kvq_decode_workspace_size(const kvq_cache *c, int32_t n_q_heads, int32_t t_q,
                                      int32_t max_len, const int32_t *head_map, size_t *bytes);
+
+/*
+ * One decode call for kvq_decode_attn_multi: the arguments of kvq_decode_attn
+ * that belong to one cache, with the same meaning and rules.
+ */
+typedef struct kvq_decode_desc {
+    const kvq_cache *cache;
+    const void *q16;
+    int32_t n_q_heads;
+    int32_t t_q;
+    int32_t causal_tail;
+    const int32_t *seq_lens;
+    int32_t max_len;
+    const int32_t *head_map;
+    float sm_scale;
+    float *out;
+    float *lse;
+} kvq_decode_desc;
+
+/*
+ * kvq_decode_attn_multi -- n (0..KVQ_MAX_CALLS) decode calls, e.g. the main
+ * and the draft model's caches of one speculative-decoding step, enqueued as
+ * one split-attention launch (and one combine) instead of one per call.  Each
+ * call computes exactly what kvq_decode_attn computes for it; the calls may
+ * use different caches, head counts, head maps, t_q and scales, but caches with
+ * different V formats go to separate launches.  Splits are planned over all
+ * calls together, so the GPU fills with the calls' positions at once.
+ *  calls      host array [n] (read during the call only).
+ *  workspace  as kvq_decode_attn, at least kvq_decode_multi_workspace_size().
+ * Errors: as kvq_decode_attn, checked for every call before anything is
+ * enqueued.  The pages describe single-cache decode only; fusing calls is the
+ * library's own launch plan.
+ */
+kvq_status kvq_decode_attn_multi(int32_t n, const kvq_decode_desc *calls, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/*
+ * kvq_decode_multi_workspace_size -- bytes of workspace kvq_decode_attn_multi
+ * needs for these calls (q16, seq_lens, out and lse are not read).
+ *  bytes  host out.
+ */
+kvq_status kvq_decode_multi_workspace_size(int32_t n, const kvq_decode_desc *calls, size_t *bytes);
 
 /*
  * kvq_decode_attn_noalloc -- kvq_decode_attn for callers that cannot allocate

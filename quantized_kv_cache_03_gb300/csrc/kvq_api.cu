@@ -110,271 +110,336 @@ kvq_status check_cache(const kvq_cache *c)
     return KVQ_OK;
 }
 
-// Query-head groups per kv head from head_map (host) or contiguous groups.
-kvq_status build_groups(const kvq_cache *c, int n_q_heads, const int32_t *head_map, int t_q, AttnParams &p,
-                        int &max_rows)
+// One decode call (one cache) as the planner sees it.
+struct Desc {
+    const kvq_cache *c;
+    const uint16_t *q;
+    int n_q_heads, t_q, causal;
+    const int32_t *seq_lens;
+    int max_len;
+    float sm_scale;
+    float *out, *lse;
+    int8_t *dbg_qc;
+    uint16_t *dbg_qs;
+    int32_t *dbg_scores;
+    std::vector<int> kv;   // query head -> kv head
+    int max_rows;          // query rows of the busiest kv head
+};
+
+// Validate one call's shape arguments and derive its head map.
+kvq_status prepare_desc(Desc &d, const int32_t *head_map, bool need_ptrs, bool dump)
 {
+    kvq_status st = check_cache(d.c);
+    if (st != KVQ_OK) return st;
+    const kvq_cache *c = d.c;
+    if (d.t_q < 1 || d.t_q > KVQ_MAX_T_Q || d.max_len < 0) return KVQ_ERR_INVALID_ARG;
+    if (!(std::isfinite(d.sm_scale))) return KVQ_ERR_INVALID_ARG;
     const int H = c->n_kv_heads;
-    if (n_q_heads < 1 || n_q_heads > KVQ_MAX_HEADS) return KVQ_ERR_INVALID_ARG;
-    std::vector<int> kv(n_q_heads);
+    if (d.n_q_heads < 1 || d.n_q_heads > KVQ_MAX_HEADS) return KVQ_ERR_INVALID_ARG;
+    d.kv.assign(d.n_q_heads, 0);
     if (head_map) {
-        for (int h = 0; h < n_q_heads; ++h) {
+        for (int h = 0; h < d.n_q_heads; ++h) {
             if (head_map[h] < 0 || head_map[h] >= H) return KVQ_ERR_INVALID_ARG;
-            kv[h] = head_map[h];
+            d.kv[h] = head_map[h];
         }
     } else {
-        if (n_q_heads % H) return KVQ_ERR_INVALID_ARG;
-        const int gsz = n_q_heads / H;
-        for (int h = 0; h < n_q_heads; ++h) kv[h] = h / gsz;
+        if (d.n_q_heads % H) return KVQ_ERR_INVALID_ARG;
+        const int gsz = d.n_q_heads / H;
+        for (int h = 0; h < d.n_q_heads; ++h) d.kv[h] = h / gsz;
     }
-    int n = 0, gmax = 0;
-    for (int k = 0; k < H; ++k) {
-        p.grp_begin[k] = (uint16_t)n;
-        for (int h = 0; h < n_q_heads; ++h)
-            if (kv[h] == k) p.grp_q[n++] = (uint8_t)h;
-        gmax = std::max(gmax, n - (int)p.grp_begin[k]);
+    std::vector<int> cnt(H, 0);
+    for (int h = 0; h < d.n_q_heads; ++h) ++cnt[d.kv[h]];
+    int gmax = 0;
+    for (int k = 0; k < H; ++k) gmax = std::max(gmax, cnt[k]);
+    d.max_rows = gmax * d.t_q;
+    if (d.max_rows > KVQ_MAX_ROWS) return KVQ_ERR_UNSUPPORTED;
+    if (need_ptrs && c->n_seqs > 0) {
+        if (!d.q || !aligned16(d.q) || !d.seq_lens) return KVQ_ERR_INVALID_ARG;
+        if (dump ? (!d.dbg_qc || !d.dbg_qs || !d.dbg_scores) : (!d.out || !d.lse)) return KVQ_ERR_INVALID_ARG;
+        if (!dump && (!aligned16(d.out) || (reinterpret_cast<uintptr_t>(d.lse) & 3u))) return KVQ_ERR_INVALID_ARG;
     }
-    p.grp_begin[H] = (uint16_t)n;
-    max_rows = gmax * t_q;
-    if (max_rows > KVQ_MAX_ROWS) return KVQ_ERR_UNSUPPORTED;
     return KVQ_OK;
 }
 
 int tiles8_for(int rows) { return rows <= 8 ? 1 : rows <= 16 ? 2 : 4; }
-
-struct Group {
-    int b0, nb;          // sequences [b0, b0 + nb)
-    int n_split, chunk;
-    size_t ws_off;       // bytes
-};
-
 int round_up(long long x, int m) { return (int)((x + m - 1) / m * m); }
 
-// Split policy: enough CTAs to fill every SM with whole waves.  Uniform lengths:
-// the smallest split count (>= one wave) whose last wave is >= 90% full.
-// Ragged lengths: a chunk of about a quarter wave's share of the positions.
-// Chunks are multiples of gran (one stage per warp of the CTA) so that every
-// warp gets the same number of stages; a chunk forced through KVQ_SPLIT only
-// needs the 64-position segment alignment.
-void choose_split(const kvq_cache *c, const Group &g, int max_len, int slots, int gran, int &n_split, int &chunk)
+// Positions of sequence b that the kernel may visit: the end of its last
+// segment's capacity, cut at max_len.
+int seq_reach(const kvq_cache *c, int b, int max_len)
 {
-    const int H = c->n_kv_heads;
-    long long total = 0;
-    int lmax = 0, lmin = 0x7fffffff;
-    for (int b = g.b0; b < g.b0 + g.nb; ++b) {
-        if (c->n_segs[b] == 0) {
-            lmin = 0;
-            continue;
-        }
-        const kvq_segment &sl = seg_of(c, b, c->n_segs[b] - 1);
-        const int L = std::min(max_len, sl.pos0 + sl.len);
-        const int Lcap = std::min(max_len, sl.pos0 + sl.cap);
-        total += (long long)L * H;
-        lmax = std::max(lmax, Lcap);
-        lmin = std::min(lmin, L);
-    }
-    if (lmax <= 0) {
-        n_split = 1;
-        chunk = KVQ_SEG_ALIGN;
-        return;
-    }
+    if (c->n_segs[b] == 0) return 0;
+    const kvq_segment &sl = seg_of(c, b, c->n_segs[b] - 1);
+    return std::max(0, std::min(max_len, sl.pos0 + sl.cap));
+}
+
+// A work group: sequences [b0, b0 + nb) of call d.
+struct Unit {
+    int d, b0, nb;
+    int reach;          // max seq_reach over the unit
+    int n_split;
+    size_t ws_off;      // bytes
+    int cta0, row0;
+};
+
+// A split launch: units of calls with one V format, run in one grid.
+struct Launch {
+    int v_type = 0, nt = 1;
+    int chunk = KVQ_SEG_ALIGN;
+    int n_ctas = 0, n_rows = 0;   // split CTAs, combine rows
+    std::vector<Unit> units;
+};
+
+// Split policy, one chunk per launch so that CTAs of every unit do the same
+// amount of work.  For a candidate chunk c the launch has n CTAs with work
+// W (kv positions) in total; with `slots` CTAs resident at once and a fixed
+// cost of about kOverhead positions per CTA, the finish time is estimated as
+// c + overhead when one wave holds every CTA, else (W + n * overhead) / slots
+// plus one more CTA for the tail.  The cheapest candidate wins (the larger
+// chunk on ties).  Chunks are multiples of gran (one stage per warp of the
+// CTA) and at least 256 positions; KVQ_SPLIT forces a chunk (rounded to the
+// 64-position segment alignment).
+constexpr int kOverhead = 512;
+int choose_chunk(const std::vector<Desc> &ds, const Launch &ln, int slots, int gran)
+{
+    int lmax = 0;
+    for (const Unit &u : ln.units) lmax = std::max(lmax, u.reach);
+    if (lmax <= 0) return KVQ_SEG_ALIGN;
     const char *env = std::getenv("KVQ_SPLIT");
+    int chunk;
     if (env && std::atoi(env) > 0) {
         chunk = round_up(std::atoi(env), KVQ_SEG_ALIGN);
     } else {
-        const int pairs = g.nb * H;
-        const int max_n = std::max(1, (lmax + 255) / 256);   // at least 256 positions per split
-        int n = 1;
-        if (lmin * 2 >= lmax || total == 0) {
-            const int n_min = std::max(1, (slots + pairs - 1) / pairs);
-            double best = -1.0;
-            n = std::min(n_min, max_n);   // short contexts: as many splits as the 256-position floor allows
-            for (int k = n_min; k <= 4 * n_min && k <= max_n; ++k) {
-                const double waves = (double)pairs * k / slots;
-                const double eff = waves / std::ceil(waves);
-                if (eff > best + 1e-9) {
-                    best = eff;
-                    n = k;
-                }
-                if (eff >= 0.9) break;
-            }
-            n = std::min(std::max(n, 1), max_n);
-        } else {
-            const long long per_cta = std::max<long long>(256, total / std::max(1, 4 * slots));
-            n = (int)std::min<long long>(max_n, (lmax + per_cta - 1) / per_cta);
-        }
-        chunk = round_up((lmax + n - 1) / n, gran);
-    }
-    n_split = (lmax + chunk - 1) / chunk;
-    if (n_split > 1024) {
-        chunk = round_up((lmax + 1023) / 1024, gran);
-        n_split = (lmax + chunk - 1) / chunk;
-    }
-}
-
-// Partition the batch into launch groups (<= 64 sequences and <= 64 segments).
-void make_groups(const kvq_cache *c, std::vector<Group> &gs)
-{
-    int b = 0;
-    while (b < c->n_seqs) {
-        Group g{b, 0, 1, KVQ_SEG_ALIGN, 0};
-        int segs = 0;
-        while (b < c->n_seqs && g.nb < kMaxSeqsLaunch && segs + c->n_segs[b] <= kMaxSegsLaunch) {
-            segs += c->n_segs[b];
-            ++g.nb;
-            ++b;
-        }
-        gs.push_back(g);
-    }
-}
-
-void fill_segments(const kvq_cache *c, const Group &g, AttnParams &p)
-{
-    int n = 0;
-    for (int i = 0; i < g.nb; ++i) {
-        const int b = g.b0 + i;
-        p.seq_seg0[i] = (uint8_t)n;
-        p.seq_nseg[i] = (uint8_t)c->n_segs[b];
-        for (int k = 0; k < c->n_segs[b]; ++k, ++n) {
-            const kvq_segment &s = seg_of(c, b, k);
-            p.seg[n].kq = static_cast<const uint8_t *>(s.k_q);
-            p.seg[n].ks = static_cast<const uint16_t *>(s.k_s);
-            p.seg[n].vq = static_cast<const uint8_t *>(s.v_q);
-            p.seg[n].vs = static_cast<const uint16_t *>(s.v_s);
-            p.seg[n].pos0 = s.pos0;
-            p.seg[n].cap = s.cap;
-        }
-    }
-}
-
-struct DecodeArgs {
-    const kvq_cache *c;
-    const void *q16;
-    int n_q_heads, t_q, causal;
-    const int32_t *seq_lens;
-    int max_len;
-    const int32_t *head_map;
-    float sm_scale;
-    float *out, *lse;
-    void *workspace;
-    size_t workspace_bytes;
-    size_t *size_out;    // size query only: store the required workspace and return
-    int8_t *dbg_qc;
-    uint16_t *dbg_qs;
-    int32_t *dbg_scores;
-    bool dump;
-    cudaStream_t stream;
-};
-
-kvq_status run_decode(const DecodeArgs &a)
-{
-    const kvq_cache *c = a.c;
-    kvq_status st = check_cache(c);
-    if (st != KVQ_OK) return st;
-    if (a.t_q < 1 || a.t_q > KVQ_MAX_T_Q || a.max_len < 0) return KVQ_ERR_INVALID_ARG;
-    if (!(std::isfinite(a.sm_scale))) return KVQ_ERR_INVALID_ARG;
-    static thread_local AttnParams p;   // ~4 KB; kept off the stack
-    std::memset(&p, 0, sizeof(p));
-    int max_rows = 0;
-    st = build_groups(c, a.n_q_heads, a.head_map, a.t_q, p, max_rows);
-    if (st != KVQ_OK) return st;
-    if (c->n_seqs == 0) {
-        if (a.size_out) *a.size_out = 0;
-        return KVQ_OK;
-    }
-    if (!a.size_out) {
-        if (!a.q16 || !aligned16(a.q16) || !a.seq_lens) return KVQ_ERR_INVALID_ARG;
-        if (a.dump ? (!a.dbg_qc || !a.dbg_qs || !a.dbg_scores) : (!a.out || !a.lse)) return KVQ_ERR_INVALID_ARG;
-        if (!a.dump && (!aligned16(a.out) || (reinterpret_cast<uintptr_t>(a.lse) & 3u))) return KVQ_ERR_INVALID_ARG;
-    }
-
-    DeviceInfo *dev = nullptr;
-    st = device_setup(&dev);
-    if (st != KVQ_OK) return st;
-    const int nt = tiles8_for(max_rows);
-    const int slots = std::max(1, dev->n_sms * std::max(1, dev->ctas[c->v_type][nt]));
-
-    std::vector<Group> gs;
-    make_groups(c, gs);
-    size_t ws = 0;
-    const size_t rows_per_seq = (size_t)a.t_q * a.n_q_heads;
-    for (Group &g : gs) {
-        choose_split(c, g, a.max_len, slots, split_warps(nt) * kWTile, g.n_split, g.chunk);
-        if (g.n_split > 1 && !a.dump) {
-            g.ws_off = ws;
-            const size_t bytes = (size_t)g.nb * rows_per_seq * g.n_split * (kD + 1) * sizeof(float);
-            ws += (bytes + 255) / 256 * 256;
-        }
-    }
-    if (a.size_out) {
-        *a.size_out = ws;
-        return KVQ_OK;
-    }
-    if (!a.dump && ws) {
-        if (!a.workspace || a.workspace_bytes < ws || (reinterpret_cast<uintptr_t>(a.workspace) & 255u))
-            return KVQ_ERR_WORKSPACE;
-    }
-
-    const bool pdl = pdl_enabled();
-    const uint16_t *q = static_cast<const uint16_t *>(a.q16);
-    for (const Group &g : gs) {
-        fill_segments(c, g, p);
-        const size_t r0 = (size_t)g.b0 * rows_per_seq;
-        p.q = q + r0 * kD;
-        p.seq_lens = a.seq_lens + g.b0;
-        p.n_seqs = g.nb;
-        p.n_kv_heads = c->n_kv_heads;
-        p.n_q_heads = a.n_q_heads;
-        p.t_q = a.t_q;
-        p.causal = a.causal ? 1 : 0;
-        p.max_len = a.max_len;
-        p.n_split = g.n_split;
-        p.chunk = g.chunk;
-        p.qk_scale_log2 = a.sm_scale * 1.4426950408889634f;
-        p.timeouts = dev->timeouts;
-        if (a.dump) {
-            p.dbg_qc = a.dbg_qc + r0 * kD;
-            p.dbg_qs = a.dbg_qs + r0 * kNB;
-            p.dbg_scores = a.dbg_scores + r0 * (size_t)a.max_len * kNB;
-            p.out = nullptr;
-            p.lse = nullptr;
-            p.ws_o = p.ws_lse = nullptr;
-        } else {
-            p.dbg_qc = nullptr;
-            p.dbg_qs = nullptr;
-            p.dbg_scores = nullptr;
-            p.out = a.out + r0 * kD;
-            p.lse = a.lse + r0;
-            if (g.n_split > 1) {
-                char *w = static_cast<char *>(a.workspace) + g.ws_off;
-                p.ws_o = reinterpret_cast<float *>(w);
-                p.ws_lse = p.ws_o + (size_t)g.nb * rows_per_seq * g.n_split * kD;
-            } else {
-                p.ws_o = p.ws_lse = nullptr;
+        std::vector<std::pair<int, int>> seqs;   // (kv heads, reach)
+        long long W = 0;
+        for (const Unit &u : ln.units) {
+            const kvq_cache *c = ds[u.d].c;
+            for (int b = u.b0; b < u.b0 + u.nb; ++b) {
+                const int r = seq_reach(c, b, ds[u.d].max_len);
+                seqs.push_back({c->n_kv_heads, r});
+                W += (long long)r * c->n_kv_heads;
             }
         }
-        cudaError_t e = (c->v_type == KVQ_V_Q4_0) ? launch_split_q4(p, nt, a.dump, a.stream, pdl)
-                                                  : launch_split_q8(p, nt, a.dump, a.stream, pdl);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            return KVQ_ERR_CUDA;
+        const int max_n = std::max(1, std::min(1024, (lmax + 255) / 256));
+        double best = 1e300;
+        chunk = round_up(lmax, gran);
+        int prev = -1;
+        for (int n = 1; n <= max_n; n = (n < 128) ? n + 1 : n + n / 16) {
+            const int cand = std::max(round_up(256, gran), round_up((lmax + n - 1) / n, gran));
+            if (cand == prev) continue;
+            prev = cand;
+            long long ctas = 0;
+            for (const auto &q : seqs) ctas += (long long)q.first * std::max(1, (q.second + cand - 1) / cand);
+            const double cmax = std::min(cand, lmax) + kOverhead;
+            const double est = ctas <= slots ? cmax : (double)(W + ctas * kOverhead) / slots + cmax;
+            if (est < best - 1e-9) {
+                best = est;
+                chunk = cand;
+            }
         }
-        if (!a.dump && g.n_split > 1) {
-            CombineParams cp;
-            cp.ws_o = p.ws_o;
-            cp.ws_lse = p.ws_lse;
-            cp.out = p.out;
-            cp.lse = p.lse;
-            cp.n_rows = (int)(g.nb * rows_per_seq);
-            cp.n_split = g.n_split;
-            e = launch_combine(cp, a.stream, pdl);
-            if (e != cudaSuccess) {
-                cudaGetLastError();
-                return KVQ_ERR_CUDA;
+    }
+    if ((lmax + chunk - 1) / chunk > 1024) chunk = round_up((lmax + 1023) / 1024, gran);
+    return chunk;
+}
+
+// Pack the calls' sequences into launches (tables of AttnParams bound the
+// segments, sequences, groups and head-table entries of one launch).
+kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<Launch> &out, size_t &ws)
+{
+    out.clear();
+    ws = 0;
+    Launch cur;
+    int segs = 0, seqs = 0, heads = 0, kvs = 0, last_d = -1;
+    auto flush = [&]() {
+        if (!cur.units.empty()) out.push_back(cur);
+        cur = Launch();
+        segs = seqs = heads = kvs = 0;
+        last_d = -1;
+    };
+    for (int di = 0; di < (int)ds.size(); ++di) {
+        const kvq_cache *c = ds[di].c;
+        if (c->n_seqs == 0) continue;
+        if (!cur.units.empty() && cur.v_type != c->v_type) flush();
+        int b = 0;
+        while (b < c->n_seqs) {
+            const bool new_desc = last_d != di;
+            const int need_heads = new_desc ? ds[di].n_q_heads : 0, need_kv = new_desc ? c->n_kv_heads + 1 : 0;
+            if (cur.units.size() == (size_t)kMaxGroups || seqs == kMaxSeqsLaunch ||
+                segs + c->n_segs[b] > kMaxSegsLaunch || heads + need_heads > kMaxHeadTab ||
+                kvs + need_kv > kMaxHeadTab + kMaxGroups) {
+                flush();
+                continue;
+            }
+            if (cur.units.empty()) cur.v_type = c->v_type;
+            heads += need_heads;
+            kvs += need_kv;
+            last_d = di;
+            Unit u{di, b, 0, 0, 1, 0, 0, 0};
+            while (b < c->n_seqs && seqs < kMaxSeqsLaunch && segs + c->n_segs[b] <= kMaxSegsLaunch) {
+                segs += c->n_segs[b];
+                u.reach = std::max(u.reach, seq_reach(c, b, ds[di].max_len));
+                ++seqs;
+                ++u.nb;
+                ++b;
+            }
+            cur.nt = std::max(cur.nt, tiles8_for(ds[di].max_rows));
+            cur.units.push_back(u);
+        }
+    }
+    flush();
+    for (Launch &ln : out) {
+        const int slots = std::max(1, dev->n_sms * std::max(1, dev->ctas[ln.v_type][ln.nt]));
+        ln.chunk = choose_chunk(ds, ln, slots, split_warps(ln.nt) * kWTile);
+        for (Unit &u : ln.units) {
+            const Desc &d = ds[u.d];
+            u.n_split = std::max(1, (u.reach + ln.chunk - 1) / ln.chunk);
+            u.cta0 = ln.n_ctas;
+            ln.n_ctas += u.n_split * d.c->n_kv_heads * u.nb;
+            if (u.n_split > 1 && !dump) {
+                const size_t rows = (size_t)u.nb * d.t_q * d.n_q_heads;
+                u.row0 = ln.n_rows;
+                ln.n_rows += (int)rows;
+                u.ws_off = ws;
+                ws += (rows * u.n_split * (kD + 1) * sizeof(float) + 255) / 256 * 256;
             }
         }
     }
     return KVQ_OK;
+}
+
+void fill_launch(const std::vector<Desc> &ds, const Launch &ln, bool dump, void *workspace, unsigned int *timeouts,
+                 AttnParams &p, CombineParams &cp)
+{
+    std::memset(&p, 0, sizeof(p));
+    std::memset(&cp, 0, sizeof(cp));
+    int nseg = 0, nseq = 0, nhead = 0, nkv = 0, last_d = -1, head0 = 0;
+    for (const Unit &u : ln.units) {
+        const Desc &d = ds[u.d];
+        const kvq_cache *c = d.c;
+        if (u.d != last_d) {   // this call's head table
+            head0 = nkv;
+            for (int k = 0; k < c->n_kv_heads; ++k) {
+                p.grp_begin[nkv++] = (uint16_t)nhead;
+                for (int h = 0; h < d.n_q_heads; ++h)
+                    if (d.kv[h] == k) p.grp_q[nhead++] = (uint16_t)h;
+            }
+            p.grp_begin[nkv++] = (uint16_t)nhead;
+            last_d = u.d;
+        }
+        GroupDesc &G = p.grp[p.n_groups];
+        const size_t rows_per_seq = (size_t)d.t_q * d.n_q_heads;
+        const size_t r0 = (size_t)u.b0 * rows_per_seq;
+        G.q = d.q ? d.q + r0 * kD : nullptr;
+        G.seq_lens = d.seq_lens ? d.seq_lens + u.b0 : nullptr;
+        G.cta0 = u.cta0;
+        G.seq0 = nseq;
+        G.head0 = head0;
+        G.n_seqs = u.nb;
+        G.n_kv_heads = c->n_kv_heads;
+        G.n_q_heads = d.n_q_heads;
+        G.t_q = d.t_q;
+        G.causal = d.causal ? 1 : 0;
+        G.max_len = d.max_len;
+        G.n_split = u.n_split;
+        G.chunk = ln.chunk;
+        G.qk_scale_log2 = d.sm_scale * 1.4426950408889634f;
+        if (dump) {
+            G.dbg_qc = d.dbg_qc + r0 * kD;
+            G.dbg_qs = d.dbg_qs + r0 * kNB;
+            G.dbg_scores = d.dbg_scores + r0 * (size_t)d.max_len * kNB;
+        } else {
+            G.out = d.out + r0 * kD;
+            G.lse = d.lse + r0;
+            if (u.n_split > 1) {
+                char *w = static_cast<char *>(workspace) + u.ws_off;
+                G.ws_o = reinterpret_cast<float *>(w);
+                G.ws_lse = G.ws_o + (size_t)u.nb * rows_per_seq * u.n_split * kD;
+                CombineGroup &cg = cp.grp[cp.n_groups++];
+                cg.ws_o = G.ws_o;
+                cg.ws_lse = G.ws_lse;
+                cg.out = G.out;
+                cg.lse = G.lse;
+                cg.row0 = u.row0;
+                cg.n_split = u.n_split;
+            }
+        }
+        ++p.n_groups;
+        for (int i = 0; i < u.nb; ++i) {
+            const int b = u.b0 + i;
+            p.seq_seg0[nseq] = (uint8_t)nseg;
+            p.seq_nseg[nseq] = (uint8_t)c->n_segs[b];
+            ++nseq;
+            for (int k = 0; k < c->n_segs[b]; ++k, ++nseg) {
+                const kvq_segment &s = seg_of(c, b, k);
+                p.seg[nseg].kq = static_cast<const uint8_t *>(s.k_q);
+                p.seg[nseg].ks = static_cast<const uint16_t *>(s.k_s);
+                p.seg[nseg].vq = static_cast<const uint8_t *>(s.v_q);
+                p.seg[nseg].vs = static_cast<const uint16_t *>(s.v_s);
+                p.seg[nseg].pos0 = s.pos0;
+                p.seg[nseg].cap = s.cap;
+            }
+        }
+    }
+    p.timeouts = timeouts;
+}
+
+// Plan, check the workspace and launch (or, with size_out, only report the
+// workspace the calls need).
+kvq_status run(std::vector<Desc> &ds, bool dump, void *workspace, size_t workspace_bytes, size_t *size_out,
+               cudaStream_t stream)
+{
+    DeviceInfo *dev = nullptr;
+    bool any = false;
+    for (const Desc &d : ds) any = any || d.c->n_seqs > 0;
+    if (!any) {
+        if (size_out) *size_out = 0;
+        return KVQ_OK;
+    }
+    kvq_status st = device_setup(&dev);
+    if (st != KVQ_OK) return st;
+    std::vector<Launch> lns;
+    size_t ws = 0;
+    st = plan(ds, dev, dump, lns, ws);
+    if (st != KVQ_OK) return st;
+    if (size_out) {
+        *size_out = ws;
+        return KVQ_OK;
+    }
+    if (!dump && ws) {
+        if (!workspace || workspace_bytes < ws || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+            return KVQ_ERR_WORKSPACE;
+    }
+    static thread_local AttnParams p;        // ~6 KB; kept off the stack
+    static thread_local CombineParams cp;
+    const bool pdl = pdl_enabled();
+    for (const Launch &ln : lns) {
+        fill_launch(ds, ln, dump, workspace, dev->timeouts, p, cp);
+        cudaError_t e = (ln.v_type == KVQ_V_Q4_0) ? launch_split_q4(p, ln.nt, ln.n_ctas, dump, stream, pdl)
+                                                  : launch_split_q8(p, ln.nt, ln.n_ctas, dump, stream, pdl);
+        if (e == cudaSuccess && ln.n_rows > 0) e = launch_combine(cp, ln.n_rows, stream, pdl);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return KVQ_ERR_CUDA;
+        }
+    }
+    return KVQ_OK;
+}
+
+// kvq_decode_desc (public) -> Desc, validated.
+kvq_status to_desc(const kvq_decode_desc &x, bool need_ptrs, Desc &d)
+{
+    d = Desc();
+    d.c = x.cache;
+    d.q = static_cast<const uint16_t *>(x.q16);
+    d.n_q_heads = x.n_q_heads;
+    d.t_q = x.t_q;
+    d.causal = x.causal_tail;
+    d.seq_lens = x.seq_lens;
+    d.max_len = x.max_len;
+    d.sm_scale = x.sm_scale;
+    d.out = x.out;
+    d.lse = x.lse;
+    return prepare_desc(d, x.head_map, need_ptrs, false);
 }
 
 }  // namespace
@@ -467,60 +532,60 @@ kvq_status kvq_decode_attn(const kvq_cache *c, const void *q16, int32_t n_q_head
                            const int32_t *head_map, float sm_scale, float *out, float *lse, void *workspace,
                            size_t workspace_bytes, void *stream)
 {
-    DecodeArgs a{};
-    a.c = c;
-    a.q16 = q16;
-    a.n_q_heads = n_q_heads;
-    a.t_q = t_q;
-    a.causal = causal_tail;
-    a.seq_lens = seq_lens;
-    a.max_len = max_len;
-    a.head_map = head_map;
-    a.sm_scale = sm_scale;
-    a.out = out;
-    a.lse = lse;
-    a.workspace = workspace;
-    a.workspace_bytes = workspace_bytes;
-    a.dump = false;
-    a.stream = static_cast<cudaStream_t>(stream);
-    return run_decode(a);
+    const kvq_decode_desc x{c, q16, n_q_heads, t_q, causal_tail, seq_lens, max_len, head_map, sm_scale, out, lse};
+    return kvq_decode_attn_multi(1, &x, workspace, workspace_bytes, stream);
 }
 
 kvq_status kvq_decode_workspace_size(const kvq_cache *c, int32_t n_q_heads, int32_t t_q, int32_t max_len,
                                      const int32_t *head_map, size_t *bytes)
 {
-    if (!bytes) return KVQ_ERR_INVALID_ARG;
-    DecodeArgs a{};
-    a.c = c;
-    a.n_q_heads = n_q_heads;
-    a.t_q = t_q;
-    a.max_len = max_len;
-    a.head_map = head_map;
-    a.sm_scale = 1.0f;
-    a.size_out = bytes;
-    return run_decode(a);
+    const kvq_decode_desc x{c, nullptr, n_q_heads, t_q, 0, nullptr, max_len, head_map, 1.0f, nullptr, nullptr};
+    return kvq_decode_multi_workspace_size(1, &x, bytes);
+}
+
+kvq_status kvq_decode_attn_multi(int32_t n, const kvq_decode_desc *calls, void *workspace, size_t workspace_bytes,
+                                 void *stream)
+{
+    if (n < 0 || n > KVQ_MAX_CALLS || (n > 0 && !calls)) return KVQ_ERR_INVALID_ARG;
+    std::vector<Desc> ds(n);
+    for (int i = 0; i < n; ++i) {
+        kvq_status st = to_desc(calls[i], true, ds[i]);
+        if (st != KVQ_OK) return st;
+    }
+    return run(ds, false, workspace, workspace_bytes, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+kvq_status kvq_decode_multi_workspace_size(int32_t n, const kvq_decode_desc *calls, size_t *bytes)
+{
+    if (!bytes || n < 0 || n > KVQ_MAX_CALLS || (n > 0 && !calls)) return KVQ_ERR_INVALID_ARG;
+    std::vector<Desc> ds(n);
+    for (int i = 0; i < n; ++i) {
+        kvq_status st = to_desc(calls[i], false, ds[i]);
+        if (st != KVQ_OK) return st;
+    }
+    return run(ds, false, nullptr, 0, bytes, nullptr);
 }
 
 kvq_status kvq_debug_qk(const kvq_cache *c, const void *q16, int32_t n_q_heads, int32_t t_q,
                         const int32_t *seq_lens, int32_t max_len, const int32_t *head_map, int8_t *q_codes,
                         uint16_t *q_scales, int32_t *scores, void *stream)
 {
-    DecodeArgs a{};
-    a.c = c;
-    a.q16 = q16;
-    a.n_q_heads = n_q_heads;
-    a.t_q = t_q;
-    a.causal = 0;
-    a.seq_lens = seq_lens;
-    a.max_len = max_len;
-    a.head_map = head_map;
-    a.sm_scale = 1.0f;
-    a.dbg_qc = q_codes;
-    a.dbg_qs = q_scales;
-    a.dbg_scores = scores;
-    a.dump = true;
-    a.stream = static_cast<cudaStream_t>(stream);
-    return run_decode(a);
+    std::vector<Desc> ds(1);
+    Desc &d = ds[0];
+    d.c = c;
+    d.q = static_cast<const uint16_t *>(q16);
+    d.n_q_heads = n_q_heads;
+    d.t_q = t_q;
+    d.causal = 0;
+    d.seq_lens = seq_lens;
+    d.max_len = max_len;
+    d.sm_scale = 1.0f;
+    d.dbg_qc = q_codes;
+    d.dbg_qs = q_scales;
+    d.dbg_scores = scores;
+    kvq_status st = prepare_desc(d, head_map, true, true);
+    if (st != KVQ_OK) return st;
+    return run(ds, true, nullptr, 0, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -240,33 +240,29 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
     constexpr float kBias = 1152.0f;                 // K codes enter the MMA as 1152 + code
     extern __shared__ __align__(128) uint8_t smem[];
 
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // ---- the group, sequence, kv head and split of this CTA ----
+    int gi = 0;
+#pragma unroll 1
+    for (int k = 1; k < p.n_groups; ++k)
+        if ((int)blockIdx.x >= p.grp[k].cta0) gi = k;
+    const GroupDesc &G = p.grp[gi];
+    const int lb = (int)blockIdx.x - G.cta0;
+    const int split = lb % G.n_split, h = (lb / G.n_split) % G.n_kv_heads, b = lb / G.n_split / G.n_kv_heads;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
-    const int gb = p.grp_begin[h], gsz = p.grp_begin[h + 1] - gb;
-    const int R = gsz * p.t_q;
-    const int seg0 = p.seq_seg0[b], nseg = p.seq_nseg[b];
-    const int lcap = nseg ? min(p.max_len, p.seg[seg0 + nseg - 1].pos0 + p.seg[seg0 + nseg - 1].cap) : 0;
+    const int gb = p.grp_begin[G.head0 + h], gsz = p.grp_begin[G.head0 + h + 1] - gb;
+    const int R = gsz * G.t_q;
+    const int seg0 = p.seq_seg0[G.seq0 + b], nseg = p.seq_nseg[G.seq0 + b];
+    const int lcap = nseg ? min(G.max_len, p.seg[seg0 + nseg - 1].pos0 + p.seg[seg0 + nseg - 1].cap) : 0;
+    // The split's positions as far as the segment table knows them: the
+    // sequence length, read below, can only cut them shorter.  Copies of the
+    // range go out before that read returns; positions at or past the length
+    // are masked like any other invisible position.
+    const int r0 = split * G.chunk, r1c = min(lcap, r0 + G.chunk);
 
     // Nothing above reads memory written by an earlier kernel.
     pdl_wait();
     pdl_trigger();
-
-    const int L = max(0, min(p.seq_lens[b], lcap));
-    const int r0 = split * p.chunk, r1 = min(L, r0 + p.chunk);
-
-    if (r0 >= r1) {                                  // no position in this split
-        if (!DUMP && tid < R) {
-            const int i = tid / gsz, hq = p.grp_q[gb + tid % gsz];
-            const size_t row = ((size_t)b * p.t_q + i) * p.n_q_heads + hq;
-            if (p.n_split == 1) {
-                p.lse[row] = -INFINITY;
-                for (int d = 0; d < kD; ++d) p.out[row * kD + d] = 0.f;
-            } else {
-                p.ws_lse[row * p.n_split + split] = -INFINITY;
-            }
-        }
-        return;
-    }
+    const int len_b = G.seq_lens[b];
 
     // ---- the query rows' loads go out first: they are tiny, and issued after the
     // K/V prefetch below they would queue behind it ----
@@ -276,14 +272,14 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
     for (int k = 0; k < QPW; ++k) {
         const int r = warp + kWarps * k;
         qraw[k] = make_uint2(0u, 0u);
-        if (r < R) {
+        if (r < R && r0 < r1c) {
             const int i = r / gsz, hq = p.grp_q[gb + r % gsz];
-            qraw[k] = *reinterpret_cast<const uint2 *>(p.q + (((size_t)b * p.t_q + i) * p.n_q_heads + hq) * kD + lane * 4);
+            qraw[k] = *reinterpret_cast<const uint2 *>(G.q + (((size_t)b * G.t_q + i) * G.n_q_heads + hq) * kD + lane * 4);
         }
     }
     // ---- this warp's sub-range and its first copies (before the query prologue) ----
-    const int span = (r1 - r0 + kWarps * kWTile - 1) / (kWarps * kWTile) * kWTile;
-    const int w0 = min(r1, r0 + warp * span), w1 = min(r1, w0 + span);
+    const int span = (r1c - r0 + kWarps * kWTile - 1) / (kWarps * kWTile) * kWTile;
+    const int w0 = min(r1c, r0 + warp * span), w1 = min(r1c, w0 + span);
     int n_tiles = 0;
     if (w0 < w1)
         for (int k = 0; k < nseg; ++k) {
@@ -320,6 +316,23 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
     for (int st = 0; st < S - 1; ++st)
         if (st < n_tiles) issue(st);
 
+    const int L = max(0, min(len_b, lcap));
+    const int r1 = min(L, r0 + G.chunk);
+    if (r0 >= r1) {                                  // no position in this split
+        for (int j = 0; j < issued; ++j) mbar_wait(bar_s + (j % S) * 8, (j / S) & 1);
+        if (!DUMP && tid < R) {
+            const int i = tid / gsz, hq = p.grp_q[gb + tid % gsz];
+            const size_t row = ((size_t)b * G.t_q + i) * G.n_q_heads + hq;
+            if (G.n_split == 1) {
+                G.lse[row] = -INFINITY;
+                for (int d = 0; d < kD; ++d) G.out[row * kD + d] = 0.f;
+            } else {
+                G.ws_lse[row * G.n_split + split] = -INFINITY;
+            }
+        }
+        return;
+    }
+
     // ---- quantize the query rows of this kv head (int8 rule, fp16 scale) ----
     uint32_t *qw = reinterpret_cast<uint32_t *>(smem + C::Q_OFF);
     float *qs = reinterpret_cast<float *>(smem + C::QS_OFF);
@@ -332,7 +345,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
         int sum = 0;
         if (r < R) {
             const int i = r / gsz, hq = p.grp_q[gb + r % gsz];
-            const size_t qrow = ((size_t)b * p.t_q + i) * p.n_q_heads + hq;
+            const size_t qrow = ((size_t)b * G.t_q + i) * G.n_q_heads + hq;
             float x[4];
             unpack4h(qraw[k], x);
             float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
@@ -348,8 +361,8 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
                 sum += code;
             }
             if (DUMP && split == 0) {
-                reinterpret_cast<uint32_t *>(p.dbg_qc)[qrow * (kD / 4) + lane] = word;
-                if ((lane & 7) == 0) p.dbg_qs[qrow * kNB + (lane >> 3)] = __half_as_ushort(sh);
+                reinterpret_cast<uint32_t *>(G.dbg_qc)[qrow * (kD / 4) + lane] = word;
+                if ((lane & 7) == 0) G.dbg_qs[qrow * kNB + (lane >> 3)] = __half_as_ushort(sh);
             }
         }
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
@@ -357,7 +370,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
         sum += __shfl_xor_sync(0xffffffffu, sum, 4);
         qw[r * (kD / 4) + lane] = word;
         if ((lane & 7) == 0) {
-            qs[r * kNB + (lane >> 3)] = s * p.qk_scale_log2;
+            qs[r * kNB + (lane >> 3)] = s * G.qk_scale_log2;
             qsum[r * kNB + (lane >> 3)] = sum;
         }
     }
@@ -417,11 +430,11 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int row = 8 * nt + g;
-        lim[nt] = (row < R) ? (p.causal ? L - p.t_q + row / gsz : L - 1) : -1;
+        lim[nt] = (row < R) ? (G.causal ? L - G.t_q + row / gsz : L - 1) : -1;
         m[nt] = -INFINITY;
         l[nt] = 0.f;
     }
-    const int lim_min = p.causal ? L - p.t_q : L - 1;   // smallest limit over live rows
+    const int lim_min = G.causal ? L - G.t_q : L - 1;   // smallest limit over live rows
     float acc[8][NT][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
@@ -549,11 +562,11 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
                             if (row < R && tok >= la && tok < le && pos < L) {
                                 const int mq = nt >> 1, idx = 2 * (nt & 1) + e;
                                 const int i = row / gsz, hq = p.grp_q[gb + row % gsz];
-                                const size_t o = ((((size_t)b * p.t_q + i) * p.n_q_heads + hq) * p.max_len + pos) * kNB;
+                                const size_t o = ((((size_t)b * G.t_q + i) * G.n_q_heads + hq) * G.max_len + pos) * kNB;
                                 int4 v;
                                 v.x = (int)sc[mq][0][idx]; v.y = (int)sc[mq][1][idx];
                                 v.z = (int)sc[mq][2][idx]; v.w = (int)sc[mq][3][idx];
-                                *reinterpret_cast<int4 *>(p.dbg_scores + o) = v;
+                                *reinterpret_cast<int4 *>(G.dbg_scores + o) = v;
                             }
                         }
                 }
@@ -609,8 +622,8 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
             for (int sub = 0; sub < 2; ++sub) {
                 const int ut = 8 * sub + 2 * c;
                 vsr[sub] = *reinterpret_cast<const uint4 *>(st + C::VS_OFF + ut * kNB * 2);
-                okv[sub][0] = FULL || (tb + ut >= la && tb + ut < le);
-                okv[sub][1] = FULL || (tb + ut + 1 >= la && tb + ut + 1 < le);
+                okv[sub][0] = FULL || (tb + ut >= la && tb + ut < le && pos_base + ut < L);
+                okv[sub][1] = FULL || (tb + ut + 1 >= la && tb + ut + 1 < le && pos_base + ut + 1 < L);
 #pragma unroll
                 for (int hb = 0; hb < NVL; ++hb)
                     vv[sub][hb] = *reinterpret_cast<const uint4 *>(st + C::V_OFF + (NVL * sub + hb) * 512 + lane * 16);
@@ -754,7 +767,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
                 if (mw != -INFINITY) Lsum += sm_l[w * 8 * NT + row] * fast_exp2(mw - M);
             }
             const int i = row / gsz, hq = p.grp_q[gb + row % gsz];
-            const size_t orow = ((size_t)b * p.t_q + i) * p.n_q_heads + hq;
+            const size_t orow = ((size_t)b * G.t_q + i) * G.n_q_heads + hq;
             const bool any = Lsum > 0.f;
             float inv, lg;
             asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(Lsum));
@@ -762,22 +775,22 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
             float o = any ? sm_o[row * kD + d] * inv : 0.f;
             float ls = any ? (M + lg) * 0.69314718055994531f : -INFINITY;
             if (poisoned) o = ls = __int_as_float(0x7fc00000);   // NaN: the CTA lost a stage
-            if (p.n_split == 1) {
-                p.out[orow * kD + d] = o;
-                if (d == 0) p.lse[orow] = ls;
+            if (G.n_split == 1) {
+                G.out[orow * kD + d] = o;
+                if (d == 0) G.lse[orow] = ls;
             } else {
-                p.ws_o[(orow * p.n_split + split) * kD + d] = o;
-                if (d == 0) p.ws_lse[orow * p.n_split + split] = ls;
+                G.ws_o[(orow * G.n_split + split) * kD + d] = o;
+                if (d == 0) G.ws_lse[orow * G.n_split + split] = ls;
             }
         }
     }
 }
 
 template <int NT, int VT>
-cudaError_t launch_split_t(const AttnParams &p, bool dump, cudaStream_t s, bool pdl)
+cudaError_t launch_split_t(const AttnParams &p, int n_ctas, bool dump, cudaStream_t s, bool pdl)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.n_split, p.n_kv_heads, p.n_seqs);
+    cfg.gridDim = dim3(n_ctas);
     cfg.blockDim = dim3(SplitCfg<NT, VT>::THREADS);
     cfg.dynamicSmemBytes = SplitCfg<NT, VT>::SMEM;
     cfg.stream = s;
@@ -803,12 +816,12 @@ cudaError_t prepare_split_t(bool dump, int *ctas_per_sm)
 }
 
 #define KVQ_DEFINE_SPLIT_ENTRY(SUFFIX, VT)                                                   \
-    cudaError_t launch_split_##SUFFIX(const AttnParams &p, int nt, bool dump, cudaStream_t s, bool pdl) \
+    cudaError_t launch_split_##SUFFIX(const AttnParams &p, int nt, int n_ctas, bool dump, cudaStream_t s, bool pdl) \
     {                                                                                        \
         switch (nt) {                                                                        \
-        case 1: return launch_split_t<1, VT>(p, dump, s, pdl);                               \
-        case 2: return launch_split_t<2, VT>(p, dump, s, pdl);                               \
-        case 4: return launch_split_t<4, VT>(p, dump, s, pdl);                               \
+        case 1: return launch_split_t<1, VT>(p, n_ctas, dump, s, pdl);                       \
+        case 2: return launch_split_t<2, VT>(p, n_ctas, dump, s, pdl);                       \
+        case 4: return launch_split_t<4, VT>(p, n_ctas, dump, s, pdl);                       \
         default: return cudaErrorInvalidValue;                                               \
         }                                                                                    \
     }                                                                                        \

@@ -72,12 +72,11 @@ struct SegDesc {
     int cap;              // tokens, multiple of KVQ_SEG_ALIGN
 };
 
-struct AttnParams {
-    SegDesc seg[kMaxSegsLaunch];
-    uint8_t seq_seg0[kMaxSeqsLaunch];      // first table entry of each sequence
-    uint8_t seq_nseg[kMaxSeqsLaunch];
-    uint8_t grp_q[KVQ_MAX_HEADS];          // query heads listed kv head by kv head
-    uint16_t grp_begin[KVQ_MAX_HEADS + 1]; // kv head h owns grp_q[grp_begin[h] .. grp_begin[h+1])
+// One work group of a split launch: sequences [b0, b0 + n_seqs) of one cache
+// of one decode call.  A launch runs up to kMaxGroups groups (of one or more
+// caches) in a single 1-D grid; CTA cta0 + (b * n_kv_heads + h) * n_split + s
+// of the group attends split s of kv head h of its sequence b.
+struct GroupDesc {
     const uint16_t *q;                     // [n_seqs][t_q][Hq][kD] fp16 bits
     const int *seq_lens;                   // [n_seqs]
     float *out;                            // [n_seqs][t_q][Hq][kD]       (n_split == 1)
@@ -87,20 +86,43 @@ struct AttnParams {
     int8_t *dbg_qc;                        // test hook outputs (DUMP kernels only)
     uint16_t *dbg_qs;
     int32_t *dbg_scores;
+    int cta0;                              // first CTA of the group
+    int seq0;                              // first entry of seq_seg0 / seq_nseg
+    int head0;                             // first entry of grp_begin (this cache's kv heads)
     int n_seqs, n_kv_heads, n_q_heads, t_q, causal;
     int max_len;                           // positions >= max_len are ignored
     int n_split, chunk;                    // split s covers [s*chunk, (s+1)*chunk)
     float qk_scale_log2;                   // sm_scale * log2(e)
+};
+
+constexpr int kMaxGroups = 8;              // work groups per launch
+constexpr int kMaxHeadTab = 512;           // query-head list entries per launch
+
+struct AttnParams {
+    SegDesc seg[kMaxSegsLaunch];
+    uint8_t seq_seg0[kMaxSeqsLaunch];      // first table entry of each sequence
+    uint8_t seq_nseg[kMaxSeqsLaunch];
+    uint16_t grp_q[kMaxHeadTab];           // query heads listed kv head by kv head
+    uint16_t grp_begin[kMaxHeadTab + kMaxGroups];   // kv head h of group g owns
+                                           // grp_q[grp_begin[head0 + h] .. grp_begin[head0 + h + 1])
+    GroupDesc grp[kMaxGroups];
+    int n_groups;
     unsigned int *timeouts;                // bumped when a copy wait gives up (never in a correct run)
 };
 
-struct CombineParams {
+// Split combine of one group: rows [row0, row0 + n_rows) of the launch.
+struct CombineGroup {
     const float *ws_o;
     const float *ws_lse;
     float *out;
     float *lse;
-    int n_rows;                            // n_seqs * t_q * Hq
+    int row0;                              // first CTA (row) of the group
     int n_split;
+};
+
+struct CombineParams {
+    CombineGroup grp[kMaxGroups];
+    int n_groups;
 };
 
 struct AppendEntry {
@@ -126,9 +148,9 @@ struct AppendParams {
 // Implemented in kvq_small.cu / kvq_attn_q4.cu / kvq_attn_q8.cu.
 // n_tiles8 = query rows per kv head rounded up to 1, 2 or 4 tiles of 8.
 cudaError_t launch_append(const AppendParams &p, int v_type, int max_rows, cudaStream_t s, bool pdl);
-cudaError_t launch_combine(const CombineParams &p, cudaStream_t s, bool pdl);
-cudaError_t launch_split_q4(const AttnParams &p, int n_tiles8, bool dump, cudaStream_t s, bool pdl);
-cudaError_t launch_split_q8(const AttnParams &p, int n_tiles8, bool dump, cudaStream_t s, bool pdl);
+cudaError_t launch_combine(const CombineParams &p, int n_rows, cudaStream_t s, bool pdl);
+cudaError_t launch_split_q4(const AttnParams &p, int n_tiles8, int n_ctas, bool dump, cudaStream_t s, bool pdl);
+cudaError_t launch_split_q8(const AttnParams &p, int n_tiles8, int n_ctas, bool dump, cudaStream_t s, bool pdl);
 cudaError_t prepare_split_q4(int n_tiles8, bool dump, int *ctas_per_sm);
 cudaError_t prepare_split_q8(int n_tiles8, bool dump, int *ctas_per_sm);
 

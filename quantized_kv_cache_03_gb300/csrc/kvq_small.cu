@@ -110,93 +110,90 @@ cudaError_t launch_append(const AppendParams &p, int v_type, int max_rows, cudaS
 
 // ---------------------------------------------------------------------------
 // Split combine: per query row, M = max_s lse_s, w_s = exp(lse_s - M),
-// out = sum_s w_s o_s / sum_s w_s, lse = M + log(sum_s w_s).  One CTA per row;
-// 8 warps take every 8th split and each lane four head dims (float4), with four
-// partials in flight per warp, then the warps' sums are added in a fixed
-// order.  Splits with lse = -inf (no visible position) weigh 0 and their o is
-// never read.
+// out = sum_s w_s o_s / sum_s w_s, lse = M + log(sum_s w_s).  One CTA per row
+// (rows of every group of the launch in one grid).  Warp w takes splits
+// w, w + 8, ... four at a time, loading their lse and o (each lane four head
+// dims, float4) in one round trip, and keeps a running (max, weight sum,
+// weighted o) with rescaling; warp 0 then merges the eight warp states in a
+// fixed order.  Splits with lse = -inf (no visible position) weigh 0 and their
+// o is never used.
 // ---------------------------------------------------------------------------
-constexpr int kMaxSplit = 1024;
 constexpr int kCombineWarps = 8;
 
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __grid_constant__ CombineParams p)
 {
-    __shared__ float w_s[kMaxSplit];
-    __shared__ float red[kCombineWarps];
+    __shared__ float sm_m[kCombineWarps], sm_w[kCombineWarps];
     __shared__ float4 part[kCombineWarps][32];
+    int gi = 0;
+#pragma unroll 1
+    for (int k = 1; k < p.n_groups; ++k)
+        if ((int)blockIdx.x >= p.grp[k].row0) gi = k;
+    const CombineGroup &G = p.grp[gi];
+    const int row = (int)blockIdx.x - G.row0, warp = threadIdx.x >> 5, lane = threadIdx.x & 31, n = G.n_split;
     pdl_wait();
     pdl_trigger();
-    const int row = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, n = p.n_split;
-    const float *ls = p.ws_lse + (size_t)row * n;
-    float M = -INFINITY;
-    for (int s = tid; s < n; s += kCombineWarps * 32) {
-        const float v = ls[s];
-        w_s[s] = v;
-        M = fmaxf(M, v);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if (lane == 0) red[warp] = M;
-    __syncthreads();
-    M = red[0];
-#pragma unroll
-    for (int w = 1; w < kCombineWarps; ++w) M = fmaxf(M, red[w]);
-    float W = 0.f;
-    for (int s = tid; s < n; s += kCombineWarps * 32) {
-        const float v = w_s[s];
-        const float wv = (v == -INFINITY) ? 0.f : expf(v - M);
-        w_s[s] = wv;
-        W += wv;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
-    __syncthreads();   // all reads of red[] above are done; w_s complete
-    if (lane == 0) red[warp] = W;
-    __syncthreads();
-    W = 0.f;
-#pragma unroll
-    for (int w = 0; w < kCombineWarps; ++w) W += red[w];
-
-    const float4 *o = reinterpret_cast<const float4 *>(p.ws_o + (size_t)row * n * kD) + lane;
+    const float *ls = G.ws_lse + (size_t)row * n;
+    const float4 *o = reinterpret_cast<const float4 *>(G.ws_o + (size_t)row * n * kD) + lane;
+    float m = -INFINITY, W = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = warp; s0 < n; s0 += 4 * kCombineWarps) {
+        float lv[4];
         float4 v[4];
-        float wv[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int s = s0 + k * kCombineWarps;
-            wv[k] = (s < n) ? w_s[s] : 0.f;
-            v[k] = wv[k] != 0.f ? o[(size_t)s * (kD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+            lv[k] = (s < n) ? ls[s] : -INFINITY;
+            v[k] = (s < n) ? o[(size_t)s * (kD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        const float mx = fmaxf(fmaxf(m, fmaxf(lv[0], lv[1])), fmaxf(lv[2], lv[3]));
+        if (mx == -INFINITY) continue;
+        const float a = (m == -INFINITY) ? 0.f : expf(m - mx);
+        W *= a;
+        acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            acc.x = fmaf(wv[k], v[k].x, acc.x);
-            acc.y = fmaf(wv[k], v[k].y, acc.y);
-            acc.z = fmaf(wv[k], v[k].z, acc.z);
-            acc.w = fmaf(wv[k], v[k].w, acc.w);
+            const float w = (lv[k] == -INFINITY) ? 0.f : expf(lv[k] - mx);
+            W += w;
+            if (w != 0.f) {
+                acc.x = fmaf(w, v[k].x, acc.x);
+                acc.y = fmaf(w, v[k].y, acc.y);
+                acc.z = fmaf(w, v[k].z, acc.z);
+                acc.w = fmaf(w, v[k].w, acc.w);
+            }
         }
+        m = mx;
+    }
+    if (lane == 0) {
+        sm_m[warp] = m;
+        sm_w[warp] = W;
     }
     part[warp][lane] = acc;
     __syncthreads();
     if (warp == 0) {
-        float4 t = part[0][lane];
+        float M = -INFINITY;
 #pragma unroll
-        for (int w = 1; w < kCombineWarps; ++w) {
-            t.x += part[w][lane].x; t.y += part[w][lane].y; t.z += part[w][lane].z; t.w += part[w][lane].w;
+        for (int w = 0; w < kCombineWarps; ++w) M = fmaxf(M, sm_m[w]);
+        float Wt = 0.f;
+        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kCombineWarps; ++w) {
+            if (sm_m[w] == -INFINITY) continue;
+            const float f = expf(sm_m[w] - M);
+            Wt = fmaf(sm_w[w], f, Wt);
+            const float4 q = part[w][lane];
+            t.x = fmaf(q.x, f, t.x); t.y = fmaf(q.y, f, t.y); t.z = fmaf(q.z, f, t.z); t.w = fmaf(q.w, f, t.w);
         }
-        const bool any = W > 0.f;
-        const float inv = any ? 1.f / W : 0.f;
-        float4 r = make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
-        reinterpret_cast<float4 *>(p.out + (size_t)row * kD)[lane] = r;
-        if (lane == 0) p.lse[row] = any ? M + logf(W) : -INFINITY;
+        const bool any = Wt > 0.f;
+        const float inv = any ? 1.f / Wt : 0.f;
+        reinterpret_cast<float4 *>(G.out + (size_t)row * kD)[lane] = make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
+        if (lane == 0) G.lse[row] = any ? M + logf(Wt) : -INFINITY;
     }
 }
 
-cudaError_t launch_combine(const CombineParams &p, cudaStream_t s, bool pdl)
+cudaError_t launch_combine(const CombineParams &p, int n_rows, cudaStream_t s, bool pdl)
 {
-    if (p.n_split > kMaxSplit) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.n_rows);
+    cfg.gridDim = dim3(n_rows);
     cfg.blockDim = dim3(kCombineWarps * 32);
     cfg.stream = s;
     cudaLaunchAttribute at[1];

@@ -83,3 +83,20 @@ class DecodeSet:
         up to 64 sequences, and a combine per group when sequences are split."""
         groups = (self.B + 63) // 64
         return 1 + groups * (2 if self.ws_bytes else 1)
+
+
+class StepSet:
+    """Every cache of one workload copy decoded by one kvq_decode_attn_multi
+    call (one split launch and one combine for all of them)."""
+
+    def __init__(self, sets, q16=None):
+        self.sets = list(sets)
+        self.calls = [dict(cache=ds.cache, q16=ds.q16 if q16 is None else q16[i], n_q_heads=ds.Hq, t_q=ds.tq,
+                           causal_tail=ds.spec.causal, seq_lens=ds.lens, max_len=ds.max_len, head_map=None,
+                           sm_scale=SM_SCALE, out=ds.out, lse=ds.lse) for i, ds in enumerate(self.sets)]
+        self.call = kvq.MultiCall(self.calls)
+        n = self.call.workspace_size()
+        self.call.ws = torch.empty(n, dtype=torch.uint8, device=self.sets[0].device) if n else None
+
+    def decode(self, stream=None):
+        self.call(stream)

@@ -29,8 +29,10 @@ HEAD_DIM = 128
 SEG_ALIGN = 64
 QBLOCK = 32
 
-EXPORTED = ("kvq_append", "kvq_decode_attn", "kvq_decode_workspace_size", "kvq_decode_attn_noalloc",
-            "kvq_wait_timeouts", "kvq_status_string", "kvq_debug_qk")
+EXPORTED = ("kvq_append", "kvq_decode_attn", "kvq_decode_workspace_size", "kvq_decode_attn_multi",
+            "kvq_decode_multi_workspace_size", "kvq_decode_attn_noalloc", "kvq_wait_timeouts",
+            "kvq_status_string", "kvq_debug_qk")
+MAX_CALLS = 16
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -43,6 +45,12 @@ class KvqCache(ctypes.Structure):
     _fields_ = [("n_seqs", c_int32), ("n_kv_heads", c_int32), ("head_dim", c_int32),
                 ("v_type", c_int32), ("max_segs", c_int32), ("n_segs", POINTER(c_int32)),
                 ("segs", POINTER(KvqSegment))]
+
+
+class KvqDecodeDesc(ctypes.Structure):
+    _fields_ = [("cache", POINTER(KvqCache)), ("q16", c_void_p), ("n_q_heads", c_int32), ("t_q", c_int32),
+                ("causal_tail", c_int32), ("seq_lens", c_void_p), ("max_len", c_int32),
+                ("head_map", POINTER(c_int32)), ("sm_scale", c_float), ("out", c_void_p), ("lse", c_void_p)]
 
 
 class KvqError(RuntimeError):
@@ -75,6 +83,10 @@ def load():
             lib.kvq_decode_workspace_size.restype = c_int32
             lib.kvq_decode_workspace_size.argtypes = [POINTER(KvqCache), c_int32, c_int32, c_int32,
                                                       POINTER(c_int32), POINTER(c_size_t)]
+            lib.kvq_decode_attn_multi.restype = c_int32
+            lib.kvq_decode_attn_multi.argtypes = [c_int32, POINTER(KvqDecodeDesc), c_void_p, c_size_t, c_void_p]
+            lib.kvq_decode_multi_workspace_size.restype = c_int32
+            lib.kvq_decode_multi_workspace_size.argtypes = [c_int32, POINTER(KvqDecodeDesc), POINTER(c_size_t)]
             lib.kvq_decode_attn_noalloc.restype = c_int32
             lib.kvq_decode_attn_noalloc.argtypes = [POINTER(KvqCache), c_void_p, c_int32, c_int32, c_int32,
                                                     c_void_p, c_int32, POINTER(c_int32), c_float, c_void_p,
@@ -247,6 +259,68 @@ def kvq_decode_attn(cache: Cache, q16: torch.Tensor, n_q_heads: int, t_q: int, c
                                 _stream(stream))
     if st:
         raise KvqError(st, "kvq_decode_attn")
+
+
+def _descs(calls):
+    """calls: sequence of dicts with the per-cache arguments of kvq_decode_attn
+    (cache, q16, n_q_heads, t_q, causal_tail, seq_lens, max_len, head_map,
+    sm_scale, out, lse); tensors may be None for a size query."""
+    arr = (KvqDecodeDesc * max(1, len(calls)))()
+    keep = []
+    for i, c in enumerate(calls):
+        hm = c.get("head_map")
+        hm_arr = None if hm is None else _i32(hm)
+        keep.append(hm_arr)
+        arr[i] = KvqDecodeDesc(ctypes.pointer(c["cache"].desc), _ptr(c.get("q16")), c["n_q_heads"], c["t_q"],
+                               int(c.get("causal_tail", False)), _ptr(c.get("seq_lens")), c["max_len"],
+                               ctypes.cast(hm_arr, POINTER(c_int32)) if hm_arr is not None else None,
+                               float(c.get("sm_scale", 1.0)), _ptr(c.get("out")), _ptr(c.get("lse")))
+    return arr, keep
+
+
+def kvq_decode_multi_workspace_size(calls) -> int:
+    """Bytes of workspace kvq_decode_attn_multi needs for these calls."""
+    arr, keep = _descs(calls)
+    size = c_size_t(0)
+    st = load().kvq_decode_multi_workspace_size(len(calls), arr, ctypes.byref(size))
+    if st:
+        raise KvqError(st, "kvq_decode_multi_workspace_size")
+    return int(size.value)
+
+
+def kvq_decode_attn_multi(calls, workspace, stream=None) -> None:
+    """kvq_decode_attn_multi of include/kvq.h: several decode calls (list of
+    dicts, see _descs) in one launch."""
+    arr, keep = _descs(calls)
+    st = load().kvq_decode_attn_multi(len(calls), arr, _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                                      _stream(stream))
+    if st:
+        raise KvqError(st, "kvq_decode_attn_multi")
+
+
+class MultiCall:
+    """A prepared kvq_decode_attn_multi: the descriptor array is built once and
+    each call only passes the stream (the caches' host tables are read at call
+    time, so appends between calls are seen)."""
+
+    def __init__(self, calls, workspace=None):
+        self.calls = list(calls)
+        self.arr, self._keep = _descs(self.calls)
+        self.ws = workspace
+
+    def workspace_size(self) -> int:
+        size = c_size_t(0)
+        st = load().kvq_decode_multi_workspace_size(len(self.calls), self.arr, ctypes.byref(size))
+        if st:
+            raise KvqError(st, "kvq_decode_multi_workspace_size")
+        return int(size.value)
+
+    def __call__(self, stream=None):
+        ws = self.ws
+        st = load().kvq_decode_attn_multi(len(self.calls), self.arr, _ptr(ws), 0 if ws is None else ws.numel(),
+                                          _stream(stream))
+        if st:
+            raise KvqError(st, "kvq_decode_attn_multi")
 
 
 def kvq_decode_attn_noalloc(cache: Cache, q16: torch.Tensor, n_q_heads: int, t_q: int, causal_tail: bool,

@@ -107,3 +107,24 @@ def test_no_device_is_reported(lib):
     assert _decode(lib, c) == kvq.KVQ_ERR_UNSUPPORTED
     assert _append(lib, c, [0], [1]) == kvq.KVQ_ERR_UNSUPPORTED
     assert c._keep[0][0].len == 100
+
+
+def _desc(c, Hq=4, t_q=1, max_len=128):
+    return kvq.KvqDecodeDesc(ctypes.pointer(c), ctypes.c_void_p(0x20000), Hq, t_q, 0, ctypes.c_void_p(0x30000),
+                             max_len, None, 0.1, ctypes.c_void_p(0x40000), ctypes.c_void_p(0x50000))
+
+
+def test_multi_argument_errors(lib):
+    c1, c2 = _fake_cache(), _fake_cache(H=4)
+    arr = (kvq.KvqDecodeDesc * 2)(_desc(c1), _desc(c2, Hq=6))                  # 6 % 4 != 0 without a map
+    assert lib.kvq_decode_attn_multi(2, arr, None, 0, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_decode_attn_multi(-1, arr, None, 0, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_decode_attn_multi(kvq.MAX_CALLS + 1, arr, None, 0, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_decode_attn_multi(1, None, None, 0, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_decode_attn_multi(0, None, None, 0, None) == kvq.KVQ_OK   # nothing to do
+    size = ctypes.c_size_t(7)
+    assert lib.kvq_decode_multi_workspace_size(2, arr, None) == kvq.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_decode_multi_workspace_size(2, arr, ctypes.byref(size)) == kvq.KVQ_ERR_INVALID_ARG
+    arr[1].t_q = 9
+    arr[1].n_q_heads = 8
+    assert lib.kvq_decode_attn_multi(2, arr, None, 0, None) == kvq.KVQ_ERR_INVALID_ARG
