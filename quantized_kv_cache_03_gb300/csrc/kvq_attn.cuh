@@ -1,6 +1,6 @@
 // kvq_attn.cuh -- split-KV decode attention over the quantized cache (sm_103a).
 //
-// One CTA = (split s, kv head h, sequence b): it attends the query rows of kv
+// One CTA = (split s, kv head h, sequence b) of one work group of the launch: it attends the query rows of kv
 // head h (t_q query tokens x the query heads mapped to h, at most 32 rows) over
 // the positions [s*chunk, (s+1)*chunk) of sequence b and writes either the
 // final output (one split) or a partial (normalised o, lse) for the combine.
@@ -15,26 +15,31 @@
 // __syncwarp and the stage barriers run in the main loop; the block
 // synchronizes once for the query prologue and once to merge the warps.
 //
-//   * QK^T: fp16 tensor-core MMA m16n8k16 on exact integers -- A = the query
-//     codes (rows), B = the K codes of 8 positions entered as 1152 + code (one
-//     xor and two byte-permutes per packed word), two MMAs per 32-block into
-//     one accumulator that starts at -1152 * (sum of the row's codes in the
-//     block).  Every partial sum is an integer below 2^24, so the fp32
-//     accumulator ends exactly at the integer block dot I_b (never summed
+//   * QK^T: fp16 tensor-core MMA m16n8k16 on exact integers -- A = the K codes
+//     of the stage's 16 positions entered as 1152 + code (one xor and two
+//     byte-permutes per packed word), B = 8 query rows' codes, two MMAs per
+//     32-block into one accumulator that starts at -1152 * (sum of the row's
+//     codes in the block).  Every partial sum is an integer below 2^24, so the
+//     fp32 accumulator ends exactly at the integer block dot I_b (never summed
 //     across blocks before scaling).  (GB300's int8 mma.sync issues ~8x slower
 //     than the fp16 one, which is why the integer dot runs on the fp16 path.)
+//     Each lane ends up with positions g, g + 8 of rows 2c, 2c + 1.
 //   * score = sum_b I_b * (sq_b * sk_b) * sm_scale*log2(e), masked to -inf
 //     outside the sequence / causal range; online softmax in base 2 with the
-//     running max only raised when some row's maximum grows.
+//     row's reference max only raised when a score passes it by more than 3
+//     (p <= 8), which skips the cross-lane max on almost every stage.
 //   * P.V: fp16 tensor-core MMA m16n8k16 with fp32 accumulation.  The V codes
 //     enter as exact small integers in fp16 (binary16 exponent trick: 0x6400|n
 //     is 1024+n).  The tile layout puts the same head dims of two adjacent
 //     positions side by side, which gives the (position, position) pairs the
-//     MMA's k dimension needs without a transpose.  The per-(position, block) scale d rides on the P side:
-//     B = p*d split into an fp16 high part and an fp16 low part (two MMAs), so
-//     P.V keeps ~22 bits of the fp32 product.
+//     MMA's k dimension needs without a transpose.  The per-(position, block)
+//     scale d rides on the P side: B = p*d split into an fp16 high part and an fp16 low part (two MMAs), so
+//     P.V keeps ~22 bits of the fp32 product; each part is packed at
+//     (position, row) and turned to (row, position) order with movmatrix.  The
+//     P.V accumulators' columns are the same rows 2c, 2c + 1, so the softmax
+//     rescale needs no shuffles.
 //
-// Each warp keeps its own (m, l, acc); the four states are merged through
+// Each warp keeps its own (m, l, acc); the warps' states are merged through
 // shared memory at the end in a fixed order.
 #pragma once
 
@@ -45,10 +50,16 @@
 namespace kvq {
 
 #ifndef KVQ_STAGES_Q4
-#define KVQ_STAGES_Q4 3   // 16-position stages per warp ring (q4_0 V)
+#define KVQ_STAGES_Q4 2   // stages per warp ring (q4_0 V)
+#endif
+#ifndef KVQ_TPS_Q4
+#define KVQ_TPS_Q4 2      // 16-position tiles per stage (q4_0 V)
 #endif
 #ifndef KVQ_STAGES_Q8
 #define KVQ_STAGES_Q8 3   // (q8_0 V)
+#endif
+#ifndef KVQ_TPS_Q8
+#define KVQ_TPS_Q8 1
 #endif
 
 
@@ -60,37 +71,42 @@ struct SplitCfg {
     // the <= 8-row kernels are held to 128 registers per thread (512 threads per SM x 4 CTAs of 4 warps,
     // or one CTA of 16 warps); the others take what they need
     static constexpr int MIN_CTAS = (NT == 1) ? (16 / WARPS > 0 ? 16 / WARPS : 1) : 1;
-    static constexpr int MTQ = (NT + 1) / 2;                  // 16-row QK m-tiles
-    static constexpr int QROWS = 16 * MTQ;                    // query rows kept in smem
+    static constexpr int QROWS = (8 * NT > WARPS) ? 8 * NT : WARPS;   // query rows kept in smem
     static_assert(QROWS % WARPS == 0, "every warp quantizes the same number of query rows");
     static constexpr int STAGES = (VT == KVQ_V_Q4_0) ? KVQ_STAGES_Q4 : KVQ_STAGES_Q8;   // ring depth per warp
+    static constexpr int TPS = (VT == KVQ_V_Q4_0) ? KVQ_TPS_Q4 : KVQ_TPS_Q8;         // tiles per stage
     static constexpr int VCODE = (VT == KVQ_V_Q4_0) ? kD / 2 : kD;            // V code bytes per position
-    // one warp stage: one tile of K codes, K scales, V codes, V scales (cache order)
+    static constexpr int TILE_K = kWTile * kD, TILE_S = kWTile * kNB * 2, TILE_V = kWTile * VCODE;
+    static constexpr int TILE = TILE_K + TILE_S + TILE_V + TILE_S;            // bytes of one tile
+    // one warp stage: up to TPS consecutive tiles of one segment, each array's
+    // tiles side by side as in the cache (K codes, K scales, V codes, V scales)
     static constexpr int K_OFF = 0;
-    static constexpr int KS_OFF = K_OFF + kWTile * kD;
-    static constexpr int V_OFF = KS_OFF + kWTile * kNB * 2;
-    static constexpr int VS_OFF = V_OFF + kWTile * VCODE;
-    static constexpr int STAGE = VS_OFF + kWTile * kNB * 2;   // = bytes the four copies land
+    static constexpr int KS_OFF = K_OFF + TPS * TILE_K;
+    static constexpr int V_OFF = KS_OFF + TPS * TILE_S;
+    static constexpr int VS_OFF = V_OFF + TPS * TILE_V;
+    static constexpr int STAGE = VS_OFF + TPS * TILE_S;
     static constexpr int RING = STAGES * STAGE;               // per warp
     static constexpr int Q_OFF = WARPS * RING;                // int8 [QROWS][kD]
     static constexpr int QS_OFF = Q_OFF + QROWS * kD;         // fp32 [QROWS][kNB]
     static constexpr int QSUM_OFF = QS_OFF + QROWS * kNB * 4; // int32 [QROWS][kNB]
     static constexpr int ML_OFF = QSUM_OFF + QROWS * kNB * 4; // fp32 m, l [WARPS][8*NT]
     // Per-lane query table, [chunk][lane][4 words] (16-byte chunks, lane-major
-    // so a warp's LDS.128 of one chunk is conflict free): the query MMA
-    // fragments (for NT == 1 only the a0/a2 words of rows 0..7), the lane's
-    // query-row scales [NT][kNB] and the QK accumulator seeds.
-    static constexpr int QA_CHUNKS = (NT == 1) ? kNB : MTQ * kNB * 2;
-    static constexpr int SQ_CHUNKS = NT;
-    static constexpr int CI_CHUNKS = (NT == 1) ? 1 : MTQ * 2;
-    static constexpr int QF_CHUNKS = QA_CHUNKS + SQ_CHUNKS + CI_CHUNKS;
+    // so a warp's LDS.128 of one chunk is conflict free): per (8-row tile nt,
+    // block) the query MMA B fragments of both k16 steps and the accumulator
+    // seeds of the lane's two rows, and per (nt, row) the row's block scales.
+    static constexpr int QB_CHUNKS = NT * kNB;
+    static constexpr int SEED_CHUNKS = NT * kNB;
+    static constexpr int SQ_CHUNKS = NT * 2;
+    static constexpr int QF_CHUNKS = QB_CHUNKS + SEED_CHUNKS + SQ_CHUNKS;
     static constexpr int QF_OFF = ML_OFF + 2 * WARPS * 8 * NT * 4;
-    static constexpr int TI_OFF = QF_OFF + QF_CHUNKS * 32 * 16;  // int4 tile record [WARPS][STAGES]
-    static constexpr int BAR_OFF = TI_OFF + WARPS * STAGES * 16; // uint64 mbarrier [WARPS][STAGES]
+    static constexpr int TI_OFF = QF_OFF + QF_CHUNKS * 32 * 16;  // int4 tile record [WARPS][STAGES][TPS]
+    static constexpr int NS_OFF = TI_OFF + WARPS * STAGES * TPS * 16;   // int tiles in stage [WARPS][STAGES]
+    static constexpr int BAR_OFF = (NS_OFF + WARPS * STAGES * 4 + 7) / 8 * 8;   // uint64 mbarrier [WARPS][STAGES]
     static constexpr int FLAG_OFF = BAR_OFF + WARPS * STAGES * 8;
     static constexpr int SMEM = FLAG_OFF + 16;
     static_assert(8 * NT * kD * 4 <= WARPS * RING, "merge buffer must fit in the stage rings");
     static_assert(STAGE % 16 == 0 && KS_OFF % 16 == 0 && V_OFF % 16 == 0 && VS_OFF % 16 == 0, "16-byte granules");
+    static_assert(TPS == 1 || TPS == 2, "one or two tiles per stage");
 };
 
 // The pieces of a sequence's segments that fall in [r0, r1), walked in order
@@ -132,20 +148,21 @@ __device__ __forceinline__ void walk_next(const AttnParams &p, int seg0, int nse
     if (w.T * kWTile >= w.le) walk_seek(p, seg0, nseg, h, r0, r1, w.k + 1, vcode, w);
 }
 
-// Lane 0 fills ring slot `dst` (shared address) with the walk's current tile:
-// four contiguous bulk copies whose bytes complete on the slot's barrier.
-// Positions of the tile outside [la, le) are copied too (they are cache rows
-// of the same segment, possibly never written) and masked where they are used.
+// Lane 0 fills ring slot `dst` (shared address) with n consecutive tiles of
+// one segment starting at the walk's current tile: four contiguous bulk copies
+// whose bytes complete on the slot's barrier.  Positions of a tile outside
+// [la, le) are copied too (they are cache rows of the same segment, possibly
+// never written) and masked where they are used.
 template <int NT, int VT>
-__device__ __forceinline__ void tile_issue(const Walk &w, uint32_t dst, uint32_t bar)
+__device__ __forceinline__ void tile_issue(const Walk &w, int n, uint32_t dst, uint32_t bar)
 {
     using C = SplitCfg<NT, VT>;
     const size_t tb = (size_t)w.T * kWTile;
-    mbar_arrive_expect_tx(bar, C::STAGE);
-    bulk_g2s(dst + C::K_OFF, w.kq + tb * kD, kWTile * kD, bar);
-    bulk_g2s(dst + C::KS_OFF, w.ks + tb * kNB * 2, kWTile * kNB * 2, bar);
-    bulk_g2s(dst + C::V_OFF, w.vq + tb * C::VCODE, kWTile * C::VCODE, bar);
-    bulk_g2s(dst + C::VS_OFF, w.vs + tb * kNB * 2, kWTile * kNB * 2, bar);
+    mbar_arrive_expect_tx(bar, n * C::TILE);
+    bulk_g2s(dst + C::K_OFF, w.kq + tb * kD, n * C::TILE_K, bar);
+    bulk_g2s(dst + C::KS_OFF, w.ks + tb * kNB * 2, n * C::TILE_S, bar);
+    bulk_g2s(dst + C::V_OFF, w.vq + tb * C::VCODE, n * C::TILE_V, bar);
+    bulk_g2s(dst + C::VS_OFF, w.vs + tb * kNB * 2, n * C::TILE_S, bar);
 }
 
 // Head-dim index of accumulator row rho (0..15) of PV m-tile mt = 2*block + h2.
@@ -235,9 +252,11 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
     using C = SplitCfg<NT, VT>;
     constexpr int kWarps = C::WARPS;
     constexpr int kThreads = C::THREADS;
-    constexpr int MTQ = C::MTQ;
     constexpr int S = C::STAGES;
     constexpr float kBias = 1152.0f;                 // K codes enter the MMA as 1152 + code
+    // p = 2^(s - m) may reach 2^kSlack before m is raised; with the largest V
+    // scale (65504 / 8) p * d then still fits fp16's range.
+    constexpr float kSlack = 3.0f;
     extern __shared__ __align__(128) uint8_t smem[];
 
     // ---- the group, sequence, kv head and split of this CTA ----
@@ -280,18 +299,11 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
     // ---- this warp's sub-range and its first copies (before the query prologue) ----
     const int span = (r1c - r0 + kWarps * kWTile - 1) / (kWarps * kWTile) * kWTile;
     const int w0 = min(r1c, r0 + warp * span), w1 = min(r1c, w0 + span);
-    int n_tiles = 0;
-    if (w0 < w1)
-        for (int k = 0; k < nseg; ++k) {
-            const SegDesc &s = p.seg[seg0 + k];
-            const int end = (k + 1 < nseg) ? p.seg[seg0 + k + 1].pos0 : s.pos0 + s.cap;
-            const int a = max(w0, s.pos0) - s.pos0, e = min(min(w1, end), s.pos0 + s.cap) - s.pos0;
-            if (a < e) n_tiles += (e - 1) / kWTile - a / kWTile + 1;
-        }
     uint8_t *ring = smem + warp * C::RING;
     const uint32_t ring_s = smem_u32(ring);
     const uint32_t bar_s = smem_u32(smem + C::BAR_OFF) + warp * S * 8;
-    int4 *tile_rec = reinterpret_cast<int4 *>(smem + C::TI_OFF) + warp * S;
+    int4 *tile_rec = reinterpret_cast<int4 *>(smem + C::TI_OFF) + warp * S * C::TPS;
+    int *stage_n = reinterpret_cast<int *>(smem + C::NS_OFF) + warp * S;
     int *bad_flag = reinterpret_cast<int *>(smem + C::FLAG_OFF);
     if (tid == 0) *bad_flag = 0;
     if (lane == 0) {
@@ -302,19 +314,33 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
     __syncwarp();
     Walk pw;
     walk_seek(p, seg0, nseg, h, w0, w1, 0, C::VCODE, pw);
-    int issued = 0;   // tiles handed to the copy engine
+    int issued = 0;   // stages handed to the copy engine
+    // Hand the next stage (up to TPS tiles of the current segment piece) to the
+    // copy engine; the walk is advanced by every lane alike.
     auto issue = [&](int slot) {
-        if (lane == 0) {
-            const int tb = pw.T * kWTile;
-            tile_rec[slot] = make_int4(tb, pw.la, pw.le, pw.pos0 + tb);
-            tile_issue<NT, VT>(pw, ring_s + slot * C::STAGE, bar_s + slot * 8);
-        }
+        const Walk first = pw;
+        const int tb0 = pw.T * kWTile;
+        const int4 rec0 = make_int4(tb0, pw.la, pw.le, pw.pos0 + tb0);
         walk_next(p, seg0, nseg, h, w0, w1, C::VCODE, pw);
+        int n = 1;
+        int4 rec1 = rec0;
+        if (C::TPS == 2 && pw.k == first.k && pw.T == first.T + 1) {
+            const int tb1 = pw.T * kWTile;
+            rec1 = make_int4(tb1, pw.la, pw.le, pw.pos0 + tb1);
+            walk_next(p, seg0, nseg, h, w0, w1, C::VCODE, pw);
+            n = 2;
+        }
+        if (lane == 0) {
+            tile_rec[slot * C::TPS] = rec0;
+            if (C::TPS == 2) tile_rec[slot * C::TPS + C::TPS - 1] = rec1;
+            stage_n[slot] = n;
+            tile_issue<NT, VT>(first, n, ring_s + slot * C::STAGE, bar_s + slot * 8);
+        }
         ++issued;
     };
 #pragma unroll
     for (int st = 0; st < S - 1; ++st)
-        if (st < n_tiles) issue(st);
+        if (pw.k < nseg) issue(st);
 
     const int L = max(0, min(len_b, lcap));
     const int r1 = min(L, r0 + G.chunk);
@@ -376,64 +402,54 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
     }
     __syncthreads();   // query codes visible
 
-    // Query A fragments (fp16, exact codes).  Within block bb, k16 step ks, this
+    // Query B fragments (fp16, exact codes).  Within block bb, k16 step ks, this
     // lane's k slots (2c, 2c+1 | 2c+8, 2c+9) carry head dims
     // 32bb + 8c + 4ks + (0, 1 | 2, 3): the bytes of word 8bb + 2c + ks, the same
     // word the lane reads from K, so q.k is unchanged.  Warp 0 writes them, with
-    // the row scales and the accumulator seeds (-1152 * sum of the row's codes
-    // in the block), to the per-lane table that every stage reads back.
+    // the accumulator seeds (-1152 * sum of the row's codes in the block) of
+    // rows 2c, 2c+1 and those rows' scales, to the per-lane table that every
+    // stage reads back (row scales as (row 2c, row 2c+1) pairs per block).
     uint4 *qf = reinterpret_cast<uint4 *>(smem + C::QF_OFF) + lane;   // chunk k at qf[32 * k]
     if (warp == 0) {
 #pragma unroll
-        for (int mq = 0; mq < MTQ; ++mq)
+        for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
             for (int bb = 0; bb < kNB; ++bb) {
-                uint32_t f[2][4];
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {
-                    const uint32_t wa = qw[(16 * mq + g) * (kD / 4) + 8 * bb + 2 * c + ks];
-                    const uint32_t wb = qw[(16 * mq + g + 8) * (kD / 4) + 8 * bb + 2 * c + ks];
-                    f[ks][0] = q_pair(wa, 0);
-                    f[ks][1] = q_pair(wb, 0);
-                    f[ks][2] = q_pair(wa, 2);
-                    f[ks][3] = q_pair(wb, 2);
-                }
-                if (NT == 1) {
-                    qf[32 * bb] = make_uint4(f[0][0], f[0][2], f[1][0], f[1][2]);
-                } else {
-                    qf[32 * ((mq * kNB + bb) * 2 + 0)] = make_uint4(f[0][0], f[0][1], f[0][2], f[0][3]);
-                    qf[32 * ((mq * kNB + bb) * 2 + 1)] = make_uint4(f[1][0], f[1][1], f[1][2], f[1][3]);
-                }
+                const uint32_t w0 = qw[(8 * nt + g) * (kD / 4) + 8 * bb + 2 * c];
+                const uint32_t w1 = qw[(8 * nt + g) * (kD / 4) + 8 * bb + 2 * c + 1];
+                qf[32 * (nt * kNB + bb)] = make_uint4(q_pair(w0, 0), q_pair(w0, 2), q_pair(w1, 0), q_pair(w1, 2));
+                const float s0 = -kBias * (float)qsum[(8 * nt + 2 * c) * kNB + bb];
+                const float s1 = -kBias * (float)qsum[(8 * nt + 2 * c + 1) * kNB + bb];
+                qf[32 * (C::QB_CHUNKS + nt * kNB + bb)] =
+                    make_uint4(__float_as_uint(s0), __float_as_uint(s1), __float_as_uint(s0), __float_as_uint(s1));
             }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int row = 8 * nt + g;
-            qf[32 * (C::QA_CHUNKS + nt)] =
-                make_uint4(__float_as_uint(qs[row * kNB + 0]), __float_as_uint(qs[row * kNB + 1]),
-                           __float_as_uint(qs[row * kNB + 2]), __float_as_uint(qs[row * kNB + 3]));
+            for (int hb = 0; hb < 2; ++hb) {   // (row 2c, row 2c+1) scale pairs of blocks 2hb, 2hb+1
+                const int r0 = 8 * nt + 2 * c;
+                qf[32 * (C::QB_CHUNKS + C::SEED_CHUNKS + nt * 2 + hb)] =
+                    make_uint4(__float_as_uint(qs[r0 * kNB + 2 * hb]), __float_as_uint(qs[(r0 + 1) * kNB + 2 * hb]),
+                               __float_as_uint(qs[r0 * kNB + 2 * hb + 1]),
+                               __float_as_uint(qs[(r0 + 1) * kNB + 2 * hb + 1]));
+            }
         }
-#pragma unroll
-        for (int mq = 0; mq < MTQ; ++mq)
-#pragma unroll
-            for (int hf = 0; hf < (NT == 1 ? 1 : 2); ++hf) {
-                const int row = 16 * mq + 8 * hf + g;
-                qf[32 * (C::QA_CHUNKS + C::SQ_CHUNKS + mq * 2 + hf)] =
-                    make_uint4(__float_as_uint(-kBias * (float)qsum[row * kNB + 0]),
-                               __float_as_uint(-kBias * (float)qsum[row * kNB + 1]),
-                               __float_as_uint(-kBias * (float)qsum[row * kNB + 2]),
-                               __float_as_uint(-kBias * (float)qsum[row * kNB + 3]));
-            }
     }
     __syncthreads();   // query table visible
-    float m[NT], l[NT];
-    int lim[NT];
+    // This lane's rows are 8nt + 2c + e (e = 0, 1): the columns of its QK
+    // accumulators and of its P.V accumulators alike.
+    float m[NT][2], l[NT][2];
+    int lim[NT][2];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int row = 8 * nt + g;
-        lim[nt] = (row < R) ? (G.causal ? L - G.t_q + row / gsz : L - 1) : -1;
-        m[nt] = -INFINITY;
-        l[nt] = 0.f;
-    }
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int row = 8 * nt + 2 * c + e;
+            lim[nt][e] = (row < R) ? (G.causal ? L - G.t_q + row / gsz : L - 1) : -1;
+            m[nt][e] = -INFINITY;
+            l[nt][e] = 0.f;
+        }
+    float2 mu[NT];   // exponent offsets: m, or 0 while m is -inf
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mu[nt] = make_float2(0.f, 0.f);
     const int lim_min = G.causal ? L - G.t_q : L - 1;   // smallest limit over live rows
     float acc[8][NT][4];
 #pragma unroll
@@ -444,217 +460,193 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
             for (int k = 0; k < 4; ++k) acc[mt][nt][k] = 0.f;
 
     bool bad = false;   // a stage never arrived (the warp then stops and drains)
-    for (int j = 0; j < n_tiles; ++j) {
-        const bool landed = mbar_wait(bar_s + (j % S) * 8, (j / S) & 1);
+    int slot = 0, phase = 0, prev = S - 1, done = 0;   // done % S, (done / S) & 1, (done + S - 1) % S
+    while (done < issued) {
+        const bool landed = mbar_wait(bar_s + slot * 8, phase);
         if (!__all_sync(0xffffffffu, landed)) {
             bad = true;
             break;
         }
-        __syncwarp();   // every lane is done with stage j-1, whose slot is refilled next
-        if (j + S - 1 < n_tiles) {
+        __syncwarp();   // every lane is done with the previous stage, whose slot is refilled next
+        if (pw.k < nseg) {
             if (lane == 0) fence_proxy_async_smem();
-            issue((j + S - 1) % S);
+            issue(prev);
         }
-
-        const uint8_t *st = ring + (j % S) * C::STAGE;
-        const int4 rec = tile_rec[j % S];
+        const int ns = stage_n[slot];
+        const uint8_t *stg = ring + slot * C::STAGE;
+        const int4 *recs = tile_rec + slot * C::TPS;
+        prev = slot;
+        if (++slot == S) {
+            slot = 0;
+            phase ^= 1;
+        }
+        ++done;
+#pragma unroll 1
+        for (int t = 0; t < ns; ++t) {
+        const uint8_t *stK = stg + C::K_OFF + t * C::TILE_K, *stKS = stg + C::KS_OFF + t * C::TILE_S;
+        const uint8_t *stV = stg + C::V_OFF + t * C::TILE_V, *stVS = stg + C::VS_OFF + t * C::TILE_S;
+        const int4 rec = recs[t];
         const int tb = rec.x, la = rec.y, le = rec.z, pos_base = rec.w;
-        // every position of the stage valid and visible to every live row?
+        // every position of the tile valid and visible to every live row?
         const bool full = tb >= la && tb + kWTile <= le && pos_base + kWTile - 1 <= lim_min;
 
         auto chunk = [&](auto full_tag) {
             constexpr bool FULL = decltype(full_tag)::value;
-            // ---- S = Q K^T per 32-block (exact integers in fp32), scaled scores ----
-            uint32_t qa[MTQ][kNB][2][4];
-            float cinit[MTQ][kNB][2], sqf[NT][kNB];
+            // ---- S^T = K Q^T per 32-block (exact integers in fp32): A = the K
+            // codes of the stage's 16 positions (rows g and g + 8 of the MMA),
+            // B = 8 query rows ----
+            uint4 kk[2][2];   // [position g / g + 8][blocks 0-1 / 2-3]
 #pragma unroll
-            for (int mq = 0; mq < MTQ; ++mq)
-#pragma unroll
-                for (int bb = 0; bb < kNB; ++bb) {
-                    if (NT == 1) {
-                        const uint4 f = qf[32 * bb];
-                        qa[mq][bb][0][0] = f.x; qa[mq][bb][0][2] = f.y;
-                        qa[mq][bb][1][0] = f.z; qa[mq][bb][1][2] = f.w;
-                        qa[mq][bb][0][1] = qa[mq][bb][0][3] = qa[mq][bb][1][1] = qa[mq][bb][1][3] = 0u;
-                    } else {
-                        const uint4 f0 = qf[32 * ((mq * kNB + bb) * 2 + 0)];
-                        const uint4 f1 = qf[32 * ((mq * kNB + bb) * 2 + 1)];
-                        qa[mq][bb][0][0] = f0.x; qa[mq][bb][0][1] = f0.y; qa[mq][bb][0][2] = f0.z; qa[mq][bb][0][3] = f0.w;
-                        qa[mq][bb][1][0] = f1.x; qa[mq][bb][1][1] = f1.y; qa[mq][bb][1][2] = f1.z; qa[mq][bb][1][3] = f1.w;
-                    }
-                }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const uint4 f = qf[32 * (C::QA_CHUNKS + nt)];
-                sqf[nt][0] = __uint_as_float(f.x); sqf[nt][1] = __uint_as_float(f.y);
-                sqf[nt][2] = __uint_as_float(f.z); sqf[nt][3] = __uint_as_float(f.w);
-            }
-#pragma unroll
-            for (int mq = 0; mq < MTQ; ++mq)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    if (NT == 1 && hf == 1) {
-#pragma unroll
-                        for (int bb = 0; bb < kNB; ++bb) cinit[mq][bb][1] = 0.f;
-                    } else {
-                        const uint4 f = qf[32 * (C::QA_CHUNKS + C::SQ_CHUNKS + mq * 2 + hf)];
-                        cinit[mq][0][hf] = __uint_as_float(f.x); cinit[mq][1][hf] = __uint_as_float(f.y);
-                        cinit[mq][2][hf] = __uint_as_float(f.z); cinit[mq][3][hf] = __uint_as_float(f.w);
-                    }
-                }
-            float s[2][NT][2];
-#pragma unroll
-            for (int sub = 0; sub < 2; ++sub) {
-                // K column 8sub + g: load 2sub + hb holds its codes 8c..8c+7 of
-                // blocks 2hb and 2hb + 1
-                uint4 kk[2];
+            for (int pp = 0; pp < 2; ++pp)
 #pragma unroll
                 for (int hb = 0; hb < 2; ++hb)
-                    kk[hb] = *reinterpret_cast<const uint4 *>(st + C::K_OFF + (2 * sub + hb) * 512 + lane * 16);
-                float sc[MTQ][kNB][4];
+                    kk[pp][hb] = *reinterpret_cast<const uint4 *>(stK + (2 * pp + hb) * 512 + lane * 16);
+            float sc[NT][kNB][4];   // (pos g, row 2c), (pos g, row 2c+1), (pos g+8, row 2c), (pos g+8, row 2c+1)
 #pragma unroll
-                for (int bb = 0; bb < kNB; ++bb) {
-                    const uint32_t kx = (bb & 1) ? kk[bb >> 1].z : kk[bb >> 1].x;
-                    const uint32_t ky = (bb & 1) ? kk[bb >> 1].w : kk[bb >> 1].y;
-                    uint32_t b00, b01, b10, b11;
-                    k_word_biased(kx, b00, b01);
-                    k_word_biased(ky, b10, b11);
+            for (int bb = 0; bb < kNB; ++bb) {
+                const uint4 &u0 = kk[0][bb >> 1], &u1 = kk[1][bb >> 1];
+                uint32_t a0[4], a1[4];   // k16 steps 0 and 1 of the block
+                k_word_biased((bb & 1) ? u0.z : u0.x, a0[0], a0[2]);
+                k_word_biased((bb & 1) ? u1.z : u1.x, a0[1], a0[3]);
+                k_word_biased((bb & 1) ? u0.w : u0.y, a1[0], a1[2]);
+                k_word_biased((bb & 1) ? u1.w : u1.y, a1[1], a1[3]);
 #pragma unroll
-                    for (int mq = 0; mq < MTQ; ++mq) {
-                        mma_f16_16816_c(sc[mq][bb], qa[mq][bb][0], b00, b01, cinit[mq][bb][0], cinit[mq][bb][1]);
-                        mma_f16_16816(sc[mq][bb], qa[mq][bb][1], b10, b11);
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint4 qb = qf[32 * (nt * kNB + bb)];
+                    const uint4 sd = qf[32 * (C::QB_CHUNKS + nt * kNB + bb)];
+                    mma_f16_16816_c4(sc[nt][bb], a0, qb.x, qb.y, sd);
+                    mma_f16_16816(sc[nt][bb], a1, qb.z, qb.w);
+                }
+            }
+            // K scales of this lane's positions g and g + 8
+            float sk[2][kNB];
+            unpack4h(*reinterpret_cast<const uint2 *>(stKS + g * kNB * 2), sk[0]);
+            unpack4h(*reinterpret_cast<const uint2 *>(stKS + (g + 8) * kNB * 2), sk[1]);
+            float2 s[NT][2];   // [nt][position g / g + 8] = (row 2c, row 2c + 1)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float2 sq[kNB];   // (row 2c, row 2c + 1) scales of each block
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    const uint4 q4 = qf[32 * (C::QB_CHUNKS + C::SEED_CHUNKS + nt * 2 + hb)];
+                    sq[2 * hb] = make_float2(__uint_as_float(q4.x), __uint_as_float(q4.y));
+                    sq[2 * hb + 1] = make_float2(__uint_as_float(q4.z), __uint_as_float(q4.w));
+                }
+#pragma unroll
+                for (int pp = 0; pp < 2; ++pp) {
+                    float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int bb = 0; bb < kNB; ++bb) {
+                        const float2 i2 = make_float2(sc[nt][bb][2 * pp], sc[nt][bb][2 * pp + 1]);
+                        a = fma2(mul2(i2, sq[bb]), make_float2(sk[pp][bb], sk[pp][bb]), a);
                     }
+                    if (!FULL) {
+                        const int tok = tb + 8 * pp + g, pos = pos_base + 8 * pp + g;
+                        const bool okp = tok >= la && tok < le;
+                        a.x = (okp && pos <= lim[nt][0]) ? a.x : -INFINITY;
+                        a.y = (okp && pos <= lim[nt][1]) ? a.y : -INFINITY;
+                    }
+                    s[nt][pp] = a;
                 }
-                // K scales of this lane's two score columns (positions 8sub + 2c + e)
-                const int ut = 8 * sub + 2 * c;
-                const uint4 ksr = *reinterpret_cast<const uint4 *>(st + C::KS_OFF + ut * kNB * 2);
-                float sk[2][kNB];
-                {
-                    const float2 a0 = __half22float2(*reinterpret_cast<const __half2 *>(&ksr.x));
-                    const float2 a1 = __half22float2(*reinterpret_cast<const __half2 *>(&ksr.y));
-                    const float2 a2 = __half22float2(*reinterpret_cast<const __half2 *>(&ksr.z));
-                    const float2 a3 = __half22float2(*reinterpret_cast<const __half2 *>(&ksr.w));
-                    sk[0][0] = a0.x; sk[0][1] = a0.y; sk[0][2] = a1.x; sk[0][3] = a1.y;
-                    sk[1][0] = a2.x; sk[1][1] = a2.y; sk[1][2] = a3.x; sk[1][3] = a3.y;
-                }
+            }
+            if (DUMP) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int mq = nt >> 1, idx = 2 * (nt & 1) + e;
-                        float a = 0.f;
-#pragma unroll
-                        for (int bb = 0; bb < kNB; ++bb) a = fmaf(sc[mq][bb][idx], sqf[nt][bb] * sk[e][bb], a);
-                        if (FULL) {
-                            s[sub][nt][e] = a;
-                        } else {
-                            const int tok = tb + ut + e;
-                            const bool ok = tok >= la && tok < le && pos_base + ut + e <= lim[nt];
-                            s[sub][nt][e] = ok ? a : -INFINITY;
-                        }
-                    }
-                if (DUMP) {
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
+                    for (int pp = 0; pp < 2; ++pp)
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
-                            const int row = 8 * nt + g, tok = tb + ut + e, pos = pos_base + ut + e;
+                            const int row = 8 * nt + 2 * c + e, tok = tb + 8 * pp + g, pos = pos_base + 8 * pp + g;
                             if (row < R && tok >= la && tok < le && pos < L) {
-                                const int mq = nt >> 1, idx = 2 * (nt & 1) + e;
                                 const int i = row / gsz, hq = p.grp_q[gb + row % gsz];
                                 const size_t o = ((((size_t)b * G.t_q + i) * G.n_q_heads + hq) * G.max_len + pos) * kNB;
                                 int4 v;
-                                v.x = (int)sc[mq][0][idx]; v.y = (int)sc[mq][1][idx];
-                                v.z = (int)sc[mq][2][idx]; v.w = (int)sc[mq][3][idx];
+                                v.x = (int)sc[nt][0][2 * pp + e]; v.y = (int)sc[nt][1][2 * pp + e];
+                                v.z = (int)sc[nt][2][2 * pp + e]; v.w = (int)sc[nt][3][2 * pp + e];
                                 *reinterpret_cast<int4 *>(G.dbg_scores + o) = v;
                             }
                         }
-                }
+                return;
             }
-            if (DUMP) return;
 
-            // ---- online softmax (base 2) ----
-            bool grow = false;
-            float mnew[NT];
+            // ---- online softmax (base 2) with a lazily raised reference max: a
+            // row's 16 scores sit in the 8 lanes of one c, and the exact max over
+            // them (three shuffles) is only taken when some score exceeds the
+            // row's reference by more than kSlack, so p stays <= 2^kSlack ----
+            bool need = false;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float mx = fmaxf(fmaxf(s[0][nt][0], s[0][nt][1]), fmaxf(s[1][nt][0], s[1][nt][1]));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                mnew[nt] = fmaxf(m[nt], mx);
-                grow |= mnew[nt] > m[nt];
+                need |= fmaxf(s[nt][0].x, s[nt][1].x) > m[nt][0] + kSlack;
+                need |= fmaxf(s[nt][0].y, s[nt][1].y) > m[nt][1] + kSlack;
             }
-            if (__any_sync(0xffffffffu, grow)) {
+            if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const float al = (mnew[nt] == -INFINITY) ? 1.f : fast_exp2(m[nt] - mnew[nt]);
-                    l[nt] *= al;
-                    m[nt] = mnew[nt];
-                    const float a0 = __shfl_sync(0xffffffffu, al, 8 * c);       // row 8nt + 2c
-                    const float a1 = __shfl_sync(0xffffffffu, al, 8 * c + 4);   // row 8nt + 2c + 1
+                    float al[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        float mx = e ? fmaxf(s[nt][0].y, s[nt][1].y) : fmaxf(s[nt][0].x, s[nt][1].x);
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                        const float mnew = fmaxf(m[nt][e], mx);
+                        al[e] = (mnew == -INFINITY) ? 1.f : fast_exp2(m[nt][e] - mnew);
+                        l[nt][e] *= al[e];
+                        m[nt][e] = mnew;
+                    }
+                    mu[nt] = make_float2(m[nt][0] == -INFINITY ? 0.f : m[nt][0], m[nt][1] == -INFINITY ? 0.f : m[nt][1]);
+                    const float2 a2 = make_float2(al[0], al[1]);
 #pragma unroll
                     for (int mt = 0; mt < 8; ++mt) {
-                        acc[mt][nt][0] *= a0; acc[mt][nt][1] *= a1;
-                        acc[mt][nt][2] *= a0; acc[mt][nt][3] *= a1;
+                        const float2 lo = mul2(make_float2(acc[mt][nt][0], acc[mt][nt][1]), a2);
+                        const float2 hi = mul2(make_float2(acc[mt][nt][2], acc[mt][nt][3]), a2);
+                        acc[mt][nt][0] = lo.x; acc[mt][nt][1] = lo.y;
+                        acc[mt][nt][2] = hi.x; acc[mt][nt][3] = hi.y;
                     }
                 }
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const float mu = (m[nt] == -INFINITY) ? 0.f : m[nt];
+                float2 lsum = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int sub = 0; sub < 2; ++sub)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        s[sub][nt][e] = fast_exp2(s[sub][nt][e] - mu);
-                        l[nt] += s[sub][nt][e];
-                    }
+                for (int pp = 0; pp < 2; ++pp) {
+                    const float2 t = sub2(s[nt][pp], mu[nt]);
+                    s[nt][pp] = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+                    lsum = add2(lsum, s[nt][pp]);
+                }
+                l[nt][0] += lsum.x;
+                l[nt][1] += lsum.y;
             }
 
-            // ---- O += P . V  (per 32-block: B = p*d as fp16 hi + lo, A = V codes) ----
-            uint4 vsr[2];   // V scales of this lane's B columns (positions 8sub + 2c, +1)
-            bool okv[2][2];
+            // ---- O += P . V  (per 32-block: A = V codes, B = p*d as fp16 hi + lo,
+            // formed at (position, row) and transposed to (row, position) with
+            // movmatrix) ----
+            float dv[2][kNB];   // V scales of positions g, g + 8 (0 where invisible)
+            unpack4h(*reinterpret_cast<const uint2 *>(stVS + g * kNB * 2), dv[0]);
+            unpack4h(*reinterpret_cast<const uint2 *>(stVS + (g + 8) * kNB * 2), dv[1]);
+            if (!FULL) {
+#pragma unroll
+                for (int pp = 0; pp < 2; ++pp) {
+                    const int tok = tb + 8 * pp + g;
+                    const bool ok = tok >= la && tok < le && pos_base + 8 * pp + g < L;
+#pragma unroll
+                    for (int bb = 0; bb < kNB; ++bb) dv[pp][bb] = ok ? dv[pp][bb] : 0.f;
+                }
+            }
             // V code words of positions (8sub + 2c, +1): q4_0 one load per sub
             // (word bb = block bb), q8_0 two (load 2sub + hb: blocks 2hb, 2hb + 1)
             constexpr int NVL = (VT == KVQ_V_Q4_0) ? 1 : 2;
             uint4 vv[2][NVL];
 #pragma unroll
-            for (int sub = 0; sub < 2; ++sub) {
-                const int ut = 8 * sub + 2 * c;
-                vsr[sub] = *reinterpret_cast<const uint4 *>(st + C::VS_OFF + ut * kNB * 2);
-                okv[sub][0] = FULL || (tb + ut >= la && tb + ut < le && pos_base + ut < L);
-                okv[sub][1] = FULL || (tb + ut + 1 >= la && tb + ut + 1 < le && pos_base + ut + 1 < L);
+            for (int sub = 0; sub < 2; ++sub)
 #pragma unroll
                 for (int hb = 0; hb < NVL; ++hb)
-                    vv[sub][hb] = *reinterpret_cast<const uint4 *>(st + C::V_OFF + (NVL * sub + hb) * 512 + lane * 16);
-            }
+                    vv[sub][hb] = *reinterpret_cast<const uint4 *>(stV + (NVL * sub + hb) * 512 + lane * 16);
 #pragma unroll
             for (int bb = 0; bb < kNB; ++bb) {
-                uint32_t bhi[NT][2], blo[NT][2];
                 uint32_t a[2][4];   // [h2] A fragment of m-tile 2bb + h2
 #pragma unroll
                 for (int sub = 0; sub < 2; ++sub) {
-                    // V scale of block bb for the two positions (fp16 -> fp32), 0 if invalid
-                    const uint32_t w0 = (bb < 2) ? vsr[sub].x : vsr[sub].y;
-                    const uint32_t w1 = (bb < 2) ? vsr[sub].z : vsr[sub].w;
-                    float d0 = __half2float(__ushort_as_half((uint16_t)((bb & 1) ? (w0 >> 16) : (w0 & 0xffffu))));
-                    float d1 = __half2float(__ushort_as_half((uint16_t)((bb & 1) ? (w1 >> 16) : (w1 & 0xffffu))));
-                    if (!FULL) {
-                        d0 = okv[sub][0] ? d0 : 0.f;
-                        d1 = okv[sub][1] ? d1 : 0.f;
-                    }
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        // x = p*d split as hi (x with its low 13 mantissa bits cleared:
-                        // exact in fp16 when x is in fp16's normal range) + lo (x - hi,
-                        // exact in fp32, then rounded to fp16)
-                        const float x0 = s[sub][nt][0] * d0;
-                        const float x1 = s[sub][nt][1] * d1;
-                        const float h0 = __uint_as_float(__float_as_uint(x0) & 0xffffe000u);
-                        const float h1 = __uint_as_float(__float_as_uint(x1) & 0xffffe000u);
-                        bhi[nt][sub] = pack_half2(h0, h1);
-                        blo[nt][sub] = pack_half2(x0 - h0, x1 - h1);
-                    }
                     uint32_t r[2][2];
                     if (VT == KVQ_V_Q4_0) {
                         const uint4 &v = vv[sub][0];
@@ -669,25 +661,39 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
                     a[1][2 * sub + 1] = r[1][1];
                 }
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2)
+                for (int nt = 0; nt < NT; ++nt) {
+                    uint32_t bh[2], bl[2];   // [positions 0-7 / 8-15]
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        mma_f16_16816(acc[2 * bb + h2][nt], a[h2], bhi[nt][0], bhi[nt][1]);
-                        mma_f16_16816(acc[2 * bb + h2][nt], a[h2], blo[nt][0], blo[nt][1]);
+                    for (int pp = 0; pp < 2; ++pp) {
+                        // x = p*d split as hi (x with its low 13 mantissa bits cleared:
+                        // exact in fp16 when x is in fp16's normal range) + lo (x - hi,
+                        // exact in fp32, then rounded to fp16)
+                        const float2 x = mul2(s[nt][pp], make_float2(dv[pp][bb], dv[pp][bb]));
+                        const float2 h = make_float2(__uint_as_float(__float_as_uint(x.x) & 0xffffe000u),
+                                                     __uint_as_float(__float_as_uint(x.y) & 0xffffe000u));
+                        const float2 lo = sub2(x, h);
+                        bh[pp] = movmatrix_t(pack_half2(h.x, h.y));
+                        bl[pp] = movmatrix_t(pack_half2(lo.x, lo.y));
                     }
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        mma_f16_16816(acc[2 * bb + h2][nt], a[h2], bh[0], bh[1]);
+                        mma_f16_16816(acc[2 * bb + h2][nt], a[h2], bl[0], bl[1]);
+                    }
+                }
             }
         };
         if (full)
             chunk(std::integral_constant<bool, true>());
         else
             chunk(std::integral_constant<bool, false>());
+        }
     }
 
     if (bad) {
         // a wait gave up: wait (bounded) for this warp's copies still in flight,
         // then poison the CTA's results
-        for (int j = issued - (S - 1) > 0 ? issued - (S - 1) : 0; j < issued; ++j)
-            mbar_wait(bar_s + (j % S) * 8, (j / S) & 1);
+        for (int j = done; j < issued; ++j) mbar_wait(bar_s + (j % S) * 8, (j / S) & 1);
         if (lane == 0) {
             atomicOr(bad_flag, 1);
             atomicAdd(p.timeouts, 1u);
@@ -696,20 +702,25 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
     if constexpr (!DUMP) {
         // ---- merge the four warps' (m, l, acc) and write ----
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            l[nt] += __shfl_xor_sync(0xffffffffu, l[nt], 1);
-            l[nt] += __shfl_xor_sync(0xffffffffu, l[nt], 2);
-        }
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                l[nt][e] += __shfl_xor_sync(0xffffffffu, l[nt][e], 4);
+                l[nt][e] += __shfl_xor_sync(0xffffffffu, l[nt][e], 8);
+                l[nt][e] += __shfl_xor_sync(0xffffffffu, l[nt][e], 16);
+            }
         __syncthreads();   // every warp is done with the stage rings
         float *sm_m = reinterpret_cast<float *>(smem + C::ML_OFF);
         float *sm_l = sm_m + kWarps * 8 * NT;
         float *sm_o = reinterpret_cast<float *>(smem);   // [8*NT][kD]
-        if (c == 0)
+        if (g == 0)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                sm_m[warp * 8 * NT + 8 * nt + g] = m[nt];
-                sm_l[warp * 8 * NT + 8 * nt + g] = l[nt];
-            }
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    sm_m[warp * 8 * NT + 8 * nt + 2 * c + e] = m[nt][e];
+                    sm_l[warp * 8 * NT + 8 * nt + 2 * c + e] = l[nt][e];
+                }
         __syncthreads();
         // Merge in a fixed order so results do not depend on scheduling.  Each
         // (row, dim) belongs to one lane per warp; a warp's accumulator is
