@@ -89,7 +89,7 @@ struct SplitCfg {
     static constexpr int Q_OFF = WARPS * RING;                // int8 [QROWS][kD]
     static constexpr int QS_OFF = Q_OFF + QROWS * kD;         // fp32 [QROWS][kNB]
     static constexpr int QSUM_OFF = QS_OFF + QROWS * kNB * 4; // int32 [QROWS][kNB]
-    static constexpr int ML_OFF = QSUM_OFF + QROWS * kNB * 4; // fp32 m, l [WARPS][8*NT]
+    static constexpr int ML_OFF = QSUM_OFF + QROWS * kNB * 4; // fp32 m, l [WARPS][8*NT]; M, 1/L, lse [8*NT]
     // Per-lane query table, [chunk][lane][4 words] (16-byte chunks, lane-major
     // so a warp's LDS.128 of one chunk is conflict free): per (8-row tile nt,
     // block) the query MMA B fragments of both k16 steps and the accumulator
@@ -98,13 +98,14 @@ struct SplitCfg {
     static constexpr int SEED_CHUNKS = NT * kNB;
     static constexpr int SQ_CHUNKS = NT * 2;
     static constexpr int QF_CHUNKS = QB_CHUNKS + SEED_CHUNKS + SQ_CHUNKS;
-    static constexpr int QF_OFF = ML_OFF + 2 * WARPS * 8 * NT * 4;
+    static constexpr int QF_OFF = (ML_OFF + (2 * WARPS + 3) * 8 * NT * 4 + 15) / 16 * 16;
+    static constexpr int OROW = kD + 4;                        // merge slice row (floats, padded)
     static constexpr int TI_OFF = QF_OFF + QF_CHUNKS * 32 * 16;  // int4 tile record [WARPS][STAGES][TPS]
     static constexpr int NS_OFF = TI_OFF + WARPS * STAGES * TPS * 16;   // int tiles in stage [WARPS][STAGES]
     static constexpr int BAR_OFF = (NS_OFF + WARPS * STAGES * 4 + 7) / 8 * 8;   // uint64 mbarrier [WARPS][STAGES]
     static constexpr int FLAG_OFF = BAR_OFF + WARPS * STAGES * 8;
     static constexpr int SMEM = FLAG_OFF + 16;
-    static_assert(8 * NT * kD * 4 <= WARPS * RING, "merge buffer must fit in the stage rings");
+    static_assert(8 * NT * OROW * 4 <= WARPS * RING, "merge buffer must fit in the stage rings");
     static_assert(STAGE % 16 == 0 && KS_OFF % 16 == 0 && V_OFF % 16 == 0 && VS_OFF % 16 == 0, "16-byte granules");
     static_assert(TPS == 1 || TPS == 2, "one or two tiles per stage");
 };
@@ -405,32 +406,29 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
     // Query B fragments (fp16, exact codes).  Within block bb, k16 step ks, this
     // lane's k slots (2c, 2c+1 | 2c+8, 2c+9) carry head dims
     // 32bb + 8c + 4ks + (0, 1 | 2, 3): the bytes of word 8bb + 2c + ks, the same
-    // word the lane reads from K, so q.k is unchanged.  Warp 0 writes them, with
+    // word the lane reads from K, so q.k is unchanged.  The warps write them, with
     // the accumulator seeds (-1152 * sum of the row's codes in the block) of
     // rows 2c, 2c+1 and those rows' scales, to the per-lane table that every
     // stage reads back (row scales as (row 2c, row 2c+1) pairs per block).
     uint4 *qf = reinterpret_cast<uint4 *>(smem + C::QF_OFF) + lane;   // chunk k at qf[32 * k]
-    if (warp == 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-            for (int bb = 0; bb < kNB; ++bb) {
-                const uint32_t w0 = qw[(8 * nt + g) * (kD / 4) + 8 * bb + 2 * c];
-                const uint32_t w1 = qw[(8 * nt + g) * (kD / 4) + 8 * bb + 2 * c + 1];
-                qf[32 * (nt * kNB + bb)] = make_uint4(q_pair(w0, 0), q_pair(w0, 2), q_pair(w1, 0), q_pair(w1, 2));
-                const float s0 = -kBias * (float)qsum[(8 * nt + 2 * c) * kNB + bb];
-                const float s1 = -kBias * (float)qsum[(8 * nt + 2 * c + 1) * kNB + bb];
-                qf[32 * (C::QB_CHUNKS + nt * kNB + bb)] =
-                    make_uint4(__float_as_uint(s0), __float_as_uint(s1), __float_as_uint(s0), __float_as_uint(s1));
-            }
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {   // (row 2c, row 2c+1) scale pairs of blocks 2hb, 2hb+1
-                const int r0 = 8 * nt + 2 * c;
-                qf[32 * (C::QB_CHUNKS + C::SEED_CHUNKS + nt * 2 + hb)] =
-                    make_uint4(__float_as_uint(qs[r0 * kNB + 2 * hb]), __float_as_uint(qs[(r0 + 1) * kNB + 2 * hb]),
-                               __float_as_uint(qs[r0 * kNB + 2 * hb + 1]),
-                               __float_as_uint(qs[(r0 + 1) * kNB + 2 * hb + 1]));
-            }
+    // (nt, block) entries are spread over the warps: entry k goes to warp k % WARPS.
+    for (int k = warp; k < NT * kNB + NT * 2; k += kWarps) {
+        if (k < NT * kNB) {
+            const int nt = k / kNB, bb = k % kNB;
+            const uint32_t w0 = qw[(8 * nt + g) * (kD / 4) + 8 * bb + 2 * c];
+            const uint32_t w1 = qw[(8 * nt + g) * (kD / 4) + 8 * bb + 2 * c + 1];
+            qf[32 * (nt * kNB + bb)] = make_uint4(q_pair(w0, 0), q_pair(w0, 2), q_pair(w1, 0), q_pair(w1, 2));
+            const float s0 = -kBias * (float)qsum[(8 * nt + 2 * c) * kNB + bb];
+            const float s1 = -kBias * (float)qsum[(8 * nt + 2 * c + 1) * kNB + bb];
+            qf[32 * (C::QB_CHUNKS + nt * kNB + bb)] =
+                make_uint4(__float_as_uint(s0), __float_as_uint(s1), __float_as_uint(s0), __float_as_uint(s1));
+        } else {
+            // (row 2c, row 2c+1) scale pairs of blocks 2hb, 2hb+1
+            const int nt = (k - NT * kNB) / 2, hb = (k - NT * kNB) % 2;
+            const int r0 = 8 * nt + 2 * c;
+            qf[32 * (C::QB_CHUNKS + C::SEED_CHUNKS + nt * 2 + hb)] =
+                make_uint4(__float_as_uint(qs[r0 * kNB + 2 * hb]), __float_as_uint(qs[(r0 + 1) * kNB + 2 * hb]),
+                           __float_as_uint(qs[r0 * kNB + 2 * hb + 1]), __float_as_uint(qs[(r0 + 1) * kNB + 2 * hb + 1]));
         }
     }
     __syncthreads();   // query table visible
@@ -700,7 +698,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
         }
     }
     if constexpr (!DUMP) {
-        // ---- merge the four warps' (m, l, acc) and write ----
+        // ---- merge the warps' (m, l, acc) in a fixed order and write ----
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -710,22 +708,41 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
                 l[nt][e] += __shfl_xor_sync(0xffffffffu, l[nt][e], 16);
             }
         __syncthreads();   // every warp is done with the stage rings
-        float *sm_m = reinterpret_cast<float *>(smem + C::ML_OFF);
-        float *sm_l = sm_m + kWarps * 8 * NT;
-        float *sm_o = reinterpret_cast<float *>(smem);   // [8*NT][kD]
+        constexpr int RW = 8 * NT;                          // rows per warp state
+        float *sm_m = reinterpret_cast<float *>(smem + C::ML_OFF);   // [warp][RW]
+        float *sm_l = sm_m + kWarps * RW;
+        float *sm_M = sm_l + kWarps * RW, *sm_inv = sm_M + RW, *sm_lse = sm_inv + RW;   // [RW]
+        float *sm_o = reinterpret_cast<float *>(smem);      // slices [warp][RW][OROW]
         if (g == 0)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    sm_m[warp * 8 * NT + 8 * nt + 2 * c + e] = m[nt][e];
-                    sm_l[warp * 8 * NT + 8 * nt + 2 * c + e] = l[nt][e];
+                    sm_m[warp * RW + 8 * nt + 2 * c + e] = m[nt][e];
+                    sm_l[warp * RW + 8 * nt + 2 * c + e] = l[nt][e];
                 }
         __syncthreads();
-        // Merge in a fixed order so results do not depend on scheduling.  Each
-        // (row, dim) belongs to one lane per warp; a warp's accumulator is
-        // scaled by exp2(m_warp - M) for the row's overall max M.
-        constexpr bool kSlices = kWarps * 8 * NT * kD * 4 <= kWarps * C::RING;
+        if (tid < R) {   // row totals: M = max_w m_w, L = sum_w l_w 2^(m_w - M)
+            float M = -INFINITY;
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * RW + tid]);
+            float Lsum = 0.f;
+            for (int w = 0; w < kWarps; ++w) {
+                const float mw = sm_m[w * RW + tid];
+                if (mw != -INFINITY) Lsum += sm_l[w * RW + tid] * fast_exp2(mw - M);
+            }
+            float inv, lg;
+            asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(Lsum));
+            asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(Lsum));
+            const bool any = Lsum > 0.f;
+            sm_M[tid] = M;
+            sm_inv[tid] = any ? inv : 0.f;
+            sm_lse[tid] = any ? (M + lg) * 0.69314718055994531f : -INFINITY;
+        }
+        __syncthreads();
+        // Each (row, dim) belongs to one lane per warp; a warp's accumulator is
+        // scaled by 2^(m_warp - M) / L.  Head dims pv_dim(mt, g) and
+        // pv_dim(mt, g + 8) are adjacent, so a lane stores them as one pair.
+        constexpr bool kSlices = kWarps * RW * C::OROW * 4 <= kWarps * C::RING;
         auto put = [&](float *dst, bool add) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -733,64 +750,51 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
                 for (int e = 0; e < 2; ++e) {
                     const int row = 8 * nt + 2 * c + e;
                     if (row >= R) continue;
-                    float M = -INFINITY;
-#pragma unroll
-                    for (int v = 0; v < kWarps; ++v) M = fmaxf(M, sm_m[v * 8 * NT + row]);
-                    const float mw = sm_m[warp * 8 * NT + row];
-                    const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
+                    const float mw = m[nt][e];
+                    const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - sm_M[row]) * sm_inv[row];
 #pragma unroll
                     for (int mt = 0; mt < 8; ++mt) {
-                        float *o0 = &dst[row * kD + pv_dim<VT>(mt, g)];
-                        float *o1 = &dst[row * kD + pv_dim<VT>(mt, g + 8)];
-                        *o0 = (add ? *o0 : 0.f) + acc[mt][nt][e] * f;
-                        *o1 = (add ? *o1 : 0.f) + acc[mt][nt][2 + e] * f;
+                        float2 *o = reinterpret_cast<float2 *>(&dst[row * C::OROW + pv_dim<VT>(mt, g)]);
+                        float2 v = make_float2(acc[mt][nt][e] * f, acc[mt][nt][2 + e] * f);
+                        if (add) {
+                            const float2 q = *o;
+                            v.x += q.x;
+                            v.y += q.y;
+                        }
+                        *o = v;
                     }
                 }
         };
         if (kSlices) {
-            // every warp writes its own slice, then the slices are added 0..3
-            put(sm_o + warp * 8 * NT * kD, false);
-            __syncthreads();
-            for (int i = tid; i < R * kD; i += kThreads) {
-                float t = sm_o[i];
-#pragma unroll
-                for (int w = 1; w < kWarps; ++w) t += sm_o[w * 8 * NT * kD + i];
-                sm_o[i] = t;
-            }
+            put(sm_o + warp * RW * C::OROW, false);
             __syncthreads();
         } else {
-            // warp 0 stores, warps 1..3 add in turn
+            // warp 0 stores, the others add in turn
             for (int w = 0; w < kWarps; ++w) {
                 if (warp == w) put(sm_o, w > 0);
                 __syncthreads();
             }
         }
         const bool poisoned = *bad_flag != 0;   // set before the merge's first barrier
-        for (int i0 = tid; i0 < R * kD; i0 += kThreads) {
-            const int row = i0 / kD, d = i0 % kD;
-            float M = -INFINITY;
+        for (int i4 = tid; i4 < R * (kD / 4); i4 += kThreads) {
+            const int row = i4 / (kD / 4), d = (i4 % (kD / 4)) * 4;
+            float4 t = *reinterpret_cast<const float4 *>(&sm_o[row * C::OROW + d]);
+            if (kSlices) {
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * 8 * NT + row]);
-            float Lsum = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float mw = sm_m[w * 8 * NT + row];
-                if (mw != -INFINITY) Lsum += sm_l[w * 8 * NT + row] * fast_exp2(mw - M);
+                for (int w = 1; w < kWarps; ++w) {
+                    const float4 q = *reinterpret_cast<const float4 *>(&sm_o[(w * RW + row) * C::OROW + d]);
+                    t.x += q.x; t.y += q.y; t.z += q.z; t.w += q.w;
+                }
             }
+            float ls = sm_lse[row];
+            if (poisoned) t.x = t.y = t.z = t.w = ls = __int_as_float(0x7fc00000);   // NaN: the CTA lost a stage
             const int i = row / gsz, hq = p.grp_q[gb + row % gsz];
             const size_t orow = ((size_t)b * G.t_q + i) * G.n_q_heads + hq;
-            const bool any = Lsum > 0.f;
-            float inv, lg;
-            asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(Lsum));
-            asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(Lsum));
-            float o = any ? sm_o[row * kD + d] * inv : 0.f;
-            float ls = any ? (M + lg) * 0.69314718055994531f : -INFINITY;
-            if (poisoned) o = ls = __int_as_float(0x7fc00000);   // NaN: the CTA lost a stage
             if (G.n_split == 1) {
-                G.out[orow * kD + d] = o;
+                *reinterpret_cast<float4 *>(G.out + orow * kD + d) = t;
                 if (d == 0) G.lse[orow] = ls;
             } else {
-                G.ws_o[(orow * G.n_split + split) * kD + d] = o;
+                *reinterpret_cast<float4 *>(G.ws_o + (orow * G.n_split + split) * kD + d) = t;
                 if (d == 0) G.ws_lse[orow * G.n_split + split] = ls;
             }
         }
