@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="time budget of the reference arm (warm-up + timed steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--mode", default="bench", choices=["bench", "profile"],
                     help="profile: one cache copy, a few directly launched steps, no timing (for ncu)")
@@ -68,6 +70,20 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def job_rate(ms_local, world, steps, tokens_per_step, device=None):
+    """Whole-job timing across ranks: the max of the ranks' timed milliseconds
+    (all-reduce MAX when world > 1) -> (ms per step, tokens/s of all ranks)."""
+    ms = float(ms_local)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / steps
+    return ms_per_step, tokens_per_step * world / (ms_per_step * 1e-3)
 
 
 def measured_peaks():
@@ -172,9 +188,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ oracle --
 
-def run_oracle(specs_data, seconds, threads):
-    """The fp64 oracle on the host: quantize the caches (untimed), then time
-    whole decode steps over all caches until `seconds` have passed."""
+def _oracle_caches(specs_data):
     import oracle
     caches = []
     for d in specs_data:
@@ -182,6 +196,14 @@ def run_oracle(specs_data, seconds, threads):
         for b in range(s.n_seqs):
             k, v = d.kv[b]
             caches.append((s, b, oracle.quantize_kv(k, v, s.v_type), d.q[b]))
+    return caches
+
+
+def run_oracle(specs_data, seconds, threads):
+    """The fp64 oracle on the host: quantize the caches (untimed), then time
+    whole decode steps over all caches until `seconds` have passed."""
+    import oracle
+    caches = _oracle_caches(specs_data)
     tokens_per_step = sum(d.spec.n_seqs * d.spec.t_q for d in specs_data)
     n = 0
     t0 = time.perf_counter()
@@ -194,6 +216,49 @@ def run_oracle(specs_data, seconds, threads):
         if el >= seconds:
             break
     return tokens_per_step * n / el, n, el
+
+
+def run_oracle_rows(specs_data, steps, warmup, threads, budget_s):
+    """Reference arm: the oracle on a bounded sample of the workload.  A step
+    decodes `threads` query rows (cycling over every row of every cache, one
+    OpenMP thread per row); a whole decode step of the workload is all its rows,
+    so tokens/s = rows done * (tokens per step / rows per step) / seconds.
+    Warm-up and timed steps stop early when the time budget is spent."""
+    import oracle
+    caches = _oracle_caches(specs_data)
+    rows = [(ci, r) for ci, (s, b, c, q) in enumerate(caches) for r in range(s.t_q * s.n_q_heads)]
+    tokens_per_step = sum(d.spec.n_seqs * d.spec.t_q for d in specs_data)
+    pos = 0
+
+    def one_step():
+        nonlocal pos
+        pick = [rows[(pos + i) % len(rows)] for i in range(min(threads, len(rows)))]
+        pos = (pos + len(pick)) % len(rows)
+        by_cache = {}
+        for ci, r in pick:
+            by_cache.setdefault(ci, []).append(r)
+        for ci, rs in by_cache.items():
+            s, b, c, q = caches[ci]
+            mask = np.zeros(s.t_q * s.n_q_heads, np.uint8)
+            mask[rs] = 1
+            oracle.decode_seq(c, q, oracle.default_head_map(s.n_q_heads, s.n_kv_heads), s.causal,
+                              1.0 / np.sqrt(128.0), s.v_type, row_mask=mask, n_threads=threads)
+        return len(pick)
+
+    t_start = time.perf_counter()
+    w = 0
+    while w < warmup and time.perf_counter() - t_start < 0.2 * budget_s:
+        one_step()
+        w += 1
+    n, done_rows = 0, 0
+    t0 = time.perf_counter()
+    while n < max(1, steps):
+        done_rows += one_step()
+        n += 1
+        if time.perf_counter() - t0 >= 0.8 * budget_s:
+            break
+    el = time.perf_counter() - t0
+    return done_rows * tokens_per_step / len(rows) / el, n, w, el, done_rows, len(rows)
 
 
 # ---------------------------------------------------------------- GPU arm --
@@ -215,14 +280,16 @@ def main():
         import oracle
         oracle.build()
         data = [HostData(s) for s in specs]
-        secs = max(1.0, args.cpu_seconds)
-        tps, n, el = run_oracle(data, secs, threads)
+        tps, n, w, el, done_rows, n_rows = run_oracle_rows(data, args.steps, args.warmup, threads,
+                                                           max(10.0, args.ref_seconds))
+        sample = ("%d steps of %d query rows each (%d of the workload's %d rows per decode step, cycling), "
+                  "fp64 oracle, OpenMP over rows, %.1f s timed" % (n, min(threads, n_rows), done_rows, n_rows, el))
         line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus,
-                "steps": n, "warmup": 0, "ms_per_step": 1e3 * el / n, "higher_is_better": True,
+                "steps": n, "warmup": w, "ms_per_step": 1e3 * el / n, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": WORKLOADS[args.workload], "oracle_threads": threads},
                 "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                                 "sample": "%d whole decode steps of the workload (%.1f s)" % (n, el)},
+                                 "sample": sample},
                 "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -337,12 +404,7 @@ def main():
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    ms_per_step = ms / steps
+    ms_per_step, value = job_rate(e0.elapsed_time(e1), world, steps, tokens_per_step, dev)
 
     # ---- one decode call per cache instead of the fused call (same steps) ----
     sreps = max(1, min(reps, 2000 // n_rot))
@@ -420,8 +482,7 @@ def main():
 
     if rank != 0:
         return
-    value = tokens_per_step * world / (ms_per_step * 1e-3)
-    kv_gbs = kv_bytes / (ms_per_step * 1e-3) / 1e9
+    kv_gbs = kv_bytes / (ms_per_step * 1e-3) / 1e9   # per GPU
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
         "warmup": warm * n_rot, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
