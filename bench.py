@@ -2,9 +2,11 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long] [--impl reference]
 
-A step = one pass of the whole decode path over one batch: kvq_append of the
-newest token(s) of every cache, then kvq_decode_attn (split-KV attention +
-log-sum-exp combine) of every cache.  The default workload is the long-context
+A step = one pass of the whole decode path over one batch: the newest token(s)
+of every cache are appended and every cache is decoded, by one
+kvq_decode_attn_multi call with the appends fused into the attention kernel
+(split-KV attention + log-sum-exp combine).  The same step through kvq_append
+and kvq_decode_attn per cache is timed beside it.  The default workload is the long-context
 decode: a main cache (40 query / 8 kv heads) and a draft cache (16 / 4), each
 131072 positions built in 4 append-only segments, q4_0 V, one query token each.
 
@@ -106,13 +108,14 @@ def kernel_source_hash():
 
 
 def launches_of(grp, fused):
-    """Kernels one step launches: one append per cache, then the fused decode's
-    split kernel (one per launch group of <= 64 sequences / 64 segments / 8
-    work groups) and, when any sequence is split, its combine."""
+    """Kernels one step launches: the fused call's split kernel (one per launch
+    group of <= 64 sequences / 64 segments / 8 work groups; the appends run
+    inside it) and, when any sequence is split, its combine; plus one append
+    per cache when the appends are not fused."""
     seqs = sum(ds.B for ds in grp)
     segs = sum(len(x) for ds in grp for x in ds.spec.segments)
     groups = max(-(-seqs // 64), -(-segs // 64), -(-len(grp) // 8))
-    return len(grp) + groups * (2 if fused.call.ws is not None else 1)
+    return (0 if fused.append else len(grp)) + groups * (2 if fused.call.ws is not None else 1)
 
 
 def profiled_traffic(workload):
@@ -311,10 +314,8 @@ def main():
         grp = [DecodeSet(d, dev) for d in data]
         for ds in grp:
             ds.staging = None
-        fused = StepSet(grp)
+        fused = StepSet(grp, append=True)
         for _ in range(max(1, args.warmup) + max(1, args.steps)):
-            for ds in grp:
-                ds.append_step()
             fused.decode()
             for ds in grp:
                 ds.rewind()
@@ -335,19 +336,20 @@ def main():
         for ds in grp:
             ds.staging = None
     torch.cuda.synchronize()
-    fused = [StepSet(grp) for grp in sets]
+    fused = [StepSet(grp, append=True) for grp in sets]
     launches_per_step = launches_of(sets[0], fused[0])
 
     stream = torch.cuda.Stream(device=dev)
 
     def step(grp, fz=None):
-        """One step: append every cache's new tokens, decode all caches (one
-        fused call, or one call per cache when fz is None), rewind."""
-        for ds in grp:
-            ds.append_step(stream=stream)
+        """One step: append every cache's new tokens and decode all caches --
+        one kvq_decode_attn_multi call with the appends fused (fz), or per cache
+        a kvq_append and a kvq_decode_attn (fz None) -- then rewind."""
         if fz is not None:
             fz.decode(stream=stream)
         else:
+            for ds in grp:
+                ds.append_step(stream=stream)
             for ds in grp:
                 ds.decode(stream=stream)
         for ds in grp:
@@ -363,7 +365,7 @@ def main():
     with torch.cuda.graph(g_all, stream=stream):
         for grp, fz in zip(sets, fused):
             step(grp, fz)
-    # the same steps with one decode call per cache (reported beside the fused number)
+    # the same steps through kvq_append + kvq_decode_attn per cache (reported beside the fused number)
     g_sep = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_sep, stream=stream):
         for grp in sets:
@@ -375,8 +377,6 @@ def main():
                  torch.cuda.Event(enable_timing=True, external=True)) for _ in sets]
     with torch.cuda.graph(g_ev, stream=stream):
         for grp, fz, (a, b) in zip(sets, fused, ev_pairs):
-            for ds in grp:
-                ds.append_step(stream=stream)
             a.record(stream)
             fz.decode(stream=stream)
             b.record(stream)
@@ -442,15 +442,13 @@ def main():
               for a, b, c in h_in)
     d2h = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in h_out)
 
-    e2e_call = StepSet(grp, q16=[dq for dq, _, _ in d_in])
+    e2e_call = StepSet(grp, q16=[dq for dq, _, _ in d_in], append=True, kv_new=[(dk, dv) for _, dk, dv in d_in])
 
     def e2e_step():
         for (hq, hk, hv), (dq, dk, dv) in zip(h_in, d_in):
             dq.copy_(hq, non_blocking=True)
             dk.copy_(hk, non_blocking=True)
             dv.copy_(hv, non_blocking=True)
-        for ds, (dq, dk, dv) in zip(grp, d_in):
-            ds.append_step(dk, dv, stream=stream)
         e2e_call.decode(stream=stream)
         for ds, (ho, hl) in zip(grp, h_out):
             ho.copy_(ds.out, non_blocking=True)
@@ -493,7 +491,7 @@ def main():
                    "kv_bytes_per_step": kv_bytes, "tokens_per_step": tokens_per_step},
         "kv_gbs": kv_gbs, "kv_frac_of_8tbs": kv_gbs / NOMINAL_HBM_GBS,
         "kv_frac_of_measured_copy": kv_gbs / peak,
-        "roofline": {"bound": "hbm", "kernel": "split_attn (+ its combine), all caches in one launch",
+        "roofline": {"bound": "hbm", "kernel": "split_attn with fused append (+ its combine), all caches in one launch",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
                      "traffic": profiled_traffic(args.workload),

@@ -197,7 +197,18 @@ kvq_status kvq_decode_workspace_size(const kvq_cache *c, int32_t n_q_heads, int3
 
 /*
  * One decode call for kvq_decode_attn_multi: the arguments of kvq_decode_attn
- * that belong to one cache, with the same meaning and rules.
+ * that belong to one cache, with the same meaning and rules, plus an optional
+ * fused append:
+ *  k16_new, v16_new  NULL, or device fp16 [n_seqs][t_q][n_kv_heads][head_dim]
+ *            (16-byte aligned): the step's t_q new tokens of every sequence.
+ *            The call then does what kvq_append of these tokens followed by
+ *            the decode would do, in the attention kernel itself: the tokens
+ *            are quantized by the append rules and stored at the end of each
+ *            sequence's open segment, and the decode sees them.  Every
+ *            sequence needs an open segment with room for t_q more tokens
+ *            (else KVQ_ERR_CAPACITY, nothing enqueued); seq_lens must already
+ *            count the new tokens; the host len of each open segment grows by
+ *            t_q when the call succeeds.
  */
 typedef struct kvq_decode_desc {
     const kvq_cache *cache;
@@ -211,6 +222,8 @@ typedef struct kvq_decode_desc {
     float sm_scale;
     float *out;
     float *lse;
+    const void *k16_new;
+    const void *v16_new;
 } kvq_decode_desc;
 
 /*
@@ -223,8 +236,8 @@ typedef struct kvq_decode_desc {
  * calls together, so the GPU fills with the calls' positions at once.
  *  calls      host array [n] (read during the call only).
  *  workspace  as kvq_decode_attn, at least kvq_decode_multi_workspace_size().
- * Errors: as kvq_decode_attn, checked for every call before anything is
- * enqueued.  The pages describe single-cache decode only; fusing calls is the
+ * Errors: as kvq_decode_attn (and kvq_append for a fused append), checked for
+ * every call before anything is enqueued.  The pages describe single-cache decode only; fusing calls is the
  * library's own launch plan.
  */
 kvq_status kvq_decode_attn_multi(int32_t n, const kvq_decode_desc *calls, void *workspace,

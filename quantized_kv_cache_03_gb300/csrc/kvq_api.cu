@@ -122,6 +122,7 @@ struct Desc {
     int8_t *dbg_qc;
     uint16_t *dbg_qs;
     int32_t *dbg_scores;
+    const uint16_t *k_new, *v_new;   // fused append of t_q tokens per sequence, or null
     std::vector<int> kv;   // query head -> kv head
     int max_rows;          // query rows of the busiest kv head
 };
@@ -153,6 +154,15 @@ kvq_status prepare_desc(Desc &d, const int32_t *head_map, bool need_ptrs, bool d
     for (int k = 0; k < H; ++k) gmax = std::max(gmax, cnt[k]);
     d.max_rows = gmax * d.t_q;
     if (d.max_rows > KVQ_MAX_ROWS) return KVQ_ERR_UNSUPPORTED;
+    if ((d.k_new != nullptr) != (d.v_new != nullptr)) return KVQ_ERR_INVALID_ARG;
+    if (d.k_new) {
+        if (dump || !aligned16(d.k_new) || !aligned16(d.v_new)) return KVQ_ERR_INVALID_ARG;
+        for (int b = 0; b < c->n_seqs; ++b) {
+            if (c->n_segs[b] < 1) return KVQ_ERR_INVALID_ARG;   // no open segment
+            const kvq_segment &sl = seg_of(c, b, c->n_segs[b] - 1);
+            if ((long long)sl.len + d.t_q > sl.cap) return KVQ_ERR_CAPACITY;
+        }
+    }
     if (need_ptrs && c->n_seqs > 0) {
         if (!d.q || !aligned16(d.q) || !d.seq_lens) return KVQ_ERR_INVALID_ARG;
         if (dump ? (!d.dbg_qc || !d.dbg_qs || !d.dbg_scores) : (!d.out || !d.lse)) return KVQ_ERR_INVALID_ARG;
@@ -330,6 +340,11 @@ void fill_launch(const std::vector<Desc> &ds, const Launch &ln, bool dump, void 
         const size_t rows_per_seq = (size_t)d.t_q * d.n_q_heads;
         const size_t r0 = (size_t)u.b0 * rows_per_seq;
         G.q = d.q ? d.q + r0 * kD : nullptr;
+        if (d.k_new) {
+            const size_t t0 = (size_t)u.b0 * d.t_q * c->n_kv_heads * kD;
+            G.k_new = d.k_new + t0;
+            G.v_new = d.v_new + t0;
+        }
         G.seq_lens = d.seq_lens ? d.seq_lens + u.b0 : nullptr;
         G.cta0 = u.cta0;
         G.seq0 = nseq;
@@ -368,6 +383,10 @@ void fill_launch(const std::vector<Desc> &ds, const Launch &ln, bool dump, void 
             const int b = u.b0 + i;
             p.seq_seg0[nseq] = (uint8_t)nseg;
             p.seq_nseg[nseq] = (uint8_t)c->n_segs[b];
+            if (c->n_segs[b] > 0) {
+                const kvq_segment &sl = seg_of(c, b, c->n_segs[b] - 1);
+                p.app_pos[nseq] = sl.pos0 + sl.len;
+            }
             ++nseq;
             for (int k = 0; k < c->n_segs[b]; ++k, ++nseg) {
                 const kvq_segment &s = seg_of(c, b, k);
@@ -422,6 +441,10 @@ kvq_status run(std::vector<Desc> &ds, bool dump, void *workspace, size_t workspa
             return KVQ_ERR_CUDA;
         }
     }
+    for (const Desc &d : ds)   // fused appends: the open segments grew
+        if (d.k_new)
+            for (int b = 0; b < d.c->n_seqs; ++b)
+                const_cast<kvq_cache *>(d.c)->segs[(size_t)b * d.c->max_segs + d.c->n_segs[b] - 1].len += d.t_q;
     return KVQ_OK;
 }
 
@@ -439,6 +462,8 @@ kvq_status to_desc(const kvq_decode_desc &x, bool need_ptrs, Desc &d)
     d.sm_scale = x.sm_scale;
     d.out = x.out;
     d.lse = x.lse;
+    d.k_new = static_cast<const uint16_t *>(x.k16_new);
+    d.v_new = static_cast<const uint16_t *>(x.v16_new);
     return prepare_desc(d, x.head_map, need_ptrs, false);
 }
 
@@ -532,14 +557,16 @@ kvq_status kvq_decode_attn(const kvq_cache *c, const void *q16, int32_t n_q_head
                            const int32_t *head_map, float sm_scale, float *out, float *lse, void *workspace,
                            size_t workspace_bytes, void *stream)
 {
-    const kvq_decode_desc x{c, q16, n_q_heads, t_q, causal_tail, seq_lens, max_len, head_map, sm_scale, out, lse};
+    const kvq_decode_desc x{c, q16, n_q_heads, t_q, causal_tail, seq_lens, max_len, head_map, sm_scale, out, lse,
+                            nullptr, nullptr};
     return kvq_decode_attn_multi(1, &x, workspace, workspace_bytes, stream);
 }
 
 kvq_status kvq_decode_workspace_size(const kvq_cache *c, int32_t n_q_heads, int32_t t_q, int32_t max_len,
                                      const int32_t *head_map, size_t *bytes)
 {
-    const kvq_decode_desc x{c, nullptr, n_q_heads, t_q, 0, nullptr, max_len, head_map, 1.0f, nullptr, nullptr};
+    const kvq_decode_desc x{c, nullptr, n_q_heads, t_q, 0, nullptr, max_len, head_map, 1.0f, nullptr, nullptr,
+                            nullptr, nullptr};
     return kvq_decode_multi_workspace_size(1, &x, bytes);
 }
 

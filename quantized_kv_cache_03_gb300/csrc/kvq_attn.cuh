@@ -102,12 +102,14 @@ struct SplitCfg {
     static constexpr int OROW = kD + 4;                        // merge slice row (floats, padded)
     static constexpr int TI_OFF = QF_OFF + QF_CHUNKS * 32 * 16;  // int4 tile record [WARPS][STAGES][TPS]
     static constexpr int NS_OFF = TI_OFF + WARPS * STAGES * TPS * 16;   // int tiles in stage [WARPS][STAGES]
-    static constexpr int BAR_OFF = (NS_OFF + WARPS * STAGES * 4 + 7) / 8 * 8;   // uint64 mbarrier [WARPS][STAGES]
+    static constexpr int NEW_OFF = (NS_OFF + WARPS * STAGES * 4 + 15) / 16 * 16;  // appended rows [KVQ_MAX_T_Q][32 lanes][3 words]
+    static constexpr int BAR_OFF = NEW_OFF + KVQ_MAX_T_Q * 32 * 12;                 // uint64 mbarrier [WARPS][STAGES]
     static constexpr int FLAG_OFF = BAR_OFF + WARPS * STAGES * 8;
     static constexpr int SMEM = FLAG_OFF + 16;
     static_assert(8 * NT * OROW * 4 <= WARPS * RING, "merge buffer must fit in the stage rings");
     static_assert(STAGE % 16 == 0 && KS_OFF % 16 == 0 && V_OFF % 16 == 0 && VS_OFF % 16 == 0, "16-byte granules");
     static_assert(TPS == 1 || TPS == 2, "one or two tiles per stage");
+    static_assert(SMEM <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
 };
 
 // The pieces of a sequence's segments that fall in [r0, r1), walked in order
@@ -360,6 +362,33 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
         return;
     }
 
+    // ---- tokens this call appends that fall in this split (fused append):
+    // quantized by the append rules, stored to the open segment for later calls
+    // and kept in shared memory to patch into this call's staged tiles ----
+    int na0 = 0, nn = 0;   // absolute positions [na0, na0 + nn)
+    uint32_t *newrow = reinterpret_cast<uint32_t *>(smem + C::NEW_OFF);
+    if (G.k_new != nullptr) {
+        const int ap = p.app_pos[G.seq0 + b];
+        const int lo = max(ap, r0), hi = min(ap + G.t_q, r0 + G.chunk);
+        if (lo < hi) {
+            na0 = lo;
+            nn = hi - lo;
+        }
+        const SegDesc &sl = p.seg[seg0 + nseg - 1];   // the open segment
+        for (int i = warp; i < nn; i += kWarps) {
+            const size_t src = (((size_t)b * G.t_q + (na0 + i - ap)) * G.n_kv_heads + h) * kD;
+            const TokenRow t = quant_token<VT>(G.k_new + src, G.v_new + src, lane);
+            const int local = na0 + i - sl.pos0, u = local % kWTile;
+            const size_t tile = (size_t)h * sl.cap + local - u;
+            store_token<VT>(t, u, lane, const_cast<uint8_t *>(sl.kq) + tile * kD,
+                            const_cast<uint16_t *>(sl.ks) + (tile + u) * kNB,
+                            const_cast<uint8_t *>(sl.vq) + tile * C::VCODE, const_cast<uint16_t *>(sl.vs) + (tile + u) * kNB);
+            newrow[(i * 32 + lane) * 3 + 0] = t.kw;
+            newrow[(i * 32 + lane) * 3 + 1] = t.vw;
+            newrow[(i * 32 + lane) * 3 + 2] = (uint32_t)t.ks | ((uint32_t)t.vs << 16);
+        }
+    }
+
     // ---- quantize the query rows of this kv head (int8 rule, fp16 scale) ----
     uint32_t *qw = reinterpret_cast<uint32_t *>(smem + C::Q_OFF);
     float *qs = reinterpret_cast<float *>(smem + C::QS_OFF);
@@ -487,6 +516,23 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
         const int tb = rec.x, la = rec.y, le = rec.z, pos_base = rec.w;
         // every position of the tile valid and visible to every live row?
         const bool full = tb >= la && tb + kWTile <= le && pos_base + kWTile - 1 <= lim_min;
+        if (nn > 0 && pos_base < na0 + nn && pos_base + kWTile > na0) {
+            // this call's appended tokens: the staged copy may predate their
+            // store, so write their rows into the stage
+            for (int a = max(na0, pos_base); a < min(na0 + nn, pos_base + kWTile); ++a) {
+                const int i = a - na0;
+                TokenRow t;
+                t.kw = newrow[(i * 32 + lane) * 3 + 0];
+                t.vw = newrow[(i * 32 + lane) * 3 + 1];
+                const uint32_t sv = newrow[(i * 32 + lane) * 3 + 2];
+                t.ks = (uint16_t)(sv & 0xffffu);
+                t.vs = (uint16_t)(sv >> 16);
+                const int u = a - pos_base;
+                store_token<VT>(t, u, lane, const_cast<uint8_t *>(stK), reinterpret_cast<uint16_t *>(const_cast<uint8_t *>(stKS)) + u * kNB,
+                                const_cast<uint8_t *>(stV), reinterpret_cast<uint16_t *>(const_cast<uint8_t *>(stVS)) + u * kNB);
+            }
+            __syncwarp();
+        }
 
         auto chunk = [&](auto full_tag) {
             constexpr bool FULL = decltype(full_tag)::value;

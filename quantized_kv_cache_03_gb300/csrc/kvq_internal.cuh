@@ -86,6 +86,7 @@ struct GroupDesc {
     int8_t *dbg_qc;                        // test hook outputs (DUMP kernels only)
     uint16_t *dbg_qs;
     int32_t *dbg_scores;
+    const uint16_t *k_new, *v_new;         // [n_seqs][t_q][Hkv][kD] fp16 tokens appended by this call, or null
     int cta0;                              // first CTA of the group
     int seq0;                              // first entry of seq_seg0 / seq_nseg
     int head0;                             // first entry of grp_begin (this cache's kv heads)
@@ -102,6 +103,7 @@ struct AttnParams {
     SegDesc seg[kMaxSegsLaunch];
     uint8_t seq_seg0[kMaxSeqsLaunch];      // first table entry of each sequence
     uint8_t seq_nseg[kMaxSeqsLaunch];
+    int app_pos[kMaxSeqsLaunch];           // absolute position of a sequence's first appended token
     uint16_t grp_q[kMaxHeadTab];           // query heads listed kv head by kv head
     uint16_t grp_begin[kMaxHeadTab + kMaxGroups];   // kv head h of group g owns
                                            // grp_q[grp_begin[head0 + h] .. grp_begin[head0 + h + 1])
@@ -296,6 +298,93 @@ __device__ __forceinline__ int quant_q4(float x, float d)
     if (d == 0.f) return 8;
     float c = roundf(__fdiv_rn(x, d)) + 8.f;
     return (int)fminf(fmaxf(c, 0.f), 15.f);
+}
+
+
+// ---- one (token, kv head) row through the append rules (warp-wide) ----
+// Lane l holds elements 4l..4l+3, so lanes 8b..8b+7 hold 32-block b and a
+// 3-step xor shuffle gives the block absmax.
+__device__ __forceinline__ float block_absmax(const float (&x)[4])
+{
+    float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+    return a;
+}
+
+__device__ __forceinline__ void load4h(const uint16_t *p, float (&x)[4])
+{
+    const uint2 raw = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
+}
+
+// int8 rule on one row: returns this lane's packed word and the block scale bits.
+__device__ __forceinline__ uint32_t quant_row_i8(const float (&x)[4], uint16_t &s16)
+{
+    const float a = block_absmax(x);
+    const __half sh = __float2half_rn(__fdiv_rn(a, 127.f));
+    const float s = __half2float(sh);
+    s16 = __half_as_ushort(sh);
+    uint32_t w = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w |= (uint32_t)(quant_i8(x[k], s) & 0xff) << (8 * k);
+    return w;
+}
+
+// A quantized (token, kv head) row as the lanes hold it: kw = K codes 4l..4l+3;
+// ks = block (l/8) K scale bits; vw = q8_0 codes 4l..4l+3, or for q4_0 lanes
+// with l%8 < 4 the code bytes 4(l%4)..+3 of block l/8 (byte j = q[j] | q[j+16] << 4);
+// vs = block (l/8) V scale bits.
+struct TokenRow {
+    uint32_t kw, vw;
+    uint16_t ks, vs;
+};
+
+template <int VT>
+__device__ __forceinline__ TokenRow quant_token(const uint16_t *k_row, const uint16_t *v_row, int lane)
+{
+    TokenRow t;
+    float x[4];
+    load4h(k_row + lane * 4, x);
+    t.kw = quant_row_i8(x, t.ks);
+    load4h(v_row + lane * 4, x);
+    if (VT == KVQ_V_Q8_0) {
+        t.vw = quant_row_i8(x, t.vs);
+    } else {
+        const float a = block_absmax(x);
+        const __half dh = __float2half_rn(a * 0.125f);   // absmax/8, exact before rounding
+        const float d = __half2float(dh);
+        uint32_t q = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) q |= (uint32_t)quant_q4(x[k], d) << (8 * k);
+        const uint32_t qhi = __shfl_down_sync(0xffffffffu, q, 4);   // elements 16.. of the block
+        t.vw = q | (qhi << 4);
+        t.vs = __half_as_ushort(dh);
+    }
+    return t;
+}
+
+// Store a quantized row at tile position u of the code tiles kt / vt (K codes,
+// V codes) and at scale rows ksr / vsr (4 fp16 each), in the cache's tile order.
+// Works for a tile in global memory and for a staged copy in shared memory.
+template <int VT>
+__device__ __forceinline__ void store_token(const TokenRow &t, int u, int lane, uint8_t *kt, uint16_t *ksr,
+                                            uint8_t *vt, uint16_t *vsr)
+{
+    *reinterpret_cast<uint32_t *>(kt + k_tile_off(u, 4 * lane)) = t.kw;
+    if ((lane & 7) == 0) ksr[lane >> 3] = t.ks;
+    if (VT == KVQ_V_Q8_0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) vt[v8_tile_off(u, 4 * lane + k)] = (uint8_t)(t.vw >> (8 * k));
+    } else if ((lane & 7) < 4) {
+        const int j = 16 * (lane >> 3) + 4 * (lane & 3);
+        *reinterpret_cast<uint16_t *>(vt + v4_tile_off(u, j)) = (uint16_t)t.vw;
+        *reinterpret_cast<uint16_t *>(vt + v4_tile_off(u, j + 2)) = (uint16_t)(t.vw >> 16);
+    }
+    if ((lane & 7) == 0) vsr[lane >> 3] = t.vs;
 }
 
 }  // namespace kvq

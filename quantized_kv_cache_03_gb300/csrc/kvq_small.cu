@@ -4,45 +4,14 @@
 namespace kvq {
 
 // ---------------------------------------------------------------------------
-// Append-quantize.  One warp per (token, kv head) row of 128 fp16 values: lane
-// l holds elements 4l..4l+3 (one 8-byte load), so lanes 8b..8b+7 hold 32-block
-// b and a 3-step xor shuffle gives the block absmax.  Codes go to their place
-// in the position's 16-position tile (k_tile_off / v4_tile_off / v8_tile_off):
-// a K lane's four codes stay one word; q4_0 lanes 0..3 of each block pull the
-// codes of elements 16.. from lanes 4..7, form bytes j = q[j] | q[j+16] << 4 and
-// store them as two byte pairs; q8_0 codes are stored byte by byte (the tile
+// Append-quantize.  One warp per (token, kv head) row of 128 fp16 values
+// (quant_token / store_token): codes go to their place in the position's
+// 16-position tile (k_tile_off / v4_tile_off / v8_tile_off): a K lane's four
+// codes stay one word; q4_0 lanes 0..3 of each block pull the codes of
+// elements 16.. from lanes 4..7, form bytes j = q[j] | q[j+16] << 4 and store
+// them as two byte pairs; q8_0 codes are stored byte by byte (the tile
 // interleaves neighbouring positions).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float block_absmax(const float (&x)[4])
-{
-    float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-    return a;
-}
-
-__device__ __forceinline__ void load4h(const uint16_t *p, float (&x)[4])
-{
-    const uint2 raw = *reinterpret_cast<const uint2 *>(p);
-    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
-}
-
-// int8 rule on one row: returns this lane's packed word and the block scale bits.
-__device__ __forceinline__ uint32_t quant_row_i8(const float (&x)[4], uint16_t &s16)
-{
-    const float a = block_absmax(x);
-    const __half sh = __float2half_rn(__fdiv_rn(a, 127.f));
-    const float s = __half2float(sh);
-    s16 = __half_as_ushort(sh);
-    uint32_t w = 0;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) w |= (uint32_t)(quant_i8(x[k], s) & 0xff) << (8 * k);
-    return w;
-}
-
 template <int VT>
 __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ AppendParams p)
 {
@@ -54,43 +23,12 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
     const int row = blockIdx.x * 4 + warp;
     const int tok = row / H, h = row - tok * H;
     if (tok >= e.n) return;   // warp-uniform
-    const size_t src = ((size_t)(e.src + tok) * H + h) * kD + lane * 4;
-    const size_t dst = (size_t)h * e.cap + e.dst + tok;   // token row in the segment
-
+    const size_t src = ((size_t)(e.src + tok) * H + h) * kD;
     const int u = (e.dst + tok) % kWTile;                      // position in its tile
     const size_t tile = (size_t)h * e.cap + e.dst + tok - u;    // first row of the tile
-
-    float x[4];
-    uint16_t s16;
-    load4h(p.k16 + src, x);
-    const uint32_t kw = quant_row_i8(x, s16);
-    *reinterpret_cast<uint32_t *>(e.kq + tile * kD + k_tile_off(u, 4 * lane)) = kw;
-    if ((lane & 7) == 0) e.ks[dst * kNB + (lane >> 3)] = s16;
-
-    load4h(p.v16 + src, x);
-    if (VT == KVQ_V_Q8_0) {
-        const uint32_t vw = quant_row_i8(x, s16);
-        uint8_t *t = e.vq + tile * kD;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) t[v8_tile_off(u, 4 * lane + k)] = (uint8_t)(vw >> (8 * k));
-        if ((lane & 7) == 0) e.vs[dst * kNB + (lane >> 3)] = s16;
-    } else {
-        const float a = block_absmax(x);
-        const __half dh = __float2half_rn(a * 0.125f);   // absmax/8, exact before rounding
-        const float d = __half2float(dh);
-        uint32_t q = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) q |= (uint32_t)quant_q4(x[k], d) << (8 * k);
-        const uint32_t qhi = __shfl_down_sync(0xffffffffu, q, 4);   // elements 16.. of the block
-        if ((lane & 7) < 4) {
-            const uint32_t w = q | (qhi << 4);                       // bytes 4(l%4)..+3 of block l/8
-            const int j = 16 * (lane >> 3) + 4 * (lane & 3);
-            uint8_t *t = e.vq + tile * (kD / 2);
-            *reinterpret_cast<uint16_t *>(t + v4_tile_off(u, j)) = (uint16_t)w;
-            *reinterpret_cast<uint16_t *>(t + v4_tile_off(u, j + 2)) = (uint16_t)(w >> 16);
-        }
-        if ((lane & 7) == 0) e.vs[dst * kNB + (lane >> 3)] = __half_as_ushort(dh);
-    }
+    const TokenRow t = quant_token<VT>(p.k16 + src, p.v16 + src, lane);
+    store_token<VT>(t, u, lane, e.kq + tile * kD, e.ks + (tile + u) * kNB, e.vq + tile * (VT == KVQ_V_Q4_0 ? kD / 2 : kD),
+                    e.vs + (tile + u) * kNB);
 }
 
 cudaError_t launch_append(const AppendParams &p, int v_type, int max_rows, cudaStream_t s, bool pdl)

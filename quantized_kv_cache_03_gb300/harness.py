@@ -87,13 +87,22 @@ class DecodeSet:
 
 class StepSet:
     """Every cache of one workload copy decoded by one kvq_decode_attn_multi
-    call (one split launch and one combine for all of them)."""
+    call (one split launch and one combine for all of them).  With append=True
+    the call also appends each cache's step tokens (fused append), so a step is
+    that one call; else the caller runs kvq_append first."""
 
-    def __init__(self, sets, q16=None):
+    def __init__(self, sets, q16=None, append=False, kv_new=None):
         self.sets = list(sets)
-        self.calls = [dict(cache=ds.cache, q16=ds.q16 if q16 is None else q16[i], n_q_heads=ds.Hq, t_q=ds.tq,
-                           causal_tail=ds.spec.causal, seq_lens=ds.lens, max_len=ds.max_len, head_map=None,
-                           sm_scale=SM_SCALE, out=ds.out, lse=ds.lse) for i, ds in enumerate(self.sets)]
+        self.append = append
+        self.calls = []
+        for i, ds in enumerate(self.sets):
+            c = dict(cache=ds.cache, q16=ds.q16 if q16 is None else q16[i], n_q_heads=ds.Hq, t_q=ds.tq,
+                     causal_tail=ds.spec.causal, seq_lens=ds.lens, max_len=ds.max_len, head_map=None,
+                     sm_scale=SM_SCALE, out=ds.out, lse=ds.lse)
+            if append:
+                k, v = (ds.k_new, ds.v_new) if kv_new is None else kv_new[i]
+                c.update(k16_new=k, v16_new=v)
+            self.calls.append(c)
         self.call = kvq.MultiCall(self.calls)
         n = self.call.workspace_size()
         self.call.ws = torch.empty(n, dtype=torch.uint8, device=self.sets[0].device) if n else None

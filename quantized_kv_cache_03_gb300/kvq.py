@@ -50,7 +50,8 @@ class KvqCache(ctypes.Structure):
 class KvqDecodeDesc(ctypes.Structure):
     _fields_ = [("cache", POINTER(KvqCache)), ("q16", c_void_p), ("n_q_heads", c_int32), ("t_q", c_int32),
                 ("causal_tail", c_int32), ("seq_lens", c_void_p), ("max_len", c_int32),
-                ("head_map", POINTER(c_int32)), ("sm_scale", c_float), ("out", c_void_p), ("lse", c_void_p)]
+                ("head_map", POINTER(c_int32)), ("sm_scale", c_float), ("out", c_void_p), ("lse", c_void_p),
+                ("k16_new", c_void_p), ("v16_new", c_void_p)]
 
 
 class KvqError(RuntimeError):
@@ -264,7 +265,8 @@ def kvq_decode_attn(cache: Cache, q16: torch.Tensor, n_q_heads: int, t_q: int, c
 def _descs(calls):
     """calls: sequence of dicts with the per-cache arguments of kvq_decode_attn
     (cache, q16, n_q_heads, t_q, causal_tail, seq_lens, max_len, head_map,
-    sm_scale, out, lse); tensors may be None for a size query."""
+    sm_scale, out, lse) and optionally k16_new / v16_new (fused append);
+    tensors may be None for a size query."""
     arr = (KvqDecodeDesc * max(1, len(calls)))()
     keep = []
     for i, c in enumerate(calls):
@@ -274,7 +276,8 @@ def _descs(calls):
         arr[i] = KvqDecodeDesc(ctypes.pointer(c["cache"].desc), _ptr(c.get("q16")), c["n_q_heads"], c["t_q"],
                                int(c.get("causal_tail", False)), _ptr(c.get("seq_lens")), c["max_len"],
                                ctypes.cast(hm_arr, POINTER(c_int32)) if hm_arr is not None else None,
-                               float(c.get("sm_scale", 1.0)), _ptr(c.get("out")), _ptr(c.get("lse")))
+                               float(c.get("sm_scale", 1.0)), _ptr(c.get("out")), _ptr(c.get("lse")),
+                               _ptr(c.get("k16_new")), _ptr(c.get("v16_new")))
     return arr, keep
 
 
