@@ -55,6 +55,9 @@ namespace kvq {
 #ifndef KVQ_TPS_Q4
 #define KVQ_TPS_Q4 2      // 16-position tiles per stage (q4_0 V)
 #endif
+#ifndef KVQ_HILO_MASK
+#define KVQ_HILO_MASK 0   // 1: split p*d by masking mantissa bits (ALU) instead of fp16 rounding
+#endif
 #ifndef KVQ_STAGES_Q8
 #define KVQ_STAGES_Q8 3   // (q8_0 V)
 #endif
@@ -100,8 +103,8 @@ struct SplitCfg {
     static constexpr int QF_CHUNKS = QB_CHUNKS + SEED_CHUNKS + SQ_CHUNKS;
     static constexpr int QF_OFF = (ML_OFF + (2 * WARPS + 3) * 8 * NT * 4 + 15) / 16 * 16;
     static constexpr int OROW = kD + 4;                        // merge slice row (floats, padded)
-    static constexpr int TI_OFF = QF_OFF + QF_CHUNKS * 32 * 16;  // int4 tile record [WARPS][STAGES][TPS]
-    static constexpr int NS_OFF = TI_OFF + WARPS * STAGES * TPS * 16;   // int tiles in stage [WARPS][STAGES]
+    static constexpr int TI_OFF = QF_OFF + QF_CHUNKS * 32 * 16;  // int4 record of a stage's first tile [WARPS][STAGES]
+    static constexpr int NS_OFF = TI_OFF + WARPS * STAGES * 16;         // int tiles in stage [WARPS][STAGES]
     static constexpr int NEW_OFF = (NS_OFF + WARPS * STAGES * 4 + 15) / 16 * 16;  // appended rows [KVQ_MAX_T_Q][32 lanes][3 words]
     static constexpr int BAR_OFF = NEW_OFF + KVQ_MAX_T_Q * 32 * 12;                 // uint64 mbarrier [WARPS][STAGES]
     static constexpr int FLAG_OFF = BAR_OFF + WARPS * STAGES * 8;
@@ -113,13 +116,14 @@ struct SplitCfg {
 };
 
 // The pieces of a sequence's segments that fall in [r0, r1), walked in order
-// in tiles of kWTile positions (local token index T * kWTile of segment k).
+// in tiles of kWTile positions: T is the next tile of segment k, Tend the end of
+// the piece, and gk..gvs point at tile T's data in the four arrays.
 struct Walk {
-    int k;            // segment table entry (relative to the sequence's first)
-    int T;            // tile index inside the segment
+    int k;            // segment table entry (relative to the sequence's first); nseg when done
+    int T, Tend;      // next tile inside the segment, end tile (exclusive) of the piece
     int la, le;       // local range [la, le) of the current piece
     int pos0;
-    const uint8_t *kq, *ks, *vq, *vs;   // kv head h's rows of the current segment
+    const uint8_t *gk, *gks, *gv, *gvs;
 };
 
 __device__ __forceinline__ void walk_seek(const AttnParams &p, int seg0, int nseg, int h, int r0, int r1, int k,
@@ -133,26 +137,20 @@ __device__ __forceinline__ void walk_seek(const AttnParams &p, int seg0, int nse
             w.la = a - s.pos0;
             w.le = e - s.pos0;
             w.T = w.la / kWTile;
+            w.Tend = (w.le + kWTile - 1) / kWTile;
             w.pos0 = s.pos0;
-            const size_t row = (size_t)h * s.cap;
-            w.kq = reinterpret_cast<const uint8_t *>(s.kq) + row * kD;
-            w.ks = reinterpret_cast<const uint8_t *>(s.ks) + row * kNB * 2;
-            w.vq = s.vq + row * vcode;
-            w.vs = reinterpret_cast<const uint8_t *>(s.vs) + row * kNB * 2;
+            const size_t row = (size_t)h * s.cap + (size_t)w.T * kWTile;
+            w.gk = reinterpret_cast<const uint8_t *>(s.kq) + row * kD;
+            w.gks = reinterpret_cast<const uint8_t *>(s.ks) + row * kNB * 2;
+            w.gv = s.vq + row * vcode;
+            w.gvs = reinterpret_cast<const uint8_t *>(s.vs) + row * kNB * 2;
             return;
         }
     }
 }
 
-__device__ __forceinline__ void walk_next(const AttnParams &p, int seg0, int nseg, int h, int r0, int r1, int vcode,
-                                          Walk &w)
-{
-    ++w.T;
-    if (w.T * kWTile >= w.le) walk_seek(p, seg0, nseg, h, r0, r1, w.k + 1, vcode, w);
-}
-
 // Lane 0 fills ring slot `dst` (shared address) with n consecutive tiles of
-// one segment starting at the walk's current tile: four contiguous bulk copies
+// one segment starting at the walk's next tile: four contiguous bulk copies
 // whose bytes complete on the slot's barrier.  Positions of a tile outside
 // [la, le) are copied too (they are cache rows of the same segment, possibly
 // never written) and masked where they are used.
@@ -160,12 +158,11 @@ template <int NT, int VT>
 __device__ __forceinline__ void tile_issue(const Walk &w, int n, uint32_t dst, uint32_t bar)
 {
     using C = SplitCfg<NT, VT>;
-    const size_t tb = (size_t)w.T * kWTile;
     mbar_arrive_expect_tx(bar, n * C::TILE);
-    bulk_g2s(dst + C::K_OFF, w.kq + tb * kD, n * C::TILE_K, bar);
-    bulk_g2s(dst + C::KS_OFF, w.ks + tb * kNB * 2, n * C::TILE_S, bar);
-    bulk_g2s(dst + C::V_OFF, w.vq + tb * C::VCODE, n * C::TILE_V, bar);
-    bulk_g2s(dst + C::VS_OFF, w.vs + tb * kNB * 2, n * C::TILE_S, bar);
+    bulk_g2s(dst + C::K_OFF, w.gk, n * C::TILE_K, bar);
+    bulk_g2s(dst + C::KS_OFF, w.gks, n * C::TILE_S, bar);
+    bulk_g2s(dst + C::V_OFF, w.gv, n * C::TILE_V, bar);
+    bulk_g2s(dst + C::VS_OFF, w.gvs, n * C::TILE_S, bar);
 }
 
 // Head-dim index of accumulator row rho (0..15) of PV m-tile mt = 2*block + h2.
@@ -305,7 +302,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
     uint8_t *ring = smem + warp * C::RING;
     const uint32_t ring_s = smem_u32(ring);
     const uint32_t bar_s = smem_u32(smem + C::BAR_OFF) + warp * S * 8;
-    int4 *tile_rec = reinterpret_cast<int4 *>(smem + C::TI_OFF) + warp * S * C::TPS;
+    int4 *tile_rec = reinterpret_cast<int4 *>(smem + C::TI_OFF) + warp * S;
     int *stage_n = reinterpret_cast<int *>(smem + C::NS_OFF) + warp * S;
     int *bad_flag = reinterpret_cast<int *>(smem + C::FLAG_OFF);
     if (tid == 0) *bad_flag = 0;
@@ -321,24 +318,19 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
     // Hand the next stage (up to TPS tiles of the current segment piece) to the
     // copy engine; the walk is advanced by every lane alike.
     auto issue = [&](int slot) {
-        const Walk first = pw;
-        const int tb0 = pw.T * kWTile;
-        const int4 rec0 = make_int4(tb0, pw.la, pw.le, pw.pos0 + tb0);
-        walk_next(p, seg0, nseg, h, w0, w1, C::VCODE, pw);
-        int n = 1;
-        int4 rec1 = rec0;
-        if (C::TPS == 2 && pw.k == first.k && pw.T == first.T + 1) {
-            const int tb1 = pw.T * kWTile;
-            rec1 = make_int4(tb1, pw.la, pw.le, pw.pos0 + tb1);
-            walk_next(p, seg0, nseg, h, w0, w1, C::VCODE, pw);
-            n = 2;
-        }
+        const int n = min(C::TPS, pw.Tend - pw.T);
         if (lane == 0) {
-            tile_rec[slot * C::TPS] = rec0;
-            if (C::TPS == 2) tile_rec[slot * C::TPS + C::TPS - 1] = rec1;
+            const int tb = pw.T * kWTile;
+            tile_rec[slot] = make_int4(tb, pw.la, pw.le, pw.pos0 + tb);
             stage_n[slot] = n;
-            tile_issue<NT, VT>(first, n, ring_s + slot * C::STAGE, bar_s + slot * 8);
+            tile_issue<NT, VT>(pw, n, ring_s + slot * C::STAGE, bar_s + slot * 8);
         }
+        pw.T += n;
+        pw.gk += n * C::TILE_K;
+        pw.gks += n * C::TILE_S;
+        pw.gv += n * C::TILE_V;
+        pw.gvs += n * C::TILE_S;
+        if (pw.T >= pw.Tend) walk_seek(p, seg0, nseg, h, w0, w1, pw.k + 1, C::VCODE, pw);
         ++issued;
     };
 #pragma unroll
@@ -501,7 +493,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
         }
         const int ns = stage_n[slot];
         const uint8_t *stg = ring + slot * C::STAGE;
-        const int4 *recs = tile_rec + slot * C::TPS;
+        const int4 rec0 = tile_rec[slot];
         prev = slot;
         if (++slot == S) {
             slot = 0;
@@ -512,8 +504,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
         for (int t = 0; t < ns; ++t) {
         const uint8_t *stK = stg + C::K_OFF + t * C::TILE_K, *stKS = stg + C::KS_OFF + t * C::TILE_S;
         const uint8_t *stV = stg + C::V_OFF + t * C::TILE_V, *stVS = stg + C::VS_OFF + t * C::TILE_S;
-        const int4 rec = recs[t];
-        const int tb = rec.x, la = rec.y, le = rec.z, pos_base = rec.w;
+        const int tb = rec0.x + t * kWTile, la = rec0.y, le = rec0.z, pos_base = rec0.w + t * kWTile;
         // every position of the tile valid and visible to every live row?
         const bool full = tb >= la && tb + kWTile <= le && pos_base + kWTile - 1 <= lim_min;
         if (nn > 0 && pos_base < na0 + nn && pos_base + kWTile > na0) {
@@ -709,14 +700,19 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
                     uint32_t bh[2], bl[2];   // [positions 0-7 / 8-15]
 #pragma unroll
                     for (int pp = 0; pp < 2; ++pp) {
-                        // x = p*d split as hi (x with its low 13 mantissa bits cleared:
-                        // exact in fp16 when x is in fp16's normal range) + lo (x - hi,
-                        // exact in fp32, then rounded to fp16)
+                        // x = p*d split as hi = fp16(x) (rounded) + lo = fp16(x - hi), with
+                        // x - hi exact in fp32: about 22 bits of x survive
                         const float2 x = mul2(s[nt][pp], make_float2(dv[pp][bb], dv[pp][bb]));
+#if KVQ_HILO_MASK
                         const float2 h = make_float2(__uint_as_float(__float_as_uint(x.x) & 0xffffe000u),
                                                      __uint_as_float(__float_as_uint(x.y) & 0xffffe000u));
+                        const uint32_t hp = pack_half2(h.x, h.y);
+#else
+                        const uint32_t hp = pack_half2(x.x, x.y);
+                        const float2 h = __half22float2(*reinterpret_cast<const __half2 *>(&hp));
+#endif
                         const float2 lo = sub2(x, h);
-                        bh[pp] = movmatrix_t(pack_half2(h.x, h.y));
+                        bh[pp] = movmatrix_t(hp);
                         bl[pp] = movmatrix_t(pack_half2(lo.x, lo.y));
                     }
 #pragma unroll
