@@ -432,27 +432,45 @@ def main():
     peak, peak_kind = measured_peaks()
 
     # ---- end to end through the public API with host buffers ----
+    # A step's inputs (q, new K, new V of every cache) sit in one pinned host
+    # buffer and go over in one H2D copy; its results (out, lse of every
+    # cache) come back in one D2H copy.  Each piece starts on a 256-byte
+    # boundary (the API wants 16).
     grp = sets[0]
-    pin = lambda t: t.detach().cpu().pin_memory()
-    h_in = [(pin(ds.q16), pin(ds.k_new), pin(ds.v_new)) for ds in grp]
-    h_out = [(torch.empty_like(ds.out, device="cpu").pin_memory(),
-              torch.empty_like(ds.lse, device="cpu").pin_memory()) for ds in grp]
-    d_in = [(torch.empty_like(ds.q16), torch.empty_like(ds.k_new), torch.empty_like(ds.v_new)) for ds in grp]
-    h2d = sum(a.numel() * a.element_size() + b.numel() * b.element_size() + c.numel() * c.element_size()
-              for a, b, c in h_in)
-    d2h = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in h_out)
 
-    e2e_call = StepSet(grp, q16=[dq for dq, _, _ in d_in], append=True, kv_new=[(dk, dv) for _, dk, dv in d_in])
+    def pack(tensors):
+        offs, n = [], 0
+        for t in tensors:
+            offs.append(n)
+            n += -(-(t.numel() * t.element_size()) // 256) * 256
+        return offs, n
+
+    ins = [t for ds in grp for t in (ds.q16, ds.k_new, ds.v_new)]
+    outs = [t for ds in grp for t in (ds.out, ds.lse)]
+    in_offs, in_bytes = pack(ins)
+    out_offs, out_bytes = pack(outs)
+    h_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
+    for t, o in zip(ins, in_offs):
+        nb = t.numel() * t.element_size()
+        h_in[o:o + nb].copy_(t.detach().contiguous().view(-1).view(torch.uint8).cpu())
+    d_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
+    h_out = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+
+    def view(buf, t, off):
+        nb = t.numel() * t.element_size()
+        return buf[off:off + nb].view(t.dtype).view(t.shape)
+
+    dv_in = [view(d_in, t, o) for t, o in zip(ins, in_offs)]
+    dv_out = [view(d_out, t, o) for t, o in zip(outs, out_offs)]
+    h2d, d2h = in_bytes, out_bytes
+    e2e_call = StepSet(grp, q16=dv_in[0::3], append=True, kv_new=list(zip(dv_in[1::3], dv_in[2::3])),
+                       outs=list(zip(dv_out[0::2], dv_out[1::2])))
 
     def e2e_step():
-        for (hq, hk, hv), (dq, dk, dv) in zip(h_in, d_in):
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
         e2e_call.decode(stream=stream)
-        for ds, (ho, hl) in zip(grp, h_out):
-            ho.copy_(ds.out, non_blocking=True)
-            hl.copy_(ds.lse, non_blocking=True)
+        h_out.copy_(d_out, non_blocking=True)
         for ds in grp:
             ds.rewind()
 

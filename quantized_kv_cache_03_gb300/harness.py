@@ -91,14 +91,15 @@ class StepSet:
     the call also appends each cache's step tokens (fused append), so a step is
     that one call; else the caller runs kvq_append first."""
 
-    def __init__(self, sets, q16=None, append=False, kv_new=None):
+    def __init__(self, sets, q16=None, append=False, kv_new=None, outs=None):
         self.sets = list(sets)
         self.append = append
         self.calls = []
         for i, ds in enumerate(self.sets):
+            out, lse = (ds.out, ds.lse) if outs is None else outs[i]
             c = dict(cache=ds.cache, q16=ds.q16 if q16 is None else q16[i], n_q_heads=ds.Hq, t_q=ds.tq,
                      causal_tail=ds.spec.causal, seq_lens=ds.lens, max_len=ds.max_len, head_map=None,
-                     sm_scale=SM_SCALE, out=ds.out, lse=ds.lse)
+                     sm_scale=SM_SCALE, out=out, lse=lse)
             if append:
                 k, v = (ds.k_new, ds.v_new) if kv_new is None else kv_new[i]
                 c.update(k16_new=k, v16_new=v)
