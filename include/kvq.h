@@ -208,7 +208,8 @@ kvq_status kvq_decode_workspace_size(const kvq_cache *c, int32_t n_q_heads, int3
  *            sequence needs an open segment with room for t_q more tokens
  *            (else KVQ_ERR_CAPACITY, nothing enqueued); seq_lens must already
  *            count the new tokens; the host len of each open segment grows by
- *            t_q when the call succeeds.
+ *            t_q when the call succeeds.  A cache that receives tokens may
+ *            appear in only one call of a kvq_decode_attn_multi.
  */
 typedef struct kvq_decode_desc {
     const kvq_cache *cache;

@@ -578,6 +578,8 @@ kvq_status kvq_decode_attn_multi(int32_t n, const kvq_decode_desc *calls, void *
     for (int i = 0; i < n; ++i) {
         kvq_status st = to_desc(calls[i], true, ds[i]);
         if (st != KVQ_OK) return st;
+        for (int j = 0; j < i; ++j)   // a cache that receives tokens may appear only once
+            if (ds[j].c == ds[i].c && (ds[i].k_new || ds[j].k_new)) return KVQ_ERR_INVALID_ARG;
     }
     return run(ds, false, workspace, workspace_bytes, nullptr, static_cast<cudaStream_t>(stream));
 }

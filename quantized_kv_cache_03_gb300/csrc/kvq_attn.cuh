@@ -55,9 +55,6 @@ namespace kvq {
 #ifndef KVQ_TPS_Q4
 #define KVQ_TPS_Q4 2      // 16-position tiles per stage (q4_0 V)
 #endif
-#ifndef KVQ_HILO_MASK
-#define KVQ_HILO_MASK 0   // 1: split p*d by masking mantissa bits (ALU) instead of fp16 rounding
-#endif
 #ifndef KVQ_STAGES_Q8
 #define KVQ_STAGES_Q8 3   // (q8_0 V)
 #endif
@@ -703,14 +700,8 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
                         // x = p*d split as hi = fp16(x) (rounded) + lo = fp16(x - hi), with
                         // x - hi exact in fp32: about 22 bits of x survive
                         const float2 x = mul2(s[nt][pp], make_float2(dv[pp][bb], dv[pp][bb]));
-#if KVQ_HILO_MASK
-                        const float2 h = make_float2(__uint_as_float(__float_as_uint(x.x) & 0xffffe000u),
-                                                     __uint_as_float(__float_as_uint(x.y) & 0xffffe000u));
-                        const uint32_t hp = pack_half2(h.x, h.y);
-#else
                         const uint32_t hp = pack_half2(x.x, x.y);
                         const float2 h = __half22float2(*reinterpret_cast<const __half2 *>(&hp));
-#endif
                         const float2 lo = sub2(x, h);
                         bh[pp] = movmatrix_t(hp);
                         bl[pp] = movmatrix_t(pack_half2(lo.x, lo.y));

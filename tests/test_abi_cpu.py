@@ -128,3 +128,14 @@ def test_multi_argument_errors(lib):
     arr[1].t_q = 9
     arr[1].n_q_heads = 8
     assert lib.kvq_decode_attn_multi(2, arr, None, 0, None) == kvq.KVQ_ERR_INVALID_ARG
+
+
+def test_multi_rejects_a_cache_that_receives_tokens_twice(lib):
+    c = _fake_cache()
+    d0, d1 = _desc(c), _desc(c)
+    d1.k16_new = d1.v16_new = 0x60000
+    arr = (kvq.KvqDecodeDesc * 2)(d0, d1)
+    assert lib.kvq_decode_attn_multi(2, arr, None, 0, None) == kvq.KVQ_ERR_INVALID_ARG
+    d1.v16_new = None                                  # k without v
+    arr = (kvq.KvqDecodeDesc * 1)(d1)
+    assert lib.kvq_decode_attn_multi(1, arr, None, 0, None) == kvq.KVQ_ERR_INVALID_ARG

@@ -72,3 +72,24 @@ def test_full_open_segment_is_rejected():
         kvq.kvq_decode_attn_multi([_call(case)], None)
     assert e.value.status == kvq.KVQ_ERR_CAPACITY
     assert case.cache.lengths() == before
+
+
+def test_fused_append_max_tokens_with_a_head_map(monkeypatch):
+    # t_q = 8 (the limit), 4 query heads per kv head -> 32 rows, several segments,
+    # an uneven explicit head map, splits forced small so the tokens cross splits
+    monkeypatch.setenv("KVQ_SPLIT", "128")
+    spec = W.make_spec("verify", ctx=1300, n_seqs=2, t_q=8, n_q_heads=24, n_seg=3)[0]
+    case = Case(spec).build(append_step=False)
+    counts = [4, 4, 4, 4, 4, 2, 1, 1]                       # query heads per kv head
+    hm = [k for k, n in enumerate(counts) for _ in range(n)]
+    hm = [hm[(7 * h) % case.Hq] for h in range(case.Hq)]    # interleaved
+    assert sorted(hm.count(k) for k in range(8)) == sorted(counts)
+    call = _call(case)
+    call["head_map"] = hm
+    kvq.kvq_decode_attn_multi([call], torch.zeros(kvq.kvq_decode_multi_workspace_size([call]), dtype=torch.uint8, device=dev()))
+    torch.cuda.synchronize()
+    assert case.cache.lengths() == case.lens
+    o, l = call["out"].cpu().numpy(), call["lse"].cpu().numpy()
+    for b in range(case.B):
+        assert_cache_bytes(case, b)
+        assert_close(o[b], l[b], case.oracle_decode(b, head_map=hm), what="seq %d" % b)
