@@ -68,3 +68,43 @@ def test_single_full_size_all_rows():
     case = Case(spec).build()
     out, lse = case.decode()
     assert_close(out[0], lse[0], case.oracle_decode(0))
+
+
+def test_long_context_step_as_bench_runs_it():
+    """The bench's launch configuration: both full-size caches (131072
+    positions, 4 segments each) decoded by one kvq_decode_attn_multi call that
+    also appends the step's token (fused append); sampled rows and cache
+    positions against the oracle, the appended token's bytes in full."""
+    import torch
+    from quantized_kv_cache_03_gb300 import kvq
+    from kvq_cases import SM_SCALE, dev, to_dev
+
+    rng = np.random.default_rng(1)
+    cases = [Case(s).build(append_step=False) for s in W.make_spec("long")]
+    calls = []
+    for case in cases:
+        L = case.lens[0]
+        calls.append(dict(cache=case.cache, q16=to_dev(case.q), n_q_heads=case.Hq, t_q=case.tq,
+                          causal_tail=case.spec.causal, seq_lens=torch.tensor(case.lens, dtype=torch.int32, device=dev()),
+                          max_len=case.max_len, head_map=None, sm_scale=SM_SCALE,
+                          out=torch.full((1, case.tq, case.Hq, 128), float("nan"), device=dev()),
+                          lse=torch.full((1, case.tq, case.Hq), float("nan"), device=dev()),
+                          k16_new=to_dev(case.kv[0][0][L - case.tq:L]), v16_new=to_dev(case.kv[0][1][L - case.tq:L])))
+    n = kvq.kvq_decode_multi_workspace_size(calls)
+    kvq.kvq_decode_attn_multi(calls, torch.empty(n, dtype=torch.uint8, device=dev()) if n else None)
+    torch.cuda.synchronize()
+    for case, call in zip(cases, calls):
+        L = case.lens[0]
+        assert case.cache.lengths() == case.lens
+        oc = case.oracle_cache(0)
+        got = export_logical(case.cache, 0)
+        pos = np.unique(np.concatenate([np.arange(L - 64, L), rng.integers(0, L, 2000)]))
+        for name in ("kq", "ks", "vq", "vs"):
+            assert np.array_equal(got[name].view(np.uint8)[:, pos], oc[name].view(np.uint8)[:, pos]), name
+        nr = case.tq * case.Hq
+        rows = np.unique(np.concatenate([[0, nr - 1], rng.integers(0, nr, 5)]))
+        mask = np.zeros(nr, np.uint8)
+        mask[rows] = 1
+        ref = case.oracle_decode(0, row_mask=mask)
+        assert_close(call["out"][0].cpu().numpy(), call["lse"][0].cpu().numpy(), ref, rows=rows,
+                     what=case.spec.name)
