@@ -428,7 +428,10 @@ def main():
                 tot += a.elapsed_time(b)
     dec_ms = tot / (kreps * n_rot)                     # per step (all caches)
     dec_bytes = float(kv_bytes)
-    achieved = float(dec_bytes / (dec_ms * 1e-3) / 1e9)
+    # The split kernel runs once per step (one launch for all caches): its
+    # average launch duration is at most the timed region's time per step,
+    # which also holds the small combine; that bound gives the achieved rate.
+    achieved = float(dec_bytes / (ms_per_step * 1e-3) / 1e9)
     peak, peak_kind = measured_peaks()
 
     # ---- end to end through the public API with host buffers ----
@@ -509,11 +512,13 @@ def main():
                    "kv_bytes_per_step": kv_bytes, "tokens_per_step": tokens_per_step},
         "kv_gbs": kv_gbs, "kv_frac_of_8tbs": kv_gbs / NOMINAL_HBM_GBS,
         "kv_frac_of_measured_copy": kv_gbs / peak,
-        "roofline": {"bound": "hbm", "kernel": "split_attn with fused append (+ its combine), all caches in one launch",
+        "roofline": {"bound": "hbm", "kernel": "split_attn (appends fused), all caches in one launch per step",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
                      "traffic": profiled_traffic(args.workload),
-                     "decode_us": 1e3 * dec_ms, "algorithmic_bytes": int(dec_bytes)},
+                     "duration_us": 1e3 * ms_per_step,
+                     "duration_basis": "timed region / split launches (the per-step combine included)",
+                     "decode_call_us_event_bracketed": 1e3 * dec_ms, "algorithmic_bytes": int(dec_bytes)},
         "per_cache_calls_ms_per_step": sep_ms_per_step,
         "e2e": {"value": tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},

@@ -279,11 +279,6 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-__device__ __forceinline__ float half_bits_to_float(uint16_t b)
-{
-    return __half2float(__ushort_as_half(b));
-}
-
 // int8 rule of one element given its block scale s (fp32 copy of the fp16 scale).
 __device__ __forceinline__ int quant_i8(float x, float s)
 {
