@@ -37,6 +37,7 @@ sys.path.insert(0, ROOT)
 METRIC = "decode attn tokens/s and KV HBM GB/s (% of 8 TB/s) at 128k ctx, 1 GB300"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 L2_BYTES = 129 * 1024 * 1024
 
 WORKLOADS = {
@@ -46,6 +47,8 @@ WORKLOADS = {
     "batched": "batched decode: 64 sequences, lengths U[1024, 32768], 32q/8kv heads, V q8_0, outliers x10",
     "verify": "multi-token verify: 16 sequences x 4 causal query tokens, 32768 positions, 64q/8kv heads, V q4_0",
     "tiny": "tiny: 1 kv head, 4 query heads, 256 positions, V q8_0",
+    "prefill": "chunked prefill: one 512-token chunk (causal among its tokens) over 32768 positions, "
+               "32q/8kv heads, V q4_0; the chunk is appended by kvq_append, then attended",
 }
 
 
@@ -88,14 +91,16 @@ def job_rate(ms_local, world, steps, tokens_per_step, device=None):
     return ms_per_step, tokens_per_step * world / (ms_per_step * 1e-3)
 
 
-def measured_peaks():
+def measured_peaks(kind="hbm_gbs"):
+    """(peak, 'measured'|'fallback'): HBM copy GB/s, or the bf16 GEMM TFLOP/s
+    sustained over seconds (kind='bf16_tflops_sustained')."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        if d.get("hbm_gbs"):
-            return float(d["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        if d.get(kind):
+            return float(d[kind]), "measured"
+    return (FALLBACK_HBM_GBS if kind == "hbm_gbs" else FALLBACK_BF16_TFLOPS_SUSTAINED), "fallback"
 
 
 def kernel_source_hash():
@@ -310,12 +315,18 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     data = [HostData(s) for s in specs]
+    # the step's appends run inside the attention kernel when every cache
+    # takes at most KVQ_MAX_T_Q_APPEND tokens per step; else kvq_append first
+    fusable = all(s.t_q <= kvq.MAX_T_Q_APPEND for s in specs)
     if args.mode == "profile":
         grp = [DecodeSet(d, dev) for d in data]
         for ds in grp:
             ds.staging = None
-        fused = StepSet(grp, append=True)
+        fused = StepSet(grp, append=fusable)
         for _ in range(max(1, args.warmup) + max(1, args.steps)):
+            if not fusable:
+                for ds in grp:
+                    ds.append_step()
             fused.decode()
             for ds in grp:
                 ds.rewind()
@@ -336,7 +347,7 @@ def main():
         for ds in grp:
             ds.staging = None
     torch.cuda.synchronize()
-    fused = [StepSet(grp, append=True) for grp in sets]
+    fused = [StepSet(grp, append=fusable) for grp in sets]
     launches_per_step = launches_of(sets[0], fused[0])
 
     stream = torch.cuda.Stream(device=dev)
@@ -346,6 +357,9 @@ def main():
         one kvq_decode_attn_multi call with the appends fused (fz), or per cache
         a kvq_append and a kvq_decode_attn (fz None) -- then rewind."""
         if fz is not None:
+            if not fz.append:
+                for ds in grp:
+                    ds.append_step(stream=stream)
             fz.decode(stream=stream)
         else:
             for ds in grp:
@@ -377,6 +391,9 @@ def main():
                  torch.cuda.Event(enable_timing=True, external=True)) for _ in sets]
     with torch.cuda.graph(g_ev, stream=stream):
         for grp, fz, (a, b) in zip(sets, fused, ev_pairs):
+            if not fz.append:
+                for ds in grp:
+                    ds.append_step(stream=stream)
             a.record(stream)
             fz.decode(stream=stream)
             b.record(stream)
@@ -433,6 +450,14 @@ def main():
     # which also holds the small combine; that bound gives the achieved rate.
     achieved = float(dec_bytes / (ms_per_step * 1e-3) / 1e9)
     peak, peak_kind = measured_peaks()
+    # Long query chunks (prefill) make the attention a dense contraction: each
+    # KV byte feeds t_q x group query rows.  Above the machine balance
+    # (measured bf16 FLOP/s over copy bytes/s) the kernel is bound by the
+    # tensor pipe, and its roofline is FLOPs over the bracketed attention call
+    # (the chunk's kvq_append launch is outside the brackets).
+    flops = W.step_attn_flops(specs)
+    tpeak, tpeak_kind = measured_peaks("bf16_tflops_sustained")
+    tensor_bound = flops / max(1, kv_bytes) > tpeak * 1e12 / (peak * 1e9)
 
     # ---- end to end through the public API with host buffers ----
     # A step's inputs (q, new K, new V of every cache) sit in one pinned host
@@ -467,11 +492,15 @@ def main():
     dv_in = [view(d_in, t, o) for t, o in zip(ins, in_offs)]
     dv_out = [view(d_out, t, o) for t, o in zip(outs, out_offs)]
     h2d, d2h = in_bytes, out_bytes
-    e2e_call = StepSet(grp, q16=dv_in[0::3], append=True, kv_new=list(zip(dv_in[1::3], dv_in[2::3])),
+    kv_in = list(zip(dv_in[1::3], dv_in[2::3]))
+    e2e_call = StepSet(grp, q16=dv_in[0::3], append=fusable, kv_new=kv_in,
                        outs=list(zip(dv_out[0::2], dv_out[1::2])))
 
     def e2e_step():
         d_in.copy_(h_in, non_blocking=True)
+        if not fusable:
+            for ds, (k, v) in zip(grp, kv_in):
+                ds.append_step(k_new=k, v_new=v, stream=stream)
         e2e_call.decode(stream=stream)
         h_out.copy_(d_out, non_blocking=True)
         for ds in grp:
@@ -512,13 +541,21 @@ def main():
                    "kv_bytes_per_step": kv_bytes, "tokens_per_step": tokens_per_step},
         "kv_gbs": kv_gbs, "kv_frac_of_8tbs": kv_gbs / NOMINAL_HBM_GBS,
         "kv_frac_of_measured_copy": kv_gbs / peak,
-        "roofline": {"bound": "hbm", "kernel": "split_attn (appends fused), all caches in one launch per step",
-                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": achieved / peak, "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
-                     "traffic": profiled_traffic(args.workload),
-                     "duration_us": 1e3 * ms_per_step,
-                     "duration_basis": "timed region / split launches (the per-step combine included)",
-                     "decode_call_us_event_bracketed": 1e3 * dec_ms, "algorithmic_bytes": int(dec_bytes)},
+        "roofline": ({"bound": "hbm", "kernel": "split_attn (appends fused), all caches in one launch per step",
+                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                      "frac": achieved / peak, "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
+                      "traffic": profiled_traffic(args.workload),
+                      "duration_us": 1e3 * ms_per_step,
+                      "duration_basis": "timed region / split launches (the per-step combine included)",
+                      "decode_call_us_event_bracketed": 1e3 * dec_ms, "algorithmic_bytes": int(dec_bytes)}
+                     if not tensor_bound else
+                     {"bound": "tensor", "kernel": "split_attn over row tiles (fp16 mma.sync) + combine",
+                      "achieved": flops / (dec_ms * 1e-3) / 1e12, "peak": tpeak,
+                      "peak_kind": tpeak_kind + " bf16 cuBLAS sustained (fp16 has the same nominal rate)",
+                      "unit": "TFLOP/s", "frac": flops / (dec_ms * 1e-3) / 1e12 / tpeak,
+                      "traffic": profiled_traffic(args.workload), "duration_us": 1e3 * dec_ms,
+                      "duration_basis": "event-bracketed attention call (split + combine), appends outside",
+                      "algorithmic_flops": int(flops), "kv_bytes": int(dec_bytes)}),
         "per_cache_calls_ms_per_step": sep_ms_per_step,
         "e2e": {"value": tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},

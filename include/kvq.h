@@ -49,8 +49,9 @@ extern "C" {
 #define KVQ_QBLOCK 32          /* quantization block (head-dim elements)          */
 #define KVQ_HEAD_DIM 128       /* the only head_dim this build supports           */
 #define KVQ_SEG_ALIGN 64       /* segment capacity must be a multiple of this     */
-#define KVQ_MAX_ROWS 32        /* query rows per kv head: t_q * (q heads of it)   */
-#define KVQ_MAX_T_Q 8          /* query tokens per sequence per call              */
+#define KVQ_MAX_ROWS 32        /* query rows one attention CTA takes (row tile)   */
+#define KVQ_MAX_T_Q 4096       /* query tokens per sequence per call              */
+#define KVQ_MAX_T_Q_APPEND 8   /* ... when the call also appends them (fused)     */
 #define KVQ_MAX_HEADS 256      /* n_q_heads and n_kv_heads limit                  */
 #define KVQ_MAX_CALLS 16       /* decode calls fused by kvq_decode_attn_multi     */
 
@@ -153,7 +154,12 @@ kvq_status kvq_append(kvq_cache *c, int32_t n_seqs_in, const int32_t *seq_ids,
  *  q16       device fp16 [n_seqs][t_q][n_q_heads][head_dim], 16-byte aligned.
  *            The t_q query tokens of a sequence are its last t_q positions.
  *  n_q_heads query heads.
- *  t_q       query tokens per sequence, 1..KVQ_MAX_T_Q.
+ *  t_q       query tokens per sequence, 1..KVQ_MAX_T_Q: one decode token,
+ *            a few tokens to verify (speculative decoding), or a chunk of
+ *            prompt tokens (chunked prefill over the cache, causal_tail set).
+ *            A kv head's t_q x (query heads of it) rows are attended in row
+ *            tiles of up to KVQ_MAX_ROWS rows, one CTA per tile and split;
+ *            each tile streams the positions its split covers.
  *  causal_tail nonzero: query token i sees positions 0 .. L-t_q+i (a causal mask
  *            among the t_q newest positions); zero: every query token sees
  *            0 .. L-1.
@@ -163,8 +169,7 @@ kvq_status kvq_append(kvq_cache *c, int32_t n_seqs_in, const int32_t *seq_ids,
  *  max_len   host: upper bound of seq_lens, sizes the grid.
  *  head_map  host int32 [n_q_heads]: kv head read by each query head, or NULL
  *            for contiguous groups (query head h reads kv head
- *            h / (n_q_heads/n_kv_heads)).  t_q times the largest group must
- *            not exceed KVQ_MAX_ROWS.
+ *            h / (n_q_heads/n_kv_heads)).
  *  sm_scale  softmax scale applied to q.k (e.g. 1/sqrt(head_dim)).
  *  out       device fp32 [n_seqs][t_q][n_q_heads][head_dim], 16-byte aligned:
  *            softmax(q.k*sm_scale).v

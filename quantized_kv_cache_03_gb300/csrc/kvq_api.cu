@@ -1,6 +1,7 @@
 // kvq_api.cu -- the C ABI of libkvq.so: argument validation, segment-table
 // marshalling, split policy and kernel launches.  No allocation, and no host
 // sync except in kvq_wait_timeouts.
+#include <climits>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -152,11 +153,11 @@ kvq_status prepare_desc(Desc &d, const int32_t *head_map, bool need_ptrs, bool d
     for (int h = 0; h < d.n_q_heads; ++h) ++cnt[d.kv[h]];
     int gmax = 0;
     for (int k = 0; k < H; ++k) gmax = std::max(gmax, cnt[k]);
-    d.max_rows = gmax * d.t_q;
-    if (d.max_rows > KVQ_MAX_ROWS) return KVQ_ERR_UNSUPPORTED;
+    d.max_rows = gmax * d.t_q;   // at most 256 * 4096: row tiles of <= KVQ_MAX_ROWS
     if ((d.k_new != nullptr) != (d.v_new != nullptr)) return KVQ_ERR_INVALID_ARG;
     if (d.k_new) {
         if (dump || !aligned16(d.k_new) || !aligned16(d.v_new)) return KVQ_ERR_INVALID_ARG;
+        if (d.t_q > KVQ_MAX_T_Q_APPEND) return KVQ_ERR_UNSUPPORTED;
         for (int b = 0; b < c->n_seqs; ++b) {
             if (c->n_segs[b] < 1) return KVQ_ERR_INVALID_ARG;   // no open segment
             const kvq_segment &sl = seg_of(c, b, c->n_segs[b] - 1);
@@ -187,6 +188,7 @@ int seq_reach(const kvq_cache *c, int b, int max_len)
 struct Unit {
     int d, b0, nb;
     int reach;          // max seq_reach over the unit
+    int n_rt;           // row tiles of 8 * NT query rows per kv head
     int n_split;
     size_t ws_off;      // bytes
     int cta0, row0;
@@ -220,14 +222,15 @@ int choose_chunk(const std::vector<Desc> &ds, const Launch &ln, int slots, int g
     if (env && std::atoi(env) > 0) {
         chunk = round_up(std::atoi(env), KVQ_SEG_ALIGN);
     } else {
-        std::vector<std::pair<int, int>> seqs;   // (kv heads, reach)
+        std::vector<std::pair<int, int>> seqs;   // (kv heads x row tiles, reach)
         long long W = 0;
         for (const Unit &u : ln.units) {
             const kvq_cache *c = ds[u.d].c;
+            const int n_rt = (ds[u.d].max_rows + 8 * ln.nt - 1) / (8 * ln.nt);
             for (int b = u.b0; b < u.b0 + u.nb; ++b) {
                 const int r = seq_reach(c, b, ds[u.d].max_len);
-                seqs.push_back({c->n_kv_heads, r});
-                W += (long long)r * c->n_kv_heads;
+                seqs.push_back({c->n_kv_heads * n_rt, r});
+                W += (long long)r * c->n_kv_heads * n_rt;
             }
         }
         const int max_n = std::max(1, std::min(1024, (lmax + 255) / 256));
@@ -284,7 +287,7 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
             heads += need_heads;
             kvs += need_kv;
             last_d = di;
-            Unit u{di, b, 0, 0, 1, 0, 0, 0};
+            Unit u{di, b, 0, 0, 1, 1, 0, 0, 0};
             while (b < c->n_seqs && seqs < kMaxSeqsLaunch && segs + c->n_segs[b] <= kMaxSegsLaunch) {
                 segs += c->n_segs[b];
                 u.reach = std::max(u.reach, seq_reach(c, b, ds[di].max_len));
@@ -292,7 +295,7 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
                 ++u.nb;
                 ++b;
             }
-            cur.nt = std::max(cur.nt, tiles8_for(ds[di].max_rows));
+            cur.nt = std::max(cur.nt, tiles8_for(std::min(ds[di].max_rows, KVQ_MAX_ROWS)));
             cur.units.push_back(u);
         }
     }
@@ -303,8 +306,11 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
         for (Unit &u : ln.units) {
             const Desc &d = ds[u.d];
             u.n_split = std::max(1, (u.reach + ln.chunk - 1) / ln.chunk);
+            u.n_rt = (d.max_rows + 8 * ln.nt - 1) / (8 * ln.nt);
+            const long long n = (long long)u.n_rt * u.n_split * d.c->n_kv_heads * u.nb;
+            if (ln.n_ctas + n > INT_MAX) return KVQ_ERR_UNSUPPORTED;
             u.cta0 = ln.n_ctas;
-            ln.n_ctas += u.n_split * d.c->n_kv_heads * u.nb;
+            ln.n_ctas += (int)n;
             if (u.n_split > 1 && !dump) {
                 const size_t rows = (size_t)u.nb * d.t_q * d.n_q_heads;
                 u.row0 = ln.n_rows;
@@ -356,6 +362,7 @@ void fill_launch(const std::vector<Desc> &ds, const Launch &ln, bool dump, void 
         G.causal = d.causal ? 1 : 0;
         G.max_len = d.max_len;
         G.n_split = u.n_split;
+        G.n_rt = u.n_rt;
         G.chunk = ln.chunk;
         G.qk_scale_log2 = d.sm_scale * 1.4426950408889634f;
         if (dump) {

@@ -1,9 +1,10 @@
 // kvq_attn.cuh -- split-KV decode attention over the quantized cache (sm_103a).
 //
-// One CTA = (split s, kv head h, sequence b) of one work group of the launch: it attends the query rows of kv
-// head h (t_q query tokens x the query heads mapped to h, at most 32 rows) over
-// the positions [s*chunk, (s+1)*chunk) of sequence b and writes either the
-// final output (one split) or a partial (normalised o, lse) for the combine.
+// One CTA = (row tile, split s, kv head h, sequence b) of one work group of the
+// launch: it attends up to 8 NT query rows of kv head h (of its t_q query tokens
+// x the query heads mapped to h) over the positions [s*chunk, (s+1)*chunk) of
+// sequence b and writes either the final output (one split) or a partial
+// (normalised o, lse) for the combine.
 //
 // Data path: every warp streams its own contiguous share of the CTA's
 // positions through a private ring of 16-position stages in shared memory.
@@ -102,8 +103,8 @@ struct SplitCfg {
     static constexpr int OROW = kD + 4;                        // merge slice row (floats, padded)
     static constexpr int TI_OFF = QF_OFF + QF_CHUNKS * 32 * 16;  // int4 record of a stage's first tile [WARPS][STAGES]
     static constexpr int NS_OFF = TI_OFF + WARPS * STAGES * 16;         // int tiles in stage [WARPS][STAGES]
-    static constexpr int NEW_OFF = (NS_OFF + WARPS * STAGES * 4 + 15) / 16 * 16;  // appended rows [KVQ_MAX_T_Q][32 lanes][3 words]
-    static constexpr int BAR_OFF = NEW_OFF + KVQ_MAX_T_Q * 32 * 12;                 // uint64 mbarrier [WARPS][STAGES]
+    static constexpr int NEW_OFF = (NS_OFF + WARPS * STAGES * 4 + 15) / 16 * 16;  // appended rows [KVQ_MAX_T_Q_APPEND][32 lanes][3 words]
+    static constexpr int BAR_OFF = NEW_OFF + KVQ_MAX_T_Q_APPEND * 32 * 12;          // uint64 mbarrier [WARPS][STAGES]
     static constexpr int FLAG_OFF = BAR_OFF + WARPS * STAGES * 8;
     static constexpr int SMEM = FLAG_OFF + 16;
     static_assert(8 * NT * OROW * 4 <= WARPS * RING, "merge buffer must fit in the stage rings");
@@ -263,17 +264,29 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
         if ((int)blockIdx.x >= p.grp[k].cta0) gi = k;
     const GroupDesc &G = p.grp[gi];
     const int lb = (int)blockIdx.x - G.cta0;
-    const int split = lb % G.n_split, h = (lb / G.n_split) % G.n_kv_heads, b = lb / G.n_split / G.n_kv_heads;
+    const int rt = lb % G.n_rt, ls = lb / G.n_rt;   // row tile: rows [rt * 8NT, (rt + 1) * 8NT) of the kv head
+    const int split = ls % G.n_split, h = (ls / G.n_split) % G.n_kv_heads, b = ls / G.n_split / G.n_kv_heads;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
     const int gb = p.grp_begin[G.head0 + h], gsz = p.grp_begin[G.head0 + h + 1] - gb;
-    const int R = gsz * G.t_q;
+    // This CTA's query rows: row0 + r (r < R) of the kv head's t_q x gsz rows,
+    // row g being query token g / gsz of query head grp_q[gb + g % gsz].
+    const int row0 = rt * 8 * NT;
+    const int R = min(8 * NT, gsz * G.t_q - row0);
+    if (R <= 0) return;   // a row tile past this kv head's rows (smaller group)
     const int seg0 = p.seq_seg0[G.seq0 + b], nseg = p.seq_nseg[G.seq0 + b];
     const int lcap = nseg ? min(G.max_len, p.seg[seg0 + nseg - 1].pos0 + p.seg[seg0 + nseg - 1].cap) : 0;
     // The split's positions as far as the segment table knows them: the
     // sequence length, read below, can only cut them shorter.  Copies of the
     // range go out before that read returns; positions at or past the length
-    // are masked like any other invisible position.
-    const int r0 = split * G.chunk, r1c = min(lcap, r0 + G.chunk);
+    // are masked like any other invisible position.  Under the causal tail the
+    // tile's last query token sees positions up to L - t_q + its index, and
+    // L <= lcap bounds that from above.
+    const int r0 = split * G.chunk;
+    const int r1c = max(r0, min(min(lcap, r0 + G.chunk),
+                                G.causal ? lcap - G.t_q + (row0 + R - 1) / gsz + 1 : lcap));
+    // The row tile holding the kv head's last query token sees every position
+    // below L: it alone stores the appended tokens (fused append).
+    const bool app_store = rt == (gsz * G.t_q - 1) / (8 * NT);
 
     // Nothing above reads memory written by an earlier kernel.
     pdl_wait();
@@ -289,7 +302,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
         const int r = warp + kWarps * k;
         qraw[k] = make_uint2(0u, 0u);
         if (r < R && r0 < r1c) {
-            const int i = r / gsz, hq = p.grp_q[gb + r % gsz];
+            const int i = (row0 + r) / gsz, hq = p.grp_q[gb + (row0 + r) % gsz];
             qraw[k] = *reinterpret_cast<const uint2 *>(G.q + (((size_t)b * G.t_q + i) * G.n_q_heads + hq) * kD + lane * 4);
         }
     }
@@ -335,11 +348,11 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
         if (pw.k < nseg) issue(st);
 
     const int L = max(0, min(len_b, lcap));
-    const int r1 = min(L, r0 + G.chunk);
+    const int r1 = min(min(L, r0 + G.chunk), r1c);
     if (r0 >= r1) {                                  // no position in this split
         for (int j = 0; j < issued; ++j) mbar_wait(bar_s + (j % S) * 8, (j / S) & 1);
         if (!DUMP && tid < R) {
-            const int i = tid / gsz, hq = p.grp_q[gb + tid % gsz];
+            const int i = (row0 + tid) / gsz, hq = p.grp_q[gb + (row0 + tid) % gsz];
             const size_t row = ((size_t)b * G.t_q + i) * G.n_q_heads + hq;
             if (G.n_split == 1) {
                 G.lse[row] = -INFINITY;
@@ -369,9 +382,11 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
             const TokenRow t = quant_token<VT>(G.k_new + src, G.v_new + src, lane);
             const int local = na0 + i - sl.pos0, u = local % kWTile;
             const size_t tile = (size_t)h * sl.cap + local - u;
-            store_token<VT>(t, u, lane, const_cast<uint8_t *>(sl.kq) + tile * kD,
-                            const_cast<uint16_t *>(sl.ks) + (tile + u) * kNB,
-                            const_cast<uint8_t *>(sl.vq) + tile * C::VCODE, const_cast<uint16_t *>(sl.vs) + (tile + u) * kNB);
+            if (app_store)
+                store_token<VT>(t, u, lane, const_cast<uint8_t *>(sl.kq) + tile * kD,
+                                const_cast<uint16_t *>(sl.ks) + (tile + u) * kNB,
+                                const_cast<uint8_t *>(sl.vq) + tile * C::VCODE,
+                                const_cast<uint16_t *>(sl.vs) + (tile + u) * kNB);
             newrow[(i * 32 + lane) * 3 + 0] = t.kw;
             newrow[(i * 32 + lane) * 3 + 1] = t.vw;
             newrow[(i * 32 + lane) * 3 + 2] = (uint32_t)t.ks | ((uint32_t)t.vs << 16);
@@ -389,7 +404,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
         float s = 0.f;
         int sum = 0;
         if (r < R) {
-            const int i = r / gsz, hq = p.grp_q[gb + r % gsz];
+            const int i = (row0 + r) / gsz, hq = p.grp_q[gb + (row0 + r) % gsz];
             const size_t qrow = ((size_t)b * G.t_q + i) * G.n_q_heads + hq;
             float x[4];
             unpack4h(qraw[k], x);
@@ -459,14 +474,14 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int row = 8 * nt + 2 * c + e;
-            lim[nt][e] = (row < R) ? (G.causal ? L - G.t_q + row / gsz : L - 1) : -1;
+            lim[nt][e] = (row < R) ? (G.causal ? L - G.t_q + (row0 + row) / gsz : L - 1) : -1;
             m[nt][e] = -INFINITY;
             l[nt][e] = 0.f;
         }
     float2 mu[NT];   // exponent offsets: m, or 0 while m is -inf
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) mu[nt] = make_float2(0.f, 0.f);
-    const int lim_min = G.causal ? L - G.t_q : L - 1;   // smallest limit over live rows
+    const int lim_min = G.causal ? L - G.t_q + row0 / gsz : L - 1;   // smallest limit over live rows
     float acc[8][NT][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
@@ -590,7 +605,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
                         for (int e = 0; e < 2; ++e) {
                             const int row = 8 * nt + 2 * c + e, tok = tb + 8 * pp + g, pos = pos_base + 8 * pp + g;
                             if (row < R && tok >= la && tok < le && pos < L) {
-                                const int i = row / gsz, hq = p.grp_q[gb + row % gsz];
+                                const int i = (row0 + row) / gsz, hq = p.grp_q[gb + (row0 + row) % gsz];
                                 const size_t o = ((((size_t)b * G.t_q + i) * G.n_q_heads + hq) * G.max_len + pos) * kNB;
                                 int4 v;
                                 v.x = (int)sc[nt][0][2 * pp + e]; v.y = (int)sc[nt][1][2 * pp + e];
@@ -821,7 +836,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
             }
             float ls = sm_lse[row];
             if (poisoned) t.x = t.y = t.z = t.w = ls = __int_as_float(0x7fc00000);   // NaN: the CTA lost a stage
-            const int i = row / gsz, hq = p.grp_q[gb + row % gsz];
+            const int i = (row0 + row) / gsz, hq = p.grp_q[gb + (row0 + row) % gsz];
             const size_t orow = ((size_t)b * G.t_q + i) * G.n_q_heads + hq;
             if (G.n_split == 1) {
                 *reinterpret_cast<float4 *>(G.out + orow * kD + d) = t;

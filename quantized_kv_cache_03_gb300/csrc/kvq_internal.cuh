@@ -74,8 +74,10 @@ struct SegDesc {
 
 // One work group of a split launch: sequences [b0, b0 + n_seqs) of one cache
 // of one decode call.  A launch runs up to kMaxGroups groups (of one or more
-// caches) in a single 1-D grid; CTA cta0 + (b * n_kv_heads + h) * n_split + s
-// of the group attends split s of kv head h of its sequence b.
+// caches) in a single 1-D grid; CTA cta0 + ((b * n_kv_heads + h) * n_split + s)
+// * n_rt + rt of the group attends split s of kv head h of its sequence b for
+// row tile rt (the fastest-varying index, so a kv head's row tiles stream the
+// same positions side by side).
 struct GroupDesc {
     const uint16_t *q;                     // [n_seqs][t_q][Hq][kD] fp16 bits
     const int *seq_lens;                   // [n_seqs]
@@ -93,6 +95,7 @@ struct GroupDesc {
     int n_seqs, n_kv_heads, n_q_heads, t_q, causal;
     int max_len;                           // positions >= max_len are ignored
     int n_split, chunk;                    // split s covers [s*chunk, (s+1)*chunk)
+    int n_rt;                              // row tiles of 8*NT query rows per kv head
     float qk_scale_log2;                   // sm_scale * log2(e)
 };
 

@@ -33,6 +33,8 @@ EXPORTED = ("kvq_append", "kvq_decode_attn", "kvq_decode_workspace_size", "kvq_d
             "kvq_decode_multi_workspace_size", "kvq_decode_attn_noalloc", "kvq_wait_timeouts",
             "kvq_status_string", "kvq_debug_qk")
 MAX_CALLS = 16
+MAX_T_Q = 4096
+MAX_T_Q_APPEND = 8
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 

@@ -23,6 +23,11 @@ sequence can be regenerated on its own):
 * ``verify``   16 sequences x 4 query tokens with a causal mask among the 4
                newest positions, 32768 positions each, 64 query / 8 kv heads
                (32 query rows per kv head), V q4_0, N(0,1), seed 5.
+* ``prefill``  one chunk of chunked prefill: 1 sequence of 32768 positions whose
+               last 512 are the chunk's tokens (causal among themselves), the
+               earlier ones cached in 2 segments (one cut uniform in [1, L-1]
+               with at least 512 positions after it); 32 query / 8 kv heads
+               (2048 query rows per kv head), V q4_0, N(0,1), seed 6.
 
 Every sequence's last ``t_q`` positions are the step's new tokens: the cache is
 built from the first ``L - t_q`` tokens and the step appends the rest.
@@ -37,7 +42,7 @@ import numpy as np
 V_Q4_0 = 0
 V_Q8_0 = 1
 
-CONFIG_NAMES = ("tiny", "single", "long", "batched", "verify")
+CONFIG_NAMES = ("tiny", "single", "long", "batched", "verify", "prefill")
 
 
 @dataclasses.dataclass
@@ -102,6 +107,9 @@ def make_spec(name: str, ctx: int | None = None, n_seqs: int | None = None,
     elif name == "verify":
         base = [dict(seed=5, n_seqs=16, n_kv_heads=8, n_q_heads=64, ctx=32768, t_q=4, causal=True,
                      v_type=V_Q4_0, n_seg=1, outliers=0)]
+    elif name == "prefill":
+        base = [dict(seed=6, n_seqs=1, n_kv_heads=8, n_q_heads=32, ctx=32768, t_q=512, causal=True,
+                     v_type=V_Q4_0, n_seg=2, outliers=0)]
     else:
         raise KeyError(name)
     specs = []
@@ -185,3 +193,17 @@ def step_kv_bytes(specs: List[CacheSpec]) -> int:
     """Algorithmic KV bytes one decode step reads over all caches."""
     return int(sum(int(s.lengths.sum()) * s.n_kv_heads * kv_bytes_per_token_head(s.head_dim, s.v_type)
                    for s in specs))
+
+
+def step_attn_flops(specs: List[CacheSpec]) -> int:
+    """Algorithmic multiply-add FLOPs of one step's attention over all caches:
+    per (query head, visible position) 2 x head_dim for q.k and 2 x head_dim
+    for p.v; a query token i of t_q sees L - t_q + i + 1 positions under the
+    causal tail, else all L."""
+    total = 0
+    for s in specs:
+        for L in s.lengths:
+            L, t = int(L), s.t_q
+            vis = (t * (L - t) + t * (t + 1) // 2) if s.causal else t * L
+            total += 4 * s.head_dim * s.n_q_heads * vis
+    return int(total)

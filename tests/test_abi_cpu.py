@@ -70,10 +70,9 @@ def test_decode_argument_errors(lib):
     assert _decode(lib, _fake_cache(vt=7)) == kvq.KVQ_ERR_INVALID_ARG
     c = _fake_cache()
     assert _decode(lib, c, t_q=0) == kvq.KVQ_ERR_INVALID_ARG
-    assert _decode(lib, c, t_q=9) == kvq.KVQ_ERR_INVALID_ARG
+    assert _decode(lib, c, t_q=kvq.MAX_T_Q + 1) == kvq.KVQ_ERR_INVALID_ARG
     assert _decode(lib, c, Hq=5) == kvq.KVQ_ERR_INVALID_ARG                       # 5 % 2 != 0 without a map
     assert _decode(lib, c, Hq=3, head_map=[0, 2, 1]) == kvq.KVQ_ERR_INVALID_ARG   # kv head out of range
-    assert _decode(lib, c, Hq=40, t_q=2) == kvq.KVQ_ERR_UNSUPPORTED               # 20 * 2 rows > 32
     assert _decode(lib, c, max_len=-1) == kvq.KVQ_ERR_INVALID_ARG
 
 
@@ -125,7 +124,7 @@ def test_multi_argument_errors(lib):
     size = ctypes.c_size_t(7)
     assert lib.kvq_decode_multi_workspace_size(2, arr, None) == kvq.KVQ_ERR_INVALID_ARG
     assert lib.kvq_decode_multi_workspace_size(2, arr, ctypes.byref(size)) == kvq.KVQ_ERR_INVALID_ARG
-    arr[1].t_q = 9
+    arr[1].t_q = kvq.MAX_T_Q + 1
     arr[1].n_q_heads = 8
     assert lib.kvq_decode_attn_multi(2, arr, None, 0, None) == kvq.KVQ_ERR_INVALID_ARG
 

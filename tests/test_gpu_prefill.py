@@ -1,0 +1,136 @@
+"""Chunked prefill over the quantized cache: many query tokens per sequence
+(t_q up to 4096), the chunk causal among its own tokens.  The attention kernel
+takes the t_q x group query rows of a kv head in row tiles of up to 32 rows;
+these cases span several row tiles with a ragged last one, splits that lie
+wholly past a tile's causal limit, uneven head maps (tiles past a small
+group's rows), an empty context, a non-causal chunk and a mixed launch with a
+decode call.  All against the oracle on the same seeded inputs: cache bytes
+and int32 block scores bit-exact, out within 2e-3 and lse within 1e-4."""
+
+import numpy as np
+import pytest
+import torch
+
+from quantized_kv_cache_03_gb300 import kvq
+from quantized_kv_cache_03_gb300 import workloads as W
+
+from kvq_cases import SM_SCALE, Case, assert_cache_bytes, assert_close, dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _check_all(case, head_map=None, scores=False):
+    out, lse = case.decode(head_map=head_map)
+    for b in range(case.B):
+        assert_cache_bytes(case, b)
+        ref = case.oracle_decode(b, head_map=head_map, want_scores=scores)
+        assert_close(out[b], lse[b], ref, what="seq %d" % b)
+    return out, lse
+
+
+@pytest.mark.parametrize("vt", [0, 1])
+def test_chunk_of_64_tokens_all_rows_and_scores(vt):
+    # 64 tokens x 4 query heads = 256 rows per kv head: 8 row tiles
+    spec = W.make_spec("prefill", ctx=1000, t_q=64, v_type=vt)[0]
+    case = Case(spec).build()
+    _check_all(case)
+    qc, qs, sc = case.debug_qk()
+    ref = case.oracle_decode(0, want_scores=True)
+    assert np.array_equal(qc[0], ref["q_codes"]) and np.array_equal(qs[0], ref["q_scales"])
+    L = case.lens[0]
+    for i in range(case.tq):
+        vis = L - case.tq + i + 1
+        assert np.array_equal(sc[0, i, :, :vis], ref["scores"][i, :, :vis]), "int32 block scores, token %d" % i
+
+
+def test_splits_past_a_row_tiles_causal_limit(monkeypatch):
+    # context of 100 positions, chunk of 600: the first row tiles see ~100
+    # positions, so with 64-position splits most of their splits hold nothing
+    monkeypatch.setenv("KVQ_SPLIT", "64")
+    spec = W.make_spec("prefill", ctx=700, t_q=600, n_q_heads=8, n_kv_heads=2, v_type=0)[0]
+    _check_all(Case(spec).build())
+
+
+@pytest.mark.parametrize("vt", [0, 1])
+def test_prefill_of_an_empty_context(vt):
+    # the whole sequence is the chunk; 300 x 4 = 1200 rows: 37.5 row tiles
+    spec = W.make_spec("prefill", ctx=300, t_q=300, n_seg=1, n_q_heads=16, n_kv_heads=4, v_type=vt)[0]
+    out, lse = _check_all(Case(spec).build())
+    assert np.all(np.isfinite(lse))
+
+
+def test_uneven_head_map_ragged_row_tiles():
+    # kv head 0 takes 9 query heads (360 rows, 12 tiles), kv head 7 one (40 rows)
+    spec = W.make_spec("prefill", ctx=1500, t_q=40, n_q_heads=24, v_type=1)[0]
+    hm = [0] * 9 + [1, 1, 1, 2, 2, 2, 3, 3, 4, 4, 5, 5, 6, 6, 7]
+    assert len(hm) == 24
+    _check_all(Case(spec).build(), head_map=hm)
+
+
+def test_non_causal_chunk():
+    spec = W.make_spec("prefill", ctx=2000, t_q=100, causal=False, v_type=0)[0]
+    _check_all(Case(spec).build())
+
+
+def test_chunk_and_decode_calls_in_one_launch():
+    """A prefill chunk and a decode step of another cache fused in one
+    kvq_decode_attn_multi call (one launch at the chunk's row-tile size)."""
+    pre = Case(W.make_spec("prefill", ctx=1200, t_q=48, v_type=0)[0]).build()
+    dec = Case(W.make_spec("long", ctx=2000)[0]).build()
+    calls = []
+    for case in (pre, dec):
+        calls.append(dict(cache=case.cache, q16=to_dev(case.q), n_q_heads=case.Hq, t_q=case.tq,
+                          causal_tail=case.spec.causal,
+                          seq_lens=torch.tensor(case.lens, dtype=torch.int32, device=dev()),
+                          max_len=case.max_len, head_map=None, sm_scale=SM_SCALE,
+                          out=torch.full((case.B, case.tq, case.Hq, 128), float("nan"), device=dev()),
+                          lse=torch.full((case.B, case.tq, case.Hq), float("nan"), device=dev())))
+    n = kvq.kvq_decode_multi_workspace_size(calls)
+    kvq.kvq_decode_attn_multi(calls, torch.empty(n, dtype=torch.uint8, device=dev()) if n else None)
+    torch.cuda.synchronize()
+    for case, call in zip((pre, dec), calls):
+        assert_close(call["out"][0].cpu().numpy(), call["lse"][0].cpu().numpy(), case.oracle_decode(0),
+                     what=case.spec.name)
+
+
+def test_fused_append_is_limited_to_short_chunks():
+    spec = W.make_spec("prefill", ctx=640, t_q=kvq.MAX_T_Q_APPEND + 1, v_type=0)[0]
+    case = Case(spec).build(append_step=False)
+    L = case.lens[0]
+    call = dict(cache=case.cache, q16=to_dev(case.q), n_q_heads=case.Hq, t_q=case.tq, causal_tail=True,
+                seq_lens=torch.tensor(case.lens, dtype=torch.int32, device=dev()), max_len=L, head_map=None,
+                sm_scale=SM_SCALE, out=torch.empty((1, case.tq, case.Hq, 128), device=dev()),
+                lse=torch.empty((1, case.tq, case.Hq), device=dev()),
+                k16_new=to_dev(case.kv[0][0][L - case.tq:]), v16_new=to_dev(case.kv[0][1][L - case.tq:]))
+    with pytest.raises(kvq.KvqError) as ei:
+        kvq.kvq_decode_attn_multi([call], None)
+    assert ei.value.status == kvq.KVQ_ERR_UNSUPPORTED
+    assert case.cache.lengths() == [L - case.tq]
+
+
+def test_chunk_full_size_sampled_rows():
+    """The 512-token chunk over 32768 positions as the benchmark runs it:
+    sampled rows (first, last, random) and cache positions against the oracle."""
+    spec = W.make_spec("prefill")[0]
+    case = Case(spec).build()
+    out, lse = case.decode()
+    rng = np.random.default_rng(0)
+    L = case.lens[0]
+    oc = case.oracle_cache(0)
+    from kvq_cases import export_logical
+    got = export_logical(case.cache, 0)
+    pos = np.unique(np.concatenate([np.arange(L - 600, L), rng.integers(0, L, 2000)]))
+    for name in ("kq", "ks", "vq", "vs"):
+        assert np.array_equal(got[name].view(np.uint8)[:, pos], oc[name].view(np.uint8)[:, pos]), name
+    nr = case.tq * case.Hq
+    rows = np.unique(np.concatenate([[0, 1, 31, 32, nr - 1], rng.integers(0, nr, 24)]))
+    mask = np.zeros(nr, np.uint8)
+    mask[rows] = 1
+    ref = case.oracle_decode(0, row_mask=mask)
+    assert_close(out[0], lse[0], ref, rows=rows, what="prefill full size")
