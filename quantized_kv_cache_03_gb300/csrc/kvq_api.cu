@@ -62,6 +62,10 @@ kvq_status device_setup(DeviceInfo **out)
                 return KVQ_ERR_CUDA;
             }
         }
+        if (prepare_prefill_q4() != cudaSuccess || prepare_prefill_q8() != cudaSuccess) {
+            cudaGetLastError();
+            return KVQ_ERR_CUDA;
+        }
         void *t = nullptr;
         if (cudaGetSymbolAddress(&t, g_wait_timeouts) != cudaSuccess || !t) {
             cudaGetLastError();
@@ -173,6 +177,15 @@ kvq_status prepare_desc(Desc &d, const int32_t *head_map, bool need_ptrs, bool d
 }
 
 int tiles8_for(int rows) { return rows <= 8 ? 1 : rows <= 16 ? 2 : 4; }
+
+
+// Calls with long query chunks go to the tcgen05 kernel unless KVQ_PREFILL=0.
+bool prefill_kernel_for(const Desc &d, bool dump)
+{
+    const char *e = std::getenv("KVQ_PREFILL");
+    const bool on = !(e && e[0] == '0');
+    return on && !dump && !d.k_new && d.max_rows > KVQ_MAX_ROWS;
+}
 int round_up(long long x, int m) { return (int)((x + m - 1) / m * m); }
 
 // Positions of sequence b that the kernel may visit: the end of its last
@@ -194,13 +207,19 @@ struct Unit {
     int cta0, row0;
 };
 
-// A split launch: units of calls with one V format, run in one grid.
+// A split launch: units of calls with one V format and one kernel, run in one
+// grid.  prefill: the tcgen05 kernel (128-row tiles) for calls with more query
+// rows per kv head than the split kernel's 32-row tile and no fused append.
 struct Launch {
     int v_type = 0, nt = 1;
+    bool prefill = false;
     int chunk = KVQ_SEG_ALIGN;
     int n_ctas = 0, n_rows = 0;   // split CTAs, combine rows
     std::vector<Unit> units;
 };
+
+// Query rows one CTA of the launch takes per kv head.
+int tile_rows(const Launch &ln) { return ln.prefill ? kPrefillRows : 8 * ln.nt; }
 
 // Split policy, one chunk per launch so that CTAs of every unit do the same
 // amount of work.  For a candidate chunk c the launch has n CTAs with work
@@ -226,7 +245,7 @@ int choose_chunk(const std::vector<Desc> &ds, const Launch &ln, int slots, int g
         long long W = 0;
         for (const Unit &u : ln.units) {
             const kvq_cache *c = ds[u.d].c;
-            const int n_rt = (ds[u.d].max_rows + 8 * ln.nt - 1) / (8 * ln.nt);
+            const int n_rt = (ds[u.d].max_rows + tile_rows(ln) - 1) / tile_rows(ln);
             for (int b = u.b0; b < u.b0 + u.nb; ++b) {
                 const int r = seq_reach(c, b, ds[u.d].max_len);
                 seqs.push_back({c->n_kv_heads * n_rt, r});
@@ -272,7 +291,8 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
     for (int di = 0; di < (int)ds.size(); ++di) {
         const kvq_cache *c = ds[di].c;
         if (c->n_seqs == 0) continue;
-        if (!cur.units.empty() && cur.v_type != c->v_type) flush();
+        const bool pf = prefill_kernel_for(ds[di], dump);
+        if (!cur.units.empty() && (cur.v_type != c->v_type || cur.prefill != pf)) flush();
         int b = 0;
         while (b < c->n_seqs) {
             const bool new_desc = last_d != di;
@@ -283,7 +303,10 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
                 flush();
                 continue;
             }
-            if (cur.units.empty()) cur.v_type = c->v_type;
+            if (cur.units.empty()) {
+                cur.v_type = c->v_type;
+                cur.prefill = pf;
+            }
             heads += need_heads;
             kvs += need_kv;
             last_d = di;
@@ -301,12 +324,12 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
     }
     flush();
     for (Launch &ln : out) {
-        const int slots = std::max(1, dev->n_sms * std::max(1, dev->ctas[ln.v_type][ln.nt]));
-        ln.chunk = choose_chunk(ds, ln, slots, split_warps(ln.nt) * kWTile);
+        const int slots = ln.prefill ? dev->n_sms : std::max(1, dev->n_sms * std::max(1, dev->ctas[ln.v_type][ln.nt]));
+        ln.chunk = choose_chunk(ds, ln, slots, ln.prefill ? kPrefillPositions : split_warps(ln.nt) * kWTile);
         for (Unit &u : ln.units) {
             const Desc &d = ds[u.d];
             u.n_split = std::max(1, (u.reach + ln.chunk - 1) / ln.chunk);
-            u.n_rt = (d.max_rows + 8 * ln.nt - 1) / (8 * ln.nt);
+            u.n_rt = (d.max_rows + tile_rows(ln) - 1) / tile_rows(ln);
             const long long n = (long long)u.n_rt * u.n_split * d.c->n_kv_heads * u.nb;
             if (ln.n_ctas + n > INT_MAX) return KVQ_ERR_UNSUPPORTED;
             u.cta0 = ln.n_ctas;
@@ -440,8 +463,13 @@ kvq_status run(std::vector<Desc> &ds, bool dump, void *workspace, size_t workspa
     const bool pdl = pdl_enabled();
     for (const Launch &ln : lns) {
         fill_launch(ds, ln, dump, workspace, dev->timeouts, p, cp);
-        cudaError_t e = (ln.v_type == KVQ_V_Q4_0) ? launch_split_q4(p, ln.nt, ln.n_ctas, dump, stream, pdl)
-                                                  : launch_split_q8(p, ln.nt, ln.n_ctas, dump, stream, pdl);
+        cudaError_t e;
+        if (ln.prefill)
+            e = (ln.v_type == KVQ_V_Q4_0) ? launch_prefill_q4(p, ln.n_ctas, stream, pdl)
+                                          : launch_prefill_q8(p, ln.n_ctas, stream, pdl);
+        else
+            e = (ln.v_type == KVQ_V_Q4_0) ? launch_split_q4(p, ln.nt, ln.n_ctas, dump, stream, pdl)
+                                          : launch_split_q8(p, ln.nt, ln.n_ctas, dump, stream, pdl);
         if (e == cudaSuccess && ln.n_rows > 0) e = launch_combine(cp, ln.n_rows, stream, pdl);
         if (e != cudaSuccess) {
             cudaGetLastError();

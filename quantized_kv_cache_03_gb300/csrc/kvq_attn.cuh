@@ -113,40 +113,6 @@ struct SplitCfg {
     static_assert(SMEM <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
 };
 
-// The pieces of a sequence's segments that fall in [r0, r1), walked in order
-// in tiles of kWTile positions: T is the next tile of segment k, Tend the end of
-// the piece, and gk..gvs point at tile T's data in the four arrays.
-struct Walk {
-    int k;            // segment table entry (relative to the sequence's first); nseg when done
-    int T, Tend;      // next tile inside the segment, end tile (exclusive) of the piece
-    int la, le;       // local range [la, le) of the current piece
-    int pos0;
-    const uint8_t *gk, *gks, *gv, *gvs;
-};
-
-__device__ __forceinline__ void walk_seek(const AttnParams &p, int seg0, int nseg, int h, int r0, int r1, int k,
-                                          int vcode, Walk &w)
-{
-    for (w.k = k; w.k < nseg; ++w.k) {
-        const SegDesc &s = p.seg[seg0 + w.k];
-        const int end = (w.k + 1 < nseg) ? p.seg[seg0 + w.k + 1].pos0 : s.pos0 + s.cap;
-        const int a = max(r0, s.pos0), e = min(min(r1, end), s.pos0 + s.cap);
-        if (a < e) {
-            w.la = a - s.pos0;
-            w.le = e - s.pos0;
-            w.T = w.la / kWTile;
-            w.Tend = (w.le + kWTile - 1) / kWTile;
-            w.pos0 = s.pos0;
-            const size_t row = (size_t)h * s.cap + (size_t)w.T * kWTile;
-            w.gk = reinterpret_cast<const uint8_t *>(s.kq) + row * kD;
-            w.gks = reinterpret_cast<const uint8_t *>(s.ks) + row * kNB * 2;
-            w.gv = s.vq + row * vcode;
-            w.gvs = reinterpret_cast<const uint8_t *>(s.vs) + row * kNB * 2;
-            return;
-        }
-    }
-}
-
 // Lane 0 fills ring slot `dst` (shared address) with n consecutive tiles of
 // one segment starting at the walk's next tile: four contiguous bulk copies
 // whose bytes complete on the slot's barrier.  Positions of a tile outside
@@ -216,13 +182,6 @@ __device__ __forceinline__ void unpack4h(uint2 raw, float (&x)[4])
     const float2 a = __half22float2(*reinterpret_cast<__half2 *>(&raw.x));
     const float2 b = __half22float2(*reinterpret_cast<__half2 *>(&raw.y));
     x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;
-}
-
-__device__ __forceinline__ float fast_exp2(float x)
-{
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
 }
 
 // Four signed int8 K codes -> two fp16 pairs holding 1152 + code (exact): the

@@ -24,6 +24,8 @@ constexpr int kWTile = 16;              // positions per warp pipeline stage
 // contiguous sub-range of the split, so split chunks are rounded to a multiple
 // of split_warps(nt) * kWTile positions.
 constexpr int split_warps(int nt) { return nt == 1 ? KVQ_WARPS_NT1 : KVQ_WARPS_NTX; }
+constexpr int kPrefillRows = 128;       // query rows per CTA of the tcgen05 kernel
+constexpr int kPrefillPositions = 64;   // positions per KV tile of the tcgen05 kernel
 constexpr int kMaxSegsLaunch = 64;      // segment-table entries per launch
 constexpr int kMaxSeqsLaunch = 64;      // sequences per launch
 
@@ -150,7 +152,7 @@ struct AppendParams {
 };
 
 // ------------------------------------------------------------ host launchers --
-// Implemented in kvq_small.cu / kvq_attn_q4.cu / kvq_attn_q8.cu.
+// Implemented in kvq_small.cu / kvq_attn_q4.cu / kvq_attn_q8.cu / kvq_prefill_q*.cu.
 // n_tiles8 = query rows per kv head rounded up to 1, 2 or 4 tiles of 8.
 cudaError_t launch_append(const AppendParams &p, int v_type, int max_rows, cudaStream_t s, bool pdl);
 cudaError_t launch_combine(const CombineParams &p, int n_rows, cudaStream_t s, bool pdl);
@@ -158,6 +160,12 @@ cudaError_t launch_split_q4(const AttnParams &p, int n_tiles8, int n_ctas, bool 
 cudaError_t launch_split_q8(const AttnParams &p, int n_tiles8, int n_ctas, bool dump, cudaStream_t s, bool pdl);
 cudaError_t prepare_split_q4(int n_tiles8, bool dump, int *ctas_per_sm);
 cudaError_t prepare_split_q8(int n_tiles8, bool dump, int *ctas_per_sm);
+// tcgen05 kernel for long query chunks (kvq_prefill_q4.cu / kvq_prefill_q8.cu):
+// 128 query rows per CTA, one CTA per SM.
+cudaError_t launch_prefill_q4(const AttnParams &p, int n_ctas, cudaStream_t s, bool pdl);
+cudaError_t launch_prefill_q8(const AttnParams &p, int n_ctas, cudaStream_t s, bool pdl);
+cudaError_t prepare_prefill_q4();
+cudaError_t prepare_prefill_q8();
 
 // ------------------------------------------------------------- device helpers --
 
@@ -217,6 +225,40 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 
 
 
+// The pieces of a sequence's segments that fall in [r0, r1), walked in order
+// in tiles of kWTile positions: T is the next tile of segment k, Tend the end of
+// the piece, and gk..gvs point at tile T's data in the four arrays.
+struct Walk {
+    int k;            // segment table entry (relative to the sequence's first); nseg when done
+    int T, Tend;      // next tile inside the segment, end tile (exclusive) of the piece
+    int la, le;       // local range [la, le) of the current piece
+    int pos0;
+    const uint8_t *gk, *gks, *gv, *gvs;
+};
+
+__device__ __forceinline__ void walk_seek(const AttnParams &p, int seg0, int nseg, int h, int r0, int r1, int k,
+                                          int vcode, Walk &w)
+{
+    for (w.k = k; w.k < nseg; ++w.k) {
+        const SegDesc &s = p.seg[seg0 + w.k];
+        const int end = (w.k + 1 < nseg) ? p.seg[seg0 + w.k + 1].pos0 : s.pos0 + s.cap;
+        const int a = max(r0, s.pos0), e = min(min(r1, end), s.pos0 + s.cap);
+        if (a < e) {
+            w.la = a - s.pos0;
+            w.le = e - s.pos0;
+            w.T = w.la / kWTile;
+            w.Tend = (w.le + kWTile - 1) / kWTile;
+            w.pos0 = s.pos0;
+            const size_t row = (size_t)h * s.cap + (size_t)w.T * kWTile;
+            w.gk = reinterpret_cast<const uint8_t *>(s.kq) + row * kD;
+            w.gks = reinterpret_cast<const uint8_t *>(s.ks) + row * kNB * 2;
+            w.gv = s.vq + row * vcode;
+            w.gvs = reinterpret_cast<const uint8_t *>(s.vs) + row * kNB * 2;
+            return;
+        }
+    }
+}
+
 // D = A(16x16 f16, row) * B(16x8 f16, col) + C, C given as four floats (bit patterns).
 __device__ __forceinline__ void mma_f16_16816_c4(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
                                                  const uint4 &c)
@@ -273,6 +315,14 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x)
 {
     uint32_t y;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// 2^x (hardware approximation, flushes subnormals).
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 

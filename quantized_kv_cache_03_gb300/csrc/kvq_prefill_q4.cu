@@ -1,0 +1,10 @@
+// tcgen05 attention kernel for long query chunks, q4_0 V.
+#include "kvq_prefill.cuh"
+
+namespace kvq {
+cudaError_t launch_prefill_q4(const AttnParams &p, int n_ctas, cudaStream_t s, bool pdl)
+{
+    return launch_prefill_t<KVQ_V_Q4_0>(p, n_ctas, s, pdl);
+}
+cudaError_t prepare_prefill_q4() { return prepare_prefill_t<KVQ_V_Q4_0>(); }
+}  // namespace kvq

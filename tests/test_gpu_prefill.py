@@ -1,7 +1,9 @@
 """Chunked prefill over the quantized cache: many query tokens per sequence
-(t_q up to 4096), the chunk causal among its own tokens.  The attention kernel
-takes the t_q x group query rows of a kv head in row tiles of up to 32 rows;
-these cases span several row tiles with a ragged last one, splits that lie
+(t_q up to 4096), the chunk causal among its own tokens.  Calls with more than
+32 query rows per kv head run on the tcgen05 kernel (128-row tiles, TMEM
+accumulators); KVQ_PREFILL=0 sends them to the split kernel's 32-row tiles, and
+every case below runs on both.  The cases span several row tiles with a ragged
+last one, splits that lie
 wholly past a tile's causal limit, uneven head maps (tiles past a small
 group's rows), an empty context, a non-causal chunk and a mixed launch with a
 decode call.  All against the oracle on the same seeded inputs: cache bytes
@@ -23,6 +25,12 @@ pytestmark = pytest.mark.gpu
 def _built():
     import __graft_entry__
     __graft_entry__.build()
+
+
+@pytest.fixture(params=["tcgen05", "rowtile"], autouse=True)
+def kernel(request, monkeypatch):
+    monkeypatch.setenv("KVQ_PREFILL", "1" if request.param == "tcgen05" else "0")
+    return request.param
 
 
 def _check_all(case, head_map=None, scores=False):
