@@ -71,19 +71,14 @@ struct PrefillCfg {
     static constexpr int R_K = 0, R_KS = R_K + kPSub * TILE_K, R_V = R_KS + kPSub * TILE_S;
     static constexpr int R_VS = R_V + kPSub * TILE_V, RAW = R_VS + kPSub * TILE_S;
     // operands (bytes)
-    static constexpr int Q_SBO = 16 * 128;                           // 128 dims per row group
-    static constexpr int K_SBO = 16 * 128;
-    static constexpr int PV_SBO = (kPN / 8) * 128;                   // P: 64 positions per row group
-    static constexpr int V_SBO = (kPN / 8) * 128 + 16;               // V: the same, padded so that the
+    static constexpr int K_SBO = 16 * 128;                           // 128 dims per row group
+    static constexpr int V_SBO = (kPN / 8) * 128 + 16;               // 64 positions per row group, padded so that the
                                                                      // converters' stores hit distinct banks
-    static constexpr int Q_OFF = 0;                                  // [128 rows][128 dims]
-    static constexpr int K_OFF = Q_OFF + kPM * kD * 2;               // [2][64 positions][128 dims]
+    static constexpr int K_OFF = 0;                                  // [2][64 positions][128 dims]
     static constexpr int VBUF = (kD / 8) * V_SBO;                    // [128 dims][64 positions]
     static constexpr int VH_OFF = K_OFF + 2 * kPN * kD * 2;          // [2] V buffers
     static constexpr int VL_OFF = VH_OFF + 2 * VBUF;
-    static constexpr int PH_OFF = VL_OFF + 2 * VBUF;                 // [128 rows][64 positions]
-    static constexpr int PL_OFF = PH_OFF + kPM * kPN * 2;
-    static constexpr int RAW_OFF = PL_OFF + kPM * kPN * 2;
+    static constexpr int RAW_OFF = VL_OFF + 2 * VBUF;
     static constexpr int SKF_OFF = RAW_OFF + RS * RAW;               // fp32 [2][block][64 positions]
     static constexpr int REC_OFF = SKF_OFF + 2 * kNB * kPN * 4;      // int4 [RS][kPSub] (tb, la, le, pos)
     static constexpr int NSUB_OFF = REC_OFF + RS * kPSub * 16;       // int [RS]
@@ -124,6 +119,15 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b
     asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
                  " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
                  "l"(a), "l"(b), "r"(idesc), "r"(acc)
+                 : "memory");
+}
+// The same with A in tensor memory (row r in lane r, two fp16 k elements per
+// 32-bit column, k-step columns [a, a + 8)).
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                 " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
                  : "memory");
 }
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far is done.
@@ -281,17 +285,30 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
     const bool row_ok = srole && row < R;
     int lim = -1;                            // last visible position of the row
     size_t orow = 0;
-    if (srole) {
-        uint4 *qop = reinterpret_cast<uint4 *>(smem + C::Q_OFF);
+    tc_fence_before();
+    __syncthreads();   // barriers and the TMEM base in place
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // TMEM columns: S_b at 64b (0..255), O at 256..383, the Q codes at 384..447
+    // and P at 448..479 (high parts), 480..511 (low parts); fp16 A operands
+    // hold two k elements per 32-bit column, row r in lane r
+    const uint32_t tS = tmem, tO = tmem + 4 * kPN, tQ = tmem + 4 * kPN + kD, tPH = tQ + kD / 2, tPL = tPH + kPN / 2;
+    if (srole) {   // Q codes of this row's two blocks -> TMEM columns 32hf.. of the Q area
+        const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
         float *qsl_s = reinterpret_cast<float *>(smem + C::QSL_OFF);
+        const uint4 *src = nullptr;
         if (row_ok) {
             const int i = (row0 + row) / gsz, hq = p.grp_q[gb + (row0 + row) % gsz];
             orow = ((size_t)b * G.t_q + i) * G.n_q_heads + hq;
             lim = G.causal ? L - G.t_q + i : L - 1;
-            const uint4 *src = reinterpret_cast<const uint4 *>(G.q + orow * kD);
+            src = reinterpret_cast<const uint4 *>(G.q + orow * kD);
+        }
 #pragma unroll
-            for (int b2 = 0; b2 < 2; ++b2) {
-                const int bb = 2 * hf + b2;
+        for (int b2 = 0; b2 < 2; ++b2) {
+            const int bb = 2 * hf + b2;
+            uint32_t wv[16];
+            float sc = 0.f;
+            if (row_ok) {
                 float x[32];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -307,32 +324,22 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
                 float a = 0.f;
 #pragma unroll
                 for (int k = 0; k < 32; ++k) a = fmaxf(a, fabsf(x[k]));
-                const float sc = __half2float(__float2half_rn(__fdiv_rn(a, 127.f)));
-                qsl_s[row * kNB + bb] = sc * G.qk_scale_log2;
+                sc = __half2float(__float2half_rn(__fdiv_rn(a, 127.f)));
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {   // 8 dims -> one 16-byte core-matrix row
-                    uint32_t wv[4];
+                for (int e = 0; e < 16; ++e)
+                    wv[e] = pack_half2((float)quant_i8(x[2 * e], sc), (float)quant_i8(x[2 * e + 1], sc));
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        wv[e] = pack_half2((float)quant_i8(x[8 * k + 2 * e], sc), (float)quant_i8(x[8 * k + 2 * e + 1], sc));
-                    const int dg = 4 * bb + k;
-                    qop[((row / 8) * C::Q_SBO + dg * 128 + (row % 8) * 16) / 16] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                }
+                for (int e = 0; e < 16; ++e) wv[e] = 0u;
             }
-        } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                qop[((row / 8) * C::Q_SBO + (8 * hf + k) * 128 + (row % 8) * 16) / 16] = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int b2 = 0; b2 < 2; ++b2) qsl_s[row * kNB + 2 * hf + b2] = 0.f;
+            qsl_s[row * kNB + bb] = sc * G.qk_scale_log2;
+            tmem_st16(tQ + lane_base + 16 * bb, wv);   // dims 32bb.. -> columns 16bb..
         }
-        fence_proxy_async_smem();
+        tmem_wait_st();
     }
     tc_fence_before();
-    __syncthreads();   // barriers, TMEM base and the Q operand in place
+    __syncthreads();   // the Q operand and the query scales in place
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tO = tmem + 4 * kPN;   // S_b at columns 64b, O at 256..383
 
     auto give_up = [&]() {
         if (!*bad) {
@@ -345,6 +352,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
         const bool okw = mbar_wait(b_, parity);
         return __all_sync(0xffffffffu, okw);
     };
+    auto wwait_poll = [&](uint32_t b_, uint32_t parity) {
+        const bool okw = mbar_wait_poll(b_, parity);
+        return __all_sync(0xffffffffu, okw);
+    };
     auto wbad = [&]() { return __any_sync(0xffffffffu, *bad != 0); };
 
     if (warp == kPCtlWarp) {
@@ -352,13 +363,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
         if (lane == 0) {
             // descriptors of the k16 steps differ from a base only in the start
             // address (16-byte units, no carry out of its 14 bits)
-            const uint64_t dQ = umma_desc(sbase + C::Q_OFF, 128, C::Q_SBO);
             const uint64_t dK0 = umma_desc(sbase + C::K_OFF, 128, C::K_SBO);
             const uint64_t dK1 = umma_desc(sbase + C::K_OFF + kPN * kD * 2, 128, C::K_SBO);
             for (int j = 0; j < n_tiles; ++j) {
                 if (*bad) break;
                 if (!mbar_wait(bar(C::B_KR + (j & 1)), (j >> 1) & 1)) { give_up(); break; }
-                if (j > 0 && !mbar_wait(bar(C::B_SFREE + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { give_up(); break; }
+                if (j > 0 && !mbar_wait_poll(bar(C::B_SFREE + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { give_up(); break; }
                 tc_fence_after();
                 const uint64_t dK = (j & 1) ? dK1 : dK0;
 #pragma unroll
@@ -366,7 +376,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
                         const uint64_t o = (uint64_t)((4 * bb + 2 * kk) * 8);
-                        umma_f16(tS + kPN * bb, dQ + o, dK + o, kIdQK, kk);
+                        umma_f16_ta(tS + kPN * bb, tQ + 16 * bb + 8 * kk, dK + o, kIdQK, kk);
                     }
                 umma_commit(bar(C::B_SFULL));
             }
@@ -406,15 +416,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
                 ++issued;
             };
             while (issued < min(C::RS, n_tiles)) issue();
-            const uint64_t dPH = umma_desc(sbase + C::PH_OFF, 128, C::PV_SBO);
-            const uint64_t dPL = umma_desc(sbase + C::PL_OFF, 128, C::PV_SBO);
             const uint64_t dVH0 = umma_desc(sbase + C::VH_OFF, 128, C::V_SBO);
             const uint64_t dVH1 = umma_desc(sbase + C::VH_OFF + C::VBUF, 128, C::V_SBO);
             const uint64_t dVL0 = umma_desc(sbase + C::VL_OFF, 128, C::V_SBO);
             const uint64_t dVL1 = umma_desc(sbase + C::VL_OFF + C::VBUF, 128, C::V_SBO);
             for (int j = 0; j < n_tiles; ++j) {
                 if (*bad) break;
-                if (!mbar_wait(bar(C::B_PREADY), j & 1) || !mbar_wait(bar(C::B_VR + (j & 1)), (j >> 1) & 1)) {
+                if (!mbar_wait_poll(bar(C::B_PREADY), j & 1) || !mbar_wait(bar(C::B_VR + (j & 1)), (j >> 1) & 1)) {
                     give_up();
                     break;
                 }
@@ -423,9 +431,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
 #pragma unroll
                 for (int ks = 0; ks < kPN / 16; ++ks) {
                     const uint64_t o = (uint64_t)(16 * ks);   // 2 ks * 128 bytes
-                    umma_f16(tO, dPH + o, dVH + o, kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
-                    umma_f16(tO, dPL + o, dVH + o, kIdPV, 1u);
-                    umma_f16(tO, dPH + o, dVL + o, kIdPV, 1u);
+                    umma_f16_ta(tO, tPH + 8 * ks, dVH + o, kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
+                    umma_f16_ta(tO, tPL + 8 * ks, dVH + o, kIdPV, 1u);
+                    umma_f16_ta(tO, tPH + 8 * ks, dVL + o, kIdPV, 1u);
                 }
                 umma_commit(bar(C::B_PV + (j & 1)));
                 // both converters are done with tile j's stage (the V warps
@@ -603,14 +611,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
         float *xm = reinterpret_cast<float *>(smem + C::XM_OFF);   // [parity][half][row]
         float m = -INFINITY, l = 0.f, mu = 0.f;
         bool o_live = false;   // O holds an earlier tile's P.V
-        uint4 *ph = reinterpret_cast<uint4 *>(smem + C::PH_OFF), *pl = reinterpret_cast<uint4 *>(smem + C::PL_OFF);
         constexpr int HP = kPN / 2;   // positions per half
         for (int j = 0; j < n_tiles; ++j) {
             if (wbad()) break;
             const int ob = j & 1;
             // this tile's scores, and (directly from the converters) its K
             // scales and slot records
-            if (!wwait(bar(C::B_SFULL), j & 1) || !wwait(bar(C::B_KR + ob), (j >> 1) & 1)) { give_up(); break; }
+            if (!wwait_poll(bar(C::B_SFULL), j & 1) || !wwait(bar(C::B_KR + ob), (j >> 1) & 1)) { give_up(); break; }
             tc_fence_after();
             const float *skf = reinterpret_cast<const float *>(smem + C::SKF_OFF) + ob * kNB * kPN + HP * hf;
             float s[HP];
@@ -676,7 +683,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
             xm[(ob * 2 + hf) * kPM + row] = mx;
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_X + quarter));
-            if (!wwait(bar(C::B_X + quarter), j & 1)) { give_up(); break; }
+            if (!wwait_poll(bar(C::B_X + quarter), j & 1)) { give_up(); break; }
             mx = fmaxf(mx, xm[(ob * 2 + (hf ^ 1)) * kPM + row]);
             const bool need = mx > m + kSlack;
             const bool wneed = o_live && __any_sync(0xffffffffu, need);   // rescale O (whole warp)
@@ -699,7 +706,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
             l += lsum.x + lsum.y;
             // P(j) may overwrite P(j-1) once P.V(j-1) is done; O is then stable
             if (j > 0) {
-                if (!wwait(bar(C::B_PV + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { give_up(); break; }
+                if (!wwait_poll(bar(C::B_PV + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { give_up(); break; }
                 tc_fence_after();
             }
             if (wneed) {   // O *= alpha on this half's columns (1 on the rows that keep their max)
@@ -714,24 +721,22 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
                 }
                 tmem_wait_st();
             }
+            {   // P of this half: positions 32hf.. -> columns 16hf.. of the P areas
+                uint32_t hw[HP / 2], lw[HP / 2];
 #pragma unroll
-            for (int pg = 0; pg < HP / 8; ++pg) {
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 x = make_float2(s[8 * pg + 2 * e], s[8 * pg + 2 * e + 1]);
+                for (int e = 0; e < HP / 2; ++e) {
+                    const float2 x = make_float2(s[2 * e], s[2 * e + 1]);
                     const uint32_t hp = pack_half2(x.x, x.y);
                     const float2 hf2 = __half22float2(*reinterpret_cast<const __half2 *>(&hp));
                     const float2 lo = sub2(x, hf2);
                     hw[e] = hp;
                     lw[e] = pack_half2(lo.x, lo.y);
                 }
-                const int o = ((row / 8) * C::PV_SBO + ((HP / 8) * hf + pg) * 128 + (row % 8) * 16) / 16;
-                ph[o] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                pl[o] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                tmem_st16(tPH + lane_base + (HP / 2) * hf, hw);
+                tmem_st16(tPL + lane_base + (HP / 2) * hf, lw);
+                tmem_wait_st();
             }
             o_live = true;
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_PREADY));
