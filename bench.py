@@ -123,10 +123,11 @@ def launches_of(grp, fused):
     return (0 if fused.append else len(grp)) + groups * (2 if fused.call.ws is not None else 1)
 
 
-def profiled_traffic(workload):
-    """DRAM bytes per split-kernel launch from the committed ncu summary, if it
-    was taken on the current kernel sources (else None)."""
-    p = os.path.join(ROOT, "profiles", "split_attn_%s.md" % workload)
+def profiled_traffic(workload, kernel="split_attn"):
+    """DRAM bytes per step of the dominant kernel from the committed ncu
+    summary profiles/<kernel>_<workload>.md, if it was taken on the current
+    kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload))
     if not os.path.exists(p):
         return None
     txt = open(p).read()
@@ -549,11 +550,15 @@ def main():
                       "duration_basis": "timed region / split launches (the per-step combine included)",
                       "decode_call_us_event_bracketed": 1e3 * dec_ms, "algorithmic_bytes": int(dec_bytes)}
                      if not tensor_bound else
-                     {"bound": "tensor", "kernel": "split_attn over row tiles (fp16 mma.sync) + combine",
+                     {"bound": "tensor",
+                      "kernel": "prefill_attn (tcgen05 MMAs, TMEM accumulators, 128-row tiles) + combine"
+                      if os.environ.get("KVQ_PREFILL", "1") != "0" else "split_attn over 32-row tiles (mma.sync)",
                       "achieved": flops / (dec_ms * 1e-3) / 1e12, "peak": tpeak,
                       "peak_kind": tpeak_kind + " bf16 cuBLAS sustained (fp16 has the same nominal rate)",
                       "unit": "TFLOP/s", "frac": flops / (dec_ms * 1e-3) / 1e12 / tpeak,
-                      "traffic": profiled_traffic(args.workload), "duration_us": 1e3 * dec_ms,
+                      "traffic": profiled_traffic(args.workload, "prefill_attn"
+                                                  if os.environ.get("KVQ_PREFILL", "1") != "0" else "split_attn"),
+                      "duration_us": 1e3 * dec_ms,
                       "duration_basis": "event-bracketed attention call (split + combine), appends outside",
                       "algorithmic_flops": int(flops), "kv_bytes": int(dec_bytes)}),
         "per_cache_calls_ms_per_step": sep_ms_per_step,
