@@ -31,6 +31,8 @@ _lib = None
 
 VT_Q4_0 = 0
 VT_Q8_0 = 1
+KT_I8 = 0    # K: int8 codes + fp16 scale per 32
+KT_F16 = 1   # K: the fp16 values (F16 K)
 QBLK = 32
 
 
@@ -67,6 +69,10 @@ def _load():
                 i32, i32, i32, i32, P, P, P, P,
                 i32, i32, P, i32, ctypes.c_double, P,
                 P, P, P, P, P, P, i32]
+            lib.orc_decode_seq_f16k.argtypes = [
+                i32, i32, i32, i32, P, P, P,
+                i32, i32, P, i32, ctypes.c_double, P,
+                P, P, P, i32]
             _lib = lib
     return _lib
 
@@ -121,12 +127,14 @@ def quant_q4_0_block(x16: np.ndarray):
     return packed, int(scale[0])
 
 
-def quantize_kv(k16: np.ndarray, v16: np.ndarray, v_type: int):
+def quantize_kv(k16: np.ndarray, v16: np.ndarray, v_type: int, k_type: int = KT_I8):
     """Quantize token-major fp16 K, V [n_tok][n_kv_heads][head_dim] (uint16 bit
     patterns or float16) into the head-major cache layout.
 
     Returns dict(kq int8 [H][n][D], ks uint16 [H][n][D/32],
-                 vq uint8 [H][n][D/2 or D], vs uint16 [H][n][D/32]).
+                 vq uint8 [H][n][D/2 or D], vs uint16 [H][n][D/32]); with
+    k_type KT_F16 ("F16 K" of the RDNA3 page's title and KLD tables) K is kept
+    as its fp16 bits, k16 uint16 [H][n][D], instead of kq / ks.
     """
     k = _c(np.asarray(k16).view(np.uint16), np.uint16)
     v = _c(np.asarray(v16).view(np.uint16), np.uint16)
@@ -139,6 +147,9 @@ def quantize_kv(k16: np.ndarray, v16: np.ndarray, v_type: int):
                                  _ptr(out["ks"]), _ptr(out["vq"]), _ptr(out["vs"]))
     if rc:
         raise ValueError("orc_quantize_kv failed (%d)" % rc)
+    if k_type == KT_F16:
+        del out["kq"], out["ks"]
+        out["k16"] = np.ascontiguousarray(k.transpose(1, 0, 2))
     return out
 
 
@@ -152,6 +163,10 @@ def decode_seq(cache: dict, q16: np.ndarray, head_map, causal: bool, sm_scale: f
     dict(out fp64 [t_q][Hq][D], lse fp64 [t_q][Hq]) plus, on request, the Q
     codes/scales and the exact per-block integer scores I [t_q][Hq][L][D/32].
     """
+    if "k16" in cache:
+        if want_codes or want_scores:
+            raise ValueError("an F16-K cache has no Q codes or integer block scores")
+        return _decode_seq_f16k(cache, q16, head_map, causal, sm_scale, v_type, row_mask, n_threads)
     kq, ks, vq, vs = (_c(cache["kq"], np.int8), _c(cache["ks"], np.uint16),
                       _c(cache["vq"], np.uint8), _c(cache["vs"], np.uint16))
     H, L, D = kq.shape
@@ -174,6 +189,25 @@ def decode_seq(cache: dict, q16: np.ndarray, head_map, causal: bool, sm_scale: f
                                 _ptr(rm), int(n_threads))
     if rc:
         raise ValueError("orc_decode_seq failed (%d)" % rc)
+    return res
+
+
+def _decode_seq_f16k(cache, q16, head_map, causal, sm_scale, v_type, row_mask, n_threads):
+    """Decode attention over an F16-K cache (quantize_kv with KT_F16): the
+    score is sm_scale * q.k over the fp16 values, Q not quantized."""
+    k, vq, vs = _c(cache["k16"], np.uint16), _c(cache["vq"], np.uint8), _c(cache["vs"], np.uint16)
+    H, L, D = k.shape
+    q = _c(np.asarray(q16).view(np.uint16), np.uint16)
+    t_q, Hq, Dq = q.shape
+    assert Dq == D
+    hm = _c(head_map, np.int32)
+    res = dict(out=np.zeros((t_q, Hq, D), np.float64), lse=np.zeros((t_q, Hq), np.float64))
+    rm = None if row_mask is None else _c(row_mask, np.uint8)
+    rc = _load().orc_decode_seq_f16k(L, H, D, v_type, _ptr(k), _ptr(vq), _ptr(vs), t_q, Hq, _ptr(hm),
+                                     int(bool(causal)), float(sm_scale), _ptr(q), _ptr(res["out"]),
+                                     _ptr(res["lse"]), _ptr(rm), int(n_threads))
+    if rc:
+        raise ValueError("orc_decode_seq_f16k failed (%d)" % rc)
     return res
 
 

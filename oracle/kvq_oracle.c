@@ -19,10 +19,15 @@
  *    domain, casts are deferred).
  *  - Attention is textbook softmax attention over those dequantized tensors,
  *    evaluated two-pass (max, then sum) in fp64.
+ *  - F16 K variant ("Flash Attention for llama.cpp on RDNA3", title and KLD
+ *    tables: F16 K with q4_0 V): K is kept as the fp16 values themselves and
+ *    Q is not quantized, so the score is sm_scale * sum_j q_j * k_j over the
+ *    fp16 values (orc_decode_seq_f16k).
  *
  * Byte layouts emitted (and read back) by this file:
  *  - K codes: int8 [n_kv_heads][n_tok][head_dim] (4 per 32-bit word,
  *    little-endian: byte i of word w is element 4w+i).
+ *  - F16 K: fp16 bit patterns [n_kv_heads][n_tok][head_dim].
  *  - K / V scales: fp16 bit patterns [n_kv_heads][n_tok][head_dim/32].
  *  - V q8_0 codes: int8 [n_kv_heads][n_tok][head_dim].
  *  - V q4_0 codes: uint8 [n_kv_heads][n_tok][head_dim/2]; in each 32-block,
@@ -182,6 +187,38 @@ int orc_quantize_kv(int n_tok, int n_kv_heads, int head_dim, int v_type,
 }
 
 /*
+ * Softmax over the scores s[0..n-1] of one row (two passes: max, then sum)
+ * and the weighted sum of the dequantized V rows of kv head h into o
+ * (head_dim values, zeroed by the caller).  Returns lse = m + ln(sum).
+ */
+static double orc_attend(int n, const double *s, int L, int h, int head_dim, int v_type,
+                         const uint8_t *vq, const uint16_t *vs, double *o)
+{
+    int nb = head_dim / ORC_QBLK;
+    int vbytes = (v_type == ORC_VT_Q4_0) ? head_dim / 2 : head_dim;
+    int vblk = (v_type == ORC_VT_Q4_0) ? 16 : 32;
+    double m = -INFINITY;
+    for (int t = 0; t < n; ++t)
+        if (s[t] > m)
+            m = s[t];
+    double z = 0.0;
+    for (int t = 0; t < n; ++t) {
+        double p = exp(s[t] - m);
+        size_t row = (size_t)h * L + t;
+        z += p;
+        for (int b = 0; b < nb; ++b) {
+            const uint8_t *vb = vq + row * vbytes + b * vblk;
+            double d = orc_f16_to_f64(vs[row * nb + b]);
+            for (int j = 0; j < ORC_QBLK; ++j)
+                o[b * ORC_QBLK + j] += p * orc_v_deq(v_type, vb, d, j);
+        }
+    }
+    for (int j = 0; j < head_dim; ++j)
+        o[j] /= z;
+    return m + log(z);
+}
+
+/*
  * Decode attention for ONE sequence of length L whose quantized cache is held
  * in the layout above with n_tok = L (positions 0..L-1).
  *
@@ -211,8 +248,6 @@ int orc_decode_seq(int L, int n_kv_heads, int head_dim, int v_type,
     if (head_dim % ORC_QBLK || head_dim > 1024 || L < 0 || t_q < 1)
         return 1;
     int nb = head_dim / ORC_QBLK;
-    int vbytes = (v_type == ORC_VT_Q4_0) ? head_dim / 2 : head_dim;
-    int vblk = (v_type == ORC_VT_Q4_0) ? 16 : 32;
     int n_rows = t_q * n_q_heads;
     for (int h = 0; h < n_q_heads; ++h)
         if (head_map[h] < 0 || head_map[h] >= n_kv_heads)
@@ -265,26 +300,61 @@ int orc_decode_seq(int L, int n_kv_heads, int head_dim, int v_type,
             }
             s[t] = sm_scale * acc;
         }
-        /* two-pass softmax: max, then sum */
-        double m = -INFINITY;
-        for (int t = 0; t < n; ++t)
-            if (s[t] > m)
-                m = s[t];
-        double z = 0.0;
-        for (int t = 0; t < n; ++t) {
-            double p = exp(s[t] - m);
-            size_t row = (size_t)h * L + t;
-            z += p;
-            for (int b = 0; b < nb; ++b) {
-                const uint8_t *vb = vq + row * vbytes + b * vblk;
-                double d = orc_f16_to_f64(vs[row * nb + b]);
-                for (int j = 0; j < ORC_QBLK; ++j)
-                    o[b * ORC_QBLK + j] += p * orc_v_deq(v_type, vb, d, j);
-            }
-        }
+        lse[r] = orc_attend(n, s, L, h, head_dim, v_type, vq, vs, o);
+        free(s);
+    }
+    return 0;
+}
+
+/*
+ * The same decode attention with K kept as fp16 values (k16: fp16 bits
+ * [n_kv_heads][L][head_dim]) and Q not quantized: the score of position t is
+ * sm_scale * sum_j q_j * k_tj over the fp16 values, in fp64.  V, the causal
+ * tail, out and lse as in orc_decode_seq.
+ */
+int orc_decode_seq_f16k(int L, int n_kv_heads, int head_dim, int v_type, const uint16_t *k16,
+                        const uint8_t *vq, const uint16_t *vs,
+                        int t_q, int n_q_heads, const int32_t *head_map, int causal,
+                        double sm_scale, const uint16_t *q16, double *out, double *lse,
+                        const uint8_t *row_mask, int n_threads)
+{
+    if (head_dim % ORC_QBLK || head_dim > 1024 || L < 0 || t_q < 1)
+        return 1;
+    int n_rows = t_q * n_q_heads;
+    for (int h = 0; h < n_q_heads; ++h)
+        if (head_map[h] < 0 || head_map[h] >= n_kv_heads)
+            return 2;
+    if (n_threads < 1)
+        n_threads = 1;
+
+#pragma omp parallel for schedule(dynamic, 1) num_threads(n_threads)
+    for (int r = 0; r < n_rows; ++r) {
+        if (row_mask && !row_mask[r])
+            continue;
+        int i = r / n_q_heads;
+        int h = head_map[r % n_q_heads];
+        double qv[1024];
+        const uint16_t *qx = q16 + (size_t)r * head_dim;
         for (int j = 0; j < head_dim; ++j)
-            o[j] /= z;
-        lse[r] = m + log(z);
+            qv[j] = orc_f16_to_f64(qx[j]);
+        int last = causal ? L - t_q + i : L - 1;   /* inclusive */
+        double *o = out + (size_t)r * head_dim;
+        for (int j = 0; j < head_dim; ++j)
+            o[j] = 0.0;
+        if (last < 0) {
+            lse[r] = -INFINITY;
+            continue;
+        }
+        int n = last + 1;
+        double *s = (double *)malloc(sizeof(double) * (size_t)n);
+        for (int t = 0; t < n; ++t) {
+            const uint16_t *kx = k16 + ((size_t)h * L + t) * head_dim;
+            double acc = 0.0;
+            for (int j = 0; j < head_dim; ++j)
+                acc += qv[j] * orc_f16_to_f64(kx[j]);
+            s[t] = sm_scale * acc;
+        }
+        lse[r] = orc_attend(n, s, L, h, head_dim, v_type, vq, vs, o);
         free(s);
     }
     return 0;

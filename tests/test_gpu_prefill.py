@@ -81,6 +81,15 @@ def test_uneven_head_map_ragged_row_tiles():
     _check_all(Case(spec).build(), head_map=hm)
 
 
+def test_batched_chunks_of_ragged_contexts():
+    """Three sequences, each with its own context length, one 80-token chunk
+    each, in one call (one work group of three sequences)."""
+    spec = W.make_spec("prefill", ctx=1400, t_q=80, n_seqs=3, v_type=1)[0]
+    spec.lengths[:] = [1400, 333, 980]
+    spec.segments[:] = [W._cuts(spec.rng(9, b), int(L), 2, 80) for b, L in enumerate(spec.lengths)]
+    _check_all(Case(spec).build())
+
+
 def test_non_causal_chunk():
     spec = W.make_spec("prefill", ctx=2000, t_q=100, causal=False, v_type=0)[0]
     _check_all(Case(spec).build())

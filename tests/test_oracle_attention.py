@@ -7,7 +7,11 @@
   keys return the mean of dequantized V, t_q = 1 causal equals non-causal,
   splitting the positions and merging the parts by log-sum-exp equals the
   unsplit result, and an online (running-max) softmax equals the two-pass one;
-* a row that sees no position returns out = 0, lse = -inf.
+* a row that sees no position returns out = 0, lse = -inf;
+* the F16-K variant: on integer K and Q with block absmax 127 (int8 scales
+  exactly 1, codes equal to the values) it agrees bit for bit with the int8
+  path; identical keys give the mean of V with lse = s + ln n; a dominant key
+  selects its V row; K is stored unchanged and V as on the int8 path.
 """
 import numpy as np
 import pytest
@@ -191,3 +195,91 @@ def test_workload_recipe_runs_through_oracle(orc):
     out, lse = _textbook(c, q[0], orc.default_head_map(spec.n_q_heads, spec.n_kv_heads),
                          spec.causal, 1 / np.sqrt(128), spec.v_type, orc, res)
     assert np.max(np.abs(res["out"] - out)) < 1e-11
+
+
+# ---------------------------------------------------------------- F16 K --
+# The F16-K variant ("Flash Attention for llama.cpp on RDNA3", title and KLD
+# tables: F16 K with q4_0 V) keeps K as fp16 values and does not quantize Q.
+
+def _integer_case(seed, n, Hkv, Hq, D, t_q):
+    """K and Q integers in [-127, 127] with every 32-block's absmax exactly
+    127: the int8 rule then gives scale 1 and codes equal to the values."""
+    rng = np.random.default_rng(seed)
+
+    def ints(shape):
+        x = rng.integers(-126, 127, size=shape).astype(np.float64)
+        xb = x.reshape(shape[:-1] + (shape[-1] // 32, 32))
+        xb[..., 0] = np.where(rng.integers(0, 2, size=xb.shape[:-1]) == 0, 127.0, -127.0)
+        return xb.reshape(shape).astype(np.float16)
+
+    k = ints((n, Hkv, D))
+    q = ints((t_q, Hq, D))
+    v = rng.standard_normal((n, Hkv, D)).astype(np.float16)
+    return k, v, q
+
+
+@pytest.mark.parametrize("vt", [0, 1])
+def test_f16k_equals_int8_path_on_integer_inputs(vt):
+    """On integer K and Q with block absmax 127 both K paths compute the same
+    exact scores, so out and lse agree bit for bit."""
+    import oracle
+    k, v, q = _integer_case(11, 70, 2, 6, 128, 3)
+    ci = oracle.quantize_kv(k, v, vt)
+    assert np.array_equal(ci["ks"].view(np.float16).astype(np.float64), np.ones_like(ci["ks"], np.float64))
+    assert np.array_equal(ci["kq"].astype(np.float64), k.astype(np.float64).transpose(1, 0, 2))
+    cf = oracle.quantize_kv(k, v, vt, k_type=oracle.KT_F16)
+    hm = oracle.default_head_map(6, 2)
+    for causal in (False, True):
+        a = oracle.decode_seq(ci, q, hm, causal, 0.01, vt)
+        b = oracle.decode_seq(cf, q, hm, causal, 0.01, vt)
+        assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["lse"], b["lse"])
+
+
+def test_f16k_stores_k_unchanged_and_v_as_the_int8_path():
+    import oracle
+    k, v, q = _case(12, 40, 2, 4, 128, 1, 0)
+    ci = oracle.quantize_kv(k, v, 0)
+    cf = oracle.quantize_kv(k, v, 0, k_type=oracle.KT_F16)
+    assert np.array_equal(cf["k16"], k.view(np.uint16).transpose(1, 0, 2))
+    assert np.array_equal(cf["vq"], ci["vq"]) and np.array_equal(cf["vs"], ci["vs"])
+    with pytest.raises(ValueError):
+        oracle.decode_seq(cf, q, oracle.default_head_map(4, 2), False, 0.1, 0, want_scores=True)
+
+
+@pytest.mark.parametrize("vt", [0, 1])
+def test_f16k_identical_keys_give_the_mean_of_v(vt):
+    """All keys equal: every visible position scores the same, so out is the
+    mean of the dequantized V rows a query token sees and lse = s + ln n,
+    with s = sm_scale * q.k over the fp16 values (Q unquantized)."""
+    import oracle
+    rng = np.random.default_rng(13)
+    n, D, t_q = 37, 128, 4
+    key = rng.standard_normal(D).astype(np.float16)
+    k = np.broadcast_to(key, (n, 1, D)).copy()
+    v = rng.standard_normal((n, 1, D)).astype(np.float16)
+    q = rng.standard_normal((t_q, 3, D)).astype(np.float16)
+    c = oracle.quantize_kv(k, v, vt, k_type=oracle.KT_F16)
+    V = _deq_v(oracle.quantize_kv(k, v, vt), vt, oracle)[0]
+    res = oracle.decode_seq(c, q, np.zeros(3, np.int32), True, 0.125, vt)
+    for i in range(t_q):
+        m = n - t_q + i + 1
+        for h in range(3):
+            s = 0.125 * float(np.dot(q[i, h].astype(np.float64), key.astype(np.float64)))
+            np.testing.assert_allclose(res["out"][i, h], V[:m].mean(axis=0), rtol=0, atol=1e-12)
+            assert abs(res["lse"][i, h] - (s + np.log(m))) < 1e-12
+
+
+def test_f16k_dominant_key_selects_its_value():
+    """One key aligned with the query at a large scale: the softmax puts all
+    its weight there, out equals that position's dequantized V row."""
+    import oracle
+    rng = np.random.default_rng(14)
+    n, D = 50, 128
+    q = rng.standard_normal((1, 1, D)).astype(np.float16)
+    k = (rng.standard_normal((n, 1, D)) * 0.01).astype(np.float16)
+    k[17, 0] = (q[0, 0].astype(np.float32) * 4).astype(np.float16)
+    v = rng.standard_normal((n, 1, D)).astype(np.float16)
+    c = oracle.quantize_kv(k, v, 1, k_type=oracle.KT_F16)
+    V = _deq_v(oracle.quantize_kv(k, v, 1), 1, oracle)[0]
+    res = oracle.decode_seq(c, q, np.zeros(1, np.int32), False, 1.0, 1)
+    np.testing.assert_allclose(res["out"][0, 0], V[17], rtol=0, atol=1e-9)
