@@ -47,6 +47,8 @@ WORKLOADS = {
     "batched": "batched decode: 64 sequences, lengths U[1024, 32768], 32q/8kv heads, V q8_0, outliers x10",
     "verify": "multi-token verify: 16 sequences x 4 causal query tokens, 32768 positions, 64q/8kv heads, V q4_0",
     "tiny": "tiny: 1 kv head, 4 query heads, 256 positions, V q8_0",
+    "long_f16k": "long-context decode with F16 K (K kept as fp16 values, query unquantized) and q4_0 V: "
+                 "main 40q/8kv + draft 16q/4kv heads, 131072 positions each in 4 segments, 1 query token",
     "prefill": "chunked prefill: one 512-token chunk (causal among its tokens) over 32768 positions, "
                "32q/8kv heads, V q4_0; the chunk is appended by kvq_append, then attended",
 }
@@ -318,7 +320,7 @@ def main():
     data = [HostData(s) for s in specs]
     # the step's appends run inside the attention kernel when every cache
     # takes at most KVQ_MAX_T_Q_APPEND tokens per step; else kvq_append first
-    fusable = all(s.t_q <= kvq.MAX_T_Q_APPEND for s in specs)
+    fusable = all(s.t_q <= kvq.MAX_T_Q_APPEND and s.k_type == W.K_I8 for s in specs)
     if args.mode == "profile":
         grp = [DecodeSet(d, dev) for d in data]
         for ds in grp:

@@ -71,11 +71,28 @@ typedef enum kvq_vtype {
 } kvq_vtype;
 
 /*
+ * K format.  KVQ_K_I8 (the default): int8 codes + fp16 scale per 32 values,
+ * and the query is quantized per 32-block the same way, so q.k is a sum of
+ * exact integer block dots ("Flash Attention for llama.cpp on RDNA3", first
+ * paragraph).  KVQ_K_F16: K kept as its fp16 values and the query used
+ * unquantized (the F16 K / q4_0 V configuration of the same page's title and
+ * KLD tables), score = sm_scale * q.k with fp32 accumulation.  F16 K supports
+ * kvq_append and the decode calls without fused append (k16_new / v16_new
+ * must be NULL) and not kvq_debug_qk.
+ */
+typedef enum kvq_ktype {
+    KVQ_K_I8 = 0,
+    KVQ_K_F16 = 1
+} kvq_ktype;
+
+/*
  * One append-only segment of one sequence.  All four arrays are device memory,
  * 16-byte aligned and head-major: kv head h owns cap token rows starting at row
  * h*cap, and token t of the segment is row t of its head.  Row sizes:
- *   k_q  int8 codes, head_dim bytes per row
+ *   k_q  int8 codes, head_dim bytes per row (F16 K: fp16 values, 2*head_dim
+ *        bytes per row)
  *   k_s  fp16 scales, head_dim/32 per row, plain [kv_head][token][block] order
+ *        (F16 K: unused, may be NULL)
  *   v_q  q4_0: head_dim/2 bytes per row, in each 32-block byte j holds element j
  *              (low nibble) and element j+16 (high nibble);
  *        q8_0: int8 codes, head_dim bytes per row
@@ -90,6 +107,9 @@ typedef enum kvq_vtype {
  *   v_q q4_0  (sub*32 + 4*((j%16)/2) + cu)*16 + 4*(j/16) + 2*e + j%2
  *   v_q q8_0  ((2*sub + j/64)*32 + 4*((j%32)/4) + cu)*16 + 8*((j/32)%2)
  *             + 4*((j%4)/2) + 2*(j%2) + e
+ * and for F16 K, with j the element (not byte) of the row, the fp16 value of
+ * element j of token u sits at byte offset (a 4096-byte tile)
+ *   k_q f16   (j/16)*512 + (4*(u%8) + (j%8)/2)*16 + 4*(u/8 + 2*((j%16)/8)) + 2*(j%2)
  * (head_dim 128).  Only kvq_append writes code bytes, so callers never see the
  * permutation unless they read the arrays themselves.
  * cap  : capacity in tokens, a positive multiple of KVQ_SEG_ALIGN.
@@ -125,6 +145,8 @@ typedef struct kvq_cache {
     int32_t max_segs;
     int32_t *n_segs;
     kvq_segment *segs;
+    int32_t k_type;            /* kvq_ktype (0 = KVQ_K_I8)                        */
+    int32_t reserved;
 } kvq_cache;
 
 /*

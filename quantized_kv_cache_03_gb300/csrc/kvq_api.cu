@@ -19,7 +19,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
     bool ready = false;
     int n_sms = 0;
-    int ctas[2][5] = {};   // [v_type][n_tiles8] resident split CTAs per SM
+    int ctas[2][2][5] = {};   // [k_type][v_type][n_tiles8] resident split CTAs per SM
     unsigned int *timeouts = nullptr;   // device address of g_wait_timeouts
 };
 
@@ -54,10 +54,12 @@ kvq_status device_setup(DeviceInfo **out)
         const int nts[3] = {1, 2, 4};
         for (int i = 0; i < 3; ++i) {
             const int nt = nts[i];
-            if (prepare_split_q4(nt, false, &d.ctas[KVQ_V_Q4_0][nt]) != cudaSuccess ||
-                prepare_split_q8(nt, false, &d.ctas[KVQ_V_Q8_0][nt]) != cudaSuccess ||
-                prepare_split_q4(nt, true, nullptr) != cudaSuccess ||
-                prepare_split_q8(nt, true, nullptr) != cudaSuccess) {
+            if (prepare_split_q4(nt, KVQ_K_I8, false, &d.ctas[KVQ_K_I8][KVQ_V_Q4_0][nt]) != cudaSuccess ||
+                prepare_split_q8(nt, KVQ_K_I8, false, &d.ctas[KVQ_K_I8][KVQ_V_Q8_0][nt]) != cudaSuccess ||
+                prepare_split_q4(nt, KVQ_K_F16, false, &d.ctas[KVQ_K_F16][KVQ_V_Q4_0][nt]) != cudaSuccess ||
+                prepare_split_q8(nt, KVQ_K_F16, false, &d.ctas[KVQ_K_F16][KVQ_V_Q8_0][nt]) != cudaSuccess ||
+                prepare_split_q4(nt, KVQ_K_I8, true, nullptr) != cudaSuccess ||
+                prepare_split_q8(nt, KVQ_K_I8, true, nullptr) != cudaSuccess) {
                 cudaGetLastError();
                 return KVQ_ERR_CUDA;
             }
@@ -95,6 +97,8 @@ kvq_status check_cache(const kvq_cache *c)
     if (c->n_seqs < 0 || c->n_kv_heads < 1 || c->n_kv_heads > KVQ_MAX_HEADS || c->max_segs < 1)
         return KVQ_ERR_INVALID_ARG;
     if (c->v_type != KVQ_V_Q4_0 && c->v_type != KVQ_V_Q8_0) return KVQ_ERR_INVALID_ARG;
+    if (c->k_type != KVQ_K_I8 && c->k_type != KVQ_K_F16) return KVQ_ERR_INVALID_ARG;
+    const bool f16k = c->k_type == KVQ_K_F16;   // no K scales
     if (c->head_dim != KVQ_HEAD_DIM) return c->head_dim % KVQ_QBLOCK ? KVQ_ERR_INVALID_ARG : KVQ_ERR_UNSUPPORTED;
     if (c->n_seqs == 0) return KVQ_OK;
     if (!c->n_segs || !c->segs) return KVQ_ERR_INVALID_ARG;
@@ -103,7 +107,7 @@ kvq_status check_cache(const kvq_cache *c)
         if (ns < 0 || ns > c->max_segs || ns > kMaxSegsLaunch) return KVQ_ERR_INVALID_ARG;
         for (int k = 0; k < ns; ++k) {
             const kvq_segment &s = seg_of(c, b, k);
-            if (!s.k_q || !s.k_s || !s.v_q || !s.v_s) return KVQ_ERR_INVALID_ARG;
+            if (!s.k_q || (!s.k_s && !f16k) || !s.v_q || !s.v_s) return KVQ_ERR_INVALID_ARG;
             if (!aligned16(s.k_q) || !aligned16(s.k_s) || !aligned16(s.v_q) || !aligned16(s.v_s))
                 return KVQ_ERR_INVALID_ARG;
             if (s.cap <= 0 || s.cap % KVQ_SEG_ALIGN || s.len < 0 || s.len > s.cap) return KVQ_ERR_INVALID_ARG;
@@ -158,6 +162,8 @@ kvq_status prepare_desc(Desc &d, const int32_t *head_map, bool need_ptrs, bool d
     int gmax = 0;
     for (int k = 0; k < H; ++k) gmax = std::max(gmax, cnt[k]);
     d.max_rows = gmax * d.t_q;   // at most 256 * 4096: row tiles of <= KVQ_MAX_ROWS
+    // F16 K: no fused append and no integer-score dump
+    if (c->k_type == KVQ_K_F16 && (dump || d.k_new || d.v_new)) return KVQ_ERR_UNSUPPORTED;
     if ((d.k_new != nullptr) != (d.v_new != nullptr)) return KVQ_ERR_INVALID_ARG;
     if (d.k_new) {
         if (dump || !aligned16(d.k_new) || !aligned16(d.v_new)) return KVQ_ERR_INVALID_ARG;
@@ -184,7 +190,7 @@ bool prefill_kernel_for(const Desc &d, bool dump)
 {
     const char *e = std::getenv("KVQ_PREFILL");
     const bool on = !(e && e[0] == '0');
-    return on && !dump && !d.k_new && d.max_rows > KVQ_MAX_ROWS;
+    return on && !dump && !d.k_new && d.c->k_type == KVQ_K_I8 && d.max_rows > KVQ_MAX_ROWS;
 }
 int round_up(long long x, int m) { return (int)((x + m - 1) / m * m); }
 
@@ -211,7 +217,7 @@ struct Unit {
 // grid.  prefill: the tcgen05 kernel (128-row tiles) for calls with more query
 // rows per kv head than the split kernel's 32-row tile and no fused append.
 struct Launch {
-    int v_type = 0, nt = 1;
+    int v_type = 0, k_type = 0, nt = 1;
     bool prefill = false;
     int chunk = KVQ_SEG_ALIGN;
     int n_ctas = 0, n_rows = 0;   // split CTAs, combine rows
@@ -292,7 +298,7 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
         const kvq_cache *c = ds[di].c;
         if (c->n_seqs == 0) continue;
         const bool pf = prefill_kernel_for(ds[di], dump);
-        if (!cur.units.empty() && (cur.v_type != c->v_type || cur.prefill != pf)) flush();
+        if (!cur.units.empty() && (cur.v_type != c->v_type || cur.k_type != c->k_type || cur.prefill != pf)) flush();
         int b = 0;
         while (b < c->n_seqs) {
             const bool new_desc = last_d != di;
@@ -305,6 +311,7 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
             }
             if (cur.units.empty()) {
                 cur.v_type = c->v_type;
+                cur.k_type = c->k_type;
                 cur.prefill = pf;
             }
             heads += need_heads;
@@ -324,12 +331,12 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
     }
     flush();
     for (Launch &ln : out) {
-        const int slots = ln.prefill ? dev->n_sms : std::max(1, dev->n_sms * std::max(1, dev->ctas[ln.v_type][ln.nt]));
+        const int slots = ln.prefill ? dev->n_sms : std::max(1, dev->n_sms * std::max(1, dev->ctas[ln.k_type][ln.v_type][ln.nt]));
         ln.chunk = choose_chunk(ds, ln, slots, ln.prefill ? kPrefillPositions : split_warps(ln.nt) * kWTile);
         for (Unit &u : ln.units) {
             const Desc &d = ds[u.d];
             u.n_split = std::max(1, (u.reach + ln.chunk - 1) / ln.chunk);
-            u.n_rt = (d.max_rows + tile_rows(ln) - 1) / tile_rows(ln);
+            u.n_rt = (d.max_rows + tile_rows(ln) - 1) / tile_rows(ln);   // 1 unless nt == 4 or prefill
             const long long n = (long long)u.n_rt * u.n_split * d.c->n_kv_heads * u.nb;
             if (ln.n_ctas + n > INT_MAX) return KVQ_ERR_UNSUPPORTED;
             u.cta0 = ln.n_ctas;
@@ -468,8 +475,8 @@ kvq_status run(std::vector<Desc> &ds, bool dump, void *workspace, size_t workspa
             e = (ln.v_type == KVQ_V_Q4_0) ? launch_prefill_q4(p, ln.n_ctas, stream, pdl)
                                           : launch_prefill_q8(p, ln.n_ctas, stream, pdl);
         else
-            e = (ln.v_type == KVQ_V_Q4_0) ? launch_split_q4(p, ln.nt, ln.n_ctas, dump, stream, pdl)
-                                          : launch_split_q8(p, ln.nt, ln.n_ctas, dump, stream, pdl);
+            e = (ln.v_type == KVQ_V_Q4_0) ? launch_split_q4(p, ln.nt, ln.k_type, ln.n_ctas, dump, stream, pdl)
+                                          : launch_split_q8(p, ln.nt, ln.k_type, ln.n_ctas, dump, stream, pdl);
         if (e == cudaSuccess && ln.n_rows > 0) e = launch_combine(cp, ln.n_rows, stream, pdl);
         if (e != cudaSuccess) {
             cudaGetLastError();
@@ -577,7 +584,7 @@ kvq_status kvq_append(kvq_cache *c, int32_t n_seqs_in, const int32_t *seq_ids, c
             ++i;
         }
         if (p.n_entries == 0) continue;
-        if (launch_append(p, c->v_type, max_rows, s, pdl) != cudaSuccess) {
+        if (launch_append(p, c->v_type, c->k_type, max_rows, s, pdl) != cudaSuccess) {
             cudaGetLastError();
             return KVQ_ERR_CUDA;
         }

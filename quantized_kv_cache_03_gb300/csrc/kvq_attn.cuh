@@ -65,7 +65,7 @@ namespace kvq {
 
 
 
-template <int NT, int VT>
+template <int NT, int VT, int KT = KVQ_K_I8>
 struct SplitCfg {
     static constexpr int WARPS = split_warps(NT);
     static constexpr int THREADS = WARPS * 32;
@@ -74,21 +74,25 @@ struct SplitCfg {
     static constexpr int MIN_CTAS = (NT == 1) ? (16 / WARPS > 0 ? 16 / WARPS : 1) : 1;
     static constexpr int QROWS = (8 * NT > WARPS) ? 8 * NT : WARPS;   // query rows kept in smem
     static_assert(QROWS % WARPS == 0, "every warp quantizes the same number of query rows");
-    static constexpr int STAGES = (VT == KVQ_V_Q4_0) ? KVQ_STAGES_Q4 : KVQ_STAGES_Q8;   // ring depth per warp
-    static constexpr int TPS = (VT == KVQ_V_Q4_0) ? KVQ_TPS_Q4 : KVQ_TPS_Q8;         // tiles per stage
+    static constexpr bool F16K = KT == KVQ_K_F16;
+    // ring depth per warp and tiles per stage (F16 K tiles are twice as large)
+    static constexpr int STAGES = F16K ? 2 : (VT == KVQ_V_Q4_0) ? KVQ_STAGES_Q4 : KVQ_STAGES_Q8;
+    static constexpr int TPS = F16K ? 1 : (VT == KVQ_V_Q4_0) ? KVQ_TPS_Q4 : KVQ_TPS_Q8;
     static constexpr int VCODE = (VT == KVQ_V_Q4_0) ? kD / 2 : kD;            // V code bytes per position
-    static constexpr int TILE_K = kWTile * kD, TILE_S = kWTile * kNB * 2, TILE_V = kWTile * VCODE;
-    static constexpr int TILE = TILE_K + TILE_S + TILE_V + TILE_S;            // bytes of one tile
+    static constexpr int KCODE = F16K ? 2 * kD : kD;                          // K bytes per position
+    static constexpr int TILE_K = kWTile * KCODE, TILE_S = kWTile * kNB * 2, TILE_V = kWTile * VCODE;
+    static constexpr int TILE_KS = F16K ? 0 : TILE_S;                         // K scales (none for F16 K)
+    static constexpr int TILE = TILE_K + TILE_KS + TILE_V + TILE_S;           // bytes of one tile
     // one warp stage: up to TPS consecutive tiles of one segment, each array's
     // tiles side by side as in the cache (K codes, K scales, V codes, V scales)
     static constexpr int K_OFF = 0;
     static constexpr int KS_OFF = K_OFF + TPS * TILE_K;
-    static constexpr int V_OFF = KS_OFF + TPS * TILE_S;
+    static constexpr int V_OFF = KS_OFF + TPS * TILE_KS;
     static constexpr int VS_OFF = V_OFF + TPS * TILE_V;
     static constexpr int STAGE = VS_OFF + TPS * TILE_S;
     static constexpr int RING = STAGES * STAGE;               // per warp
-    static constexpr int Q_OFF = WARPS * RING;                // int8 [QROWS][kD]
-    static constexpr int QS_OFF = Q_OFF + QROWS * kD;         // fp32 [QROWS][kNB]
+    static constexpr int Q_OFF = WARPS * RING;                // int8 codes (F16 K: fp16 values) [QROWS][kD]
+    static constexpr int QS_OFF = Q_OFF + QROWS * KCODE;      // fp32 [QROWS][kNB]
     static constexpr int QSUM_OFF = QS_OFF + QROWS * kNB * 4; // int32 [QROWS][kNB]
     static constexpr int ML_OFF = QSUM_OFF + QROWS * kNB * 4; // fp32 m, l [WARPS][8*NT]; M, 1/L, lse [8*NT]
     // Per-lane query table, [chunk][lane][4 words] (16-byte chunks, lane-major
@@ -118,13 +122,13 @@ struct SplitCfg {
 // whose bytes complete on the slot's barrier.  Positions of a tile outside
 // [la, le) are copied too (they are cache rows of the same segment, possibly
 // never written) and masked where they are used.
-template <int NT, int VT>
+template <int NT, int VT, int KT>
 __device__ __forceinline__ void tile_issue(const Walk &w, int n, uint32_t dst, uint32_t bar)
 {
-    using C = SplitCfg<NT, VT>;
+    using C = SplitCfg<NT, VT, KT>;
     mbar_arrive_expect_tx(bar, n * C::TILE);
     bulk_g2s(dst + C::K_OFF, w.gk, n * C::TILE_K, bar);
-    bulk_g2s(dst + C::KS_OFF, w.gks, n * C::TILE_S, bar);
+    if (C::TILE_KS) bulk_g2s(dst + C::KS_OFF, w.gks, n * C::TILE_KS, bar);
     bulk_g2s(dst + C::V_OFF, w.gv, n * C::TILE_V, bar);
     bulk_g2s(dst + C::VS_OFF, w.gvs, n * C::TILE_S, bar);
 }
@@ -202,11 +206,12 @@ __device__ __forceinline__ uint32_t q_pair(uint32_t w, int k0)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-template <int NT, int VT, bool DUMP>
-__global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::MIN_CTAS)
+template <int NT, int VT, int KT, bool DUMP>
+__global__ void __launch_bounds__(SplitCfg<NT, VT, KT>::THREADS, SplitCfg<NT, VT, KT>::MIN_CTAS)
     split_attn_kernel(const __grid_constant__ AttnParams p)
 {
-    using C = SplitCfg<NT, VT>;
+    using C = SplitCfg<NT, VT, KT>;
+    static_assert(!(DUMP && KT == KVQ_K_F16), "the score dump exists for int8 K only");
     constexpr int kWarps = C::WARPS;
     constexpr int kThreads = C::THREADS;
     constexpr int S = C::STAGES;
@@ -223,7 +228,10 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
         if ((int)blockIdx.x >= p.grp[k].cta0) gi = k;
     const GroupDesc &G = p.grp[gi];
     const int lb = (int)blockIdx.x - G.cta0;
-    const int rt = lb % G.n_rt, ls = lb / G.n_rt;   // row tile: rows [rt * 8NT, (rt + 1) * 8NT) of the kv head
+    // row tile: rows [rt * 8NT, (rt + 1) * 8NT) of the kv head.  The 8- and
+    // 16-row kernels are only chosen when every call of the launch has at most
+    // 8 NT rows per kv head, so for them n_rt is 1 and row0 a constant 0.
+    const int rt = (NT == 4) ? lb % G.n_rt : 0, ls = (NT == 4) ? lb / G.n_rt : lb;
     const int split = ls % G.n_split, h = (ls / G.n_split) % G.n_kv_heads, b = ls / G.n_split / G.n_kv_heads;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
     const int gb = p.grp_begin[G.head0 + h], gsz = p.grp_begin[G.head0 + h + 1] - gb;
@@ -241,11 +249,13 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
     // tile's last query token sees positions up to L - t_q + its index, and
     // L <= lcap bounds that from above.
     const int r0 = split * G.chunk;
-    const int r1c = max(r0, min(min(lcap, r0 + G.chunk),
-                                G.causal ? lcap - G.t_q + (row0 + R - 1) / gsz + 1 : lcap));
+    // (The clamp matters for long query chunks, which run on the 32-row kernel.)
+    const int r1c = (NT == 4) ? max(r0, min(min(lcap, r0 + G.chunk),
+                                            G.causal ? lcap - G.t_q + (row0 + R - 1) / gsz + 1 : lcap))
+                              : min(lcap, r0 + G.chunk);
     // The row tile holding the kv head's last query token sees every position
     // below L: it alone stores the appended tokens (fused append).
-    const bool app_store = rt == (gsz * G.t_q - 1) / (8 * NT);
+    const bool app_store = (NT == 4) ? rt == (gsz * G.t_q - 1) / (8 * NT) : true;
 
     // Nothing above reads memory written by an earlier kernel.
     pdl_wait();
@@ -282,7 +292,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
     }
     __syncwarp();
     Walk pw;
-    walk_seek(p, seg0, nseg, h, w0, w1, 0, C::VCODE, pw);
+    walk_seek(p, seg0, nseg, h, w0, w1, 0, C::VCODE, pw, C::KCODE);
     int issued = 0;   // stages handed to the copy engine
     // Hand the next stage (up to TPS tiles of the current segment piece) to the
     // copy engine; the walk is advanced by every lane alike.
@@ -292,14 +302,14 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
             const int tb = pw.T * kWTile;
             tile_rec[slot] = make_int4(tb, pw.la, pw.le, pw.pos0 + tb);
             stage_n[slot] = n;
-            tile_issue<NT, VT>(pw, n, ring_s + slot * C::STAGE, bar_s + slot * 8);
+            tile_issue<NT, VT, KT>(pw, n, ring_s + slot * C::STAGE, bar_s + slot * 8);
         }
         pw.T += n;
         pw.gk += n * C::TILE_K;
         pw.gks += n * C::TILE_S;
         pw.gv += n * C::TILE_V;
         pw.gvs += n * C::TILE_S;
-        if (pw.T >= pw.Tend) walk_seek(p, seg0, nseg, h, w0, w1, pw.k + 1, C::VCODE, pw);
+        if (pw.T >= pw.Tend) walk_seek(p, seg0, nseg, h, w0, w1, pw.k + 1, C::VCODE, pw, C::KCODE);
         ++issued;
     };
 #pragma unroll
@@ -352,75 +362,95 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
         }
     }
 
-    // ---- quantize the query rows of this kv head (int8 rule, fp16 scale) ----
-    uint32_t *qw = reinterpret_cast<uint32_t *>(smem + C::Q_OFF);
-    float *qs = reinterpret_cast<float *>(smem + C::QS_OFF);
-    int *qsum = reinterpret_cast<int *>(smem + C::QSUM_OFF);
-#pragma unroll
-    for (int k = 0; k < QPW; ++k) {
-        const int r = warp + kWarps * k;
-        uint32_t word = 0;
-        float s = 0.f;
-        int sum = 0;
-        if (r < R) {
-            const int i = (row0 + r) / gsz, hq = p.grp_q[gb + (row0 + r) % gsz];
-            const size_t qrow = ((size_t)b * G.t_q + i) * G.n_q_heads + hq;
-            float x[4];
-            unpack4h(qraw[k], x);
-            float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-            const __half sh = __float2half_rn(__fdiv_rn(a, 127.f));
-            s = __half2float(sh);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int code = quant_i8(x[k], s);
-                word |= (uint32_t)(code & 0xff) << (8 * k);
-                sum += code;
-            }
-            if (DUMP && split == 0) {
-                reinterpret_cast<uint32_t *>(G.dbg_qc)[qrow * (kD / 4) + lane] = word;
-                if ((lane & 7) == 0) G.dbg_qs[qrow * kNB + (lane >> 3)] = __half_as_ushort(sh);
-            }
-        }
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-        qw[r * (kD / 4) + lane] = word;
-        if ((lane & 7) == 0) {
-            qs[r * kNB + (lane >> 3)] = s * G.qk_scale_log2;
-            qsum[r * kNB + (lane >> 3)] = sum;
-        }
-    }
-    __syncthreads();   // query codes visible
-
-    // Query B fragments (fp16, exact codes).  Within block bb, k16 step ks, this
-    // lane's k slots (2c, 2c+1 | 2c+8, 2c+9) carry head dims
-    // 32bb + 8c + 4ks + (0, 1 | 2, 3): the bytes of word 8bb + 2c + ks, the same
-    // word the lane reads from K, so q.k is unchanged.  The warps write them, with
-    // the accumulator seeds (-1152 * sum of the row's codes in the block) of
-    // rows 2c, 2c+1 and those rows' scales, to the per-lane table that every
-    // stage reads back (row scales as (row 2c, row 2c+1) pairs per block).
     uint4 *qf = reinterpret_cast<uint4 *>(smem + C::QF_OFF) + lane;   // chunk k at qf[32 * k]
-    // (nt, block) entries are spread over the warps: entry k goes to warp k % WARPS.
-    for (int k = warp; k < NT * kNB + NT * 2; k += kWarps) {
-        if (k < NT * kNB) {
-            const int nt = k / kNB, bb = k % kNB;
-            const uint32_t w0 = qw[(8 * nt + g) * (kD / 4) + 8 * bb + 2 * c];
-            const uint32_t w1 = qw[(8 * nt + g) * (kD / 4) + 8 * bb + 2 * c + 1];
-            qf[32 * (nt * kNB + bb)] = make_uint4(q_pair(w0, 0), q_pair(w0, 2), q_pair(w1, 0), q_pair(w1, 2));
-            const float s0 = -kBias * (float)qsum[(8 * nt + 2 * c) * kNB + bb];
-            const float s1 = -kBias * (float)qsum[(8 * nt + 2 * c + 1) * kNB + bb];
-            qf[32 * (C::QB_CHUNKS + nt * kNB + bb)] =
-                make_uint4(__float_as_uint(s0), __float_as_uint(s1), __float_as_uint(s0), __float_as_uint(s1));
-        } else {
-            // (row 2c, row 2c+1) scale pairs of blocks 2hb, 2hb+1
-            const int nt = (k - NT * kNB) / 2, hb = (k - NT * kNB) % 2;
-            const int r0 = 8 * nt + 2 * c;
-            qf[32 * (C::QB_CHUNKS + C::SEED_CHUNKS + nt * 2 + hb)] =
-                make_uint4(__float_as_uint(qs[r0 * kNB + 2 * hb]), __float_as_uint(qs[(r0 + 1) * kNB + 2 * hb]),
-                           __float_as_uint(qs[r0 * kNB + 2 * hb + 1]), __float_as_uint(qs[(r0 + 1) * kNB + 2 * hb + 1]));
+    if constexpr (KT == KVQ_K_F16) {
+        // ---- F16 K: the query rows stay fp16 (not quantized).  k16 step ks of
+        // 8-row tile nt takes B registers (dims 16ks + 2c, +1 | 16ks + 2c + 8, +9)
+        // of row 8nt + g: words 8ks + c and 8ks + c + 4 of the row; chunk
+        // nt * 4 + ks/2 holds steps 2kp, 2kp + 1 ----
+        uint32_t *qh = reinterpret_cast<uint32_t *>(smem + C::Q_OFF);   // [QROWS][64 words]
+#pragma unroll
+        for (int k = 0; k < QPW; ++k) {
+            const int r = warp + kWarps * k;
+            qh[r * (kD / 2) + 2 * lane] = qraw[k].x;
+            qh[r * (kD / 2) + 2 * lane + 1] = qraw[k].y;
+        }
+        __syncthreads();
+        for (int k = warp; k < NT * 4; k += kWarps) {
+            const int nt = k / 4, kp = k % 4;
+            const uint32_t *w = qh + (8 * nt + g) * (kD / 2) + 16 * kp + c;
+            qf[32 * k] = make_uint4(w[0], w[4], w[8], w[12]);
+        }
+    } else {
+        // ---- quantize the query rows of this kv head (int8 rule, fp16 scale) ----
+        uint32_t *qw = reinterpret_cast<uint32_t *>(smem + C::Q_OFF);
+        float *qs = reinterpret_cast<float *>(smem + C::QS_OFF);
+        int *qsum = reinterpret_cast<int *>(smem + C::QSUM_OFF);
+    #pragma unroll
+        for (int k = 0; k < QPW; ++k) {
+            const int r = warp + kWarps * k;
+            uint32_t word = 0;
+            float s = 0.f;
+            int sum = 0;
+            if (r < R) {
+                const int i = (row0 + r) / gsz, hq = p.grp_q[gb + (row0 + r) % gsz];
+                const size_t qrow = ((size_t)b * G.t_q + i) * G.n_q_heads + hq;
+                float x[4];
+                unpack4h(qraw[k], x);
+                float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+                a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+                a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+                a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+                const __half sh = __float2half_rn(__fdiv_rn(a, 127.f));
+                s = __half2float(sh);
+    #pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int code = quant_i8(x[k], s);
+                    word |= (uint32_t)(code & 0xff) << (8 * k);
+                    sum += code;
+                }
+                if (DUMP && split == 0) {
+                    reinterpret_cast<uint32_t *>(G.dbg_qc)[qrow * (kD / 4) + lane] = word;
+                    if ((lane & 7) == 0) G.dbg_qs[qrow * kNB + (lane >> 3)] = __half_as_ushort(sh);
+                }
+            }
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            qw[r * (kD / 4) + lane] = word;
+            if ((lane & 7) == 0) {
+                qs[r * kNB + (lane >> 3)] = s * G.qk_scale_log2;
+                qsum[r * kNB + (lane >> 3)] = sum;
+            }
+        }
+        __syncthreads();   // query codes visible
+
+        // Query B fragments (fp16, exact codes).  Within block bb, k16 step ks, this
+        // lane's k slots (2c, 2c+1 | 2c+8, 2c+9) carry head dims
+        // 32bb + 8c + 4ks + (0, 1 | 2, 3): the bytes of word 8bb + 2c + ks, the same
+        // word the lane reads from K, so q.k is unchanged.  The warps write them, with
+        // the accumulator seeds (-1152 * sum of the row's codes in the block) of
+        // rows 2c, 2c+1 and those rows' scales, to the per-lane table that every
+        // stage reads back (row scales as (row 2c, row 2c+1) pairs per block).
+        // (nt, block) entries are spread over the warps: entry k goes to warp k % WARPS.
+        for (int k = warp; k < NT * kNB + NT * 2; k += kWarps) {
+            if (k < NT * kNB) {
+                const int nt = k / kNB, bb = k % kNB;
+                const uint32_t w0 = qw[(8 * nt + g) * (kD / 4) + 8 * bb + 2 * c];
+                const uint32_t w1 = qw[(8 * nt + g) * (kD / 4) + 8 * bb + 2 * c + 1];
+                qf[32 * (nt * kNB + bb)] = make_uint4(q_pair(w0, 0), q_pair(w0, 2), q_pair(w1, 0), q_pair(w1, 2));
+                const float s0 = -kBias * (float)qsum[(8 * nt + 2 * c) * kNB + bb];
+                const float s1 = -kBias * (float)qsum[(8 * nt + 2 * c + 1) * kNB + bb];
+                qf[32 * (C::QB_CHUNKS + nt * kNB + bb)] =
+                    make_uint4(__float_as_uint(s0), __float_as_uint(s1), __float_as_uint(s0), __float_as_uint(s1));
+            } else {
+                // (row 2c, row 2c+1) scale pairs of blocks 2hb, 2hb+1
+                const int nt = (k - NT * kNB) / 2, hb = (k - NT * kNB) % 2;
+                const int r0 = 8 * nt + 2 * c;
+                qf[32 * (C::QB_CHUNKS + C::SEED_CHUNKS + nt * 2 + hb)] =
+                    make_uint4(__float_as_uint(qs[r0 * kNB + 2 * hb]), __float_as_uint(qs[(r0 + 1) * kNB + 2 * hb]),
+                               __float_as_uint(qs[r0 * kNB + 2 * hb + 1]), __float_as_uint(qs[(r0 + 1) * kNB + 2 * hb + 1]));
+            }
         }
     }
     __syncthreads();   // query table visible
@@ -498,81 +528,116 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
 
         auto chunk = [&](auto full_tag) {
             constexpr bool FULL = decltype(full_tag)::value;
-            // ---- S^T = K Q^T per 32-block (exact integers in fp32): A = the K
-            // codes of the stage's 16 positions (rows g and g + 8 of the MMA),
-            // B = 8 query rows ----
-            uint4 kk[2][2];   // [position g / g + 8][blocks 0-1 / 2-3]
-#pragma unroll
-            for (int pp = 0; pp < 2; ++pp)
-#pragma unroll
-                for (int hb = 0; hb < 2; ++hb)
-                    kk[pp][hb] = *reinterpret_cast<const uint4 *>(stK + (2 * pp + hb) * 512 + lane * 16);
-            float sc[NT][kNB][4];   // (pos g, row 2c), (pos g, row 2c+1), (pos g+8, row 2c), (pos g+8, row 2c+1)
-#pragma unroll
-            for (int bb = 0; bb < kNB; ++bb) {
-                const uint4 &u0 = kk[0][bb >> 1], &u1 = kk[1][bb >> 1];
-                uint32_t a0[4], a1[4];   // k16 steps 0 and 1 of the block
-                k_word_biased((bb & 1) ? u0.z : u0.x, a0[0], a0[2]);
-                k_word_biased((bb & 1) ? u1.z : u1.x, a0[1], a0[3]);
-                k_word_biased((bb & 1) ? u0.w : u0.y, a1[0], a1[2]);
-                k_word_biased((bb & 1) ? u1.w : u1.y, a1[1], a1[3]);
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const uint4 qb = qf[32 * (nt * kNB + bb)];
-                    const uint4 sd = qf[32 * (C::QB_CHUNKS + nt * kNB + bb)];
-                    mma_f16_16816_c4(sc[nt][bb], a0, qb.x, qb.y, sd);
-                    mma_f16_16816(sc[nt][bb], a1, qb.z, qb.w);
-                }
-            }
-            // K scales of this lane's positions g and g + 8
-            float sk[2][kNB];
-            unpack4h(*reinterpret_cast<const uint2 *>(stKS + g * kNB * 2), sk[0]);
-            unpack4h(*reinterpret_cast<const uint2 *>(stKS + (g + 8) * kNB * 2), sk[1]);
             float2 s[NT][2];   // [nt][position g / g + 8] = (row 2c, row 2c + 1)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                float2 sq[kNB];   // (row 2c, row 2c + 1) scales of each block
-#pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
-                    const uint4 q4 = qf[32 * (C::QB_CHUNKS + C::SEED_CHUNKS + nt * 2 + hb)];
-                    sq[2 * hb] = make_float2(__uint_as_float(q4.x), __uint_as_float(q4.y));
-                    sq[2 * hb + 1] = make_float2(__uint_as_float(q4.z), __uint_as_float(q4.w));
-                }
-#pragma unroll
-                for (int pp = 0; pp < 2; ++pp) {
-                    float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int bb = 0; bb < kNB; ++bb) {
-                        const float2 i2 = make_float2(sc[nt][bb][2 * pp], sc[nt][bb][2 * pp + 1]);
-                        a = fma2(mul2(i2, sq[bb]), make_float2(sk[pp][bb], sk[pp][bb]), a);
-                    }
-                    if (!FULL) {
-                        const int tok = tb + 8 * pp + g, pos = pos_base + 8 * pp + g;
-                        const bool okp = tok >= la && tok < le;
-                        a.x = (okp && pos <= lim[nt][0]) ? a.x : -INFINITY;
-                        a.y = (okp && pos <= lim[nt][1]) ? a.y : -INFINITY;
-                    }
-                    s[nt][pp] = a;
-                }
-            }
-            if (DUMP) {
+            if constexpr (KT == KVQ_K_F16) {
+                // ---- S^T = K Q^T over the fp16 values: A = the K tile's 16
+                // positions (one 16-byte fragment load per k16 step), B = 8
+                // query rows, fp32 accumulation ----
+                float sc[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int pp = 0; pp < 2; ++pp)
+                    for (int k = 0; k < 4; ++k) sc[nt][k] = 0.f;
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int row = 8 * nt + 2 * c + e, tok = tb + 8 * pp + g, pos = pos_base + 8 * pp + g;
-                            if (row < R && tok >= la && tok < le && pos < L) {
-                                const int i = (row0 + row) / gsz, hq = p.grp_q[gb + (row0 + row) % gsz];
-                                const size_t o = ((((size_t)b * G.t_q + i) * G.n_q_heads + hq) * G.max_len + pos) * kNB;
-                                int4 v;
-                                v.x = (int)sc[nt][0][2 * pp + e]; v.y = (int)sc[nt][1][2 * pp + e];
-                                v.z = (int)sc[nt][2][2 * pp + e]; v.w = (int)sc[nt][3][2 * pp + e];
-                                *reinterpret_cast<int4 *>(G.dbg_scores + o) = v;
-                            }
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    const uint4 a4 = *reinterpret_cast<const uint4 *>(stK + ks * 512 + lane * 16);
+                    const uint32_t av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const uint4 qb = qf[32 * (nt * 4 + ks / 2)];
+                        mma_f16_16816(sc[nt], av, (ks & 1) ? qb.z : qb.x, (ks & 1) ? qb.w : qb.y);
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int pp = 0; pp < 2; ++pp) {
+                        float2 a = mul2(make_float2(sc[nt][2 * pp], sc[nt][2 * pp + 1]),
+                                        make_float2(G.qk_scale_log2, G.qk_scale_log2));
+                        if (!FULL) {
+                            const int tok = tb + 8 * pp + g, pos = pos_base + 8 * pp + g;
+                            const bool okp = tok >= la && tok < le;
+                            a.x = (okp && pos <= lim[nt][0]) ? a.x : -INFINITY;
+                            a.y = (okp && pos <= lim[nt][1]) ? a.y : -INFINITY;
                         }
-                return;
+                        s[nt][pp] = a;
+                    }
+            } else {
+                // ---- S^T = K Q^T per 32-block (exact integers in fp32): A = the K
+                // codes of the stage's 16 positions (rows g and g + 8 of the MMA),
+                // B = 8 query rows ----
+                uint4 kk[2][2];   // [position g / g + 8][blocks 0-1 / 2-3]
+    #pragma unroll
+                for (int pp = 0; pp < 2; ++pp)
+    #pragma unroll
+                    for (int hb = 0; hb < 2; ++hb)
+                        kk[pp][hb] = *reinterpret_cast<const uint4 *>(stK + (2 * pp + hb) * 512 + lane * 16);
+                float sc[NT][kNB][4];   // (pos g, row 2c), (pos g, row 2c+1), (pos g+8, row 2c), (pos g+8, row 2c+1)
+    #pragma unroll
+                for (int bb = 0; bb < kNB; ++bb) {
+                    const uint4 &u0 = kk[0][bb >> 1], &u1 = kk[1][bb >> 1];
+                    uint32_t a0[4], a1[4];   // k16 steps 0 and 1 of the block
+                    k_word_biased((bb & 1) ? u0.z : u0.x, a0[0], a0[2]);
+                    k_word_biased((bb & 1) ? u1.z : u1.x, a0[1], a0[3]);
+                    k_word_biased((bb & 1) ? u0.w : u0.y, a1[0], a1[2]);
+                    k_word_biased((bb & 1) ? u1.w : u1.y, a1[1], a1[3]);
+    #pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const uint4 qb = qf[32 * (nt * kNB + bb)];
+                        const uint4 sd = qf[32 * (C::QB_CHUNKS + nt * kNB + bb)];
+                        mma_f16_16816_c4(sc[nt][bb], a0, qb.x, qb.y, sd);
+                        mma_f16_16816(sc[nt][bb], a1, qb.z, qb.w);
+                    }
+                }
+                // K scales of this lane's positions g and g + 8
+                float sk[2][kNB];
+                unpack4h(*reinterpret_cast<const uint2 *>(stKS + g * kNB * 2), sk[0]);
+                unpack4h(*reinterpret_cast<const uint2 *>(stKS + (g + 8) * kNB * 2), sk[1]);
+    #pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float2 sq[kNB];   // (row 2c, row 2c + 1) scales of each block
+    #pragma unroll
+                    for (int hb = 0; hb < 2; ++hb) {
+                        const uint4 q4 = qf[32 * (C::QB_CHUNKS + C::SEED_CHUNKS + nt * 2 + hb)];
+                        sq[2 * hb] = make_float2(__uint_as_float(q4.x), __uint_as_float(q4.y));
+                        sq[2 * hb + 1] = make_float2(__uint_as_float(q4.z), __uint_as_float(q4.w));
+                    }
+    #pragma unroll
+                    for (int pp = 0; pp < 2; ++pp) {
+                        float2 a = make_float2(0.f, 0.f);
+    #pragma unroll
+                        for (int bb = 0; bb < kNB; ++bb) {
+                            const float2 i2 = make_float2(sc[nt][bb][2 * pp], sc[nt][bb][2 * pp + 1]);
+                            a = fma2(mul2(i2, sq[bb]), make_float2(sk[pp][bb], sk[pp][bb]), a);
+                        }
+                        if (!FULL) {
+                            const int tok = tb + 8 * pp + g, pos = pos_base + 8 * pp + g;
+                            const bool okp = tok >= la && tok < le;
+                            a.x = (okp && pos <= lim[nt][0]) ? a.x : -INFINITY;
+                            a.y = (okp && pos <= lim[nt][1]) ? a.y : -INFINITY;
+                        }
+                        s[nt][pp] = a;
+                    }
+                }
+                if constexpr (DUMP) {
+    #pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+    #pragma unroll
+                        for (int pp = 0; pp < 2; ++pp)
+    #pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int row = 8 * nt + 2 * c + e, tok = tb + 8 * pp + g, pos = pos_base + 8 * pp + g;
+                                if (row < R && tok >= la && tok < le && pos < L) {
+                                    const int i = (row0 + row) / gsz, hq = p.grp_q[gb + (row0 + row) % gsz];
+                                    const size_t o = ((((size_t)b * G.t_q + i) * G.n_q_heads + hq) * G.max_len + pos) * kNB;
+                                    int4 v;
+                                    v.x = (int)sc[nt][0][2 * pp + e]; v.y = (int)sc[nt][1][2 * pp + e];
+                                    v.z = (int)sc[nt][2][2 * pp + e]; v.w = (int)sc[nt][3][2 * pp + e];
+                                    *reinterpret_cast<int4 *>(G.dbg_scores + o) = v;
+                                }
+                            }
+                    return;
+                }
             }
 
             // ---- online softmax (base 2) with a lazily raised reference max: a
@@ -808,53 +873,77 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT>::THREADS, SplitCfg<NT, VT>::M
     }
 }
 
-template <int NT, int VT>
+template <int NT, int VT, int KT>
 cudaError_t launch_split_t(const AttnParams &p, int n_ctas, bool dump, cudaStream_t s, bool pdl)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(n_ctas);
-    cfg.blockDim = dim3(SplitCfg<NT, VT>::THREADS);
-    cfg.dynamicSmemBytes = SplitCfg<NT, VT>::SMEM;
+    cfg.blockDim = dim3(SplitCfg<NT, VT, KT>::THREADS);
+    cfg.dynamicSmemBytes = SplitCfg<NT, VT, KT>::SMEM;
     cfg.stream = s;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (dump) return cudaLaunchKernelEx(&cfg, split_attn_kernel<NT, VT, true>, p);
-    return cudaLaunchKernelEx(&cfg, split_attn_kernel<NT, VT, false>, p);
+    if constexpr (KT == KVQ_K_I8) {
+        if (dump) return cudaLaunchKernelEx(&cfg, split_attn_kernel<NT, VT, KT, true>, p);
+    } else {
+        if (dump) return cudaErrorInvalidValue;
+    }
+    return cudaLaunchKernelEx(&cfg, split_attn_kernel<NT, VT, KT, false>, p);
 }
 
-template <int NT, int VT>
+template <int NT, int VT, int KT>
 cudaError_t prepare_split_t(bool dump, int *ctas_per_sm)
 {
-    const int smem = SplitCfg<NT, VT>::SMEM;
-    const void *fn = dump ? (const void *)split_attn_kernel<NT, VT, true> : (const void *)split_attn_kernel<NT, VT, false>;
+    const int smem = SplitCfg<NT, VT, KT>::SMEM;
+    const void *fn = (const void *)split_attn_kernel<NT, VT, KT, false>;
+    if constexpr (KT == KVQ_K_I8) {
+        if (dump) fn = (const void *)split_attn_kernel<NT, VT, KT, true>;
+    } else {
+        if (dump) return cudaErrorInvalidValue;
+    }
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (ctas_per_sm)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, SplitCfg<NT, VT>::THREADS, smem);
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, SplitCfg<NT, VT, KT>::THREADS, smem);
     return cudaSuccess;
 }
 
-#define KVQ_DEFINE_SPLIT_ENTRY(SUFFIX, VT)                                                   \
-    cudaError_t launch_split_##SUFFIX(const AttnParams &p, int nt, int n_ctas, bool dump, cudaStream_t s, bool pdl) \
-    {                                                                                        \
-        switch (nt) {                                                                        \
-        case 1: return launch_split_t<1, VT>(p, n_ctas, dump, s, pdl);                       \
-        case 2: return launch_split_t<2, VT>(p, n_ctas, dump, s, pdl);                       \
-        case 4: return launch_split_t<4, VT>(p, n_ctas, dump, s, pdl);                       \
-        default: return cudaErrorInvalidValue;                                               \
-        }                                                                                    \
-    }                                                                                        \
-    cudaError_t prepare_split_##SUFFIX(int nt, bool dump, int *ctas)                         \
-    {                                                                                        \
-        switch (nt) {                                                                        \
-        case 1: return prepare_split_t<1, VT>(dump, ctas);                                   \
-        case 2: return prepare_split_t<2, VT>(dump, ctas);                                   \
-        case 4: return prepare_split_t<4, VT>(dump, ctas);                                   \
-        default: return cudaErrorInvalidValue;                                               \
-        }                                                                                    \
+template <int VT, int KT>
+cudaError_t launch_split_nt(const AttnParams &p, int nt, int n_ctas, bool dump, cudaStream_t s, bool pdl)
+{
+    switch (nt) {
+    case 1: return launch_split_t<1, VT, KT>(p, n_ctas, dump, s, pdl);
+    case 2: return launch_split_t<2, VT, KT>(p, n_ctas, dump, s, pdl);
+    case 4: return launch_split_t<4, VT, KT>(p, n_ctas, dump, s, pdl);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int VT, int KT>
+cudaError_t prepare_split_nt(int nt, bool dump, int *ctas)
+{
+    switch (nt) {
+    case 1: return prepare_split_t<1, VT, KT>(dump, ctas);
+    case 2: return prepare_split_t<2, VT, KT>(dump, ctas);
+    case 4: return prepare_split_t<4, VT, KT>(dump, ctas);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+#define KVQ_DEFINE_SPLIT_ENTRY(SUFFIX, VT)                                                              \
+    cudaError_t launch_split_##SUFFIX(const AttnParams &p, int nt, int k_type, int n_ctas, bool dump,    \
+                                      cudaStream_t s, bool pdl)                                         \
+    {                                                                                                   \
+        return (k_type == KVQ_K_F16) ? launch_split_nt<VT, KVQ_K_F16>(p, nt, n_ctas, dump, s, pdl)      \
+                                     : launch_split_nt<VT, KVQ_K_I8>(p, nt, n_ctas, dump, s, pdl);      \
+    }                                                                                                   \
+    cudaError_t prepare_split_##SUFFIX(int nt, int k_type, bool dump, int *ctas)                        \
+    {                                                                                                   \
+        return (k_type == KVQ_K_F16) ? prepare_split_nt<VT, KVQ_K_F16>(nt, dump, ctas)                  \
+                                     : prepare_split_nt<VT, KVQ_K_I8>(nt, dump, ctas);                  \
     }
 
 }  // namespace kvq

@@ -57,6 +57,14 @@ __host__ __device__ constexpr int v4_tile_off(int u, int j)
 {
     return ((u / 8) * 32 + 4 * ((j % 16) / 2) + (u % 8) / 2) * 16 + 4 * (j / 16) + 2 * (u % 2) + j % 2;
 }
+// F16 K: byte offset of fp16 element j of token u in a 4096-byte tile, the
+// mma A-fragment order (16-byte word at ks*512 + lane*16 holds the four
+// registers of k16 step ks for lane = 4*(u%8) + (j%8)/2: rows u, u+8 of
+// elements 2c, 2c+1 and 2c+8, 2c+9).
+__host__ __device__ constexpr int k16_tile_off(int u, int j)
+{
+    return (j / 16) * 512 + (4 * (u % 8) + (j % 8) / 2) * 16 + 4 * (u / 8 + 2 * ((j % 16) / 8)) + 2 * (j % 2);
+}
 __host__ __device__ constexpr int v8_tile_off(int u, int j)
 {
     return ((2 * (u / 8) + j / 64) * 32 + 4 * ((j % 32) / 4) + (u % 8) / 2) * 16 + 8 * ((j / 32) % 2) +
@@ -154,12 +162,15 @@ struct AppendParams {
 // ------------------------------------------------------------ host launchers --
 // Implemented in kvq_small.cu / kvq_attn_q4.cu / kvq_attn_q8.cu / kvq_prefill_q*.cu.
 // n_tiles8 = query rows per kv head rounded up to 1, 2 or 4 tiles of 8.
-cudaError_t launch_append(const AppendParams &p, int v_type, int max_rows, cudaStream_t s, bool pdl);
+// k_type selects the K format (kvq_ktype); dump kernels exist for KVQ_K_I8 only.
+cudaError_t launch_append(const AppendParams &p, int v_type, int k_type, int max_rows, cudaStream_t s, bool pdl);
 cudaError_t launch_combine(const CombineParams &p, int n_rows, cudaStream_t s, bool pdl);
-cudaError_t launch_split_q4(const AttnParams &p, int n_tiles8, int n_ctas, bool dump, cudaStream_t s, bool pdl);
-cudaError_t launch_split_q8(const AttnParams &p, int n_tiles8, int n_ctas, bool dump, cudaStream_t s, bool pdl);
-cudaError_t prepare_split_q4(int n_tiles8, bool dump, int *ctas_per_sm);
-cudaError_t prepare_split_q8(int n_tiles8, bool dump, int *ctas_per_sm);
+cudaError_t launch_split_q4(const AttnParams &p, int n_tiles8, int k_type, int n_ctas, bool dump, cudaStream_t s,
+                            bool pdl);
+cudaError_t launch_split_q8(const AttnParams &p, int n_tiles8, int k_type, int n_ctas, bool dump, cudaStream_t s,
+                            bool pdl);
+cudaError_t prepare_split_q4(int n_tiles8, int k_type, bool dump, int *ctas_per_sm);
+cudaError_t prepare_split_q8(int n_tiles8, int k_type, bool dump, int *ctas_per_sm);
 // tcgen05 kernel for long query chunks (kvq_prefill_q4.cu / kvq_prefill_q8.cu):
 // 128 query rows per CTA, one CTA per SM.
 cudaError_t launch_prefill_q4(const AttnParams &p, int n_ctas, cudaStream_t s, bool pdl);
@@ -237,7 +248,7 @@ struct Walk {
 };
 
 __device__ __forceinline__ void walk_seek(const AttnParams &p, int seg0, int nseg, int h, int r0, int r1, int k,
-                                          int vcode, Walk &w)
+                                          int vcode, Walk &w, int kcode = kD)
 {
     for (w.k = k; w.k < nseg; ++w.k) {
         const SegDesc &s = p.seg[seg0 + w.k];
@@ -250,7 +261,7 @@ __device__ __forceinline__ void walk_seek(const AttnParams &p, int seg0, int nse
             w.Tend = (w.le + kWTile - 1) / kWTile;
             w.pos0 = s.pos0;
             const size_t row = (size_t)h * s.cap + (size_t)w.T * kWTile;
-            w.gk = reinterpret_cast<const uint8_t *>(s.kq) + row * kD;
+            w.gk = reinterpret_cast<const uint8_t *>(s.kq) + row * kcode;
             w.gks = reinterpret_cast<const uint8_t *>(s.ks) + row * kNB * 2;
             w.gv = s.vq + row * vcode;
             w.gvs = reinterpret_cast<const uint8_t *>(s.vs) + row * kNB * 2;
@@ -406,15 +417,24 @@ __device__ __forceinline__ uint32_t quant_row_i8(const float (&x)[4], uint16_t &
 struct TokenRow {
     uint32_t kw, vw;
     uint16_t ks, vs;
+    uint32_t kw2;   // F16 K: kw, kw2 = the lane's four fp16 K values
 };
 
-template <int VT>
+template <int VT, int KT = KVQ_K_I8>
 __device__ __forceinline__ TokenRow quant_token(const uint16_t *k_row, const uint16_t *v_row, int lane)
 {
     TokenRow t;
     float x[4];
-    load4h(k_row + lane * 4, x);
-    t.kw = quant_row_i8(x, t.ks);
+    if (KT == KVQ_K_F16) {
+        const uint2 raw = *reinterpret_cast<const uint2 *>(k_row + lane * 4);
+        t.kw = raw.x;
+        t.kw2 = raw.y;
+        t.ks = 0;
+    } else {
+        load4h(k_row + lane * 4, x);
+        t.kw = quant_row_i8(x, t.ks);
+        t.kw2 = 0;
+    }
     load4h(v_row + lane * 4, x);
     if (VT == KVQ_V_Q8_0) {
         t.vw = quant_row_i8(x, t.vs);
@@ -435,12 +455,17 @@ __device__ __forceinline__ TokenRow quant_token(const uint16_t *k_row, const uin
 // Store a quantized row at tile position u of the code tiles kt / vt (K codes,
 // V codes) and at scale rows ksr / vsr (4 fp16 each), in the cache's tile order.
 // Works for a tile in global memory and for a staged copy in shared memory.
-template <int VT>
+template <int VT, int KT = KVQ_K_I8>
 __device__ __forceinline__ void store_token(const TokenRow &t, int u, int lane, uint8_t *kt, uint16_t *ksr,
                                             uint8_t *vt, uint16_t *vsr)
 {
-    *reinterpret_cast<uint32_t *>(kt + k_tile_off(u, 4 * lane)) = t.kw;
-    if ((lane & 7) == 0) ksr[lane >> 3] = t.ks;
+    if (KT == KVQ_K_F16) {   // elements 4l, 4l+1 and 4l+2, 4l+3: one 32-bit pair each
+        *reinterpret_cast<uint32_t *>(kt + k16_tile_off(u, 4 * lane)) = t.kw;
+        *reinterpret_cast<uint32_t *>(kt + k16_tile_off(u, 4 * lane + 2)) = t.kw2;
+    } else {
+        *reinterpret_cast<uint32_t *>(kt + k_tile_off(u, 4 * lane)) = t.kw;
+        if ((lane & 7) == 0) ksr[lane >> 3] = t.ks;
+    }
     if (VT == KVQ_V_Q8_0) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) vt[v8_tile_off(u, 4 * lane + k)] = (uint8_t)(t.vw >> (8 * k));

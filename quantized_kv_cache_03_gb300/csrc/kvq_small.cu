@@ -10,9 +10,10 @@ namespace kvq {
 // codes stay one word; q4_0 lanes 0..3 of each block pull the codes of
 // elements 16.. from lanes 4..7, form bytes j = q[j] | q[j+16] << 4 and store
 // them as two byte pairs; q8_0 codes are stored byte by byte (the tile
-// interleaves neighbouring positions).
+// interleaves neighbouring positions).  F16 K (KT = KVQ_K_F16): the lane's four
+// fp16 K values go to their places in the 4096-byte tile as two 32-bit pairs.
 // ---------------------------------------------------------------------------
-template <int VT>
+template <int VT, int KT>
 __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ AppendParams p)
 {
     pdl_wait();      // inputs come from earlier kernels; the cache may still be read by one
@@ -26,12 +27,12 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
     const size_t src = ((size_t)(e.src + tok) * H + h) * kD;
     const int u = (e.dst + tok) % kWTile;                      // position in its tile
     const size_t tile = (size_t)h * e.cap + e.dst + tok - u;    // first row of the tile
-    const TokenRow t = quant_token<VT>(p.k16 + src, p.v16 + src, lane);
-    store_token<VT>(t, u, lane, e.kq + tile * kD, e.ks + (tile + u) * kNB, e.vq + tile * (VT == KVQ_V_Q4_0 ? kD / 2 : kD),
-                    e.vs + (tile + u) * kNB);
+    const TokenRow t = quant_token<VT, KT>(p.k16 + src, p.v16 + src, lane);
+    store_token<VT, KT>(t, u, lane, e.kq + tile * kD * (KT == KVQ_K_F16 ? 2 : 1), e.ks + (tile + u) * kNB,
+                        e.vq + tile * (VT == KVQ_V_Q4_0 ? kD / 2 : kD), e.vs + (tile + u) * kNB);
 }
 
-cudaError_t launch_append(const AppendParams &p, int v_type, int max_rows, cudaStream_t s, bool pdl)
+cudaError_t launch_append(const AppendParams &p, int v_type, int k_type, int max_rows, cudaStream_t s, bool pdl)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((max_rows + 3) / 4, p.n_entries);
@@ -42,8 +43,11 @@ cudaError_t launch_append(const AppendParams &p, int v_type, int max_rows, cudaS
     at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (v_type == KVQ_V_Q4_0) return cudaLaunchKernelEx(&cfg, append_kernel<KVQ_V_Q4_0>, p);
-    return cudaLaunchKernelEx(&cfg, append_kernel<KVQ_V_Q8_0>, p);
+    if (k_type == KVQ_K_F16)
+        return (v_type == KVQ_V_Q4_0) ? cudaLaunchKernelEx(&cfg, append_kernel<KVQ_V_Q4_0, KVQ_K_F16>, p)
+                                      : cudaLaunchKernelEx(&cfg, append_kernel<KVQ_V_Q8_0, KVQ_K_F16>, p);
+    return (v_type == KVQ_V_Q4_0) ? cudaLaunchKernelEx(&cfg, append_kernel<KVQ_V_Q4_0, KVQ_K_I8>, p)
+                                  : cudaLaunchKernelEx(&cfg, append_kernel<KVQ_V_Q8_0, KVQ_K_I8>, p);
 }
 
 // ---------------------------------------------------------------------------

@@ -33,7 +33,8 @@ class DecodeSet:
         self.B, self.tq, self.Hq = s.n_seqs, s.t_q, s.n_q_heads
         self.lens_host = [int(x) for x in s.lengths]
         self.max_len = max(self.lens_host) if self.lens_host else 0
-        self.cache = kvq.Cache(self.B, s.n_kv_heads, s.v_type, max_segs=max(len(x) for x in s.segments))
+        self.cache = kvq.Cache(self.B, s.n_kv_heads, s.v_type, max_segs=max(len(x) for x in s.segments),
+                               k_type=s.k_type)
         # device staging of every sequence's fp16 K/V (shared between copies)
         if staging is None:
             staging = [(torch.from_numpy(k).to(self.device), torch.from_numpy(v).to(self.device))

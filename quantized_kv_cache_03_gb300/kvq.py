@@ -25,6 +25,8 @@ KVQ_ERR_CUDA = 5
 KVQ_ERR_TIMEOUT = 6
 V_Q4_0 = 0
 V_Q8_0 = 1
+K_I8 = 0    # K: int8 codes + fp16 scale per 32 (query quantized the same way)
+K_F16 = 1   # K: fp16 values (query unquantized)
 HEAD_DIM = 128
 SEG_ALIGN = 64
 QBLOCK = 32
@@ -46,7 +48,7 @@ class KvqSegment(ctypes.Structure):
 class KvqCache(ctypes.Structure):
     _fields_ = [("n_seqs", c_int32), ("n_kv_heads", c_int32), ("head_dim", c_int32),
                 ("v_type", c_int32), ("max_segs", c_int32), ("n_segs", POINTER(c_int32)),
-                ("segs", POINTER(KvqSegment))]
+                ("segs", POINTER(KvqSegment)), ("k_type", c_int32), ("reserved", c_int32)]
 
 
 class KvqDecodeDesc(ctypes.Structure):
@@ -130,15 +132,16 @@ class Cache:
     """
 
     def __init__(self, n_seqs: int, n_kv_heads: int, v_type: int, max_segs: int = 8,
-                 head_dim: int = HEAD_DIM, device=None):
+                 head_dim: int = HEAD_DIM, device=None, k_type: int = K_I8):
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
         self.n_seqs, self.n_kv_heads, self.v_type, self.head_dim = n_seqs, n_kv_heads, v_type, head_dim
+        self.k_type = k_type
         self.max_segs = max_segs
         self._segs = (KvqSegment * max(1, n_seqs * max_segs))()
         self._nsegs = (c_int32 * max(1, n_seqs))()
         self.desc = KvqCache(n_seqs, n_kv_heads, head_dim, v_type, max_segs,
                              ctypes.cast(self._nsegs, POINTER(c_int32)),
-                             ctypes.cast(self._segs, POINTER(KvqSegment)))
+                             ctypes.cast(self._segs, POINTER(KvqSegment)), k_type, 0)
         self.tensors = [[] for _ in range(n_seqs)]
 
     def seg(self, b: int, k: int) -> KvqSegment:
@@ -155,8 +158,9 @@ class Cache:
         cap = max(SEG_ALIGN, (int(cap) + SEG_ALIGN - 1) // SEG_ALIGN * SEG_ALIGN)
         H, D = self.n_kv_heads, self.head_dim
         vb = D // 2 if self.v_type == V_Q4_0 else D
-        t = dict(k_q=torch.empty((H, cap, D), dtype=torch.int8, device=self.device),
-                 k_s=torch.empty((H, cap, D // QBLOCK), dtype=torch.int16, device=self.device),
+        f16k = self.k_type == K_F16
+        t = dict(k_q=torch.empty((H, cap, D), dtype=torch.int16 if f16k else torch.int8, device=self.device),
+                 k_s=None if f16k else torch.empty((H, cap, D // QBLOCK), dtype=torch.int16, device=self.device),
                  v_q=torch.empty((H, cap, vb), dtype=torch.uint8, device=self.device),
                  v_s=torch.empty((H, cap, D // QBLOCK), dtype=torch.int16, device=self.device))
         pos0 = 0
@@ -164,7 +168,7 @@ class Cache:
             prev = self.seg(b, ns - 1)
             pos0 = prev.pos0 + prev.len
         s = self.seg(b, ns)
-        s.k_q, s.k_s, s.v_q, s.v_s = (t[n].data_ptr() for n in ("k_q", "k_s", "v_q", "v_s"))
+        s.k_q, s.k_s, s.v_q, s.v_s = (0 if t[n] is None else t[n].data_ptr() for n in ("k_q", "k_s", "v_q", "v_s"))
         s.cap, s.len, s.pos0 = cap, 0, pos0
         self.tensors[b].append(t)
         self._nsegs[b] = ns + 1
@@ -184,18 +188,21 @@ class Cache:
         """Sequence b copied to host numpy arrays.  raw=False: the filled
         positions, [H][L][row] per array in logical row order.  raw=True: one
         dict per segment with the whole arrays as stored ([H][cap][row], code
-        bytes in their in-tile order) plus its "len"."""
+        bytes in their in-tile order) plus its "len".  F16 K caches give "k16"
+        (fp16 bits) instead of "kq" and "ks"."""
         import numpy as np
-        parts = {n: [] for n in ("kq", "ks", "vq", "vs")}
+        f16k = self.k_type == K_F16
+        arrays = ((("k16", "k_q", np.uint16),) if f16k else (("kq", "k_q", np.uint8), ("ks", "k_s", np.uint16))) + \
+            (("vq", "v_q", np.uint8), ("vs", "v_s", np.uint16))
+        parts = {n: [] for n, _, _ in arrays}
         segs = []
         for k in range(self._nsegs[b]):
             s, t = self.seg(b, k), self.tensors[b][k]
             seg = {"len": s.len}
-            for name, key, view in (("kq", "k_q", np.uint8), ("ks", "k_s", np.uint16),
-                                    ("vq", "v_q", np.uint8), ("vs", "v_s", np.uint16)):
+            for name, key, view in arrays:
                 a = t[key].cpu().numpy().view(view)
                 seg[name] = a
-                if not raw and name in ("kq", "vq"):
+                if not raw and name in ("kq", "vq", "k16"):
                     a = untile_codes(a, name, self.v_type)
                 parts[name].append(a[:, :s.len])
             segs.append(seg)
@@ -211,6 +218,9 @@ def _tile_index(name: str, v_type: int):
     u = np.arange(16)[:, None]
     sub, gu, e = u // 8, u % 8, u % 2
     cu = gu // 2
+    if name == "k16":   # fp16 elements (offsets in 2-byte units)
+        j = np.arange(128)[None, :]
+        return ((j // 16) * 512 + (4 * gu + (j % 8) // 2) * 16 + 4 * (sub + 2 * ((j % 16) // 8)) + 2 * (j % 2)) // 2
     if name == "kq":
         j = np.arange(128)[None, :]
         return ((2 * sub + j // 64) * 32 + 4 * gu + (j % 32) // 8) * 16 + 8 * ((j // 32) % 2) + j % 8

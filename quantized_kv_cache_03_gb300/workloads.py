@@ -23,6 +23,8 @@ sequence can be regenerated on its own):
 * ``verify``   16 sequences x 4 query tokens with a causal mask among the 4
                newest positions, 32768 positions each, 64 query / 8 kv heads
                (32 query rows per kv head), V q4_0, N(0,1), seed 5.
+* ``long_f16k`` the ``long`` pair (same seeds and inputs) with K kept as fp16
+               values (the F16 K / q4_0 V configuration).
 * ``prefill``  one chunk of chunked prefill: 1 sequence of 32768 positions whose
                last 512 are the chunk's tokens (causal among themselves), the
                earlier ones cached in 2 segments (one cut uniform in [1, L-1]
@@ -41,8 +43,10 @@ import numpy as np
 
 V_Q4_0 = 0
 V_Q8_0 = 1
+K_I8 = 0
+K_F16 = 1
 
-CONFIG_NAMES = ("tiny", "single", "long", "batched", "verify", "prefill")
+CONFIG_NAMES = ("tiny", "single", "long", "batched", "verify", "prefill", "long_f16k")
 
 
 @dataclasses.dataclass
@@ -60,6 +64,7 @@ class CacheSpec:
     lengths: np.ndarray            # [n_seqs] positions incl. the t_q new tokens
     segments: List[np.ndarray]     # per sequence: segment lengths, sum = length
     outlier_channels: int = 0      # per kv head, K and V x10
+    k_type: int = K_I8             # K_F16: K kept as fp16 values
 
     @property
     def max_len(self) -> int:
@@ -107,6 +112,11 @@ def make_spec(name: str, ctx: int | None = None, n_seqs: int | None = None,
     elif name == "verify":
         base = [dict(seed=5, n_seqs=16, n_kv_heads=8, n_q_heads=64, ctx=32768, t_q=4, causal=True,
                      v_type=V_Q4_0, n_seg=1, outliers=0)]
+    elif name == "long_f16k":   # the long-context pair with F16 K (q4_0 V), seeds as "long"
+        base = [dict(seed=2, n_seqs=1, n_kv_heads=8, n_q_heads=40, ctx=131072, t_q=1, causal=False,
+                     v_type=V_Q4_0, n_seg=4, outliers=0, tag="main", k_type=K_F16),
+                dict(seed=3, n_seqs=1, n_kv_heads=4, n_q_heads=16, ctx=131072, t_q=1, causal=False,
+                     v_type=V_Q4_0, n_seg=4, outliers=0, tag="draft", k_type=K_F16)]
     elif name == "prefill":
         base = [dict(seed=6, n_seqs=1, n_kv_heads=8, n_q_heads=32, ctx=32768, t_q=512, causal=True,
                      v_type=V_Q4_0, n_seg=2, outliers=0)]
@@ -132,7 +142,7 @@ def make_spec(name: str, ctx: int | None = None, n_seqs: int | None = None,
                                n_seqs=B, n_kv_heads=b["n_kv_heads"], n_q_heads=b["n_q_heads"],
                                head_dim=b.get("head_dim", 128), t_q=b["t_q"], causal=b["causal"],
                                v_type=b["v_type"], lengths=lengths, segments=segs,
-                               outlier_channels=b["outliers"]))
+                               outlier_channels=b["outliers"], k_type=b.get("k_type", K_I8)))
     return specs
 
 
@@ -182,16 +192,18 @@ def gen_q(spec: CacheSpec) -> np.ndarray:
                              dtype=np.float32).astype(np.float16)
 
 
-def kv_bytes_per_token_head(head_dim: int, v_type: int) -> int:
-    """Stored bytes read per (position, kv head): int8 K + fp16 scale per 32,
-    plus the V block bytes (q4_0 18 B / q8_0 34 B per 32)."""
+def kv_bytes_per_token_head(head_dim: int, v_type: int, k_type: int = K_I8) -> int:
+    """Stored bytes read per (position, kv head): int8 K + fp16 scale per 32
+    (F16 K: 2 bytes per element), plus the V block bytes (q4_0 18 B / q8_0
+    34 B per 32)."""
     nb = head_dim // 32
-    return head_dim + 2 * nb + (head_dim // 2 if v_type == V_Q4_0 else head_dim) + 2 * nb
+    k = 2 * head_dim if k_type == K_F16 else head_dim + 2 * nb
+    return k + (head_dim // 2 if v_type == V_Q4_0 else head_dim) + 2 * nb
 
 
 def step_kv_bytes(specs: List[CacheSpec]) -> int:
     """Algorithmic KV bytes one decode step reads over all caches."""
-    return int(sum(int(s.lengths.sum()) * s.n_kv_heads * kv_bytes_per_token_head(s.head_dim, s.v_type)
+    return int(sum(int(s.lengths.sum()) * s.n_kv_heads * kv_bytes_per_token_head(s.head_dim, s.v_type, s.k_type)
                    for s in specs))
 
 

@@ -36,7 +36,8 @@ class Case:
 
     def build(self, append_step=True):
         s = self.spec
-        self.cache = kvq.Cache(self.B, s.n_kv_heads, s.v_type, max_segs=max(len(x) for x in s.segments))
+        self.cache = kvq.Cache(self.B, s.n_kv_heads, s.v_type, max_segs=max(len(x) for x in s.segments),
+                               k_type=s.k_type)
         for b in range(self.B):
             if self.lens[b] == 0:
                 continue
@@ -85,7 +86,7 @@ class Case:
 
     def oracle_cache(self, b):
         k, v = self.kv[b]
-        return oracle.quantize_kv(k, v, self.spec.v_type)
+        return oracle.quantize_kv(k, v, self.spec.v_type, k_type=self.spec.k_type)
 
     def oracle_decode(self, b, head_map=None, row_mask=None, want_scores=False, threads=8):
         s = self.spec
@@ -107,6 +108,20 @@ def lane_view_index(name, v_type):
             each half word 0 holds dims 4g, 4g+1 and word 1 dims 4g+2, 4g+3,
             each as (t, t+1, t, t+1)."""
     rows = []
+    if name == "k16":
+        # F16 K (2-byte elements): the mma A fragment of k16 step ks for lane
+        # 4g + c is four registers a0 (row g, k 2c, 2c+1), a1 (row g + 8, same
+        # k), a2 (row g, k 2c + 8, 2c + 9), a3 (row g + 8, same), stored as
+        # the 16-byte word ks * 512 + lane * 16
+        for ks in range(8):
+            for lane in range(32):
+                g, c = lane // 4, lane % 4
+                for reg in range(4):
+                    for half in range(2):
+                        u = g + 8 * (reg % 2)
+                        kk = 2 * c + 8 * (reg // 2) + half
+                        rows.append((ks * 256 + lane * 8 + reg * 2 + half, u, 16 * ks + kk))
+        return np.array(rows, dtype=np.int64)
     for lane in range(32):
         g, c = lane // 4, lane % 4
         for q in range(16):
@@ -129,12 +144,12 @@ def lane_view_index(name, v_type):
 
 
 def logical_codes(stored, name, v_type):
-    """Stored code bytes [H][cap][row] (tile order) -> logical [H][cap][row]."""
+    """Stored codes [H][cap][row] (tile order) -> logical [H][cap][row]."""
     H, cap, row = stored.shape
     idx = lane_view_index(name, v_type)
     assert len(idx) == 16 * row and len(np.unique(idx[:, 0])) == 16 * row
     tiles = stored.reshape(H, cap // 16, 16 * row)
-    out = np.empty((H, cap // 16, 16, row), dtype=np.uint8)
+    out = np.empty((H, cap // 16, 16, row), dtype=stored.dtype)
     out[:, :, idx[:, 1], idx[:, 2]] = tiles[:, :, idx[:, 0]]
     return out.reshape(H, cap, row)
 
@@ -142,13 +157,16 @@ def logical_codes(stored, name, v_type):
 def export_logical(cache, b):
     """Sequence b's filled positions in logical order, un-tiled by the lane view
     above (independently of the library's own untile helper)."""
-    parts = {n: [] for n in ("kq", "ks", "vq", "vs")}
+    names = ("k16", "vq", "vs") if cache.k_type == kvq.K_F16 else ("kq", "ks", "vq", "vs")
+    parts = {n: [] for n in names}
     for seg in cache.export(b, raw=True):
         n = seg["len"]
         for name in parts:
             a = seg[name]
             if name in ("kq", "vq"):
                 a = logical_codes(a.view(np.uint8), name, cache.v_type)
+            elif name == "k16":
+                a = logical_codes(a.view(np.uint16), name, cache.v_type)
             parts[name].append(a[:, :n])
     return {k: np.concatenate(v, axis=1) for k, v in parts.items()}
 
@@ -156,7 +174,7 @@ def export_logical(cache, b):
 def assert_cache_bytes(case, b, oc=None):
     oc = case.oracle_cache(b) if oc is None else oc
     got = export_logical(case.cache, b)
-    for name in ("kq", "ks", "vq", "vs"):
+    for name in oc:
         g, o = got[name].view(np.uint8), oc[name].view(np.uint8)
         assert g.shape == o.shape, (name, g.shape, o.shape)
         if not np.array_equal(g, o):

@@ -8,7 +8,8 @@ import pytest
 from quantized_kv_cache_03_gb300 import kvq
 from kvq_cases import lane_view_index, logical_codes
 
-CASES = [("kq", kvq.V_Q4_0, 128), ("vq", kvq.V_Q4_0, 64), ("vq", kvq.V_Q8_0, 128)]
+CASES = [("kq", kvq.V_Q4_0, 128), ("vq", kvq.V_Q4_0, 64), ("vq", kvq.V_Q8_0, 128),
+         ("k16", kvq.V_Q4_0, 128)]   # F16 K: 128 two-byte elements per row
 
 
 @pytest.mark.parametrize("name,vt,row", CASES)
@@ -23,8 +24,20 @@ def test_lane_view_is_a_permutation(name, vt, row):
 @pytest.mark.parametrize("name,vt,row", CASES)
 def test_header_formula_matches_lane_view(name, vt, row):
     rng = np.random.default_rng(7)
-    stored = rng.integers(0, 256, size=(3, 64, row), dtype=np.uint8)
+    dt = np.uint16 if name == "k16" else np.uint8
+    stored = rng.integers(0, np.iinfo(dt).max + 1, size=(3, 64, row), dtype=dt)
     assert np.array_equal(kvq.untile_codes(stored, name, vt), logical_codes(stored, name, vt))
+
+
+def test_f16_k_fragment_words():
+    # F16 K: the 16-byte word of k16 step ks for lane (g, c) holds (u, j) =
+    # (g, 16ks+2c), (g, 16ks+2c+1), (g+8, ...), (g+8, ...), (g, 16ks+2c+8), ...
+    idx = {int(o): (int(u), int(j)) for o, u, j in lane_view_index("k16", kvq.V_Q4_0)}
+    ks, g, c = 5, 6, 1
+    base = ks * 256 + (4 * g + c) * 8
+    k0 = 16 * ks + 2 * c
+    assert [idx[base + k] for k in range(8)] == [(g, k0), (g, k0 + 1), (g + 8, k0), (g + 8, k0 + 1),
+                                                 (g, k0 + 8), (g, k0 + 9), (g + 8, k0 + 8), (g + 8, k0 + 9)]
 
 
 def test_q4_0_word_pairs_positions():
