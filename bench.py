@@ -105,11 +105,20 @@ def measured_peaks(kind="hbm_gbs"):
     return (FALLBACK_HBM_GBS if kind == "hbm_gbs" else FALLBACK_BF16_TFLOPS_SUSTAINED), "fallback"
 
 
-def kernel_source_hash():
+# Source files that define each profiled kernel: a committed ncu summary stays
+# valid while these are unchanged.
+KERNEL_SOURCES = {
+    "split_attn": ["csrc/kvq_attn.cuh", "csrc/kvq_attn_q4.cu", "csrc/kvq_attn_q8.cu", "csrc/kvq_internal.cuh"],
+    "prefill_attn": ["csrc/kvq_prefill.cuh", "csrc/kvq_prefill_q4.cu", "csrc/kvq_prefill_q8.cu",
+                     "csrc/kvq_internal.cuh"],
+}
+
+
+def kernel_source_hash(kernel="split_attn"):
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "quantized_kv_cache_03_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
+    pkg = os.path.join(ROOT, "quantized_kv_cache_03_gb300")
+    for f in KERNEL_SOURCES[kernel] + ["../include/kvq.h"]:
+        with open(os.path.normpath(os.path.join(pkg, f)), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -135,7 +144,7 @@ def profiled_traffic(workload, kernel="split_attn"):
     txt = open(p).read()
     m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt)
     m_tr = re.search(r"traffic_bytes_per_step:\s*([0-9.eE+]+)", txt)
-    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash(kernel):
         return None
     return float(m_tr.group(1))
 

@@ -182,7 +182,16 @@ kvq_status prepare_desc(Desc &d, const int32_t *head_map, bool need_ptrs, bool d
     return KVQ_OK;
 }
 
-int tiles8_for(int rows) { return rows <= 8 ? 1 : rows <= 16 ? 2 : 4; }
+// 8-row tiles per CTA of the split kernel for a call with `rows` query rows per
+// kv head: 1, 2 or 4.  KVQ_ROW_TILE=16 caps calls with more than 16 rows at
+// the 16-row kernel (the kv head's rows are then taken by several row-tile
+// CTAs that stream the same positions); the 8-row kernel has no row tiles.
+int tiles8_for(int rows)
+{
+    const char *e = std::getenv("KVQ_ROW_TILE");
+    const int cap = (e && std::atoi(e) == 16) ? 2 : 4;
+    return std::min(cap, rows <= 8 ? 1 : rows <= 16 ? 2 : 4);
+}
 
 
 // Calls with long query chunks go to the tcgen05 kernel unless KVQ_PREFILL=0.
@@ -336,7 +345,7 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
         for (Unit &u : ln.units) {
             const Desc &d = ds[u.d];
             u.n_split = std::max(1, (u.reach + ln.chunk - 1) / ln.chunk);
-            u.n_rt = (d.max_rows + tile_rows(ln) - 1) / tile_rows(ln);   // 1 unless nt == 4 or prefill
+            u.n_rt = (d.max_rows + tile_rows(ln) - 1) / tile_rows(ln);   // 1 unless rows exceed the tile
             const long long n = (long long)u.n_rt * u.n_split * d.c->n_kv_heads * u.nb;
             if (ln.n_ctas + n > INT_MAX) return KVQ_ERR_UNSUPPORTED;
             u.cta0 = ln.n_ctas;

@@ -228,10 +228,10 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT, KT>::THREADS, SplitCfg<NT, VT
         if ((int)blockIdx.x >= p.grp[k].cta0) gi = k;
     const GroupDesc &G = p.grp[gi];
     const int lb = (int)blockIdx.x - G.cta0;
-    // row tile: rows [rt * 8NT, (rt + 1) * 8NT) of the kv head.  The 8- and
-    // 16-row kernels are only chosen when every call of the launch has at most
-    // 8 NT rows per kv head, so for them n_rt is 1 and row0 a constant 0.
-    const int rt = (NT == 4) ? lb % G.n_rt : 0, ls = (NT == 4) ? lb / G.n_rt : lb;
+    // row tile: rows [rt * 8NT, (rt + 1) * 8NT) of the kv head.  The 8-row
+    // kernel is only chosen when every call of the launch has at most 8 rows
+    // per kv head, so for it n_rt is 1 and row0 a constant 0.
+    const int rt = (NT >= 2) ? lb % G.n_rt : 0, ls = (NT >= 2) ? lb / G.n_rt : lb;
     const int split = ls % G.n_split, h = (ls / G.n_split) % G.n_kv_heads, b = ls / G.n_split / G.n_kv_heads;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
     const int gb = p.grp_begin[G.head0 + h], gsz = p.grp_begin[G.head0 + h + 1] - gb;
@@ -249,13 +249,13 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT, KT>::THREADS, SplitCfg<NT, VT
     // tile's last query token sees positions up to L - t_q + its index, and
     // L <= lcap bounds that from above.
     const int r0 = split * G.chunk;
-    // (The clamp matters for long query chunks, which run on the 32-row kernel.)
-    const int r1c = (NT == 4) ? max(r0, min(min(lcap, r0 + G.chunk),
+    // (The clamp matters for long query chunks, which run on row tiles.)
+    const int r1c = (NT >= 2) ? max(r0, min(min(lcap, r0 + G.chunk),
                                             G.causal ? lcap - G.t_q + (row0 + R - 1) / gsz + 1 : lcap))
                               : min(lcap, r0 + G.chunk);
     // The row tile holding the kv head's last query token sees every position
     // below L: it alone stores the appended tokens (fused append).
-    const bool app_store = (NT == 4) ? rt == (gsz * G.t_q - 1) / (8 * NT) : true;
+    const bool app_store = (NT >= 2) ? rt == (gsz * G.t_q - 1) / (8 * NT) : true;
 
     // Nothing above reads memory written by an earlier kernel.
     pdl_wait();

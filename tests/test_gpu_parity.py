@@ -46,3 +46,19 @@ def test_config_parity(name):
             for i in range(case.tq):
                 vis = L - case.tq + i + 1 if spec.causal else L
                 assert np.array_equal(sc[b, i, :, :vis], ref["scores"][i, :, :vis]), "int32 block scores"
+
+
+@pytest.mark.parametrize("name,kw", [("verify", dict(ctx=3000, n_seqs=2)), ("prefill", dict(ctx=1500, t_q=40))])
+def test_sixteen_row_tiles(name, kw, monkeypatch):
+    """KVQ_ROW_TILE=16 takes a kv head's 32 (verify) or more (a 40-token
+    chunk) query rows with several CTAs of the 16-row kernel that stream the
+    same positions, each under its own causal limit; KVQ_PREFILL=0 keeps the
+    chunk off the tcgen05 kernel."""
+    monkeypatch.setenv("KVQ_ROW_TILE", "16")
+    monkeypatch.setenv("KVQ_PREFILL", "0")
+    for spec in W.make_spec(name, **kw):
+        case = Case(spec).build()
+        out, lse = case.decode()
+        for b in range(case.B):
+            ref = case.oracle_decode(b)
+            assert_close(out[b], lse[b], ref, what="%s seq %d (16-row tiles)" % (spec.name, b))
