@@ -40,8 +40,8 @@
 // written as NaN.
 //
 // Operands live in shared memory, K-major without swizzle: 8 rows x 16 bytes
-// core matrices, a row group's core matrices side by side along K (LBO = 128
-// bytes) and row groups SBO bytes apart.
+// core matrices, a row group's core matrices LBO bytes apart along K (128 for
+// V, 160 for K, see PrefillCfg) and row groups SBO bytes apart.
 #pragma once
 
 #include "kvq_internal.cuh"
@@ -71,12 +71,18 @@ struct PrefillCfg {
     static constexpr int R_K = 0, R_KS = R_K + kPSub * TILE_K, R_V = R_KS + kPSub * TILE_S;
     static constexpr int R_VS = R_V + kPSub * TILE_V, RAW = R_VS + kPSub * TILE_S;
     // operands (bytes)
-    static constexpr int K_SBO = 16 * 128;                           // 128 dims per row group
+    // K operand: 8-position row groups of 16 core matrices (8 positions x 8
+    // dims, 128 bytes each) along the dims, K_LBO apart: 160 rather than 128
+    // so that an 8-lane phase of a converter warp (positions 0..1 x four dim
+    // groups) stores to eight distinct 16-byte bank groups
+    static constexpr int K_LBO = 160;
+    static constexpr int K_SBO = 16 * K_LBO;                         // 128 dims per row group
+    static constexpr int KBUF = (kPN / 8) * K_SBO;                   // one K operand (64 positions)
     static constexpr int V_SBO = (kPN / 8) * 128 + 16;               // 64 positions per row group, padded so that the
                                                                      // converters' stores hit distinct banks
-    static constexpr int K_OFF = 0;                                  // [2][64 positions][128 dims]
+    static constexpr int K_OFF = 0;                                  // [2] K operands [64 positions][128 dims]
     static constexpr int VBUF = (kD / 8) * V_SBO;                    // [128 dims][64 positions]
-    static constexpr int VH_OFF = K_OFF + 2 * kPN * kD * 2;          // [2] V buffers
+    static constexpr int VH_OFF = K_OFF + 2 * KBUF;                  // [2] V buffers
     static constexpr int VL_OFF = VH_OFF + 2 * VBUF;
     static constexpr int RAW_OFF = VL_OFF + 2 * VBUF;
     static constexpr int SKF_OFF = RAW_OFF + RS * RAW;               // fp32 [2][block][64 positions]
@@ -363,8 +369,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
         if (lane == 0) {
             // descriptors of the k16 steps differ from a base only in the start
             // address (16-byte units, no carry out of its 14 bits)
-            const uint64_t dK0 = umma_desc(sbase + C::K_OFF, 128, C::K_SBO);
-            const uint64_t dK1 = umma_desc(sbase + C::K_OFF + kPN * kD * 2, 128, C::K_SBO);
+            const uint64_t dK0 = umma_desc(sbase + C::K_OFF, C::K_LBO, C::K_SBO);
+            const uint64_t dK1 = umma_desc(sbase + C::K_OFF + C::KBUF, C::K_LBO, C::K_SBO);
             for (int j = 0; j < n_tiles; ++j) {
                 if (*bad) break;
                 if (!mbar_wait(bar(C::B_KR + (j & 1)), (j >> 1) & 1)) { give_up(); break; }
@@ -375,7 +381,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
                 for (int bb = 0; bb < kNB; ++bb)
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
-                        const uint64_t o = (uint64_t)((4 * bb + 2 * kk) * 8);
+                        const uint64_t o = (uint64_t)((4 * bb + 2 * kk) * (C::K_LBO / 16));
                         umma_f16_ta(tS + kPN * bb, tQ + 16 * bb + 8 * kk, dK + o, kIdQK, kk);
                     }
                 umma_commit(bar(C::B_SFULL));
@@ -485,7 +491,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
             // K codes: 16-byte chunk i of a cache tile (i = 2kw, 2kw + 1 here)
             // holds position 8(i/2) + lane/4, dims 64(i%2) + 8(lane%4) + 0..7
             // and the same + 32
-            uint8_t *kop = smem + C::K_OFF + ob * kPN * kD * 2;
+            uint8_t *kop = smem + C::K_OFF + ob * C::KBUF;
 #pragma unroll
             for (int t4 = 0; t4 < kPSub; ++t4)
 #pragma unroll
@@ -499,8 +505,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
                         lo = i8x8_to_f16(w.x, w.y);
                         hi = i8x8_to_f16(w.z, w.w);
                     }
-                    *reinterpret_cast<uint4 *>(kop + (pos / 8) * C::K_SBO + dg0 * 128 + (pos % 8) * 16) = lo;
-                    *reinterpret_cast<uint4 *>(kop + (pos / 8) * C::K_SBO + (dg0 + 4) * 128 + (pos % 8) * 16) = hi;
+                    *reinterpret_cast<uint4 *>(kop + (pos / 8) * C::K_SBO + dg0 * C::K_LBO + (pos % 8) * 16) = lo;
+                    *reinterpret_cast<uint4 *>(kop + (pos / 8) * C::K_SBO + (dg0 + 4) * C::K_LBO + (pos % 8) * 16) = hi;
                 }
             // K scales as fp32 [block][position]
             {
