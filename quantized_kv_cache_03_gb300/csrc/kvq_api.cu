@@ -64,7 +64,8 @@ kvq_status device_setup(DeviceInfo **out)
                 return KVQ_ERR_CUDA;
             }
         }
-        if (prepare_prefill_q4() != cudaSuccess || prepare_prefill_q8() != cudaSuccess) {
+        if (prepare_prefill_q4() != cudaSuccess || prepare_prefill_q8() != cudaSuccess ||
+            prepare_verify_q4() != cudaSuccess || prepare_verify_q8() != cudaSuccess) {
             cudaGetLastError();
             return KVQ_ERR_CUDA;
         }
@@ -201,6 +202,49 @@ bool prefill_kernel_for(const Desc &d, bool dump)
     const bool on = !(e && e[0] == '0');
     return on && !dump && !d.k_new && d.c->k_type == KVQ_K_I8 && d.max_rows > KVQ_MAX_ROWS;
 }
+// Calls with 9..32 query rows per kv head (multi-token verify, short chunks)
+// go to the tcgen05 verify kernel with KVQ_VERIFY=1, else to the split
+// kernel's 16- and 32-row tiles (measured faster so far).  The score dump
+// stays on the split kernel.
+bool verify_shape(const Desc &d, bool dump)
+{
+    const char *e = std::getenv("KVQ_VERIFY");
+    const bool on = e && e[0] == '1';
+    return on && !dump && d.c->k_type == KVQ_K_I8 && d.max_rows > 8 && d.max_rows <= kVerifyRows;
+}
+bool verify_kernel_for(const Desc &d, bool dump) { return !d.k_new && verify_shape(d, dump); }
+
+// The step's tokens of call d (t_q per sequence, token-major as kvq_append
+// takes them) through the append kernel: for calls whose attention runs on a
+// kernel without the fused append.  The caller bumps the host lengths.
+cudaError_t launch_step_append(const Desc &d, cudaStream_t s, bool pdl)
+{
+    static thread_local AppendParams p;
+    const kvq_cache *c = d.c;
+    int b = 0;
+    while (b < c->n_seqs) {
+        std::memset(&p, 0, sizeof(p));
+        p.k16 = d.k_new;
+        p.v16 = d.v_new;
+        p.n_kv_heads = c->n_kv_heads;
+        while (b < c->n_seqs && p.n_entries < kMaxSeqsLaunch) {
+            const kvq_segment &sg = seg_of(c, b, c->n_segs[b] - 1);
+            AppendEntry &e = p.e[p.n_entries++];
+            e.kq = static_cast<uint8_t *>(sg.k_q);
+            e.ks = static_cast<uint16_t *>(sg.k_s);
+            e.vq = static_cast<uint8_t *>(sg.v_q);
+            e.vs = static_cast<uint16_t *>(sg.v_s);
+            e.cap = sg.cap;
+            e.dst = sg.len;
+            e.src = b * d.t_q;
+            e.n = d.t_q;
+            ++b;
+        }
+        const cudaError_t err = launch_append(p, c->v_type, c->k_type, d.t_q * c->n_kv_heads, s, pdl);
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
 int round_up(long long x, int m) { return (int)((x + m - 1) / m * m); }
 
 // Positions of sequence b that the kernel may visit: the end of its last
@@ -228,13 +272,14 @@ struct Unit {
 struct Launch {
     int v_type = 0, k_type = 0, nt = 1;
     bool prefill = false;
+    bool verify = false;   // the tcgen05 kernel for 9..32 rows per kv head (one 32-row tile)
     int chunk = KVQ_SEG_ALIGN;
     int n_ctas = 0, n_rows = 0;   // split CTAs, combine rows
     std::vector<Unit> units;
 };
 
 // Query rows one CTA of the launch takes per kv head.
-int tile_rows(const Launch &ln) { return ln.prefill ? kPrefillRows : 8 * ln.nt; }
+int tile_rows(const Launch &ln) { return ln.prefill ? kPrefillRows : ln.verify ? kVerifyRows : 8 * ln.nt; }
 
 // Split policy, one chunk per launch so that CTAs of every unit do the same
 // amount of work.  For a candidate chunk c the launch has n CTAs with work
@@ -307,7 +352,10 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
         const kvq_cache *c = ds[di].c;
         if (c->n_seqs == 0) continue;
         const bool pf = prefill_kernel_for(ds[di], dump);
-        if (!cur.units.empty() && (cur.v_type != c->v_type || cur.k_type != c->k_type || cur.prefill != pf)) flush();
+        const bool vf = !pf && verify_kernel_for(ds[di], dump);
+        if (!cur.units.empty() &&
+            (cur.v_type != c->v_type || cur.k_type != c->k_type || cur.prefill != pf || cur.verify != vf))
+            flush();
         int b = 0;
         while (b < c->n_seqs) {
             const bool new_desc = last_d != di;
@@ -322,6 +370,7 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
                 cur.v_type = c->v_type;
                 cur.k_type = c->k_type;
                 cur.prefill = pf;
+                cur.verify = vf;
             }
             heads += need_heads;
             kvs += need_kv;
@@ -340,8 +389,10 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
     }
     flush();
     for (Launch &ln : out) {
-        const int slots = ln.prefill ? dev->n_sms : std::max(1, dev->n_sms * std::max(1, dev->ctas[ln.k_type][ln.v_type][ln.nt]));
-        ln.chunk = choose_chunk(ds, ln, slots, ln.prefill ? kPrefillPositions : split_warps(ln.nt) * kWTile);
+        const bool tc = ln.prefill || ln.verify;   // tcgen05 kernels: one CTA per SM
+        const int slots = tc ? dev->n_sms : std::max(1, dev->n_sms * std::max(1, dev->ctas[ln.k_type][ln.v_type][ln.nt]));
+        ln.chunk = choose_chunk(ds, ln, slots,
+                                ln.prefill ? kPrefillPositions : ln.verify ? kVerifyPositions : split_warps(ln.nt) * kWTile);
         for (Unit &u : ln.units) {
             const Desc &d = ds[u.d];
             u.n_split = std::max(1, (u.reach + ln.chunk - 1) / ln.chunk);
@@ -462,9 +513,18 @@ kvq_status run(std::vector<Desc> &ds, bool dump, void *workspace, size_t workspa
     }
     kvq_status st = device_setup(&dev);
     if (st != KVQ_OK) return st;
+    // calls whose rows go to the tcgen05 verify kernel take their step's
+    // tokens through an append launch first (that kernel has no fused append)
+    std::vector<Desc> dsp(ds);
+    std::vector<int> pre;
+    for (size_t i = 0; i < ds.size(); ++i)
+        if (ds[i].k_new && ds[i].c->n_seqs > 0 && verify_shape(ds[i], dump)) {
+            dsp[i].k_new = dsp[i].v_new = nullptr;
+            pre.push_back((int)i);
+        }
     std::vector<Launch> lns;
     size_t ws = 0;
-    st = plan(ds, dev, dump, lns, ws);
+    st = plan(dsp, dev, dump, lns, ws);
     if (st != KVQ_OK) return st;
     if (size_out) {
         *size_out = ws;
@@ -477,12 +537,20 @@ kvq_status run(std::vector<Desc> &ds, bool dump, void *workspace, size_t workspa
     static thread_local AttnParams p;        // ~6 KB; kept off the stack
     static thread_local CombineParams cp;
     const bool pdl = pdl_enabled();
+    for (int i : pre)
+        if (launch_step_append(ds[i], stream, pdl) != cudaSuccess) {
+            cudaGetLastError();
+            return KVQ_ERR_CUDA;
+        }
     for (const Launch &ln : lns) {
-        fill_launch(ds, ln, dump, workspace, dev->timeouts, p, cp);
+        fill_launch(dsp, ln, dump, workspace, dev->timeouts, p, cp);
         cudaError_t e;
         if (ln.prefill)
             e = (ln.v_type == KVQ_V_Q4_0) ? launch_prefill_q4(p, ln.n_ctas, stream, pdl)
                                           : launch_prefill_q8(p, ln.n_ctas, stream, pdl);
+        else if (ln.verify)
+            e = (ln.v_type == KVQ_V_Q4_0) ? launch_verify_q4(p, ln.n_ctas, stream, pdl)
+                                          : launch_verify_q8(p, ln.n_ctas, stream, pdl);
         else
             e = (ln.v_type == KVQ_V_Q4_0) ? launch_split_q4(p, ln.nt, ln.k_type, ln.n_ctas, dump, stream, pdl)
                                           : launch_split_q8(p, ln.nt, ln.k_type, ln.n_ctas, dump, stream, pdl);

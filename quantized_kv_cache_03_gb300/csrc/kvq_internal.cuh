@@ -26,6 +26,8 @@ constexpr int kWTile = 16;              // positions per warp pipeline stage
 constexpr int split_warps(int nt) { return nt == 1 ? KVQ_WARPS_NT1 : KVQ_WARPS_NTX; }
 constexpr int kPrefillRows = 128;       // query rows per CTA of the tcgen05 kernel
 constexpr int kPrefillPositions = 64;   // positions per KV tile of the tcgen05 kernel
+constexpr int kVerifyRows = 32;         // query rows (MMA N) of the tcgen05 verify kernel
+constexpr int kVerifyPositions = 128;   // positions per KV tile of the tcgen05 verify kernel
 constexpr int kMaxSegsLaunch = 64;      // segment-table entries per launch
 constexpr int kMaxSeqsLaunch = 64;      // sequences per launch
 
@@ -177,6 +179,12 @@ cudaError_t launch_prefill_q4(const AttnParams &p, int n_ctas, cudaStream_t s, b
 cudaError_t launch_prefill_q8(const AttnParams &p, int n_ctas, cudaStream_t s, bool pdl);
 cudaError_t prepare_prefill_q4();
 cudaError_t prepare_prefill_q8();
+// tcgen05 kernel for 9..32 query rows per kv head (kvq_verify_q4.cu /
+// kvq_verify_q8.cu): positions on the MMA's M, rows on N, one CTA per SM.
+cudaError_t launch_verify_q4(const AttnParams &p, int n_ctas, cudaStream_t s, bool pdl);
+cudaError_t launch_verify_q8(const AttnParams &p, int n_ctas, cudaStream_t s, bool pdl);
+cudaError_t prepare_verify_q4();
+cudaError_t prepare_verify_q8();
 
 // ------------------------------------------------------------- device helpers --
 

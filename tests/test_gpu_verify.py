@@ -1,0 +1,143 @@
+"""Multi-token verify over the quantized cache: calls with 9 to 32 query rows
+per kv head (t_q query tokens x the kv head's query heads).  They run on the
+tcgen05 verify kernel (cache positions on the MMA's M, the rows on N, TMEM
+accumulators); KVQ_VERIFY=0 sends them to the split kernel's 16- and 32-row
+tiles, and every case below runs on both.  The cases cover row counts that are
+not multiples of 8, ragged and short contexts (tiles cut by segment ends, by
+the sequence length and by the causal tail), several splits merged by the
+combine, q8_0 V with x10 outlier channels, a non-causal call, uneven head maps,
+the step's tokens passed to the call (appended by a launch of their own ahead of
+the tcgen05 kernel), and a launch that mixes verify and decode calls.  All
+against the oracle on the same seeded inputs: cache bytes bit-exact, out within
+2e-3 and lse within 1e-4."""
+
+import numpy as np
+import pytest
+import torch
+
+from quantized_kv_cache_03_gb300 import kvq
+from quantized_kv_cache_03_gb300 import workloads as W
+
+from kvq_cases import SM_SCALE, Case, assert_cache_bytes, assert_close, dev, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+@pytest.fixture(params=["tcgen05", "rowtile"], autouse=True)
+def kernel(request, monkeypatch):
+    monkeypatch.setenv("KVQ_VERIFY", "1" if request.param == "tcgen05" else "0")
+    return request.param
+
+
+def _check_all(case, head_map=None):
+    out, lse = case.decode(head_map=head_map)
+    for b in range(case.B):
+        assert_cache_bytes(case, b)
+        ref = case.oracle_decode(b, head_map=head_map)
+        assert_close(out[b], lse[b], ref, what="seq %d" % b)
+    assert kvq.kvq_wait_timeouts() == 0
+    return out, lse
+
+
+@pytest.mark.parametrize("vt", [0, 1])
+def test_verify_shape_two_sequences(vt):
+    # 4 causal tokens x 8 query heads = 32 rows per kv head, 3000 positions
+    spec = W.make_spec("verify", ctx=3000, n_seqs=2, v_type=vt)[0]
+    _check_all(Case(spec).build())
+
+
+@pytest.mark.parametrize("tq,hq,hkv", [(3, 20, 4), (5, 12, 4), (2, 40, 8), (9, 24, 8)])
+def test_row_counts_not_multiples_of_eight(tq, hq, hkv):
+    # 15, 15, 10 and 27 rows per kv head
+    spec = W.make_spec("verify", ctx=1700, n_seqs=1, t_q=tq, n_q_heads=hq, n_kv_heads=hkv)[0]
+    _check_all(Case(spec).build())
+
+
+def test_ragged_short_contexts_and_segments():
+    """Four sequences of very different lengths (one shorter than a KV tile),
+    three segments each: KV tiles cut by segment ends and sequence lengths."""
+    spec = W.make_spec("verify", ctx=2600, n_seqs=4, n_seg=3, v_type=1, outliers=4)[0]
+    spec.lengths[:] = [2600, 37, 611, 1290]
+    spec.segments[:] = [W._cuts(spec.rng(9, b), int(L), 3, spec.t_q) for b, L in enumerate(spec.lengths)]
+    _check_all(Case(spec).build())
+
+
+def test_context_of_the_step_tokens_only():
+    # the cache holds only the 4 tokens being verified
+    spec = W.make_spec("verify", ctx=4, n_seqs=2, n_seg=1)[0]
+    out, lse = _check_all(Case(spec).build())
+    assert np.all(np.isfinite(lse))
+
+
+@pytest.mark.parametrize("split", [128, 640])
+def test_several_splits_and_the_combine(split, monkeypatch):
+    monkeypatch.setenv("KVQ_SPLIT", str(split))
+    spec = W.make_spec("verify", ctx=2900, n_seqs=2, v_type=1, outliers=4)[0]
+    _check_all(Case(spec).build())
+
+
+def test_non_causal_rows():
+    spec = W.make_spec("verify", ctx=1500, n_seqs=1, causal=False)[0]
+    _check_all(Case(spec).build())
+
+
+def test_uneven_head_map():
+    # kv head 0 takes 7 query heads (28 rows), kv head 3 two (8 rows)
+    spec = W.make_spec("verify", ctx=1800, n_seqs=1, n_q_heads=16, n_kv_heads=4)[0]
+    hm = [0] * 7 + [1, 1, 1, 1, 2, 2, 2, 3, 3]
+    assert len(hm) == 16
+    _check_all(Case(spec).build(), head_map=hm)
+
+
+def test_step_tokens_passed_to_the_call():
+    """k16_new / v16_new with a verify call: the tokens are appended (cache
+    bytes as kvq_append writes them), the host lengths advance, and the
+    attention sees them."""
+    spec = W.make_spec("verify", ctx=1500, n_seqs=3, v_type=0)[0]
+    case = Case(spec).build(append_step=False)
+    ids = list(range(case.B))
+    ks = np.concatenate([case.kv[b][0][case.lens[b] - case.tq:] for b in ids])
+    vs = np.concatenate([case.kv[b][1][case.lens[b] - case.tq:] for b in ids])
+    before = case.cache.lengths()
+    call = dict(cache=case.cache, q16=to_dev(case.q), n_q_heads=case.Hq, t_q=case.tq, causal_tail=True,
+                seq_lens=torch.tensor(case.lens, dtype=torch.int32, device=dev()), max_len=case.max_len,
+                head_map=None, sm_scale=SM_SCALE,
+                out=torch.full((case.B, case.tq, case.Hq, 128), float("nan"), device=dev()),
+                lse=torch.full((case.B, case.tq, case.Hq), float("nan"), device=dev()),
+                k16_new=to_dev(ks), v16_new=to_dev(vs))
+    n = kvq.kvq_decode_multi_workspace_size([call])
+    kvq.kvq_decode_attn_multi([call], torch.empty(n, dtype=torch.uint8, device=dev()) if n else None)
+    torch.cuda.synchronize()
+    assert case.cache.lengths() == [x + case.tq for x in before]
+    for b in range(case.B):
+        assert_cache_bytes(case, b)
+        assert_close(call["out"][b].cpu().numpy(), call["lse"][b].cpu().numpy(), case.oracle_decode(b),
+                     what="seq %d" % b)
+
+
+def test_verify_and_decode_calls_in_one_launch():
+    """A verify call and a single-token decode of another cache in one
+    kvq_decode_attn_multi call (two launches of different kernels)."""
+    ver = Case(W.make_spec("verify", ctx=1200, n_seqs=2)[0]).build()
+    dec = Case(W.make_spec("long", ctx=2000)[0]).build()
+    calls = []
+    for case in (ver, dec):
+        calls.append(dict(cache=case.cache, q16=to_dev(case.q), n_q_heads=case.Hq, t_q=case.tq,
+                          causal_tail=case.spec.causal,
+                          seq_lens=torch.tensor(case.lens, dtype=torch.int32, device=dev()),
+                          max_len=case.max_len, head_map=None, sm_scale=SM_SCALE,
+                          out=torch.full((case.B, case.tq, case.Hq, 128), float("nan"), device=dev()),
+                          lse=torch.full((case.B, case.tq, case.Hq), float("nan"), device=dev())))
+    n = kvq.kvq_decode_multi_workspace_size(calls)
+    kvq.kvq_decode_attn_multi(calls, torch.empty(n, dtype=torch.uint8, device=dev()) if n else None)
+    torch.cuda.synchronize()
+    for case, call in zip((ver, dec), calls):
+        for b in range(case.B):
+            assert_close(call["out"][b].cpu().numpy(), call["lse"][b].cpu().numpy(), case.oracle_decode(b),
+                         what="%s seq %d" % (case.spec.name, b))
