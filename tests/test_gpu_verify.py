@@ -1,8 +1,8 @@
 """Multi-token verify over the quantized cache: calls with 9 to 32 query rows
 per kv head (t_q query tokens x the kv head's query heads).  They run on the
-tcgen05 verify kernel (cache positions on the MMA's M, the rows on N, TMEM
-accumulators); KVQ_VERIFY=0 sends them to the split kernel's 16- and 32-row
-tiles, and every case below runs on both.  The cases cover row counts that are
+split kernel's 16- and 32-row tiles, or with KVQ_VERIFY=1 on the tcgen05
+verify kernel (cache positions on the MMA's M, the rows on N, TMEM
+accumulators); every case below runs on both.  The cases cover row counts that are
 not multiples of 8, ragged and short contexts (tiles cut by segment ends, by
 the sequence length and by the causal tail), several splits merged by the
 combine, q8_0 V with x10 outlier channels, a non-causal call, uneven head maps,
