@@ -141,3 +141,21 @@ def test_verify_and_decode_calls_in_one_launch():
         for b in range(case.B):
             assert_close(call["out"][b].cpu().numpy(), call["lse"][b].cpu().numpy(), case.oracle_decode(b),
                          what="%s seq %d" % (case.spec.name, b))
+
+
+def test_full_size_sampled_rows():
+    """The verify workload at full size (16 sequences x 4 causal tokens over
+    32768 positions, 64/8 heads), in the benchmark's launch configuration:
+    sampled query rows of the first and last sequence against the oracle."""
+    spec = W.make_spec("verify")[0]
+    case = Case(spec).build()
+    out, lse = case.decode()
+    rng = np.random.default_rng(3)
+    nr = case.tq * case.Hq
+    for b in (0, case.B - 1):
+        rows = np.unique(np.concatenate([[0, nr - 1], rng.integers(0, nr, 6)]))
+        mask = np.zeros(nr, np.uint8)
+        mask[rows] = 1
+        ref = case.oracle_decode(b, row_mask=mask)
+        assert_close(out[b], lse[b], ref, rows=rows, what="seq %d" % b)
+    assert kvq.kvq_wait_timeouts() == 0
