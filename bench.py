@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--workload", default="long", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--graph-passes", type=int, default=8,
+                    help="passes over the rotating cache copies captured in one timed CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="time budget of the reference arm (warm-up + timed steps)")
@@ -387,15 +389,21 @@ def main():
             step(grp, fz)
             step(grp)
     stream.synchronize()
+    # the timed graph runs `passes` steps on every rotation copy: one replay
+    # boundary per passes * n_rot steps, as a decode loop that captures many
+    # layers per graph has (PDL chains the launches inside a graph only)
+    passes = max(1, min(args.graph_passes, args.steps // n_rot))
     g_all = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_all, stream=stream):
-        for grp, fz in zip(sets, fused):
-            step(grp, fz)
+        for _ in range(passes):
+            for grp, fz in zip(sets, fused):
+                step(grp, fz)
     # the same steps through kvq_append + kvq_decode_attn per cache (reported beside the fused number)
     g_sep = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_sep, stream=stream):
-        for grp in sets:
-            step(grp)
+        for _ in range(passes):
+            for grp in sets:
+                step(grp)
     # decode timing graph: events around each step's fused decode call (separate pass);
     # external event nodes, so their timestamps can be read after each replay
     g_ev = torch.cuda.CUDAGraph()
@@ -412,9 +420,10 @@ def main():
             for ds in grp:
                 ds.rewind()
 
-    reps = max(1, args.steps // n_rot)
-    steps = reps * n_rot
-    warm = max(1, -(-max(3, args.warmup) // n_rot))
+    per_replay = passes * n_rot
+    reps = max(1, args.steps // per_replay)
+    steps = reps * per_replay
+    warm = max(1, -(-max(3, args.warmup) // per_replay))
     with torch.cuda.stream(stream):
         for _ in range(warm):
             g_all.replay()
@@ -436,7 +445,7 @@ def main():
     ms_per_step, value = job_rate(e0.elapsed_time(e1), world, steps, tokens_per_step, dev)
 
     # ---- one decode call per cache instead of the fused call (same steps) ----
-    sreps = max(1, min(reps, 2000 // n_rot))
+    sreps = max(1, min(reps, 2000 // per_replay))
     with torch.cuda.stream(stream):
         g_sep.replay()
         e0.record(stream)
@@ -444,7 +453,7 @@ def main():
             g_sep.replay()
         e1.record(stream)
     stream.synchronize()
-    sep_ms_per_step = e0.elapsed_time(e1) / (sreps * n_rot)
+    sep_ms_per_step = e0.elapsed_time(e1) / (sreps * per_replay)
 
     # ---- kernel-level timing pass (decode = the split kernel + its combine) ----
     kreps = max(1, min(reps, 2000 // n_rot))
@@ -549,7 +558,7 @@ def main():
         "vs_baseline": None, "dtype": "int8+fp32", "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload], "parallelism": "replicas" if world > 1 else "single",
                    "l2": "rotating %d independent cache copies (%.0f MB each, L2 129 MB); CUDA-graph replays"
-                         % (n_rot, kv_bytes / 1e6),
+                         " of %d steps" % (n_rot, kv_bytes / 1e6, per_replay),
                    "kv_bytes_per_step": kv_bytes, "tokens_per_step": tokens_per_step},
         "kv_gbs": kv_gbs, "kv_frac_of_8tbs": kv_gbs / NOMINAL_HBM_GBS,
         "kv_frac_of_measured_copy": kv_gbs / peak,
