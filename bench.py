@@ -554,7 +554,7 @@ def main():
     kv_gbs = kv_bytes / (ms_per_step * 1e-3) / 1e9   # per GPU
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
-        "warmup": warm * n_rot, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": warm * per_replay, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8+fp32", "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload], "parallelism": "replicas" if world > 1 else "single",
                    "l2": "rotating %d independent cache copies (%.0f MB each, L2 129 MB); CUDA-graph replays"
