@@ -433,13 +433,22 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    # an event at every replay boundary gives the spread of the step time
+    # (replays of per_replay steps each) beside the whole region's mean
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps - 1)]
     with ClockSampler(local) as clk:
         with torch.cuda.stream(stream):
             e0.record(stream)
-            for _ in range(reps):
+            for i in range(reps):
                 g_all.replay()
+                if i < reps - 1:
+                    evs[i].record(stream)
             e1.record(stream)
         torch.cuda.synchronize()
+    marks = [e0] + evs + [e1]
+    rep_ms = np.array([a.elapsed_time(b) for a, b in zip(marks[:-1], marks[1:])]) / per_replay
+    step_pct = {"p10": float(np.percentile(rep_ms, 10)), "p50": float(np.percentile(rep_ms, 50)),
+                "p90": float(np.percentile(rep_ms, 90)), "replays": int(reps), "steps_per_replay": int(per_replay)}
     if world > 1:
         torch.distributed.barrier()
     ms_per_step, value = job_rate(e0.elapsed_time(e1), world, steps, tokens_per_step, dev)
@@ -554,7 +563,8 @@ def main():
     kv_gbs = kv_bytes / (ms_per_step * 1e-3) / 1e9   # per GPU
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
-        "warmup": warm * per_replay, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": warm * per_replay, "ms_per_step": ms_per_step, "ms_per_step_spread": step_pct,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8+fp32", "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload], "parallelism": "replicas" if world > 1 else "single",
                    "l2": "rotating %d independent cache copies (%.0f MB each, L2 129 MB); CUDA-graph replays"
