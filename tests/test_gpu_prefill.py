@@ -151,3 +151,18 @@ def test_chunk_full_size_sampled_rows():
     mask[rows] = 1
     ref = case.oracle_decode(0, row_mask=mask)
     assert_close(out[0], lse[0], ref, rows=rows, what="prefill full size")
+
+
+def test_repeats_and_pdl_on_off_bitwise_equal(monkeypatch):
+    """Five runs with programmatic dependent launch and three without give
+    identical bits: every reduction has a fixed order, so a stale read through
+    a mis-ordered barrier phase or buffer reuse would show as a difference."""
+    spec = W.make_spec("prefill", ctx=3000, t_q=96, v_type=0)[0]
+    case = Case(spec).build()
+    monkeypatch.setenv("KVQ_PDL", "1")
+    runs = [case.decode() for _ in range(5)]
+    monkeypatch.setenv("KVQ_PDL", "0")
+    runs += [case.decode() for _ in range(3)]
+    for o, l in runs[1:]:
+        assert np.array_equal(o, runs[0][0]) and np.array_equal(l, runs[0][1])
+    assert_close(runs[0][0][0], runs[0][1][0], case.oracle_decode(0))

@@ -159,3 +159,20 @@ def test_full_size_sampled_rows():
         ref = case.oracle_decode(b, row_mask=mask)
         assert_close(out[b], lse[b], ref, rows=rows, what="seq %d" % b)
     assert kvq.kvq_wait_timeouts() == 0
+
+
+def test_repeats_and_pdl_on_off_bitwise_equal(monkeypatch):
+    """Five runs with programmatic dependent launch and three without give
+    identical bits (fixed-order reductions on both kernels), with a forced
+    split so the combine runs too."""
+    monkeypatch.setenv("KVQ_SPLIT", "1024")
+    spec = W.make_spec("verify", ctx=4000, n_seqs=2, v_type=1, outliers=4)[0]
+    case = Case(spec).build()
+    monkeypatch.setenv("KVQ_PDL", "1")
+    runs = [case.decode() for _ in range(5)]
+    monkeypatch.setenv("KVQ_PDL", "0")
+    runs += [case.decode() for _ in range(3)]
+    for o, l in runs[1:]:
+        assert np.array_equal(o, runs[0][0]) and np.array_equal(l, runs[0][1])
+    for b in range(case.B):
+        assert_close(runs[0][0][b], runs[0][1][b], case.oracle_decode(b), what="seq %d" % b)
