@@ -30,13 +30,14 @@
 // Warp roles (512 threads):
 //   warps 0-7   softmax: warp w holds TMEM lane quarter w % 4 (positions
 //               32(w%4).. of a tile, head dims 32(w%4).. of O^T) and rows
-//               16(w/4)..16(w/4)+15; the final O^T read-out;
-//   warps 8-9   K converters: K codes and K scales of a tile to the K operand;
-//   warps 10-13 V converters: V codes of a tile, half by half (64 positions),
-//               to the V hi / lo operands;
-//   warp 14     QK issuer (one lane);
-//   warp 15     P.V issuer (one lane), which also walks the segments and
-//               issues the bulk copies of the tiles RS ahead.
+//               16(w/4)..16(w/4)+15; the final O^T read-out.  Lane 0 of warp
+//               0 also issues the P.V MMAs of each tile once every softmax
+//               warp has written its P, and walks the segments and issues the
+//               bulk copies of the tiles RS ahead;
+//   warps 8-11  K converters: K codes and K scales of a tile to the K operand;
+//               lane 0 of warp 8 issues the tile's QK MMAs;
+//   warps 12-15 V converters: V codes of a tile, half by half (64 positions),
+//               to the V hi / lo operands.
 // Every wait is bounded: a wait that gives up marks the CTA, the roles leave
 // their loops, in-flight copies and MMAs are waited for (bounded), TMEM is
 // released and the CTA's rows are written as NaN.
@@ -50,11 +51,10 @@ constexpr int kVM = kVerifyPositions;    // positions per KV tile (MMA M of QK^T
 constexpr int kVN = kVerifyRows;         // query rows per CTA (MMA N): 32
 constexpr int kVSub = kVM / kWTile;      // cache tiles per KV tile (8)
 constexpr int kVHalf = kVM / 2;          // positions per V operand half (64)
-constexpr int kVSoftWarps = 8;
-constexpr int kVKWarp0 = 8;              // two K converter warps
-constexpr int kVVWarp0 = 10;             // four V converter warps
-constexpr int kVQkWarp = 14;
-constexpr int kVPvWarp = 15;
+constexpr int kVSoftWarps = 8;           // warp 0's lane 0 also issues the P.V MMAs and the bulk copies
+constexpr int kVKWarp0 = 8;              // four K converter warps; lane 0 of the first issues the QK MMAs
+constexpr int kVKWarps = 4;
+constexpr int kVVWarp0 = 12;             // four V converter warps
 constexpr int kVWarps = 16;
 constexpr int kVThreads = kVWarps * 32;
 static_assert(kVN == 32, "the softmax warps hold two halves of 16 rows");
@@ -227,12 +227,13 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
     auto bar = [&](int k) { return bars + 8u * (uint32_t)k; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::MISC_OFF);
     volatile int *bad = reinterpret_cast<volatile int *>(smem + C::MISC_OFF + 4);
-    if (warp == kVQkWarp) tmem_alloc(smem_u32(tmem_slot), 512);
+    if (warp == kVKWarp0) tmem_alloc(smem_u32(tmem_slot), 512);
     if (tid == 0) {
         *bad = 0;
         for (int k = 0; k < C::NBAR; ++k) {
             int n = 1;                                                          // raw, s_full, pv_done, fin
-            if (k == C::B_KR || k == C::B_KR + 1 || k == C::B_FIN) n = 2;
+            if (k == C::B_KR || k == C::B_KR + 1) n = kVKWarps;
+            else if (k == C::B_FIN) n = 2;
             else if (k == C::B_SFREE || k == C::B_SFREE + 1 || k == C::B_PREADY) n = kVSoftWarps;
             else if (k == C::B_VR || k == C::B_VR + 1 || k == C::B_X || k == C::B_X + 1) n = 4;
             mbar_init(bar(k), n);
@@ -299,108 +300,17 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
         const bool okw = mbar_wait(b_, parity);
         return __all_sync(0xffffffffu, okw);
     };
-    auto wwait_poll = [&](uint32_t b_, uint32_t parity) {
-        const bool okw = mbar_wait_poll(b_, parity);
-        return __all_sync(0xffffffffu, okw);
-    };
     auto wbad = [&]() { return __any_sync(0xffffffffu, *bad != 0); };
 
-    if (warp == kVQkWarp) {
-        // ================= QK MMAs: S_b^T(j) = K_b(j) Q_b^T per block =================
-        if (lane == 0) {
-            // k16-step descriptors differ from a base only in the start address
-            // (16-byte units, no carry out of its 14 bits)
-            const uint64_t dK = umma_desc(sbase + C::K_OFF, C::K_LBO, C::K_SBO);
-            const uint64_t dQ = umma_desc(sbase + C::Q_OFF, 128, C::Q_SBO);
-            for (int j = 0; j < n_tiles; ++j) {
-                if (*bad) break;
-                if (!mbar_wait(bar(C::B_KR + (j & 1)), (j >> 1) & 1)) { give_up(); break; }
-                if (j >= 2 && !mbar_wait_poll(bar(C::B_SFREE + (j & 1)), ((j - 2) >> 1) & 1)) { give_up(); break; }
-                tc_fence_after();
-                const uint32_t dS = tS + 128 * (j & 1);
-#pragma unroll
-                for (int bb = 0; bb < kNB; ++bb)
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const int kc = 4 * bb + 2 * kk;   // first core matrix of the step along K
-                        umma_f16(dS + 32 * bb, dK + (uint64_t)(kc * (C::K_LBO / 16)), dQ + (uint64_t)(kc * 8), kIdQK, kk);
-                    }
-                umma_commit(bar(C::B_SFULL + (j & 1)));
-            }
-            umma_commit(bar(C::B_FIN));
-            if (!mbar_wait(bar(C::B_FIN), 0)) give_up();
-        }
-        __syncwarp();
-    } else if (warp == kVPvWarp) {
-        // ================= P.V MMAs (O^T += V^T P^T, half by half) and the
-        // bulk copies of the tiles RS ahead =================
-        if (lane == 0) {
-            int4 *rec = reinterpret_cast<int4 *>(smem + C::REC_OFF);
-            int *nsub = reinterpret_cast<int *>(smem + C::NSUB_OFF);
-            Walk w;
-            walk_seek(p, seg0, nseg, h, r0, r1, 0, C::VCODE, w);
-            int issued = 0;
-            auto issue = [&]() {
-                const int st = issued % C::RS;
-                const int n = min(kVSub, w.Tend - w.T);
-                for (int k = 0; k < kVSub; ++k) {
-                    const int tb = (w.T + k) * kWTile;
-                    rec[st * kVSub + k] = make_int4(tb, w.la, w.le, w.pos0 + tb);
-                }
-                nsub[st] = n;
-                const uint32_t dst = sbase + C::RAW_OFF + st * C::RAW, bw = bar(C::B_RAW + st);
-                mbar_arrive_expect_tx(bw, n * C::TILE);
-                bulk_g2s(dst + C::R_K, w.gk, n * C::TILE_K, bw);
-                bulk_g2s(dst + C::R_KS, w.gks, n * C::TILE_S, bw);
-                bulk_g2s(dst + C::R_V, w.gv, n * C::TILE_V, bw);
-                bulk_g2s(dst + C::R_VS, w.gvs, n * C::TILE_S, bw);
-                w.T += n;
-                w.gk += n * C::TILE_K;
-                w.gks += n * C::TILE_S;
-                w.gv += n * C::TILE_V;
-                w.gvs += n * C::TILE_S;
-                if (w.T >= w.Tend) walk_seek(p, seg0, nseg, h, r0, r1, w.k + 1, C::VCODE, w);
-                ++issued;
-            };
-            while (issued < min(C::RS, n_tiles)) issue();
-            const uint64_t dPH = umma_desc(sbase + C::PH_OFF, C::P_LBO, C::P_SBO);
-            const uint64_t dPL = umma_desc(sbase + C::PL_OFF, C::P_LBO, C::P_SBO);
-            const uint64_t dVH[2] = {umma_desc(sbase + C::VH_OFF, 128, C::V_SBO),
-                                     umma_desc(sbase + C::VH_OFF + C::VBUF, 128, C::V_SBO)};
-            const uint64_t dVL[2] = {umma_desc(sbase + C::VL_OFF, 128, C::V_SBO),
-                                     umma_desc(sbase + C::VL_OFF + C::VBUF, 128, C::V_SBO)};
-            for (int j = 0; j < n_tiles; ++j) {
-                if (*bad) break;
-                if (!mbar_wait_poll(bar(C::B_PREADY), j & 1)) { give_up(); break; }
-                bool ok = true;
-                for (int hh = 0; hh < 2 && ok; ++hh) {
-                    if (!mbar_wait(bar(C::B_VR + hh), j & 1)) { give_up(); ok = false; break; }
-                    tc_fence_after();
-#pragma unroll
-                    for (int ks = 0; ks < kVHalf / 16; ++ks) {
-                        const uint64_t ov = (uint64_t)(16 * ks);                  // 2 core matrices (256 B) along positions
-                        const uint64_t op = (uint64_t)(2 * (4 * hh + ks) * (C::P_LBO / 16));
-                        umma_f16(tO, dVH[hh] + ov, dPH + op, kIdPV, (j > 0 || hh > 0 || ks > 0) ? 1u : 0u);
-                        umma_f16(tO, dVH[hh] + ov, dPL + op, kIdPV, 1u);
-                        umma_f16(tO, dVL[hh] + ov, dPH + op, kIdPV, 1u);
-                    }
-                    umma_commit(bar(C::B_PV + hh));
-                }
-                if (!ok) break;
-                // both converters are done with tile j's raw stage (the V warps
-                // said so; the K warps before QK(j), which the softmax passed)
-                if (issued < n_tiles) issue();
-            }
-            // drain: every MMA issued here, and the copies no converter took
-            umma_commit(bar(C::B_FIN));
-            if (!mbar_wait(bar(C::B_FIN), 0)) give_up();
-            for (int k = max(0, issued - C::RS); k < issued; ++k) mbar_wait(bar(C::B_RAW + k % C::RS), (k / C::RS) & 1);
-        }
-        __syncwarp();
-    } else if (warp >= kVKWarp0) {
+    if (warp >= kVKWarp0) {
         // ================= convert: cache codes -> fp16 operands =================
         const bool kside = warp < kVVWarp0;
         const int kt = tid - 32 * kVKWarp0, ct = tid - 32 * kVVWarp0;
+        const bool qk_lane = warp == kVKWarp0 && lane == 0;   // issues the QK MMAs of each tile
+        // k16-step descriptors differ from a base only in the start address
+        // (16-byte units, no carry out of its 14 bits)
+        const uint64_t dK = umma_desc(sbase + C::K_OFF, C::K_LBO, C::K_SBO);
+        const uint64_t dQ = umma_desc(sbase + C::Q_OFF, 128, C::Q_SBO);
         for (int j = 0; j < n_tiles; ++j) {
             if (wbad()) break;
             const int st = j % C::RS, ob = j & 1;
@@ -430,8 +340,8 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
                 // and the same + 32
                 uint8_t *kop = smem + C::K_OFF;
 #pragma unroll 4
-                for (int mm = 0; mm < kVSub * (C::TILE_K / 16) / 64; ++mm) {
-                    const int cidx = kt + 64 * mm;
+                for (int mm = 0; mm < kVSub * (C::TILE_K / 16) / (32 * kVKWarps); ++mm) {
+                    const int cidx = kt + 32 * kVKWarps * mm;
                     const int t4 = cidx / (C::TILE_K / 16), ci = cidx % (C::TILE_K / 16), i = ci >> 5, ln = ci & 31;
                     const int pos = kWTile * t4 + 8 * (i >> 1) + (ln >> 2);
                     const int dg0 = 8 * (i & 1) + (ln & 3);
@@ -447,8 +357,8 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
                 // K scales as fp32 [block][position]
                 float *skf = reinterpret_cast<float *>(smem + C::SKF_OFF) + ob * kNB * kVM;
 #pragma unroll
-                for (int e = 0; e < kVM / 64; ++e) {
-                    const int pos = kt + 64 * e, t4 = pos / kWTile, u = pos % kWTile;
+                for (int e = 0; e < kVM / (32 * kVKWarps); ++e) {
+                    const int pos = kt + 32 * kVKWarps * e, t4 = pos / kWTile, u = pos % kWTile;
                     float x[4] = {0.f, 0.f, 0.f, 0.f};
                     if (slot_ok(pos)) load4h(reinterpret_cast<const uint16_t *>(raw + C::R_KS + t4 * C::TILE_S) + u * kNB, x);
 #pragma unroll
@@ -457,6 +367,28 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::B_KR + ob));
+                if (qk_lane) {
+                    // ---- QK MMAs: S_b^T(j) = K_b(j) Q_b^T, once every K warp is
+                    // done and the softmax has read S(j-2) ----
+                    bool okq = mbar_wait(bar(C::B_KR + ob), (j >> 1) & 1);
+                    if (okq && j >= 2) okq = mbar_wait(bar(C::B_SFREE + ob), ((j - 2) >> 1) & 1);
+                    if (!okq) {
+                        give_up();
+                    } else {
+                        tc_fence_after();
+                        const uint32_t dS = tS + 128 * ob;
+#pragma unroll
+                        for (int bb = 0; bb < kNB; ++bb)
+#pragma unroll
+                            for (int kk = 0; kk < 2; ++kk) {
+                                const int kc = 4 * bb + 2 * kk;   // first core matrix of the step along K
+                                umma_f16(dS + 32 * bb, dK + (uint64_t)(kc * (C::K_LBO / 16)), dQ + (uint64_t)(kc * 8),
+                                         kIdQK, kk);
+                            }
+                        umma_commit(bar(C::B_SFULL + ob));
+                    }
+                }
+                __syncwarp();
             } else {
                 // V: v / 2 = code * (d / 2) as fp16 hi + lo, stored [dim][position]
                 // in the half's operand once P.V(j-1) of that half is done
@@ -539,6 +471,11 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
                 if (!ok) break;
             }
         }
+        if (qk_lane) {
+            umma_commit(bar(C::B_FIN));
+            if (!mbar_wait(bar(C::B_FIN), 0)) give_up();
+        }
+        __syncwarp();
     } else {
         // ================= softmax: scores, P, final O =================
         // This thread: position t of each KV tile (TMEM lane t of S) and head
@@ -560,10 +497,69 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
         }
         int xph = 0;           // phases of this row half's exchange barrier so far
         bool o_live = false;   // O^T holds an earlier tile's P.V
+        // ---- warp 0, lane 0: the bulk copies of the tiles RS ahead and the P.V
+        // MMAs (O^T += V^T P^T, half by half) of each tile once every softmax
+        // warp has written its P ----
+        const bool pv_lane = warp == 0 && lane == 0;
+        int4 *rec = reinterpret_cast<int4 *>(smem + C::REC_OFF);
+        int *nsub = reinterpret_cast<int *>(smem + C::NSUB_OFF);
+        Walk w;
+        int issued = 0;
+        auto issue = [&]() {
+            const int st = issued % C::RS;
+            const int n = min(kVSub, w.Tend - w.T);
+            for (int k = 0; k < kVSub; ++k) {
+                const int tb = (w.T + k) * kWTile;
+                rec[st * kVSub + k] = make_int4(tb, w.la, w.le, w.pos0 + tb);
+            }
+            nsub[st] = n;
+            const uint32_t dst = sbase + C::RAW_OFF + st * C::RAW, bw = bar(C::B_RAW + st);
+            mbar_arrive_expect_tx(bw, n * C::TILE);
+            bulk_g2s(dst + C::R_K, w.gk, n * C::TILE_K, bw);
+            bulk_g2s(dst + C::R_KS, w.gks, n * C::TILE_S, bw);
+            bulk_g2s(dst + C::R_V, w.gv, n * C::TILE_V, bw);
+            bulk_g2s(dst + C::R_VS, w.gvs, n * C::TILE_S, bw);
+            w.T += n;
+            w.gk += n * C::TILE_K;
+            w.gks += n * C::TILE_S;
+            w.gv += n * C::TILE_V;
+            w.gvs += n * C::TILE_S;
+            if (w.T >= w.Tend) walk_seek(p, seg0, nseg, h, r0, r1, w.k + 1, C::VCODE, w);
+            ++issued;
+        };
+        if (pv_lane) {
+            walk_seek(p, seg0, nseg, h, r0, r1, 0, C::VCODE, w);
+            while (issued < min(C::RS, n_tiles)) issue();
+        }
+        __syncwarp();
+        auto pv_issue = [&](int j) {
+            const uint64_t dPH = umma_desc(sbase + C::PH_OFF, C::P_LBO, C::P_SBO);
+            const uint64_t dPL = umma_desc(sbase + C::PL_OFF, C::P_LBO, C::P_SBO);
+            if (!mbar_wait(bar(C::B_PREADY), j & 1)) return false;
+            for (int hh = 0; hh < 2; ++hh) {
+                if (!mbar_wait(bar(C::B_VR + hh), j & 1)) return false;
+                tc_fence_after();
+                const uint64_t dVH = umma_desc(sbase + C::VH_OFF + hh * C::VBUF, 128, C::V_SBO);
+                const uint64_t dVL = umma_desc(sbase + C::VL_OFF + hh * C::VBUF, 128, C::V_SBO);
+#pragma unroll
+                for (int ks = 0; ks < kVHalf / 16; ++ks) {
+                    const uint64_t ov = (uint64_t)(16 * ks);                  // 2 core matrices (256 B) along positions
+                    const uint64_t op = (uint64_t)(2 * (4 * hh + ks) * (C::P_LBO / 16));
+                    umma_f16(tO, dVH + ov, dPH + op, kIdPV, (j > 0 || hh > 0 || ks > 0) ? 1u : 0u);
+                    umma_f16(tO, dVH + ov, dPL + op, kIdPV, 1u);
+                    umma_f16(tO, dVL + ov, dPH + op, kIdPV, 1u);
+                }
+                umma_commit(bar(C::B_PV + hh));
+            }
+            // both converters are done with tile j's raw stage (the V warps said
+            // so; the K warps before QK(j), which every softmax warp passed)
+            if (issued < n_tiles) issue();
+            return true;
+        };
         for (int j = 0; j < n_tiles; ++j) {
             if (wbad()) break;
             const int ob = j & 1;
-            if (!wwait_poll(bar(C::B_SFULL + ob), (j >> 1) & 1) || !wwait(bar(C::B_KR + ob), (j >> 1) & 1)) {
+            if (!wwait(bar(C::B_SFULL + ob), (j >> 1) & 1) || !wwait(bar(C::B_KR + ob), (j >> 1) & 1)) {
                 give_up();
                 break;
             }
@@ -625,7 +621,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
             if (lane == 0) xf[(hr * 2 + par) * 4 + qq] = wneed ? 1 : 0;
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_X + hr));
-            if (!wwait_poll(bar(C::B_X + hr), par)) { give_up(); break; }
+            if (!wwait(bar(C::B_X + hr), par)) { give_up(); break; }
             ++xph;
             const int4 f4 = *reinterpret_cast<const int4 *>(xf + (hr * 2 + par) * 4);
             const bool any = (f4.x | f4.y | f4.z | f4.w) != 0;
@@ -636,7 +632,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
                 if (!(lane & 1)) xm[((hr * 2 + par) * 16 + (lane >> 1)) * 4 + qq] = tmx;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::B_X + hr));
-                if (!wwait_poll(bar(C::B_X + hr), par)) { give_up(); break; }
+                if (!wwait(bar(C::B_X + hr), par)) { give_up(); break; }
                 ++xph;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -658,7 +654,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
             }
             // P(j) may overwrite P(j-1), and O^T is stable, once P.V(j-1) is done
             if (j > 0) {
-                if (!wwait_poll(bar(C::B_PV + 1), (j - 1) & 1)) { give_up(); break; }
+                if (!wwait(bar(C::B_PV + 1), (j - 1) & 1)) { give_up(); break; }
                 tc_fence_after();
             }
             if (any && o_live) {   // O^T *= alpha on this half's columns (this warp's 32 head dims)
@@ -693,7 +689,18 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_PREADY));
             o_live = true;
+            if (warp == 0) {
+                if (pv_lane && !pv_issue(j)) give_up();
+                __syncwarp();
+            }
         }
+        // drain: every P.V MMA, and the copies no converter took
+        if (pv_lane) {
+            umma_commit(bar(C::B_FIN));
+            if (!mbar_wait(bar(C::B_FIN), 0)) give_up();
+            for (int k = max(0, issued - C::RS); k < issued; ++k) mbar_wait(bar(C::B_RAW + k % C::RS), (k / C::RS) & 1);
+        }
+        __syncwarp();
         // ---- final: the rows' sums over the 128 positions of a tile (the four
         // warps of the half), then O^T column by column ----
         bool ok = !wbad();
@@ -709,7 +716,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
                 if (!(lane & 1)) xm[((hr * 2 + par) * 16 + (lane >> 1)) * 4 + qq] = ls;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::B_X + hr));
-                ok = wwait_poll(bar(C::B_X + hr), par);
+                ok = wwait(bar(C::B_X + hr), par);
                 if (ok) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -751,7 +758,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kVQkWarp) {
+    if (warp == kVKWarp0) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
