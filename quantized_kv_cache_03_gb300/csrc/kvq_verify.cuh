@@ -91,7 +91,8 @@ struct VerifyCfg {
     static constexpr int ONSUB_OFF = OREC_OFF + 2 * kVSub * 16;      // int [2]
     static constexpr int XF_OFF = (ONSUB_OFF + 8 + 15) / 16 * 16;    // int [2 halves][2 parity][4 quarters]
     static constexpr int XM_OFF = XF_OFF + 2 * 2 * 4 * 4;            // fp32 [2 halves][2 parity][16 rows][4 quarters]
-    static constexpr int BAR_OFF = XM_OFF + 2 * 2 * 16 * 4 * 4;
+    static constexpr int WALK_OFF = XM_OFF + 2 * 2 * 16 * 4 * 4;    // the copy issuer's Walk and stage count
+    static constexpr int BAR_OFF = WALK_OFF + (int)((sizeof(Walk) + 4 + 15) / 16 * 16);
     // barriers (arrivals per phase): raw[RS] (copy bytes), k_ready[2] (2 K warps),
     // s_full[2] (commit), s_free[2] (8 softmax warps), v_ready[2 halves] (4 V warps),
     // pv_done[2 halves] (commit), p_ready (8), fin (2 commits), x[2 row halves] (4 warps)
@@ -503,8 +504,10 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
         const bool pv_lane = warp == 0 && lane == 0;
         int4 *rec = reinterpret_cast<int4 *>(smem + C::REC_OFF);
         int *nsub = reinterpret_cast<int *>(smem + C::NSUB_OFF);
-        Walk w;
-        int issued = 0;
+        // (kept in shared memory: only this lane uses them, and registers are
+        // what the softmax threads run short of)
+        Walk &w = *reinterpret_cast<Walk *>(smem + C::WALK_OFF);
+        int &issued = *reinterpret_cast<int *>(smem + C::WALK_OFF + sizeof(Walk));
         auto issue = [&]() {
             const int st = issued % C::RS;
             const int n = min(kVSub, w.Tend - w.T);
@@ -528,6 +531,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
             ++issued;
         };
         if (pv_lane) {
+            issued = 0;
             walk_seek(p, seg0, nseg, h, r0, r1, 0, C::VCODE, w);
             while (issued < min(C::RS, n_tiles)) issue();
         }
@@ -625,8 +629,8 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
             ++xph;
             const int4 f4 = *reinterpret_cast<const int4 *>(xf + (hr * 2 + par) * 4);
             const bool any = (f4.x | f4.y | f4.z | f4.w) != 0;
-            float alpha[16];
             if (any) {   // the exact tile maximum of every row of the half, then the new references
+                float alpha[16];
                 const float tmx = warp_reduce16<true>(s, lane);   // row lane / 2 over this warp's positions
                 par = xph & 1;
                 if (!(lane & 1)) xm[((hr * 2 + par) * 16 + (lane >> 1)) * 4 + qq] = tmx;
@@ -642,6 +646,17 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
                     l[i] *= alpha[i];
                     m[i] = mnew;
                 }
+                if (o_live) {   // O^T *= alpha on this half's columns (this warp's 32 head dims), once P.V(j-1) is done
+                    if (!wwait(bar(C::B_PV + 1), (j - 1) & 1)) { give_up(); break; }
+                    tc_fence_after();
+                    uint32_t o[16];
+                    tmem_ld16(tO + lane_base + 16 * hr, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha[k]);
+                    tmem_st16(tO + lane_base + 16 * hr, o);
+                    tmem_wait_st();
+                }
             }
 #pragma unroll
             for (int i = 0; i < 16; i += 2) {
@@ -656,15 +671,6 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_attn_kernel(const __grid_
             if (j > 0) {
                 if (!wwait(bar(C::B_PV + 1), (j - 1) & 1)) { give_up(); break; }
                 tc_fence_after();
-            }
-            if (any && o_live) {   // O^T *= alpha on this half's columns (this warp's 32 head dims)
-                uint32_t o[16];
-                tmem_ld16(tO + lane_base + 16 * hr, o);
-                tmem_wait_ld();
-#pragma unroll
-                for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha[k]);
-                tmem_st16(tO + lane_base + 16 * hr, o);
-                tmem_wait_st();
             }
             // P hi / lo of position t, rows 16hr + 8c8 .. + 7: one 16-byte row of a
             // core matrix of the MN-major operand
