@@ -93,3 +93,15 @@ def test_fused_append_max_tokens_with_a_head_map(monkeypatch):
     for b in range(case.B):
         assert_cache_bytes(case, b)
         assert_close(o[b], l[b], case.oracle_decode(b, head_map=hm), what="seq %d" % b)
+
+
+@pytest.mark.parametrize("split", [None, "64"])
+def test_fused_append_on_sixteen_row_tiles(split, monkeypatch):
+    """KVQ_ROW_TILE=16: the verify shape's 32 rows per kv head go to two
+    16-row CTAs that stream the same positions; only the tile holding the kv
+    head's last query token stores the appended tokens, and both see them
+    (with 64-position splits the new tokens straddle split edges too)."""
+    monkeypatch.setenv("KVQ_ROW_TILE", "16")
+    if split:
+        monkeypatch.setenv("KVQ_SPLIT", split)
+    _run_and_check([Case(s).build(append_step=False) for s in W.make_spec("verify", ctx=1538, n_seqs=2)])
