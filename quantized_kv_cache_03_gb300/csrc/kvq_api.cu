@@ -20,6 +20,7 @@ struct DeviceInfo {
     bool ready = false;
     int n_sms = 0;
     int ctas[2][2][5] = {};   // [k_type][v_type][n_tiles8] resident split CTAs per SM
+    int ctas_half[2][2] = {};   // [k_type][v_type] the same for the 8-row kernel with kWarpsHalf warps
     unsigned int *timeouts = nullptr;   // device address of g_wait_timeouts
 };
 
@@ -54,15 +55,23 @@ kvq_status device_setup(DeviceInfo **out)
         const int nts[3] = {1, 2, 4};
         for (int i = 0; i < 3; ++i) {
             const int nt = nts[i];
-            if (prepare_split_q4(nt, KVQ_K_I8, false, &d.ctas[KVQ_K_I8][KVQ_V_Q4_0][nt]) != cudaSuccess ||
-                prepare_split_q8(nt, KVQ_K_I8, false, &d.ctas[KVQ_K_I8][KVQ_V_Q8_0][nt]) != cudaSuccess ||
-                prepare_split_q4(nt, KVQ_K_F16, false, &d.ctas[KVQ_K_F16][KVQ_V_Q4_0][nt]) != cudaSuccess ||
-                prepare_split_q8(nt, KVQ_K_F16, false, &d.ctas[KVQ_K_F16][KVQ_V_Q8_0][nt]) != cudaSuccess ||
-                prepare_split_q4(nt, KVQ_K_I8, true, nullptr) != cudaSuccess ||
-                prepare_split_q8(nt, KVQ_K_I8, true, nullptr) != cudaSuccess) {
+            const int w = split_warps(nt);
+            if (prepare_split_q4(nt, w, KVQ_K_I8, false, &d.ctas[KVQ_K_I8][KVQ_V_Q4_0][nt]) != cudaSuccess ||
+                prepare_split_q8(nt, w, KVQ_K_I8, false, &d.ctas[KVQ_K_I8][KVQ_V_Q8_0][nt]) != cudaSuccess ||
+                prepare_split_q4(nt, w, KVQ_K_F16, false, &d.ctas[KVQ_K_F16][KVQ_V_Q4_0][nt]) != cudaSuccess ||
+                prepare_split_q8(nt, w, KVQ_K_F16, false, &d.ctas[KVQ_K_F16][KVQ_V_Q8_0][nt]) != cudaSuccess ||
+                prepare_split_q4(nt, w, KVQ_K_I8, true, nullptr) != cudaSuccess ||
+                prepare_split_q8(nt, w, KVQ_K_I8, true, nullptr) != cudaSuccess) {
                 cudaGetLastError();
                 return KVQ_ERR_CUDA;
             }
+        }
+        if (prepare_split_q4(1, kWarpsHalf, KVQ_K_I8, false, &d.ctas_half[KVQ_K_I8][KVQ_V_Q4_0]) != cudaSuccess ||
+            prepare_split_q8(1, kWarpsHalf, KVQ_K_I8, false, &d.ctas_half[KVQ_K_I8][KVQ_V_Q8_0]) != cudaSuccess ||
+            prepare_split_q4(1, kWarpsHalf, KVQ_K_F16, false, &d.ctas_half[KVQ_K_F16][KVQ_V_Q4_0]) != cudaSuccess ||
+            prepare_split_q8(1, kWarpsHalf, KVQ_K_F16, false, &d.ctas_half[KVQ_K_F16][KVQ_V_Q8_0]) != cudaSuccess) {
+            cudaGetLastError();
+            return KVQ_ERR_CUDA;
         }
         if (prepare_prefill_q4() != cudaSuccess || prepare_prefill_q8() != cudaSuccess ||
             prepare_verify_q4() != cudaSuccess || prepare_verify_q8() != cudaSuccess) {
@@ -271,6 +280,7 @@ struct Unit {
 // rows per kv head than the split kernel's 32-row tile and no fused append.
 struct Launch {
     int v_type = 0, k_type = 0, nt = 1;
+    int warps = 0;   // warps per split CTA (split_warps(nt), or kWarpsHalf for the 8-row kernel)
     bool prefill = false;
     bool verify = false;   // the tcgen05 kernel for 9..32 rows per kv head (one 32-row tile)
     int chunk = KVQ_SEG_ALIGN;
@@ -391,8 +401,30 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
     for (Launch &ln : out) {
         const bool tc = ln.prefill || ln.verify;   // tcgen05 kernels: one CTA per SM
         const int slots = tc ? dev->n_sms : std::max(1, dev->n_sms * std::max(1, dev->ctas[ln.k_type][ln.v_type][ln.nt]));
+        ln.warps = tc ? 0 : split_warps(ln.nt);
         ln.chunk = choose_chunk(ds, ln, slots,
-                                ln.prefill ? kPrefillPositions : ln.verify ? kVerifyPositions : split_warps(ln.nt) * kWTile);
+                                ln.prefill ? kPrefillPositions : ln.verify ? kVerifyPositions : ln.warps * kWTile);
+        // The 8-row kernel with half the warps (two CTAs per SM) when the full
+        // CTAs take more than one wave; KVQ_SPLIT_WARPS=8 or 16 forces either.
+        // A chunk forced by KVQ_SPLIT keeps the full CTAs unless asked, so that
+        // one forced chunk gives one partition of the positions.
+        const int half_ctas = dev->ctas_half[ln.k_type][ln.v_type];
+        if (!tc && ln.nt == 1 && !dump && half_ctas >= 2) {
+            const char *e = std::getenv("KVQ_SPLIT_WARPS");
+            const char *fs = std::getenv("KVQ_SPLIT");
+            const int force = e ? std::atoi(e) : 0;
+            bool half = force == kWarpsHalf;
+            if (force != kWarpsHalf && force != split_warps(1) && !(fs && std::atoi(fs) > 0)) {
+                long long n = 0;
+                for (const Unit &u : ln.units)
+                    n += (long long)std::max(1, (u.reach + ln.chunk - 1) / ln.chunk) * ds[u.d].c->n_kv_heads * u.nb;
+                half = n > slots;
+            }
+            if (half) {
+                ln.warps = kWarpsHalf;
+                ln.chunk = choose_chunk(ds, ln, dev->n_sms * half_ctas, kWarpsHalf * kWTile);
+            }
+        }
         for (Unit &u : ln.units) {
             const Desc &d = ds[u.d];
             u.n_split = std::max(1, (u.reach + ln.chunk - 1) / ln.chunk);
@@ -552,8 +584,8 @@ kvq_status run(std::vector<Desc> &ds, bool dump, void *workspace, size_t workspa
             e = (ln.v_type == KVQ_V_Q4_0) ? launch_verify_q4(p, ln.n_ctas, stream, pdl)
                                           : launch_verify_q8(p, ln.n_ctas, stream, pdl);
         else
-            e = (ln.v_type == KVQ_V_Q4_0) ? launch_split_q4(p, ln.nt, ln.k_type, ln.n_ctas, dump, stream, pdl)
-                                          : launch_split_q8(p, ln.nt, ln.k_type, ln.n_ctas, dump, stream, pdl);
+            e = (ln.v_type == KVQ_V_Q4_0) ? launch_split_q4(p, ln.nt, ln.warps, ln.k_type, ln.n_ctas, dump, stream, pdl)
+                                          : launch_split_q8(p, ln.nt, ln.warps, ln.k_type, ln.n_ctas, dump, stream, pdl);
         if (e == cudaSuccess && ln.n_rows > 0) e = launch_combine(cp, ln.n_rows, stream, pdl);
         if (e != cudaSuccess) {
             cudaGetLastError();

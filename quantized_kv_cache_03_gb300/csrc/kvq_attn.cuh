@@ -65,9 +65,9 @@ namespace kvq {
 
 
 
-template <int NT, int VT, int KT = KVQ_K_I8>
+template <int NT, int VT, int KT = KVQ_K_I8, int W = split_warps(NT)>
 struct SplitCfg {
-    static constexpr int WARPS = split_warps(NT);
+    static constexpr int WARPS = W;
     static constexpr int THREADS = WARPS * 32;
     // the <= 8-row kernels are held to 128 registers per thread (512 threads per SM x 4 CTAs of 4 warps,
     // or one CTA of 16 warps); the others take what they need
@@ -91,10 +91,15 @@ struct SplitCfg {
     static constexpr int VS_OFF = V_OFF + TPS * TILE_V;
     static constexpr int STAGE = VS_OFF + TPS * TILE_S;
     static constexpr int RING = STAGES * STAGE;               // per warp
-    static constexpr int Q_OFF = WARPS * RING;                // int8 codes (F16 K: fp16 values) [QROWS][kD]
+    // The query rows' codes, scales and code sums are read only while the
+    // query table below is built.  Every warp hands its first STAGES - 1 ring
+    // slots to the copy engine before that and its last slot only in the main
+    // loop, so they sit in the last warp's last slot when they fit there.
+    static constexpr int QBYTES = QROWS * KCODE + 2 * QROWS * kNB * 4;
+    static constexpr bool Q_IN_RING = QBYTES <= STAGE;
+    static constexpr int Q_OFF = Q_IN_RING ? (WARPS - 1) * RING + (STAGES - 1) * STAGE : WARPS * RING;
     static constexpr int QS_OFF = Q_OFF + QROWS * KCODE;      // fp32 [QROWS][kNB]
     static constexpr int QSUM_OFF = QS_OFF + QROWS * kNB * 4; // int32 [QROWS][kNB]
-    static constexpr int ML_OFF = QSUM_OFF + QROWS * kNB * 4; // fp32 m, l [WARPS][8*NT]; M, 1/L, lse [8*NT]
     // Per-lane query table, [chunk][lane][4 words] (16-byte chunks, lane-major
     // so a warp's LDS.128 of one chunk is conflict free): per (8-row tile nt,
     // block) the query MMA B fragments of both k16 steps and the accumulator
@@ -103,15 +108,20 @@ struct SplitCfg {
     static constexpr int SEED_CHUNKS = NT * kNB;
     static constexpr int SQ_CHUNKS = NT * 2;
     static constexpr int QF_CHUNKS = QB_CHUNKS + SEED_CHUNKS + SQ_CHUNKS;
-    static constexpr int QF_OFF = (ML_OFF + (2 * WARPS + 3) * 8 * NT * 4 + 15) / 16 * 16;
+    static constexpr int QF_OFF = Q_IN_RING ? WARPS * RING : (QSUM_OFF + QROWS * kNB * 4 + 15) / 16 * 16;
     static constexpr int OROW = kD + 4;                        // merge slice row (floats, padded)
+    // The merge reuses the stage rings once every stage is consumed: one
+    // [8*NT][OROW] slice per warp when they all fit (else one shared slice),
+    // then m, l [WARPS][8*NT] and M, 1/L, lse [8*NT].
+    static constexpr bool SLICES = WARPS * 8 * NT * OROW * 4 <= WARPS * STAGES * STAGE;
+    static constexpr int ML_OFF = (SLICES ? WARPS : 1) * 8 * NT * OROW * 4;
     static constexpr int TI_OFF = QF_OFF + QF_CHUNKS * 32 * 16;  // int4 record of a stage's first tile [WARPS][STAGES]
     static constexpr int NS_OFF = TI_OFF + WARPS * STAGES * 16;         // int tiles in stage [WARPS][STAGES]
     static constexpr int NEW_OFF = (NS_OFF + WARPS * STAGES * 4 + 15) / 16 * 16;  // appended rows [KVQ_MAX_T_Q_APPEND][32 lanes][3 words]
     static constexpr int BAR_OFF = NEW_OFF + KVQ_MAX_T_Q_APPEND * 32 * 12;          // uint64 mbarrier [WARPS][STAGES]
     static constexpr int FLAG_OFF = BAR_OFF + WARPS * STAGES * 8;
     static constexpr int SMEM = FLAG_OFF + 16;
-    static_assert(8 * NT * OROW * 4 <= WARPS * RING, "merge buffer must fit in the stage rings");
+    static_assert(ML_OFF + (2 * WARPS + 3) * 8 * NT * 4 <= WARPS * RING, "merge buffers must fit in the stage rings");
     static_assert(STAGE % 16 == 0 && KS_OFF % 16 == 0 && V_OFF % 16 == 0 && VS_OFF % 16 == 0, "16-byte granules");
     static_assert(TPS == 1 || TPS == 2, "one or two tiles per stage");
     static_assert(SMEM <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
@@ -206,11 +216,11 @@ __device__ __forceinline__ uint32_t q_pair(uint32_t w, int k0)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-template <int NT, int VT, int KT, bool DUMP>
-__global__ void __launch_bounds__(SplitCfg<NT, VT, KT>::THREADS, SplitCfg<NT, VT, KT>::MIN_CTAS)
+template <int NT, int VT, int KT, bool DUMP, int W>
+__global__ void __launch_bounds__(SplitCfg<NT, VT, KT, W>::THREADS, SplitCfg<NT, VT, KT, W>::MIN_CTAS)
     split_attn_kernel(const __grid_constant__ AttnParams p)
 {
-    using C = SplitCfg<NT, VT, KT>;
+    using C = SplitCfg<NT, VT, KT, W>;
     static_assert(!(DUMP && KT == KVQ_K_F16), "the score dump exists for int8 K only");
     constexpr int kWarps = C::WARPS;
     constexpr int kThreads = C::THREADS;
@@ -814,7 +824,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT, KT>::THREADS, SplitCfg<NT, VT
         // Each (row, dim) belongs to one lane per warp; a warp's accumulator is
         // scaled by 2^(m_warp - M) / L.  Head dims pv_dim(mt, g) and
         // pv_dim(mt, g + 8) are adjacent, so a lane stores them as one pair.
-        constexpr bool kSlices = kWarps * RW * C::OROW * 4 <= kWarps * C::RING;
+        constexpr bool kSlices = C::SLICES;
         auto put = [&](float *dst, bool add) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -873,77 +883,81 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT, KT>::THREADS, SplitCfg<NT, VT
     }
 }
 
-template <int NT, int VT, int KT>
+template <int NT, int VT, int KT, int W>
 cudaError_t launch_split_t(const AttnParams &p, int n_ctas, bool dump, cudaStream_t s, bool pdl)
 {
+    using C = SplitCfg<NT, VT, KT, W>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(n_ctas);
-    cfg.blockDim = dim3(SplitCfg<NT, VT, KT>::THREADS);
-    cfg.dynamicSmemBytes = SplitCfg<NT, VT, KT>::SMEM;
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = s;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if constexpr (KT == KVQ_K_I8) {
-        if (dump) return cudaLaunchKernelEx(&cfg, split_attn_kernel<NT, VT, KT, true>, p);
+    if constexpr (KT == KVQ_K_I8 && W == split_warps(NT)) {
+        if (dump) return cudaLaunchKernelEx(&cfg, split_attn_kernel<NT, VT, KT, true, W>, p);
     } else {
         if (dump) return cudaErrorInvalidValue;
     }
-    return cudaLaunchKernelEx(&cfg, split_attn_kernel<NT, VT, KT, false>, p);
+    return cudaLaunchKernelEx(&cfg, split_attn_kernel<NT, VT, KT, false, W>, p);
 }
 
-template <int NT, int VT, int KT>
+template <int NT, int VT, int KT, int W>
 cudaError_t prepare_split_t(bool dump, int *ctas_per_sm)
 {
-    const int smem = SplitCfg<NT, VT, KT>::SMEM;
-    const void *fn = (const void *)split_attn_kernel<NT, VT, KT, false>;
-    if constexpr (KT == KVQ_K_I8) {
-        if (dump) fn = (const void *)split_attn_kernel<NT, VT, KT, true>;
+    using C = SplitCfg<NT, VT, KT, W>;
+    const void *fn = (const void *)split_attn_kernel<NT, VT, KT, false, W>;
+    if constexpr (KT == KVQ_K_I8 && W == split_warps(NT)) {
+        if (dump) fn = (const void *)split_attn_kernel<NT, VT, KT, true, W>;
     } else {
         if (dump) return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    if (ctas_per_sm)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, SplitCfg<NT, VT, KT>::THREADS, smem);
+    if (ctas_per_sm) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, C::THREADS, C::SMEM);
     return cudaSuccess;
 }
 
 template <int VT, int KT>
-cudaError_t launch_split_nt(const AttnParams &p, int nt, int n_ctas, bool dump, cudaStream_t s, bool pdl)
+cudaError_t launch_split_nt(const AttnParams &p, int nt, int warps, int n_ctas, bool dump, cudaStream_t s, bool pdl)
 {
+    if (nt == 1 && warps == kWarpsHalf) return launch_split_t<1, VT, KT, kWarpsHalf>(p, n_ctas, dump, s, pdl);
+    if (warps != split_warps(nt)) return cudaErrorInvalidValue;
     switch (nt) {
-    case 1: return launch_split_t<1, VT, KT>(p, n_ctas, dump, s, pdl);
-    case 2: return launch_split_t<2, VT, KT>(p, n_ctas, dump, s, pdl);
-    case 4: return launch_split_t<4, VT, KT>(p, n_ctas, dump, s, pdl);
+    case 1: return launch_split_t<1, VT, KT, split_warps(1)>(p, n_ctas, dump, s, pdl);
+    case 2: return launch_split_t<2, VT, KT, split_warps(2)>(p, n_ctas, dump, s, pdl);
+    case 4: return launch_split_t<4, VT, KT, split_warps(4)>(p, n_ctas, dump, s, pdl);
     default: return cudaErrorInvalidValue;
     }
 }
 
 template <int VT, int KT>
-cudaError_t prepare_split_nt(int nt, bool dump, int *ctas)
+cudaError_t prepare_split_nt(int nt, int warps, bool dump, int *ctas)
 {
+    if (nt == 1 && warps == kWarpsHalf) return prepare_split_t<1, VT, KT, kWarpsHalf>(dump, ctas);
+    if (warps != split_warps(nt)) return cudaErrorInvalidValue;
     switch (nt) {
-    case 1: return prepare_split_t<1, VT, KT>(dump, ctas);
-    case 2: return prepare_split_t<2, VT, KT>(dump, ctas);
-    case 4: return prepare_split_t<4, VT, KT>(dump, ctas);
+    case 1: return prepare_split_t<1, VT, KT, split_warps(1)>(dump, ctas);
+    case 2: return prepare_split_t<2, VT, KT, split_warps(2)>(dump, ctas);
+    case 4: return prepare_split_t<4, VT, KT, split_warps(4)>(dump, ctas);
     default: return cudaErrorInvalidValue;
     }
 }
 
 #define KVQ_DEFINE_SPLIT_ENTRY(SUFFIX, VT)                                                              \
-    cudaError_t launch_split_##SUFFIX(const AttnParams &p, int nt, int k_type, int n_ctas, bool dump,    \
-                                      cudaStream_t s, bool pdl)                                         \
+    cudaError_t launch_split_##SUFFIX(const AttnParams &p, int nt, int warps, int k_type, int n_ctas,    \
+                                      bool dump, cudaStream_t s, bool pdl)                              \
     {                                                                                                   \
-        return (k_type == KVQ_K_F16) ? launch_split_nt<VT, KVQ_K_F16>(p, nt, n_ctas, dump, s, pdl)      \
-                                     : launch_split_nt<VT, KVQ_K_I8>(p, nt, n_ctas, dump, s, pdl);      \
+        return (k_type == KVQ_K_F16) ? launch_split_nt<VT, KVQ_K_F16>(p, nt, warps, n_ctas, dump, s, pdl) \
+                                     : launch_split_nt<VT, KVQ_K_I8>(p, nt, warps, n_ctas, dump, s, pdl); \
     }                                                                                                   \
-    cudaError_t prepare_split_##SUFFIX(int nt, int k_type, bool dump, int *ctas)                        \
+    cudaError_t prepare_split_##SUFFIX(int nt, int warps, int k_type, bool dump, int *ctas)             \
     {                                                                                                   \
-        return (k_type == KVQ_K_F16) ? prepare_split_nt<VT, KVQ_K_F16>(nt, dump, ctas)                  \
-                                     : prepare_split_nt<VT, KVQ_K_I8>(nt, dump, ctas);                  \
+        return (k_type == KVQ_K_F16) ? prepare_split_nt<VT, KVQ_K_F16>(nt, warps, dump, ctas)           \
+                                     : prepare_split_nt<VT, KVQ_K_I8>(nt, warps, dump, ctas);           \
     }
 
 }  // namespace kvq

@@ -22,8 +22,12 @@ constexpr int kWTile = 16;              // positions per warp pipeline stage
 #endif
 // Warps per split CTA for nt 8-row query tiles; each warp streams its own
 // contiguous sub-range of the split, so split chunks are rounded to a multiple
-// of split_warps(nt) * kWTile positions.
+// of the CTA's warps * kWTile positions.  The 8-row kernel also comes with half
+// as many warps (two CTAs per SM, the same warps per SM), for launches that
+// take more than one wave of full CTAs: their work is then dealt in pieces
+// half as large, which evens out the last wave.
 constexpr int split_warps(int nt) { return nt == 1 ? KVQ_WARPS_NT1 : KVQ_WARPS_NTX; }
+constexpr int kWarpsHalf = KVQ_WARPS_NT1 / 2;
 constexpr int kPrefillRows = 128;       // query rows per CTA of the tcgen05 kernel
 constexpr int kPrefillPositions = 64;   // positions per KV tile of the tcgen05 kernel
 constexpr int kVerifyRows = 32;         // query rows (MMA N) of the tcgen05 verify kernel
@@ -163,16 +167,17 @@ struct AppendParams {
 
 // ------------------------------------------------------------ host launchers --
 // Implemented in kvq_small.cu / kvq_attn_q4.cu / kvq_attn_q8.cu / kvq_prefill_q*.cu.
-// n_tiles8 = query rows per kv head rounded up to 1, 2 or 4 tiles of 8.
-// k_type selects the K format (kvq_ktype); dump kernels exist for KVQ_K_I8 only.
+// n_tiles8 = query rows per kv head rounded up to 1, 2 or 4 tiles of 8; warps =
+// split_warps(n_tiles8), or kWarpsHalf with one tile.  k_type selects the K
+// format (kvq_ktype); dump kernels exist for KVQ_K_I8 at split_warps only.
 cudaError_t launch_append(const AppendParams &p, int v_type, int k_type, int max_rows, cudaStream_t s, bool pdl);
 cudaError_t launch_combine(const CombineParams &p, int n_rows, cudaStream_t s, bool pdl);
-cudaError_t launch_split_q4(const AttnParams &p, int n_tiles8, int k_type, int n_ctas, bool dump, cudaStream_t s,
-                            bool pdl);
-cudaError_t launch_split_q8(const AttnParams &p, int n_tiles8, int k_type, int n_ctas, bool dump, cudaStream_t s,
-                            bool pdl);
-cudaError_t prepare_split_q4(int n_tiles8, int k_type, bool dump, int *ctas_per_sm);
-cudaError_t prepare_split_q8(int n_tiles8, int k_type, bool dump, int *ctas_per_sm);
+cudaError_t launch_split_q4(const AttnParams &p, int n_tiles8, int warps, int k_type, int n_ctas, bool dump,
+                            cudaStream_t s, bool pdl);
+cudaError_t launch_split_q8(const AttnParams &p, int n_tiles8, int warps, int k_type, int n_ctas, bool dump,
+                            cudaStream_t s, bool pdl);
+cudaError_t prepare_split_q4(int n_tiles8, int warps, int k_type, bool dump, int *ctas_per_sm);
+cudaError_t prepare_split_q8(int n_tiles8, int warps, int k_type, bool dump, int *ctas_per_sm);
 // tcgen05 kernel for long query chunks (kvq_prefill_q4.cu / kvq_prefill_q8.cu):
 // 128 query rows per CTA, one CTA per SM.
 cudaError_t launch_prefill_q4(const AttnParams &p, int n_ctas, cudaStream_t s, bool pdl);

@@ -62,3 +62,37 @@ def test_sixteen_row_tiles(name, kw, monkeypatch):
         for b in range(case.B):
             ref = case.oracle_decode(b)
             assert_close(out[b], lse[b], ref, what="%s seq %d (16-row tiles)" % (spec.name, b))
+
+
+def test_half_warp_ctas(monkeypatch):
+    """The 8-row kernel also runs with half its warps (two CTAs per SM).  The
+    planner takes it when full CTAs would need more than one wave: a batch of 24
+    sequences x 8 kv heads is at least 192 CTAs on 152 SMs.  Both forms match
+    the oracle, the automatic choice is bitwise the forced half-warp result
+    there, and bitwise the forced full-warp result for a call that fits one
+    wave (the main cache of the long pair)."""
+    def run(case, force):
+        if force is None:
+            monkeypatch.delenv("KVQ_SPLIT_WARPS", raising=False)
+        else:
+            monkeypatch.setenv("KVQ_SPLIT_WARPS", force)
+        return case.decode()
+
+    spec = W.make_spec("batched", ctx=4096, n_seqs=24)[0]
+    case = Case(spec).build()
+    res = {f: run(case, f) for f in (None, "8", "16")}
+    for f in ("8", "16"):
+        out, lse = res[f]
+        for b in range(case.B):
+            ref = case.oracle_decode(b)
+            assert_close(out[b], lse[b], ref, what="batched seq %d (%s warps)" % (b, f))
+    assert np.array_equal(res[None][0], res["8"][0]) and np.array_equal(res[None][1], res["8"][1])
+
+    spec = W.make_spec("long", ctx=5000)[0]
+    case = Case(spec).build()
+    res = {f: run(case, f) for f in (None, "8", "16")}
+    for f in ("8", "16"):
+        out, lse = res[f]
+        ref = case.oracle_decode(0)
+        assert_close(out[0], lse[0], ref, what="long main (%s warps)" % f)
+    assert np.array_equal(res[None][0], res["16"][0]) and np.array_equal(res[None][1], res["16"][1])
