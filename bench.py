@@ -404,6 +404,14 @@ def main():
         for _ in range(passes):
             for grp in sets:
                 step(grp)
+    # the step's appends alone: kvq_append per cache, no attention
+    g_app = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_app, stream=stream):
+        for _ in range(passes):
+            for grp in sets:
+                for ds in grp:
+                    ds.append_step(stream=stream)
+                    ds.rewind()
     # decode timing graph: events around each step's fused decode call (separate pass);
     # external event nodes, so their timestamps can be read after each replay
     g_ev = torch.cuda.CUDAGraph()
@@ -463,6 +471,14 @@ def main():
         e1.record(stream)
     stream.synchronize()
     sep_ms_per_step = e0.elapsed_time(e1) / (sreps * per_replay)
+    with torch.cuda.stream(stream):
+        g_app.replay()
+        e0.record(stream)
+        for _ in range(sreps):
+            g_app.replay()
+        e1.record(stream)
+    stream.synchronize()
+    app_ms_per_step = e0.elapsed_time(e1) / (sreps * per_replay)
 
     # ---- kernel-level timing pass (decode = the split kernel + its combine) ----
     kreps = max(1, min(reps, 2000 // n_rot))
@@ -591,7 +607,9 @@ def main():
                       "duration_us": 1e3 * dec_ms,
                       "duration_basis": "event-bracketed attention call (split + combine), appends outside",
                       "algorithmic_flops": int(flops), "kv_bytes": int(dec_bytes)}),
+        "steps_per_s": 1e3 / ms_per_step,
         "per_cache_calls_ms_per_step": sep_ms_per_step,
+        "append_alone_ms_per_step": app_ms_per_step,
         "e2e": {"value": tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * steps,
