@@ -533,6 +533,20 @@ void fill_launch(const std::vector<Desc> &ds, const Launch &ln, bool dump, void 
 
 // Plan, check the workspace and launch (or, with size_out, only report the
 // workspace the calls need).
+// Calls whose rows go to the tcgen05 verify kernel take their step's tokens
+// through an append launch first (that kernel has no fused append): dsp is ds
+// with those calls' k_new / v_new cleared, pre their indices.
+void split_off_pre_appends(const std::vector<Desc> &ds, bool dump, std::vector<Desc> &dsp, std::vector<int> &pre)
+{
+    dsp = ds;
+    pre.clear();
+    for (size_t i = 0; i < ds.size(); ++i)
+        if (ds[i].k_new && ds[i].c->n_seqs > 0 && verify_shape(ds[i], dump)) {
+            dsp[i].k_new = dsp[i].v_new = nullptr;
+            pre.push_back((int)i);
+        }
+}
+
 kvq_status run(std::vector<Desc> &ds, bool dump, void *workspace, size_t workspace_bytes, size_t *size_out,
                cudaStream_t stream)
 {
@@ -545,15 +559,9 @@ kvq_status run(std::vector<Desc> &ds, bool dump, void *workspace, size_t workspa
     }
     kvq_status st = device_setup(&dev);
     if (st != KVQ_OK) return st;
-    // calls whose rows go to the tcgen05 verify kernel take their step's
-    // tokens through an append launch first (that kernel has no fused append)
-    std::vector<Desc> dsp(ds);
+    std::vector<Desc> dsp;
     std::vector<int> pre;
-    for (size_t i = 0; i < ds.size(); ++i)
-        if (ds[i].k_new && ds[i].c->n_seqs > 0 && verify_shape(ds[i], dump)) {
-            dsp[i].k_new = dsp[i].v_new = nullptr;
-            pre.push_back((int)i);
-        }
+    split_off_pre_appends(ds, dump, dsp, pre);
     std::vector<Launch> lns;
     size_t ws = 0;
     st = plan(dsp, dev, dump, lns, ws);
@@ -744,6 +752,54 @@ kvq_status kvq_decode_multi_workspace_size(int32_t n, const kvq_decode_desc *cal
         if (st != KVQ_OK) return st;
     }
     return run(ds, false, nullptr, 0, bytes, nullptr);
+}
+
+kvq_status kvq_debug_plan(int32_t n, const kvq_decode_desc *calls, int32_t n_sms, const int32_t *ctas_per_sm,
+                          kvq_plan_launch *out, int32_t max_out, int32_t *n_out, size_t *workspace_bytes,
+                          int32_t *n_pre_appends)
+{
+    if (n < 0 || n > KVQ_MAX_CALLS || (n > 0 && !calls) || n_sms < 1 || !ctas_per_sm || max_out < 0 ||
+        (max_out > 0 && !out) || !n_out || !workspace_bytes || !n_pre_appends)
+        return KVQ_ERR_INVALID_ARG;
+    for (int i = 0; i < 4; ++i)
+        if (ctas_per_sm[i] < 1) return KVQ_ERR_INVALID_ARG;
+    std::vector<Desc> ds(n);
+    for (int i = 0; i < n; ++i) {
+        kvq_status st = to_desc(calls[i], false, ds[i]);
+        if (st != KVQ_OK) return st;
+        for (int j = 0; j < i; ++j)
+            if (ds[j].c == ds[i].c && (ds[i].k_new || ds[j].k_new)) return KVQ_ERR_INVALID_ARG;
+    }
+    DeviceInfo dev;   // a described device, not a probed one
+    dev.n_sms = n_sms;
+    for (int kt = 0; kt < 2; ++kt)
+        for (int vt = 0; vt < 2; ++vt) {
+            dev.ctas[kt][vt][1] = ctas_per_sm[0];
+            dev.ctas_half[kt][vt] = ctas_per_sm[1];
+            dev.ctas[kt][vt][2] = ctas_per_sm[2];
+            dev.ctas[kt][vt][4] = ctas_per_sm[3];
+        }
+    std::vector<Desc> dsp;
+    std::vector<int> pre;
+    split_off_pre_appends(ds, false, dsp, pre);
+    std::vector<Launch> lns;
+    size_t ws = 0;
+    const kvq_status st = plan(dsp, &dev, false, lns, ws);
+    if (st != KVQ_OK) return st;
+    for (int i = 0; i < (int)lns.size() && i < max_out; ++i) {
+        const Launch &ln = lns[i];
+        kvq_plan_launch &r = out[i];
+        r.kernel = ln.prefill ? 1 : ln.verify ? 2 : 0;
+        r.n_tiles8 = (ln.prefill || ln.verify) ? 0 : ln.nt;
+        r.warps = ln.warps;
+        r.chunk = ln.chunk;
+        r.n_ctas = ln.n_ctas;
+        r.n_rows = ln.n_rows;
+    }
+    *n_out = (int32_t)lns.size();
+    *workspace_bytes = ws;
+    *n_pre_appends = (int32_t)pre.size();
+    return KVQ_OK;
 }
 
 kvq_status kvq_debug_qk(const kvq_cache *c, const void *q16, int32_t n_q_heads, int32_t t_q,

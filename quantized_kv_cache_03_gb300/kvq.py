@@ -33,7 +33,7 @@ QBLOCK = 32
 
 EXPORTED = ("kvq_append", "kvq_decode_attn", "kvq_decode_workspace_size", "kvq_decode_attn_multi",
             "kvq_decode_multi_workspace_size", "kvq_decode_attn_noalloc", "kvq_wait_timeouts",
-            "kvq_status_string", "kvq_debug_qk")
+            "kvq_status_string", "kvq_debug_qk", "kvq_debug_plan")
 MAX_CALLS = 16
 MAX_T_Q = 4096
 MAX_T_Q_APPEND = 8
@@ -56,6 +56,11 @@ class KvqDecodeDesc(ctypes.Structure):
                 ("causal_tail", c_int32), ("seq_lens", c_void_p), ("max_len", c_int32),
                 ("head_map", POINTER(c_int32)), ("sm_scale", c_float), ("out", c_void_p), ("lse", c_void_p),
                 ("k16_new", c_void_p), ("v16_new", c_void_p)]
+
+
+class KvqPlanLaunch(ctypes.Structure):
+    _fields_ = [("kernel", c_int32), ("n_tiles8", c_int32), ("warps", c_int32), ("chunk", c_int32),
+                ("n_ctas", c_int32), ("n_rows", c_int32)]
 
 
 class KvqError(RuntimeError):
@@ -101,6 +106,10 @@ def load():
             lib.kvq_debug_qk.restype = c_int32
             lib.kvq_debug_qk.argtypes = [POINTER(KvqCache), c_void_p, c_int32, c_int32, c_void_p, c_int32,
                                          POINTER(c_int32), c_void_p, c_void_p, c_void_p, c_void_p]
+            lib.kvq_debug_plan.restype = c_int32
+            lib.kvq_debug_plan.argtypes = [c_int32, POINTER(KvqDecodeDesc), c_int32, POINTER(c_int32),
+                                           POINTER(KvqPlanLaunch), c_int32, POINTER(c_int32), POINTER(c_size_t),
+                                           POINTER(c_int32)]
             _lib = lib
     return _lib
 
@@ -370,3 +379,24 @@ def kvq_wait_timeouts() -> int:
     if st not in (0, KVQ_ERR_TIMEOUT):
         raise KvqError(st, "kvq_wait_timeouts")
     return int(n.value)
+
+
+PLAN_KERNELS = ("split", "prefill", "verify")
+
+
+def kvq_debug_plan(calls, n_sms: int, ctas_per_sm=(1, 2, 2, 2), max_out: int = 64):
+    """kvq_debug_plan of include/kvq.h (test hook): the launches the decode
+    call would make for `calls` (dicts as for kvq_decode_attn_multi; only the
+    caches' host descriptors are read) on a described device.  Returns
+    (launches as dicts, workspace bytes, calls with a separate append launch)."""
+    arr, keep = _descs(calls)
+    ctas = _i32(ctas_per_sm)
+    out = (KvqPlanLaunch * max(1, max_out))()
+    n_out, n_pre, ws = c_int32(0), c_int32(0), c_size_t(0)
+    st = load().kvq_debug_plan(len(calls), arr, int(n_sms), ctas, out, max_out, ctypes.byref(n_out),
+                               ctypes.byref(ws), ctypes.byref(n_pre))
+    if st:
+        raise KvqError(st, "kvq_debug_plan")
+    launches = [dict(kernel=PLAN_KERNELS[r.kernel], n_tiles8=r.n_tiles8, warps=r.warps, chunk=r.chunk,
+                     n_ctas=r.n_ctas, n_rows=r.n_rows) for r in out[:min(n_out.value, max_out)]]
+    return launches, int(ws.value), int(n_pre.value)
