@@ -116,12 +116,17 @@ KERNEL_SOURCES = {
 }
 
 
+_COMMENT = re.compile(rb"/\*.*?\*/|//[^\n]*", re.S)
+
+
 def kernel_source_hash(kernel="split_attn"):
+    """Hash of the kernel's source files with C comments removed, so that
+    counters taken on a kernel stay valid across comment-only edits."""
     h = hashlib.sha256()
     pkg = os.path.join(ROOT, "quantized_kv_cache_03_gb300")
     for f in KERNEL_SOURCES[kernel] + ["../include/kvq.h"]:
         with open(os.path.normpath(os.path.join(pkg, f)), "rb") as fh:
-            h.update(fh.read())
+            h.update(_COMMENT.sub(b"", fh.read()))
     return h.hexdigest()[:16]
 
 

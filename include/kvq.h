@@ -47,7 +47,7 @@ extern "C" {
 #endif
 
 #define KVQ_QBLOCK 32          /* quantization block (head-dim elements)          */
-#define KVQ_HEAD_DIM 128       /* the only head_dim this build supports           */
+#define KVQ_HEAD_DIM 128       /* the only head_dim the library supports          */
 #define KVQ_SEG_ALIGN 64       /* segment capacity must be a multiple of this     */
 #define KVQ_MAX_ROWS 32        /* query rows one attention CTA takes (row tile)   */
 #define KVQ_MAX_T_Q 4096       /* query tokens per sequence per call              */
@@ -58,7 +58,7 @@ extern "C" {
 typedef enum kvq_status {
     KVQ_OK = 0,
     KVQ_ERR_INVALID_ARG = 1,   /* a pointer, size or layout rule is violated      */
-    KVQ_ERR_UNSUPPORTED = 2,   /* no sm_103 device, or a size this build lacks    */
+    KVQ_ERR_UNSUPPORTED = 2,   /* no sm_103 device, or a size the kernels lack    */
     KVQ_ERR_CAPACITY = 3,      /* kvq_append: the open segment is too small       */
     KVQ_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required      */
     KVQ_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed     */

@@ -213,7 +213,7 @@ bool prefill_kernel_for(const Desc &d, bool dump)
 }
 // Calls with 9..32 query rows per kv head (multi-token verify, short chunks)
 // go to the tcgen05 verify kernel with KVQ_VERIFY=1, else to the split
-// kernel's 16- and 32-row tiles (measured faster so far).  The score dump
+// kernel's 16- and 32-row tiles (measured faster).  The score dump
 // stays on the split kernel.
 bool verify_shape(const Desc &d, bool dump)
 {
