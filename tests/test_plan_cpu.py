@@ -176,3 +176,37 @@ def test_bad_arguments():
     _, f16 = calls_of("long_f16k", fused=True)
     with pytest.raises(kvq.KvqError):
         plan(f16)
+
+
+def test_workspace_is_the_split_partials():
+    """The workspace holds, per unit with more than one split, every query
+    row's per-split partial output and lse (128 + 1 floats), each unit's block
+    rounded up to 256 bytes."""
+    specs, calls = calls_of("long", fused=True)
+    lns, ws, _ = plan(calls)
+    n_split = -(-131072 // lns[0]["chunk"])
+    want = sum(-(-(s.n_seqs * s.t_q * s.n_q_heads * n_split * 129 * 4) // 256) * 256 for s in specs)
+    assert ws == want
+
+
+def test_more_than_64_sequences_take_several_launches():
+    """A launch's tables hold at most 64 sequences: a 100-sequence batch runs
+    as a launch of 64 and one of 36, each planned on its own (the second fits
+    one wave of 8-warp CTAs unsplit, so it needs no combine)."""
+    specs, calls = calls_of("batched", fused=True, ctx=4096, n_seqs=100)
+    lns, _, _ = plan(calls)
+    H, Hq = specs[0].n_kv_heads, specs[0].n_q_heads
+    assert len(lns) == 2 and all(ln["kernel"] == "split" for ln in lns)
+    for ln, nb in zip(lns, (64, 36)):
+        assert ln["n_ctas"] % (nb * H) == 0
+        n_split = ln["n_ctas"] // (nb * H)
+        assert ln["n_rows"] == (nb * Hq if n_split > 1 else 0)
+    assert lns[1]["n_ctas"] == 36 * H and lns[1]["warps"] == 8
+
+
+def test_f16k_pair_without_fused_append():
+    """F16 K decodes on the same split kernel (its own K format) once the
+    step's tokens went in through kvq_append: one launch for both caches."""
+    _, calls = calls_of("long_f16k", fused=False)
+    lns, _, pre = plan(calls)
+    assert len(lns) == 1 and lns[0]["kernel"] == "split" and lns[0]["n_rows"] == 56 and pre == 0
