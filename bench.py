@@ -39,6 +39,9 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 L2_BYTES = 129 * 1024 * 1024
+SPREAD_MIN_REPLAYS = 5      # replays behind the step-time spread
+SPREAD_MAX_REPLAYS = 4000
+SPREAD_SECONDS = 1.0        # length of the spread pass (clock samples every 100 ms)
 
 WORKLOADS = {
     "long": "long-context decode: main 40q/8kv heads + draft 16q/4kv heads, 131072 positions each "
@@ -95,6 +98,18 @@ def job_rate(ms_local, world, steps, tokens_per_step, device=None):
     return ms_per_step, tokens_per_step * world / (ms_per_step * 1e-3)
 
 
+def timing_plan(steps, n_rot, graph_passes):
+    """How exactly `steps` timed steps run as CUDA-graph replays: a graph of
+    per_replay steps (at most graph_passes whole passes over the n_rot cache
+    copies, and at most `steps`), replayed `reps` times, then one graph of the
+    remaining rem < per_replay steps.  When per_replay is below `steps` it is
+    a multiple of n_rot, so consecutive steps never decode the same copy."""
+    k = max(1, int(steps))
+    per = min(k, max(1, n_rot) * max(1, graph_passes))
+    reps, rem = divmod(k, per)
+    return per, reps, rem
+
+
 def measured_peaks(kind="hbm_gbs"):
     """(peak, 'measured'|'fallback'): HBM copy GB/s, or the bf16 GEMM TFLOP/s
     sustained over seconds (kind='bf16_tflops_sustained')."""
@@ -143,17 +158,17 @@ def launches_of(grp, fused):
 
 def profiled_traffic(workload, kernel="split_attn"):
     """DRAM bytes per step of the dominant kernel from the committed ncu
-    summary profiles/<kernel>_<workload>.md, if it was taken on the current
-    kernel sources (else None)."""
-    p = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload))
+    record profiles/<kernel>_<workload>.json (written beside each ncu
+    summary), if it was taken on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "%s_%s.json" % (kernel, workload))
     if not os.path.exists(p):
         return None
-    txt = open(p).read()
-    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt)
-    m_tr = re.search(r"traffic_bytes_per_step:\s*([0-9.eE+]+)", txt)
-    if not m_hash or not m_tr or m_hash.group(1) != kernel_source_hash(kernel):
+    with open(p) as f:
+        rec = json.load(f)
+    if rec.get("kernel_source_hash") != kernel_source_hash(kernel):
         return None
-    return float(m_tr.group(1))
+    tr = rec.get("traffic_bytes_per_step")
+    return None if tr is None else float(tr)
 
 
 class ClockSampler:
@@ -394,29 +409,35 @@ def main():
             step(grp, fz)
             step(grp)
     stream.synchronize()
-    # the timed graph runs `passes` steps on every rotation copy: one replay
-    # boundary per passes * n_rot steps, as a decode loop that captures many
-    # layers per graph has (PDL chains the launches inside a graph only)
-    passes = max(1, min(args.graph_passes, args.steps // n_rot))
-    g_all = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_all, stream=stream):
-        for _ in range(passes):
-            for grp, fz in zip(sets, fused):
-                step(grp, fz)
+    # The K timed steps run as replays of a graph of per_replay steps (whole
+    # passes over the rotation copies, at most --graph-passes of them, at most
+    # K) plus one graph of the remaining rem < per_replay steps, so exactly K
+    # steps are timed.  Step i of a graph decodes copy i % n_rot, so no two
+    # consecutive steps read the same copy.  PDL chains the launches inside a
+    # graph only: long graphs are what a decode loop capturing many layers has.
+    per_replay, reps, rem = timing_plan(args.steps, n_rot, args.graph_passes)
+    warm_steps = max(3, args.warmup)
+
+    def capture(n_steps, body):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n_steps):
+                body(i % n_rot)
+        return g
+
+    g_all = capture(per_replay, lambda r: step(sets[r], fused[r]))
+    g_rem = capture(rem, lambda r: step(sets[r], fused[r])) if rem else None
+    g_warm = capture(warm_steps, lambda r: step(sets[r], fused[r]))
     # the same steps through kvq_append + kvq_decode_attn per cache (reported beside the fused number)
-    g_sep = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_sep, stream=stream):
-        for _ in range(passes):
-            for grp in sets:
-                step(grp)
+    g_sep = capture(per_replay, lambda r: step(sets[r]))
+
     # the step's appends alone: kvq_append per cache, no attention
-    g_app = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_app, stream=stream):
-        for _ in range(passes):
-            for grp in sets:
-                for ds in grp:
-                    ds.append_step(stream=stream)
-                    ds.rewind()
+    def app_only(r):
+        for ds in sets[r]:
+            ds.append_step(stream=stream)
+            ds.rewind()
+
+    g_app = capture(per_replay, app_only)
     # decode timing graph: events around each step's fused decode call (separate pass);
     # external event nodes, so their timestamps can be read after each replay
     g_ev = torch.cuda.CUDAGraph()
@@ -433,41 +454,64 @@ def main():
             for ds in grp:
                 ds.rewind()
 
-    per_replay = passes * n_rot
-    reps = max(1, args.steps // per_replay)
-    steps = reps * per_replay
-    warm = max(1, -(-max(3, args.warmup) // per_replay))
     with torch.cuda.stream(stream):
-        for _ in range(warm):
-            g_all.replay()
+        g_warm.replay()
     stream.synchronize()
 
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    # an event at every replay boundary gives the spread of the step time
-    # (replays of per_replay steps each) beside the whole region's mean
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps - 1)]
+    # An event at every replay boundary of the timed region gives the spread of
+    # the step time when the region holds several replays.  With fewer than
+    # SPREAD_MIN_REPLAYS (a short --steps), the spread comes from a pass of
+    # replays of the same graph right after the timed region, at least
+    # SPREAD_MIN_REPLAYS of them and ~SPREAD_SECONDS long, so that the clock
+    # sampler also sees several samples under load.
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+    spread_reps = 0
     with ClockSampler(local) as clk:
+        t_region = time.perf_counter()
         with torch.cuda.stream(stream):
             e0.record(stream)
             for i in range(reps):
                 g_all.replay()
-                if i < reps - 1:
-                    evs[i].record(stream)
+                evs[i].record(stream)
+            if g_rem is not None:
+                g_rem.replay()
             e1.record(stream)
         torch.cuda.synchronize()
-    marks = [e0] + evs + [e1]
-    rep_ms = np.array([a.elapsed_time(b) for a, b in zip(marks[:-1], marks[1:])]) / per_replay
+        if reps < SPREAD_MIN_REPLAYS:
+            region_ms = e0.elapsed_time(e1)
+            spread_reps = int(min(SPREAD_MAX_REPLAYS, max(SPREAD_MIN_REPLAYS,
+                                                           SPREAD_SECONDS * 1e3 * max(1, reps) / max(region_ms, 1e-3))))
+            sev = [torch.cuda.Event(enable_timing=True) for _ in range(spread_reps + 1)]
+            with torch.cuda.stream(stream):
+                sev[0].record(stream)
+                for i in range(spread_reps):
+                    g_all.replay()
+                    sev[i + 1].record(stream)
+            torch.cuda.synchronize()
+        clk.region_s = time.perf_counter() - t_region
+    if reps >= SPREAD_MIN_REPLAYS:
+        marks = [e0] + evs
+        rep_ms = np.array([a.elapsed_time(b) for a, b in zip(marks[:-1], marks[1:])]) / per_replay
+        spread_src = "replay boundaries of the timed region"
+        n_spread = reps
+    else:
+        rep_ms = np.array([a.elapsed_time(b) for a, b in zip(sev[:-1], sev[1:])]) / per_replay
+        spread_src = "replays of the timed graph right after the timed region"
+        n_spread = spread_reps
     step_pct = {"p10": float(np.percentile(rep_ms, 10)), "p50": float(np.percentile(rep_ms, 50)),
-                "p90": float(np.percentile(rep_ms, 90)), "replays": int(reps), "steps_per_replay": int(per_replay)}
+                "p90": float(np.percentile(rep_ms, 90)), "replays": int(n_spread),
+                "steps_per_replay": int(per_replay), "source": spread_src}
     if world > 1:
         torch.distributed.barrier()
+    steps = reps * per_replay + rem
     ms_per_step, value = job_rate(e0.elapsed_time(e1), world, steps, tokens_per_step, dev)
 
     # ---- one decode call per cache instead of the fused call (same steps) ----
-    sreps = max(1, min(reps, 2000 // per_replay))
+    sreps = max(1, min(max(SPREAD_MIN_REPLAYS, reps), 2000 // per_replay))
     with torch.cuda.stream(stream):
         g_sep.replay()
         e0.record(stream)
@@ -486,7 +530,7 @@ def main():
     app_ms_per_step = e0.elapsed_time(e1) / (sreps * per_replay)
 
     # ---- kernel-level timing pass (decode = the split kernel + its combine) ----
-    kreps = max(1, min(reps, 2000 // n_rot))
+    kreps = max(SPREAD_MIN_REPLAYS, min(reps * per_replay // n_rot, 2000 // n_rot))
     tot = 0.0
     with torch.cuda.stream(stream):
         for _ in range(kreps):
@@ -584,12 +628,15 @@ def main():
     kv_gbs = kv_bytes / (ms_per_step * 1e-3) / 1e9   # per GPU
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
-        "warmup": warm * per_replay, "ms_per_step": ms_per_step, "ms_per_step_spread": step_pct,
+        "warmup": warm_steps, "ms_per_step": ms_per_step, "ms_per_step_spread": step_pct,
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8+fp32", "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload], "parallelism": "replicas" if world > 1 else "single",
                    "l2": "rotating %d independent cache copies (%.0f MB each, L2 129 MB); CUDA-graph replays"
                          " of %d steps" % (n_rot, kv_bytes / 1e6, per_replay),
+                   "timed": "%d replays of a %d-step graph + a %d-step graph; warm-up: %d steps in a graph after"
+                            " %d eager steps (first calls and capture)" % (reps, per_replay, rem, warm_steps,
+                                                                            3 * n_rot),
                    "kv_bytes_per_step": kv_bytes, "tokens_per_step": tokens_per_step},
         "kv_gbs": kv_gbs, "kv_frac_of_8tbs": kv_gbs / NOMINAL_HBM_GBS,
         "kv_frac_of_measured_copy": kv_gbs / peak,
@@ -618,7 +665,8 @@ def main():
         "e2e": {"value": tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * steps,
-        "clocks": clk.summary(),
+        "clocks": dict(clk.summary(), window="timed region + the spread pass after it (%.2f s)"
+                       % (clk.region_s,)),
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)

@@ -58,3 +58,15 @@ def test_reference_arm_runs_on_rank_0_only(monkeypatch, capsys):
     monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--gpus", "2"])
     bench.main()                     # rank 1 of the reference arm: no work, no output
     assert capsys.readouterr().out == ""
+
+
+def test_timing_plan_times_exactly_the_asked_steps():
+    sys.path.insert(0, ROOT)
+    import bench
+    for steps, n_rot, passes in [(20, 3, 8), (30000, 3, 8), (2, 3, 8), (24, 3, 8), (25, 3, 8), (100, 64, 1),
+                                 (7, 5, 1)]:
+        per, reps, rem = bench.timing_plan(steps, n_rot, passes)
+        assert reps * per + rem == steps and 0 <= rem < per and reps >= 1
+        assert per <= n_rot * passes
+        if per < steps:   # several replays: whole passes, so consecutive steps use different copies
+            assert per % n_rot == 0
