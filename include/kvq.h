@@ -319,14 +319,23 @@ kvq_status kvq_decode_attn_noalloc(const kvq_cache *c, const void *q16, int32_t 
  */
 kvq_status kvq_wait_timeouts(uint32_t *count);
 
+/*
+ * kvq_reset_wait_timeouts -- set the current device's wait counter of
+ * kvq_wait_timeouts back to 0 (synchronizes with the device).  The pages have
+ * no counterpart.
+ */
+kvq_status kvq_reset_wait_timeouts(void);
+
 /* Short English text of a status code (static storage). */
 const char *kvq_status_string(kvq_status s);
 
 /*
- * kvq_debug_qk -- TEST HOOK, not part of the decode path: runs the same
- * split-KV attention kernel as kvq_decode_attn with its outputs replaced by
- * dumps of the quantized query and the raw per-block integer scores, so tests
- * can compare them bit for bit with an independent implementation.
+ * kvq_debug_qk -- TEST HOOK, not part of the decode path: runs the attention
+ * kernel that kvq_decode_attn picks for these arguments (the split-KV kernel,
+ * or the tcgen05 kernel for more than KVQ_MAX_ROWS query rows per kv head)
+ * with its outputs replaced by dumps of the quantized query and the raw
+ * per-block integer scores as that kernel computed them, so tests can compare
+ * them bit for bit with an independent implementation.
  *
  *  q_codes   device int8 [n_seqs][t_q][n_q_heads][head_dim]
  *  q_scales  device fp16 bits [n_seqs][t_q][n_q_heads][head_dim/32]
@@ -334,12 +343,35 @@ const char *kvq_status_string(kvq_status s);
  *            I_b = sum over the 32 elements of block b of q_code*k_code, for
  *            every position < L of the sequence (causal masking is not applied
  *            here); other entries are left untouched.
+ *  kernel    host out (may be NULL): the kernel that produced the dumps,
+ *            0 the split-KV kernel, 1 the tcgen05 kernel.
  * Other arguments as kvq_decode_attn.
  */
 kvq_status kvq_debug_qk(const kvq_cache *c, const void *q16, int32_t n_q_heads,
                         int32_t t_q, const int32_t *seq_lens, int32_t max_len,
                         const int32_t *head_map, int8_t *q_codes, uint16_t *q_scales,
-                        int32_t *scores, void *stream);
+                        int32_t *scores, int32_t *kernel, void *stream);
+
+/*
+ * kvq_debug_lose_stage -- TEST HOOK, not part of the decode path: the decode
+ * call of kvq_decode_attn (same arguments and rules) on a test flavour of the
+ * split-KV kernel in which warp 0 of the first CTA arms the barrier of its
+ * second copy stage without issuing that stage's copies.  Its bounded wait on
+ * that stage (a short limit here) runs out, which drives the give-up path of
+ * kvq_wait_timeouts: the warp waits for every copy it did issue, the CTA's
+ * query rows come out as NaN (after the combine, every query row of kv head 0
+ * of sequence 0 when that CTA is its first split), the wait counter grows by
+ * one, and the device stays usable.  Nothing faults and nothing waits without
+ * a limit.  The flavour exists for the 16-warp, <= 8-row form with int8 K and
+ * q4_0 V: calls that plan otherwise, or whose first CTA's warp 0 has fewer
+ * than two copy stages of work, return KVQ_ERR_UNSUPPORTED or lose no stage.
+ * The pages have no counterpart: it tests the library's own hang guard.
+ */
+kvq_status kvq_debug_lose_stage(const kvq_cache *c, const void *q16, int32_t n_q_heads,
+                                int32_t t_q, int32_t causal_tail, const int32_t *seq_lens,
+                                int32_t max_len, const int32_t *head_map, float sm_scale,
+                                float *out, float *lse, void *workspace,
+                                size_t workspace_bytes, void *stream);
 
 /*
  * kvq_debug_plan -- TEST HOOK, not part of the decode path: the launches that
@@ -348,23 +380,21 @@ kvq_status kvq_debug_qk(const kvq_cache *c, const void *q16, int32_t n_q_heads,
  *   i = 0  the <= 8-row kernel, 16 warps;  1  the same with 8 warps;
  *   i = 2  16-row tiles;                   3  32-row tiles.
  * It reads the calls' host descriptors and the same environment knobs as the
- * decode call (KVQ_SPLIT, KVQ_SPLIT_WARPS, KVQ_ROW_TILE, KVQ_PREFILL,
- * KVQ_VERIFY).  It touches no device and dereferences no device pointer, so
- * segments and k16_new / v16_new may hold any non-null 16-byte-aligned address;
- * q16, seq_lens, out and lse may be NULL.
+ * decode call (KVQ_SPLIT, KVQ_SPLIT_WARPS, KVQ_ROW_TILE, KVQ_PREFILL).  It
+ * touches no device and dereferences no device pointer, so segments and
+ * k16_new / v16_new may hold any non-null 16-byte-aligned address; q16,
+ * seq_lens, out and lse may be NULL.
  *
  *  out              host [max_out]: launch i for i < min(*n_out, max_out), in
  *                   launch order (may be NULL when max_out is 0)
  *  n_out            host: launches of the plan
  *  workspace_bytes  host: what kvq_decode_multi_workspace_size would report
- *  n_pre_appends    host: calls whose step tokens go through a separate append
- *                   launch first (the tcgen05 verify kernel has no fused append)
  * Errors: the argument checks of kvq_decode_attn_multi (pointers aside), and
  * KVQ_ERR_INVALID_ARG for n_sms < 1, ctas_per_sm NULL or an entry < 1, or a
- * NULL n_out / workspace_bytes / n_pre_appends.
+ * NULL n_out / workspace_bytes.
  */
 typedef struct kvq_plan_launch {
-    int32_t kernel;     /* 0 split kernel, 1 tcgen05 prefill kernel, 2 tcgen05 verify kernel */
+    int32_t kernel;     /* 0 split kernel, 1 tcgen05 prefill kernel */
     int32_t n_tiles8;   /* split kernel: 8-row query tiles per CTA (1, 2 or 4); else 0 */
     int32_t warps;      /* split kernel: warps per CTA; else 0 */
     int32_t chunk;      /* kv positions per split */
@@ -374,8 +404,7 @@ typedef struct kvq_plan_launch {
 
 kvq_status kvq_debug_plan(int32_t n, const kvq_decode_desc *calls, int32_t n_sms,
                           const int32_t *ctas_per_sm, kvq_plan_launch *out,
-                          int32_t max_out, int32_t *n_out, size_t *workspace_bytes,
-                          int32_t *n_pre_appends);
+                          int32_t max_out, int32_t *n_out, size_t *workspace_bytes);
 
 #ifdef __cplusplus
 }

@@ -15,7 +15,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvq.so")
 SOURCES = ["kvq_api.cu", "kvq_small.cu", "kvq_attn_q4.cu", "kvq_attn_q8.cu", "kvq_prefill_q4.cu",
-           "kvq_prefill_q8.cu", "kvq_verify_q4.cu", "kvq_verify_q8.cu"]
+           "kvq_prefill_q8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -56,25 +56,25 @@ kvq_status device_setup(DeviceInfo **out)
         for (int i = 0; i < 3; ++i) {
             const int nt = nts[i];
             const int w = split_warps(nt);
-            if (prepare_split_q4(nt, w, KVQ_K_I8, false, &d.ctas[KVQ_K_I8][KVQ_V_Q4_0][nt]) != cudaSuccess ||
-                prepare_split_q8(nt, w, KVQ_K_I8, false, &d.ctas[KVQ_K_I8][KVQ_V_Q8_0][nt]) != cudaSuccess ||
-                prepare_split_q4(nt, w, KVQ_K_F16, false, &d.ctas[KVQ_K_F16][KVQ_V_Q4_0][nt]) != cudaSuccess ||
-                prepare_split_q8(nt, w, KVQ_K_F16, false, &d.ctas[KVQ_K_F16][KVQ_V_Q8_0][nt]) != cudaSuccess ||
-                prepare_split_q4(nt, w, KVQ_K_I8, true, nullptr) != cudaSuccess ||
-                prepare_split_q8(nt, w, KVQ_K_I8, true, nullptr) != cudaSuccess) {
+            if (prepare_split_q4(nt, w, KVQ_K_I8, kModeDecode, &d.ctas[KVQ_K_I8][KVQ_V_Q4_0][nt]) != cudaSuccess ||
+                prepare_split_q8(nt, w, KVQ_K_I8, kModeDecode, &d.ctas[KVQ_K_I8][KVQ_V_Q8_0][nt]) != cudaSuccess ||
+                prepare_split_q4(nt, w, KVQ_K_F16, kModeDecode, &d.ctas[KVQ_K_F16][KVQ_V_Q4_0][nt]) != cudaSuccess ||
+                prepare_split_q8(nt, w, KVQ_K_F16, kModeDecode, &d.ctas[KVQ_K_F16][KVQ_V_Q8_0][nt]) != cudaSuccess ||
+                prepare_split_q4(nt, w, KVQ_K_I8, kModeDump, nullptr) != cudaSuccess ||
+                prepare_split_q8(nt, w, KVQ_K_I8, kModeDump, nullptr) != cudaSuccess) {
                 cudaGetLastError();
                 return KVQ_ERR_CUDA;
             }
         }
-        if (prepare_split_q4(1, kWarpsHalf, KVQ_K_I8, false, &d.ctas_half[KVQ_K_I8][KVQ_V_Q4_0]) != cudaSuccess ||
-            prepare_split_q8(1, kWarpsHalf, KVQ_K_I8, false, &d.ctas_half[KVQ_K_I8][KVQ_V_Q8_0]) != cudaSuccess ||
-            prepare_split_q4(1, kWarpsHalf, KVQ_K_F16, false, &d.ctas_half[KVQ_K_F16][KVQ_V_Q4_0]) != cudaSuccess ||
-            prepare_split_q8(1, kWarpsHalf, KVQ_K_F16, false, &d.ctas_half[KVQ_K_F16][KVQ_V_Q8_0]) != cudaSuccess) {
+        if (prepare_split_q4(1, kWarpsHalf, KVQ_K_I8, kModeDecode, &d.ctas_half[KVQ_K_I8][KVQ_V_Q4_0]) != cudaSuccess ||
+            prepare_split_q8(1, kWarpsHalf, KVQ_K_I8, kModeDecode, &d.ctas_half[KVQ_K_I8][KVQ_V_Q8_0]) != cudaSuccess ||
+            prepare_split_q4(1, kWarpsHalf, KVQ_K_F16, kModeDecode, &d.ctas_half[KVQ_K_F16][KVQ_V_Q4_0]) != cudaSuccess ||
+            prepare_split_q8(1, kWarpsHalf, KVQ_K_F16, kModeDecode, &d.ctas_half[KVQ_K_F16][KVQ_V_Q8_0]) != cudaSuccess ||
+            prepare_split_q4(1, split_warps(1), KVQ_K_I8, kModeLoseStage, nullptr) != cudaSuccess) {
             cudaGetLastError();
             return KVQ_ERR_CUDA;
         }
-        if (prepare_prefill_q4() != cudaSuccess || prepare_prefill_q8() != cudaSuccess ||
-            prepare_verify_q4() != cudaSuccess || prepare_verify_q8() != cudaSuccess) {
+        if (prepare_prefill_q4() != cudaSuccess || prepare_prefill_q8() != cudaSuccess) {
             cudaGetLastError();
             return KVQ_ERR_CUDA;
         }
@@ -205,54 +205,13 @@ int tiles8_for(int rows)
 
 
 // Calls with long query chunks go to the tcgen05 kernel unless KVQ_PREFILL=0.
-bool prefill_kernel_for(const Desc &d, bool dump)
+// The score dump takes the same route, so it tests the kernel the decode
+// call runs.
+bool prefill_kernel_for(const Desc &d)
 {
     const char *e = std::getenv("KVQ_PREFILL");
     const bool on = !(e && e[0] == '0');
-    return on && !dump && !d.k_new && d.c->k_type == KVQ_K_I8 && d.max_rows > KVQ_MAX_ROWS;
-}
-// Calls with 9..32 query rows per kv head (multi-token verify, short chunks)
-// go to the tcgen05 verify kernel with KVQ_VERIFY=1, else to the split
-// kernel's 16- and 32-row tiles (measured faster).  The score dump
-// stays on the split kernel.
-bool verify_shape(const Desc &d, bool dump)
-{
-    const char *e = std::getenv("KVQ_VERIFY");
-    const bool on = e && e[0] == '1';
-    return on && !dump && d.c->k_type == KVQ_K_I8 && d.max_rows > 8 && d.max_rows <= kVerifyRows;
-}
-bool verify_kernel_for(const Desc &d, bool dump) { return !d.k_new && verify_shape(d, dump); }
-
-// The step's tokens of call d (t_q per sequence, token-major as kvq_append
-// takes them) through the append kernel: for calls whose attention runs on a
-// kernel without the fused append.  The caller bumps the host lengths.
-cudaError_t launch_step_append(const Desc &d, cudaStream_t s, bool pdl)
-{
-    static thread_local AppendParams p;
-    const kvq_cache *c = d.c;
-    int b = 0;
-    while (b < c->n_seqs) {
-        std::memset(&p, 0, sizeof(p));
-        p.k16 = d.k_new;
-        p.v16 = d.v_new;
-        p.n_kv_heads = c->n_kv_heads;
-        while (b < c->n_seqs && p.n_entries < kMaxSeqsLaunch) {
-            const kvq_segment &sg = seg_of(c, b, c->n_segs[b] - 1);
-            AppendEntry &e = p.e[p.n_entries++];
-            e.kq = static_cast<uint8_t *>(sg.k_q);
-            e.ks = static_cast<uint16_t *>(sg.k_s);
-            e.vq = static_cast<uint8_t *>(sg.v_q);
-            e.vs = static_cast<uint16_t *>(sg.v_s);
-            e.cap = sg.cap;
-            e.dst = sg.len;
-            e.src = b * d.t_q;
-            e.n = d.t_q;
-            ++b;
-        }
-        const cudaError_t err = launch_append(p, c->v_type, c->k_type, d.t_q * c->n_kv_heads, s, pdl);
-        if (err != cudaSuccess) return err;
-    }
-    return cudaSuccess;
+    return on && !d.k_new && d.c->k_type == KVQ_K_I8 && d.max_rows > KVQ_MAX_ROWS;
 }
 int round_up(long long x, int m) { return (int)((x + m - 1) / m * m); }
 
@@ -282,14 +241,13 @@ struct Launch {
     int v_type = 0, k_type = 0, nt = 1;
     int warps = 0;   // warps per split CTA (split_warps(nt), or kWarpsHalf for the 8-row kernel)
     bool prefill = false;
-    bool verify = false;   // the tcgen05 kernel for 9..32 rows per kv head (one 32-row tile)
     int chunk = KVQ_SEG_ALIGN;
     int n_ctas = 0, n_rows = 0;   // split CTAs, combine rows
     std::vector<Unit> units;
 };
 
 // Query rows one CTA of the launch takes per kv head.
-int tile_rows(const Launch &ln) { return ln.prefill ? kPrefillRows : ln.verify ? kVerifyRows : 8 * ln.nt; }
+int tile_rows(const Launch &ln) { return ln.prefill ? kPrefillRows : 8 * ln.nt; }
 
 // Split policy, one chunk per launch so that CTAs of every unit do the same
 // amount of work.  For a candidate chunk c the launch has n CTAs with work
@@ -361,10 +319,8 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
     for (int di = 0; di < (int)ds.size(); ++di) {
         const kvq_cache *c = ds[di].c;
         if (c->n_seqs == 0) continue;
-        const bool pf = prefill_kernel_for(ds[di], dump);
-        const bool vf = !pf && verify_kernel_for(ds[di], dump);
-        if (!cur.units.empty() &&
-            (cur.v_type != c->v_type || cur.k_type != c->k_type || cur.prefill != pf || cur.verify != vf))
+        const bool pf = prefill_kernel_for(ds[di]);
+        if (!cur.units.empty() && (cur.v_type != c->v_type || cur.k_type != c->k_type || cur.prefill != pf))
             flush();
         int b = 0;
         while (b < c->n_seqs) {
@@ -380,7 +336,6 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
                 cur.v_type = c->v_type;
                 cur.k_type = c->k_type;
                 cur.prefill = pf;
-                cur.verify = vf;
             }
             heads += need_heads;
             kvs += need_kv;
@@ -399,11 +354,10 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
     }
     flush();
     for (Launch &ln : out) {
-        const bool tc = ln.prefill || ln.verify;   // tcgen05 kernels: one CTA per SM
+        const bool tc = ln.prefill;   // the tcgen05 kernel: one CTA per SM
         const int slots = tc ? dev->n_sms : std::max(1, dev->n_sms * std::max(1, dev->ctas[ln.k_type][ln.v_type][ln.nt]));
         ln.warps = tc ? 0 : split_warps(ln.nt);
-        ln.chunk = choose_chunk(ds, ln, slots,
-                                ln.prefill ? kPrefillPositions : ln.verify ? kVerifyPositions : ln.warps * kWTile);
+        ln.chunk = choose_chunk(ds, ln, slots, ln.prefill ? kPrefillPositions : ln.warps * kWTile);
         // The 8-row kernel with half the warps (two CTAs per SM) when the full
         // CTAs take more than one wave; KVQ_SPLIT_WARPS=8 or 16 forces either.
         // A chunk forced by KVQ_SPLIT keeps the full CTAs unless asked, so that
@@ -533,22 +487,8 @@ void fill_launch(const std::vector<Desc> &ds, const Launch &ln, bool dump, void 
 
 // Plan, check the workspace and launch (or, with size_out, only report the
 // workspace the calls need).
-// Calls whose rows go to the tcgen05 verify kernel take their step's tokens
-// through an append launch first (that kernel has no fused append): dsp is ds
-// with those calls' k_new / v_new cleared, pre their indices.
-void split_off_pre_appends(const std::vector<Desc> &ds, bool dump, std::vector<Desc> &dsp, std::vector<int> &pre)
-{
-    dsp = ds;
-    pre.clear();
-    for (size_t i = 0; i < ds.size(); ++i)
-        if (ds[i].k_new && ds[i].c->n_seqs > 0 && verify_shape(ds[i], dump)) {
-            dsp[i].k_new = dsp[i].v_new = nullptr;
-            pre.push_back((int)i);
-        }
-}
-
 kvq_status run(std::vector<Desc> &ds, bool dump, void *workspace, size_t workspace_bytes, size_t *size_out,
-               cudaStream_t stream)
+               cudaStream_t stream, int32_t *kernel_out = nullptr, bool lose_stage = false)
 {
     DeviceInfo *dev = nullptr;
     bool any = false;
@@ -559,13 +499,17 @@ kvq_status run(std::vector<Desc> &ds, bool dump, void *workspace, size_t workspa
     }
     kvq_status st = device_setup(&dev);
     if (st != KVQ_OK) return st;
-    std::vector<Desc> dsp;
-    std::vector<int> pre;
-    split_off_pre_appends(ds, dump, dsp, pre);
     std::vector<Launch> lns;
     size_t ws = 0;
-    st = plan(dsp, dev, dump, lns, ws);
+    st = plan(ds, dev, dump, lns, ws);
     if (st != KVQ_OK) return st;
+    if (kernel_out) *kernel_out = (!lns.empty() && lns[0].prefill) ? 1 : 0;
+    if (lose_stage)   // the test flavour exists for one form of the split kernel
+        for (const Launch &ln : lns)
+            if (ln.prefill || ln.nt != 1 || ln.warps != split_warps(1) || ln.k_type != KVQ_K_I8 ||
+                ln.v_type != KVQ_V_Q4_0)
+                return KVQ_ERR_UNSUPPORTED;
+    const int mode = dump ? kModeDump : lose_stage ? kModeLoseStage : kModeDecode;
     if (size_out) {
         *size_out = ws;
         return KVQ_OK;
@@ -577,23 +521,15 @@ kvq_status run(std::vector<Desc> &ds, bool dump, void *workspace, size_t workspa
     static thread_local AttnParams p;        // ~6 KB; kept off the stack
     static thread_local CombineParams cp;
     const bool pdl = pdl_enabled();
-    for (int i : pre)
-        if (launch_step_append(ds[i], stream, pdl) != cudaSuccess) {
-            cudaGetLastError();
-            return KVQ_ERR_CUDA;
-        }
     for (const Launch &ln : lns) {
-        fill_launch(dsp, ln, dump, workspace, dev->timeouts, p, cp);
+        fill_launch(ds, ln, dump, workspace, dev->timeouts, p, cp);
         cudaError_t e;
         if (ln.prefill)
-            e = (ln.v_type == KVQ_V_Q4_0) ? launch_prefill_q4(p, ln.n_ctas, stream, pdl)
-                                          : launch_prefill_q8(p, ln.n_ctas, stream, pdl);
-        else if (ln.verify)
-            e = (ln.v_type == KVQ_V_Q4_0) ? launch_verify_q4(p, ln.n_ctas, stream, pdl)
-                                          : launch_verify_q8(p, ln.n_ctas, stream, pdl);
+            e = (ln.v_type == KVQ_V_Q4_0) ? launch_prefill_q4(p, ln.n_ctas, dump, stream, pdl)
+                                          : launch_prefill_q8(p, ln.n_ctas, dump, stream, pdl);
         else
-            e = (ln.v_type == KVQ_V_Q4_0) ? launch_split_q4(p, ln.nt, ln.warps, ln.k_type, ln.n_ctas, dump, stream, pdl)
-                                          : launch_split_q8(p, ln.nt, ln.warps, ln.k_type, ln.n_ctas, dump, stream, pdl);
+            e = (ln.v_type == KVQ_V_Q4_0) ? launch_split_q4(p, ln.nt, ln.warps, ln.k_type, ln.n_ctas, mode, stream, pdl)
+                                          : launch_split_q8(p, ln.nt, ln.warps, ln.k_type, ln.n_ctas, mode, stream, pdl);
         if (e == cudaSuccess && ln.n_rows > 0) e = launch_combine(cp, ln.n_rows, stream, pdl);
         if (e != cudaSuccess) {
             cudaGetLastError();
@@ -755,11 +691,10 @@ kvq_status kvq_decode_multi_workspace_size(int32_t n, const kvq_decode_desc *cal
 }
 
 kvq_status kvq_debug_plan(int32_t n, const kvq_decode_desc *calls, int32_t n_sms, const int32_t *ctas_per_sm,
-                          kvq_plan_launch *out, int32_t max_out, int32_t *n_out, size_t *workspace_bytes,
-                          int32_t *n_pre_appends)
+                          kvq_plan_launch *out, int32_t max_out, int32_t *n_out, size_t *workspace_bytes)
 {
     if (n < 0 || n > KVQ_MAX_CALLS || (n > 0 && !calls) || n_sms < 1 || !ctas_per_sm || max_out < 0 ||
-        (max_out > 0 && !out) || !n_out || !workspace_bytes || !n_pre_appends)
+        (max_out > 0 && !out) || !n_out || !workspace_bytes)
         return KVQ_ERR_INVALID_ARG;
     for (int i = 0; i < 4; ++i)
         if (ctas_per_sm[i] < 1) return KVQ_ERR_INVALID_ARG;
@@ -779,18 +714,15 @@ kvq_status kvq_debug_plan(int32_t n, const kvq_decode_desc *calls, int32_t n_sms
             dev.ctas[kt][vt][2] = ctas_per_sm[2];
             dev.ctas[kt][vt][4] = ctas_per_sm[3];
         }
-    std::vector<Desc> dsp;
-    std::vector<int> pre;
-    split_off_pre_appends(ds, false, dsp, pre);
     std::vector<Launch> lns;
     size_t ws = 0;
-    const kvq_status st = plan(dsp, &dev, false, lns, ws);
+    const kvq_status st = plan(ds, &dev, false, lns, ws);
     if (st != KVQ_OK) return st;
     for (int i = 0; i < (int)lns.size() && i < max_out; ++i) {
         const Launch &ln = lns[i];
         kvq_plan_launch &r = out[i];
-        r.kernel = ln.prefill ? 1 : ln.verify ? 2 : 0;
-        r.n_tiles8 = (ln.prefill || ln.verify) ? 0 : ln.nt;
+        r.kernel = ln.prefill ? 1 : 0;
+        r.n_tiles8 = ln.prefill ? 0 : ln.nt;
         r.warps = ln.warps;
         r.chunk = ln.chunk;
         r.n_ctas = ln.n_ctas;
@@ -798,13 +730,12 @@ kvq_status kvq_debug_plan(int32_t n, const kvq_decode_desc *calls, int32_t n_sms
     }
     *n_out = (int32_t)lns.size();
     *workspace_bytes = ws;
-    *n_pre_appends = (int32_t)pre.size();
     return KVQ_OK;
 }
 
 kvq_status kvq_debug_qk(const kvq_cache *c, const void *q16, int32_t n_q_heads, int32_t t_q,
                         const int32_t *seq_lens, int32_t max_len, const int32_t *head_map, int8_t *q_codes,
-                        uint16_t *q_scales, int32_t *scores, void *stream)
+                        uint16_t *q_scales, int32_t *scores, int32_t *kernel, void *stream)
 {
     std::vector<Desc> ds(1);
     Desc &d = ds[0];
@@ -821,7 +752,7 @@ kvq_status kvq_debug_qk(const kvq_cache *c, const void *q16, int32_t n_q_heads, 
     d.dbg_scores = scores;
     kvq_status st = prepare_desc(d, head_map, true, true);
     if (st != KVQ_OK) return st;
-    return run(ds, true, nullptr, 0, nullptr, static_cast<cudaStream_t>(stream));
+    return run(ds, true, nullptr, 0, nullptr, static_cast<cudaStream_t>(stream), kernel);
 }
 
 }  // extern "C"
@@ -873,6 +804,32 @@ extern "C" kvq_status kvq_decode_attn_noalloc(const kvq_cache *c, const void *q1
     if (st != KVQ_OK) return st;
     return kvq_decode_attn(c, q16, n_q_heads, t_q, causal_tail, seq_lens, max_len, head_map, sm_scale, out, lse,
                            scratch, KVQ_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" kvq_status kvq_debug_lose_stage(const kvq_cache *c, const void *q16, int32_t n_q_heads, int32_t t_q,
+                                           int32_t causal_tail, const int32_t *seq_lens, int32_t max_len,
+                                           const int32_t *head_map, float sm_scale, float *out, float *lse,
+                                           void *workspace, size_t workspace_bytes, void *stream)
+{
+    const kvq_decode_desc x{c, q16, n_q_heads, t_q, causal_tail, seq_lens, max_len, head_map, sm_scale, out, lse,
+                            nullptr, nullptr};
+    std::vector<Desc> ds(1);
+    const kvq_status st = to_desc(x, true, ds[0]);
+    if (st != KVQ_OK) return st;
+    return run(ds, false, workspace, workspace_bytes, nullptr, static_cast<cudaStream_t>(stream), nullptr, true);
+}
+
+extern "C" kvq_status kvq_reset_wait_timeouts(void)
+{
+    DeviceInfo *dev = nullptr;
+    const kvq_status st = device_setup(&dev);
+    if (st != KVQ_OK) return st;
+    const unsigned int zero = 0;
+    if (cudaMemcpy(dev->timeouts, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return KVQ_ERR_CUDA;
+    }
+    return KVQ_OK;
 }
 
 extern "C" kvq_status kvq_wait_timeouts(uint32_t *count)

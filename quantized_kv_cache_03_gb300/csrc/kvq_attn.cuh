@@ -216,11 +216,22 @@ __device__ __forceinline__ uint32_t q_pair(uint32_t w, int k0)
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-template <int NT, int VT, int KT, bool DUMP, int W>
+// Kernel flavours (kModeDecode, kModeDump, kModeLoseStage of kvq_internal.cuh).
+// In the lose-stage test flavour warp 0 of CTA 0 arms its second ring stage's
+// barrier without issuing the stage's copies, so that this one wait (given a
+// short limit) runs out and the give-up path runs: the warp skips that stage
+// when it drains its copies, and waits with the normal limit for every copy
+// it did issue, so no copy is in flight when the CTA exits.
+constexpr int kLostStage = 1;                // issue index of the stage armed without copies
+constexpr uint32_t kLostStageSpins = 1024;   // limit of the wait that runs out
+
+template <int NT, int VT, int KT, int MODE, int W>
 __global__ void __launch_bounds__(SplitCfg<NT, VT, KT, W>::THREADS, SplitCfg<NT, VT, KT, W>::MIN_CTAS)
     split_attn_kernel(const __grid_constant__ AttnParams p)
 {
     using C = SplitCfg<NT, VT, KT, W>;
+    constexpr bool DUMP = MODE == kModeDump;
+    constexpr bool LOSE = MODE == kModeLoseStage;
     static_assert(!(DUMP && KT == KVQ_K_F16), "the score dump exists for int8 K only");
     constexpr int kWarps = C::WARPS;
     constexpr int kThreads = C::THREADS;
@@ -306,13 +317,18 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT, KT, W>::THREADS, SplitCfg<NT,
     int issued = 0;   // stages handed to the copy engine
     // Hand the next stage (up to TPS tiles of the current segment piece) to the
     // copy engine; the walk is advanced by every lane alike.
+    // (test flavour) this warp arms one stage without its copies
+    const bool loser = LOSE && blockIdx.x == 0 && warp == 0;
     auto issue = [&](int slot) {
         const int n = min(C::TPS, pw.Tend - pw.T);
         if (lane == 0) {
             const int tb = pw.T * kWTile;
             tile_rec[slot] = make_int4(tb, pw.la, pw.le, pw.pos0 + tb);
             stage_n[slot] = n;
-            tile_issue<NT, VT, KT>(pw, n, ring_s + slot * C::STAGE, bar_s + slot * 8);
+            if (loser && issued == kLostStage)
+                mbar_arrive_expect_tx(bar_s + slot * 8, n * C::TILE);   // bytes that never come
+            else
+                tile_issue<NT, VT, KT>(pw, n, ring_s + slot * C::STAGE, bar_s + slot * 8);
         }
         pw.T += n;
         pw.gk += n * C::TILE_K;
@@ -492,7 +508,8 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT, KT, W>::THREADS, SplitCfg<NT,
     bool bad = false;   // a stage never arrived (the warp then stops and drains)
     int slot = 0, phase = 0, prev = S - 1, done = 0;   // done % S, (done / S) & 1, (done + S - 1) % S
     while (done < issued) {
-        const bool landed = mbar_wait(bar_s + slot * 8, phase);
+        const bool landed = (loser && done == kLostStage) ? mbar_wait(bar_s + slot * 8, phase, kLostStageSpins)
+                                                          : mbar_wait(bar_s + slot * 8, phase);
         if (!__all_sync(0xffffffffu, landed)) {
             bad = true;
             break;
@@ -773,7 +790,8 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT, KT, W>::THREADS, SplitCfg<NT,
     if (bad) {
         // a wait gave up: wait (bounded) for this warp's copies still in flight,
         // then poison the CTA's results
-        for (int j = done; j < issued; ++j) mbar_wait(bar_s + (j % S) * 8, (j / S) & 1);
+        for (int j = done; j < issued; ++j)
+            if (!(loser && j == kLostStage)) mbar_wait(bar_s + (j % S) * 8, (j / S) & 1);
         if (lane == 0) {
             atomicOr(bad_flag, 1);
             atomicAdd(p.timeouts, 1u);
@@ -884,7 +902,7 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT, KT, W>::THREADS, SplitCfg<NT,
 }
 
 template <int NT, int VT, int KT, int W>
-cudaError_t launch_split_t(const AttnParams &p, int n_ctas, bool dump, cudaStream_t s, bool pdl)
+cudaError_t launch_split_t(const AttnParams &p, int n_ctas, int mode, cudaStream_t s, bool pdl)
 {
     using C = SplitCfg<NT, VT, KT, W>;
     cudaLaunchConfig_t cfg = {};
@@ -898,23 +916,29 @@ cudaError_t launch_split_t(const AttnParams &p, int n_ctas, bool dump, cudaStrea
     cfg.attrs = at;
     cfg.numAttrs = 1;
     if constexpr (KT == KVQ_K_I8 && W == split_warps(NT)) {
-        if (dump) return cudaLaunchKernelEx(&cfg, split_attn_kernel<NT, VT, KT, true, W>, p);
-    } else {
-        if (dump) return cudaErrorInvalidValue;
+        if (mode == kModeDump) return cudaLaunchKernelEx(&cfg, split_attn_kernel<NT, VT, KT, kModeDump, W>, p);
     }
-    return cudaLaunchKernelEx(&cfg, split_attn_kernel<NT, VT, KT, false, W>, p);
+    if constexpr (KT == KVQ_K_I8 && VT == KVQ_V_Q4_0 && NT == 1 && W == split_warps(1)) {
+        if (mode == kModeLoseStage)
+            return cudaLaunchKernelEx(&cfg, split_attn_kernel<NT, VT, KT, kModeLoseStage, W>, p);
+    }
+    if (mode != kModeDecode) return cudaErrorInvalidValue;
+    return cudaLaunchKernelEx(&cfg, split_attn_kernel<NT, VT, KT, kModeDecode, W>, p);
 }
 
 template <int NT, int VT, int KT, int W>
-cudaError_t prepare_split_t(bool dump, int *ctas_per_sm)
+cudaError_t prepare_split_t(int mode, int *ctas_per_sm)
 {
     using C = SplitCfg<NT, VT, KT, W>;
-    const void *fn = (const void *)split_attn_kernel<NT, VT, KT, false, W>;
+    const void *fn = nullptr;
+    if (mode == kModeDecode) fn = (const void *)split_attn_kernel<NT, VT, KT, kModeDecode, W>;
     if constexpr (KT == KVQ_K_I8 && W == split_warps(NT)) {
-        if (dump) fn = (const void *)split_attn_kernel<NT, VT, KT, true, W>;
-    } else {
-        if (dump) return cudaErrorInvalidValue;
+        if (mode == kModeDump) fn = (const void *)split_attn_kernel<NT, VT, KT, kModeDump, W>;
     }
+    if constexpr (KT == KVQ_K_I8 && VT == KVQ_V_Q4_0 && NT == 1 && W == split_warps(1)) {
+        if (mode == kModeLoseStage) fn = (const void *)split_attn_kernel<NT, VT, KT, kModeLoseStage, W>;
+    }
+    if (!fn) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     if (ctas_per_sm) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, fn, C::THREADS, C::SMEM);
@@ -922,42 +946,42 @@ cudaError_t prepare_split_t(bool dump, int *ctas_per_sm)
 }
 
 template <int VT, int KT>
-cudaError_t launch_split_nt(const AttnParams &p, int nt, int warps, int n_ctas, bool dump, cudaStream_t s, bool pdl)
+cudaError_t launch_split_nt(const AttnParams &p, int nt, int warps, int n_ctas, int mode, cudaStream_t s, bool pdl)
 {
-    if (nt == 1 && warps == kWarpsHalf) return launch_split_t<1, VT, KT, kWarpsHalf>(p, n_ctas, dump, s, pdl);
+    if (nt == 1 && warps == kWarpsHalf) return launch_split_t<1, VT, KT, kWarpsHalf>(p, n_ctas, mode, s, pdl);
     if (warps != split_warps(nt)) return cudaErrorInvalidValue;
     switch (nt) {
-    case 1: return launch_split_t<1, VT, KT, split_warps(1)>(p, n_ctas, dump, s, pdl);
-    case 2: return launch_split_t<2, VT, KT, split_warps(2)>(p, n_ctas, dump, s, pdl);
-    case 4: return launch_split_t<4, VT, KT, split_warps(4)>(p, n_ctas, dump, s, pdl);
+    case 1: return launch_split_t<1, VT, KT, split_warps(1)>(p, n_ctas, mode, s, pdl);
+    case 2: return launch_split_t<2, VT, KT, split_warps(2)>(p, n_ctas, mode, s, pdl);
+    case 4: return launch_split_t<4, VT, KT, split_warps(4)>(p, n_ctas, mode, s, pdl);
     default: return cudaErrorInvalidValue;
     }
 }
 
 template <int VT, int KT>
-cudaError_t prepare_split_nt(int nt, int warps, bool dump, int *ctas)
+cudaError_t prepare_split_nt(int nt, int warps, int mode, int *ctas)
 {
-    if (nt == 1 && warps == kWarpsHalf) return prepare_split_t<1, VT, KT, kWarpsHalf>(dump, ctas);
+    if (nt == 1 && warps == kWarpsHalf) return prepare_split_t<1, VT, KT, kWarpsHalf>(mode, ctas);
     if (warps != split_warps(nt)) return cudaErrorInvalidValue;
     switch (nt) {
-    case 1: return prepare_split_t<1, VT, KT, split_warps(1)>(dump, ctas);
-    case 2: return prepare_split_t<2, VT, KT, split_warps(2)>(dump, ctas);
-    case 4: return prepare_split_t<4, VT, KT, split_warps(4)>(dump, ctas);
+    case 1: return prepare_split_t<1, VT, KT, split_warps(1)>(mode, ctas);
+    case 2: return prepare_split_t<2, VT, KT, split_warps(2)>(mode, ctas);
+    case 4: return prepare_split_t<4, VT, KT, split_warps(4)>(mode, ctas);
     default: return cudaErrorInvalidValue;
     }
 }
 
 #define KVQ_DEFINE_SPLIT_ENTRY(SUFFIX, VT)                                                              \
     cudaError_t launch_split_##SUFFIX(const AttnParams &p, int nt, int warps, int k_type, int n_ctas,    \
-                                      bool dump, cudaStream_t s, bool pdl)                              \
+                                      int mode, cudaStream_t s, bool pdl)                               \
     {                                                                                                   \
-        return (k_type == KVQ_K_F16) ? launch_split_nt<VT, KVQ_K_F16>(p, nt, warps, n_ctas, dump, s, pdl) \
-                                     : launch_split_nt<VT, KVQ_K_I8>(p, nt, warps, n_ctas, dump, s, pdl); \
+        return (k_type == KVQ_K_F16) ? launch_split_nt<VT, KVQ_K_F16>(p, nt, warps, n_ctas, mode, s, pdl) \
+                                     : launch_split_nt<VT, KVQ_K_I8>(p, nt, warps, n_ctas, mode, s, pdl); \
     }                                                                                                   \
-    cudaError_t prepare_split_##SUFFIX(int nt, int warps, int k_type, bool dump, int *ctas)             \
+    cudaError_t prepare_split_##SUFFIX(int nt, int warps, int k_type, int mode, int *ctas)              \
     {                                                                                                   \
-        return (k_type == KVQ_K_F16) ? prepare_split_nt<VT, KVQ_K_F16>(nt, warps, dump, ctas)           \
-                                     : prepare_split_nt<VT, KVQ_K_I8>(nt, warps, dump, ctas);           \
+        return (k_type == KVQ_K_F16) ? prepare_split_nt<VT, KVQ_K_F16>(nt, warps, mode, ctas)           \
+                                     : prepare_split_nt<VT, KVQ_K_I8>(nt, warps, mode, ctas);           \
     }
 
 }  // namespace kvq

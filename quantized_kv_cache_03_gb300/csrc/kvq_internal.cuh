@@ -30,8 +30,6 @@ constexpr int split_warps(int nt) { return nt == 1 ? KVQ_WARPS_NT1 : KVQ_WARPS_N
 constexpr int kWarpsHalf = KVQ_WARPS_NT1 / 2;
 constexpr int kPrefillRows = 128;       // query rows per CTA of the tcgen05 kernel
 constexpr int kPrefillPositions = 64;   // positions per KV tile of the tcgen05 kernel
-constexpr int kVerifyRows = 32;         // query rows (MMA N) of the tcgen05 verify kernel
-constexpr int kVerifyPositions = 128;   // positions per KV tile of the tcgen05 verify kernel
 constexpr int kMaxSegsLaunch = 64;      // segment-table entries per launch
 constexpr int kMaxSeqsLaunch = 64;      // sequences per launch
 
@@ -172,24 +170,23 @@ struct AppendParams {
 // format (kvq_ktype); dump kernels exist for KVQ_K_I8 at split_warps only.
 cudaError_t launch_append(const AppendParams &p, int v_type, int k_type, int max_rows, cudaStream_t s, bool pdl);
 cudaError_t launch_combine(const CombineParams &p, int n_rows, cudaStream_t s, bool pdl);
-cudaError_t launch_split_q4(const AttnParams &p, int n_tiles8, int warps, int k_type, int n_ctas, bool dump,
+// Split-kernel flavours: the decode kernel; the score-dump test hook (int8 K,
+// split_warps(n_tiles8) warps); the lose-stage test hook (int8 K, one 8-row
+// tile, 16 warps), in which one stage's wait runs out on purpose.
+constexpr int kModeDecode = 0, kModeDump = 1, kModeLoseStage = 2;
+cudaError_t launch_split_q4(const AttnParams &p, int n_tiles8, int warps, int k_type, int n_ctas, int mode,
                             cudaStream_t s, bool pdl);
-cudaError_t launch_split_q8(const AttnParams &p, int n_tiles8, int warps, int k_type, int n_ctas, bool dump,
+cudaError_t launch_split_q8(const AttnParams &p, int n_tiles8, int warps, int k_type, int n_ctas, int mode,
                             cudaStream_t s, bool pdl);
-cudaError_t prepare_split_q4(int n_tiles8, int warps, int k_type, bool dump, int *ctas_per_sm);
-cudaError_t prepare_split_q8(int n_tiles8, int warps, int k_type, bool dump, int *ctas_per_sm);
+cudaError_t prepare_split_q4(int n_tiles8, int warps, int k_type, int mode, int *ctas_per_sm);
+cudaError_t prepare_split_q8(int n_tiles8, int warps, int k_type, int mode, int *ctas_per_sm);
 // tcgen05 kernel for long query chunks (kvq_prefill_q4.cu / kvq_prefill_q8.cu):
-// 128 query rows per CTA, one CTA per SM.
-cudaError_t launch_prefill_q4(const AttnParams &p, int n_ctas, cudaStream_t s, bool pdl);
-cudaError_t launch_prefill_q8(const AttnParams &p, int n_ctas, cudaStream_t s, bool pdl);
+// 128 query rows per CTA, one CTA per SM; dump selects its test-hook flavour
+// (query codes and raw block scores instead of out / lse).
+cudaError_t launch_prefill_q4(const AttnParams &p, int n_ctas, bool dump, cudaStream_t s, bool pdl);
+cudaError_t launch_prefill_q8(const AttnParams &p, int n_ctas, bool dump, cudaStream_t s, bool pdl);
 cudaError_t prepare_prefill_q4();
 cudaError_t prepare_prefill_q8();
-// tcgen05 kernel for 9..32 query rows per kv head (kvq_verify_q4.cu /
-// kvq_verify_q8.cu): positions on the MMA's M, rows on N, one CTA per SM.
-cudaError_t launch_verify_q4(const AttnParams &p, int n_ctas, cudaStream_t s, bool pdl);
-cudaError_t launch_verify_q8(const AttnParams &p, int n_ctas, cudaStream_t s, bool pdl);
-cudaError_t prepare_verify_q4();
-cudaError_t prepare_verify_q8();
 
 // ------------------------------------------------------------- device helpers --
 
@@ -234,9 +231,9 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 // Wait for phase `parity` of the barrier to complete, giving up after
 // kMbarSpins polls (each poll may suspend the thread for a short while).
 constexpr uint32_t kMbarSpins = 1u << 22;
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t spins = kMbarSpins)
 {
-    for (uint32_t i = 0; i < kMbarSpins; ++i) {
+    for (uint32_t i = 0; i < spins; ++i) {
         uint32_t done;
         asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
                      : "=r"(done)

@@ -42,6 +42,12 @@
 // Operands live in shared memory, K-major without swizzle: 8 rows x 16 bytes
 // core matrices, a row group's core matrices LBO bytes apart along K (128 for
 // V, 160 for K, see PrefillCfg) and row groups SBO bytes apart.
+//
+// The DUMP flavour (test hook) runs the same pipeline and, instead of out and
+// lse, writes each row's quantized query (codes and fp16 scales) and the raw
+// block accumulators S_b it reads from tensor memory, as int32, for every
+// visible position of the split: the integer block dots as this kernel's
+// tensor cores computed them.
 #pragma once
 
 #include "kvq_internal.cuh"
@@ -206,7 +212,7 @@ __device__ __forceinline__ void v_hilo(uint32_t code2, __half2 d2, uint32_t &hi,
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-template <int VT>
+template <int VT, bool DUMP>
 __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid_constant__ AttnParams p)
 {
     using C = PrefillCfg<VT>;
@@ -240,7 +246,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
     int r1 = min(L, r0 + G.chunk);
     if (G.causal) r1 = min(r1, L - G.t_q + (row0 + R - 1) / gsz + 1);
     if (r0 >= r1) {   // nothing visible in this split
-        if (tid < R) {
+        if (!DUMP && tid < R) {
             const int i = (row0 + tid) / gsz, hq = p.grp_q[gb + (row0 + tid) % gsz];
             const size_t row = ((size_t)b * G.t_q + i) * G.n_q_heads + hq;
             if (G.n_split == 1) {
@@ -334,6 +340,19 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     wv[e] = pack_half2((float)quant_i8(x[2 * e], sc), (float)quant_i8(x[2 * e + 1], sc));
+                if (DUMP && split == 0) {   // the block's 32 codes and its scale bits
+                    uint32_t cw[8];
+#pragma unroll
+                    for (int w4 = 0; w4 < 8; ++w4) {
+                        cw[w4] = 0u;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) cw[w4] |= (uint32_t)(quant_i8(x[4 * w4 + e], sc) & 0xff) << (8 * e);
+                    }
+                    uint4 *qd = reinterpret_cast<uint4 *>(G.dbg_qc + orow * kD + 32 * bb);
+                    qd[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+                    qd[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+                    G.dbg_qs[orow * kNB + bb] = __half_as_ushort(__float2half_rn(sc));
+                }
             } else {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) wv[e] = 0u;
@@ -633,6 +652,21 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
 #pragma unroll
                 for (int bb = 0; bb < kNB; ++bb) tmem_ld16(tS + lane_base + kPN * bb + HP * hf + 16 * q, a[bb]);
                 tmem_wait_ld();
+                if constexpr (DUMP) {
+                    // positions 16 q + u of this half: sub-tile 2 hf + q of the KV tile
+                    const int4 r = reinterpret_cast<const int4 *>(smem + C::OREC_OFF)[ob * kPSub + 2 * hf + q];
+                    const int nsd = reinterpret_cast<const int *>(smem + C::ONSUB_OFF)[ob];
+                    if (row_ok && 2 * hf + q < nsd) {
+#pragma unroll
+                        for (int u = 0; u < kWTile; ++u) {
+                            const int tok = r.x + u, pos = r.w + u;
+                            if (tok >= r.y && tok < r.z && pos < L)
+                                *reinterpret_cast<int4 *>(G.dbg_scores + (orow * G.max_len + pos) * kNB) =
+                                    make_int4((int)__uint_as_float(a[0][u]), (int)__uint_as_float(a[1][u]),
+                                              (int)__uint_as_float(a[2][u]), (int)__uint_as_float(a[3][u]));
+                        }
+                    }
+                }
 #pragma unroll
                 for (int jj = 0; jj < 16; jj += 4) {
                     float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
@@ -763,7 +797,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
             if (!ok) give_up();
         }
         const bool lost = !ok || wbad();
-        if (lost) {   // results lost: NaN rows
+        if (DUMP) {
+            // the test hook writes no out / lse
+        } else if (lost) {   // results lost: NaN rows
             if (row_ok) {
                 const float nan = __int_as_float(0x7fc00000);
                 if (G.n_split == 1) {
@@ -811,7 +847,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
 }
 
 template <int VT>
-cudaError_t launch_prefill_t(const AttnParams &p, int n_ctas, cudaStream_t s, bool pdl)
+cudaError_t launch_prefill_t(const AttnParams &p, int n_ctas, bool dump, cudaStream_t s, bool pdl)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(n_ctas);
@@ -823,13 +859,17 @@ cudaError_t launch_prefill_t(const AttnParams &p, int n_ctas, cudaStream_t s, bo
     at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_attn_kernel<VT>, p);
+    if (dump) return cudaLaunchKernelEx(&cfg, prefill_attn_kernel<VT, true>, p);
+    return cudaLaunchKernelEx(&cfg, prefill_attn_kernel<VT, false>, p);
 }
 
 template <int VT>
 cudaError_t prepare_prefill_t()
 {
-    return cudaFuncSetAttribute(prefill_attn_kernel<VT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(prefill_attn_kernel<VT, false>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, PrefillCfg<VT>::SMEM);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(prefill_attn_kernel<VT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 PrefillCfg<VT>::SMEM);
 }
 

@@ -2,9 +2,9 @@
 #include "kvq_prefill.cuh"
 
 namespace kvq {
-cudaError_t launch_prefill_q4(const AttnParams &p, int n_ctas, cudaStream_t s, bool pdl)
+cudaError_t launch_prefill_q4(const AttnParams &p, int n_ctas, bool dump, cudaStream_t s, bool pdl)
 {
-    return launch_prefill_t<KVQ_V_Q4_0>(p, n_ctas, s, pdl);
+    return launch_prefill_t<KVQ_V_Q4_0>(p, n_ctas, dump, s, pdl);
 }
 cudaError_t prepare_prefill_q4() { return prepare_prefill_t<KVQ_V_Q4_0>(); }
 }  // namespace kvq

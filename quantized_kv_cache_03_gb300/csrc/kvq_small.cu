@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
             const float4 q = part[w][lane];
             t.x = fmaf(q.x, f, t.x); t.y = fmaf(q.y, f, t.y); t.z = fmaf(q.z, f, t.z); t.w = fmaf(q.w, f, t.w);
         }
-        const bool any = Wt > 0.f;
+        const bool any = !(Wt <= 0.f);   // a NaN weight (a poisoned partial) keeps the row NaN
         const float inv = any ? 1.f / Wt : 0.f;
         reinterpret_cast<float4 *>(G.out + (size_t)row * kD)[lane] = make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
         if (lane == 0) G.lse[row] = any ? M + logf(Wt) : -INFINITY;

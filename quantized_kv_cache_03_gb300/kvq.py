@@ -33,7 +33,8 @@ QBLOCK = 32
 
 EXPORTED = ("kvq_append", "kvq_decode_attn", "kvq_decode_workspace_size", "kvq_decode_attn_multi",
             "kvq_decode_multi_workspace_size", "kvq_decode_attn_noalloc", "kvq_wait_timeouts",
-            "kvq_status_string", "kvq_debug_qk", "kvq_debug_plan")
+            "kvq_reset_wait_timeouts", "kvq_status_string", "kvq_debug_qk", "kvq_debug_lose_stage",
+            "kvq_debug_plan")
 MAX_CALLS = 16
 MAX_T_Q = 4096
 MAX_T_Q_APPEND = 8
@@ -103,13 +104,17 @@ def load():
                                                     c_void_p, c_void_p]
             lib.kvq_wait_timeouts.restype = c_int32
             lib.kvq_wait_timeouts.argtypes = [POINTER(ctypes.c_uint32)]
+            lib.kvq_reset_wait_timeouts.restype = c_int32
+            lib.kvq_reset_wait_timeouts.argtypes = []
+            lib.kvq_debug_lose_stage.restype = c_int32
+            lib.kvq_debug_lose_stage.argtypes = lib.kvq_decode_attn.argtypes
             lib.kvq_debug_qk.restype = c_int32
             lib.kvq_debug_qk.argtypes = [POINTER(KvqCache), c_void_p, c_int32, c_int32, c_void_p, c_int32,
-                                         POINTER(c_int32), c_void_p, c_void_p, c_void_p, c_void_p]
+                                         POINTER(c_int32), c_void_p, c_void_p, c_void_p, POINTER(c_int32),
+                                         c_void_p]
             lib.kvq_debug_plan.restype = c_int32
             lib.kvq_debug_plan.argtypes = [c_int32, POINTER(KvqDecodeDesc), c_int32, POINTER(c_int32),
-                                           POINTER(KvqPlanLaunch), c_int32, POINTER(c_int32), POINTER(c_size_t),
-                                           POINTER(c_int32)]
+                                           POINTER(KvqPlanLaunch), c_int32, POINTER(c_int32), POINTER(c_size_t)]
             _lib = lib
     return _lib
 
@@ -361,14 +366,20 @@ def kvq_decode_attn_noalloc(cache: Cache, q16: torch.Tensor, n_q_heads: int, t_q
         raise KvqError(st, "kvq_decode_attn_noalloc")
 
 
+DUMP_KERNELS = ("split", "tcgen05")
+
+
 def kvq_debug_qk(cache: Cache, q16, n_q_heads, t_q, seq_lens, max_len, head_map, q_codes, q_scales, scores,
-                 stream=None) -> None:
-    """kvq_debug_qk test hook of include/kvq.h."""
+                 stream=None) -> str:
+    """kvq_debug_qk test hook of include/kvq.h; returns the kernel that
+    produced the dumps ("split" or "tcgen05")."""
     hm = None if head_map is None else _i32(head_map)
+    kern = c_int32(-1)
     st = load().kvq_debug_qk(ctypes.byref(cache.desc), _ptr(q16), n_q_heads, t_q, _ptr(seq_lens), max_len, hm,
-                             _ptr(q_codes), _ptr(q_scales), _ptr(scores), _stream(stream))
+                             _ptr(q_codes), _ptr(q_scales), _ptr(scores), ctypes.byref(kern), _stream(stream))
     if st:
         raise KvqError(st, "kvq_debug_qk")
+    return DUMP_KERNELS[kern.value]
 
 
 def kvq_wait_timeouts() -> int:
@@ -381,22 +392,43 @@ def kvq_wait_timeouts() -> int:
     return int(n.value)
 
 
-PLAN_KERNELS = ("split", "prefill", "verify")
+def kvq_reset_wait_timeouts() -> None:
+    """kvq_reset_wait_timeouts of include/kvq.h."""
+    st = load().kvq_reset_wait_timeouts()
+    if st:
+        raise KvqError(st, "kvq_reset_wait_timeouts")
+
+
+def kvq_debug_lose_stage(cache: Cache, q16: torch.Tensor, n_q_heads: int, t_q: int, causal_tail: bool,
+                         seq_lens: torch.Tensor, max_len: int, head_map, sm_scale: float, out: torch.Tensor,
+                         lse: torch.Tensor, workspace: torch.Tensor | None, stream=None) -> None:
+    """kvq_debug_lose_stage test hook of include/kvq.h (arguments as
+    kvq_decode_attn)."""
+    hm = None if head_map is None else _i32(head_map)
+    st = load().kvq_debug_lose_stage(ctypes.byref(cache.desc), _ptr(q16), n_q_heads, t_q, int(causal_tail),
+                                     _ptr(seq_lens), max_len, hm, float(sm_scale), _ptr(out), _ptr(lse),
+                                     _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                                     _stream(stream))
+    if st:
+        raise KvqError(st, "kvq_debug_lose_stage")
+
+
+PLAN_KERNELS = ("split", "prefill")
 
 
 def kvq_debug_plan(calls, n_sms: int, ctas_per_sm=(1, 2, 2, 2), max_out: int = 64):
     """kvq_debug_plan of include/kvq.h (test hook): the launches the decode
     call would make for `calls` (dicts as for kvq_decode_attn_multi; only the
     caches' host descriptors are read) on a described device.  Returns
-    (launches as dicts, workspace bytes, calls with a separate append launch)."""
+    (launches as dicts, workspace bytes)."""
     arr, keep = _descs(calls)
     ctas = _i32(ctas_per_sm)
     out = (KvqPlanLaunch * max(1, max_out))()
-    n_out, n_pre, ws = c_int32(0), c_int32(0), c_size_t(0)
+    n_out, ws = c_int32(0), c_size_t(0)
     st = load().kvq_debug_plan(len(calls), arr, int(n_sms), ctas, out, max_out, ctypes.byref(n_out),
-                               ctypes.byref(ws), ctypes.byref(n_pre))
+                               ctypes.byref(ws))
     if st:
         raise KvqError(st, "kvq_debug_plan")
     launches = [dict(kernel=PLAN_KERNELS[r.kernel], n_tiles8=r.n_tiles8, warps=r.warps, chunk=r.chunk,
                      n_ctas=r.n_ctas, n_rows=r.n_rows) for r in out[:min(n_out.value, max_out)]]
-    return launches, int(ws.value), int(n_pre.value)
+    return launches, int(ws.value)

@@ -80,7 +80,8 @@ class Case:
         qc = torch.zeros((self.B, self.tq, self.Hq, 128), dtype=torch.int8, device=dev())
         qs = torch.zeros((self.B, self.tq, self.Hq, 4), dtype=torch.int16, device=dev())
         sc = torch.zeros((self.B, self.tq, self.Hq, self.max_len, 4), dtype=torch.int32, device=dev())
-        kvq.kvq_debug_qk(self.cache, q16, self.Hq, self.tq, lens, self.max_len, head_map, qc, qs, sc)
+        self.dump_kernel = kvq.kvq_debug_qk(self.cache, q16, self.Hq, self.tq, lens, self.max_len, head_map, qc,
+                                            qs, sc)
         torch.cuda.synchronize()
         return qc.cpu().numpy(), qs.cpu().numpy().view(np.uint16), sc.cpu().numpy()
 
@@ -88,10 +89,11 @@ class Case:
         k, v = self.kv[b]
         return oracle.quantize_kv(k, v, self.spec.v_type, k_type=self.spec.k_type)
 
-    def oracle_decode(self, b, head_map=None, row_mask=None, want_scores=False, threads=8):
+    def oracle_decode(self, b, head_map=None, row_mask=None, want_scores=False, threads=8, causal=None):
         s = self.spec
         hm = oracle.default_head_map(s.n_q_heads, s.n_kv_heads) if head_map is None else np.asarray(head_map)
-        return oracle.decode_seq(self.oracle_cache(b), self.q[b], hm, s.causal, SM_SCALE, s.v_type,
+        causal = s.causal if causal is None else causal
+        return oracle.decode_seq(self.oracle_cache(b), self.q[b], hm, causal, SM_SCALE, s.v_type,
                                  want_codes=want_scores, want_scores=want_scores, row_mask=row_mask,
                                  n_threads=threads)
 

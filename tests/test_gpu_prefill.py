@@ -3,11 +3,16 @@
 32 query rows per kv head run on the tcgen05 kernel (128-row tiles, TMEM
 accumulators); KVQ_PREFILL=0 sends them to the split kernel's 32-row tiles, and
 every case below runs on both.  The cases span several row tiles with a ragged
-last one, splits that lie
-wholly past a tile's causal limit, uneven head maps (tiles past a small
-group's rows), an empty context, a non-causal chunk and a mixed launch with a
-decode call.  All against the oracle on the same seeded inputs: cache bytes
-and int32 block scores bit-exact, out within 2e-3 and lse within 1e-4."""
+last one, splits that lie wholly past a tile's causal limit, uneven head maps
+(tiles past a small group's rows), an empty context, a non-causal chunk and a
+mixed launch with a decode call, all against the oracle on the same seeded
+inputs: cache bytes bit-exact, out within 2e-3 and lse within 1e-4.
+
+The raw int32 block scores and the query codes are compared bit for bit with
+the oracle through the kvq_debug_qk hook, which runs the kernel the decode call
+picks and reports which one ran: the tests assert that it is the tcgen05
+kernel (its scores are the TMEM accumulators of its fp16 MMAs on exact integer
+operands) or the split kernel, as the fixture selects."""
 
 import numpy as np
 import pytest
@@ -15,6 +20,8 @@ import torch
 
 from quantized_kv_cache_03_gb300 import kvq
 from quantized_kv_cache_03_gb300 import workloads as W
+
+import oracle
 
 from kvq_cases import SM_SCALE, Case, assert_cache_bytes, assert_close, dev, to_dev
 
@@ -42,19 +49,88 @@ def _check_all(case, head_map=None, scores=False):
     return out, lse
 
 
+def _plan_kernel(case):
+    call = dict(cache=case.cache, n_q_heads=case.Hq, t_q=case.tq, causal_tail=case.spec.causal,
+                max_len=case.max_len, head_map=None, sm_scale=SM_SCALE)
+    lns, _ = kvq.kvq_debug_plan([call], 152)
+    return {ln["kernel"] for ln in lns}
+
+
+def _check_scores(case, kernel, rows=None):
+    """Query codes / scales and every position's int32 block scores of the
+    dump against the oracle (causal mask off: the hook dumps every position
+    below the sequence length), on the kernel the fixture selects."""
+    want = "tcgen05" if kernel == "tcgen05" else "split"
+    assert _plan_kernel(case) == {"prefill" if kernel == "tcgen05" else "split"}
+    qc, qs, sc = case.debug_qk()
+    assert case.dump_kernel == want, "the dump ran on the %s kernel" % case.dump_kernel
+    for b in range(case.B):
+        L = case.lens[b]
+        ref = case.oracle_decode(b, want_scores=True, causal=False)
+        assert np.array_equal(qc[b], ref["q_codes"]), "query codes, seq %d" % b
+        assert np.array_equal(qs[b], ref["q_scales"]), "query scales, seq %d" % b
+        got, exp = sc[b, :, :, :L], ref["scores"]
+        if not np.array_equal(got, exp):
+            bad = np.argwhere(got != exp)
+            raise AssertionError("int32 block scores differ at %d places, first (token, head, pos, block) %s"
+                                 % (len(bad), bad[:5].tolist()))
+
+
 @pytest.mark.parametrize("vt", [0, 1])
-def test_chunk_of_64_tokens_all_rows_and_scores(vt):
-    # 64 tokens x 4 query heads = 256 rows per kv head: 8 row tiles
+def test_chunk_of_64_tokens_all_rows_and_scores(vt, kernel):
+    # 64 tokens x 4 query heads = 256 rows per kv head: 2 tcgen05 row tiles (8 of 32 rows)
     spec = W.make_spec("prefill", ctx=1000, t_q=64, v_type=vt)[0]
     case = Case(spec).build()
     _check_all(case)
-    qc, qs, sc = case.debug_qk()
-    ref = case.oracle_decode(0, want_scores=True)
-    assert np.array_equal(qc[0], ref["q_codes"]) and np.array_equal(qs[0], ref["q_scales"])
-    L = case.lens[0]
-    for i in range(case.tq):
-        vis = L - case.tq + i + 1
-        assert np.array_equal(sc[0, i, :, :vis], ref["scores"][i, :, :vis]), "int32 block scores, token %d" % i
+    _check_scores(case, kernel)
+
+
+@pytest.mark.parametrize("split", [192, 640])
+def test_scores_over_splits_ragged_tiles_and_segments(split, kernel, monkeypatch):
+    """Two sequences, three segments each, 40 tokens x 6 heads (240 rows per kv
+    head: a ragged second 128-row tile), positions split in chunks that cut
+    KV tiles at split and segment edges."""
+    monkeypatch.setenv("KVQ_SPLIT", str(split))
+    spec = W.make_spec("prefill", ctx=1500, t_q=40, n_seqs=2, n_seg=3, n_q_heads=48, n_kv_heads=8, v_type=1)[0]
+    spec.lengths[:] = [1500, 777]
+    spec.segments[:] = [W._cuts(spec.rng(9, b), int(L), 3, 40) for b, L in enumerate(spec.lengths)]
+    case = Case(spec).build()
+    _check_all(case)
+    _check_scores(case, kernel)
+
+
+def test_chunk_full_size_sampled_scores(kernel):
+    """The 512-token chunk over 32768 positions as the benchmark runs it: the
+    dump of every row (8.6 GB of int32 scores on the device), compared on
+    sampled rows (first and last of the chunk, random ones) at every position."""
+    if kernel != "tcgen05":
+        pytest.skip("the split kernel's dump at full size is covered by the decode workloads")
+    spec = W.make_spec("prefill")[0]
+    case = Case(spec).build()
+    assert _plan_kernel(case) == {"prefill"}
+    L, tq, Hq = case.lens[0], case.tq, case.Hq
+    q16 = to_dev(case.q)
+    lens = torch.tensor(case.lens, dtype=torch.int32, device=dev())
+    qc = torch.zeros((1, tq, Hq, 128), dtype=torch.int8, device=dev())
+    qs = torch.zeros((1, tq, Hq, 4), dtype=torch.int16, device=dev())
+    sc = torch.zeros((1, tq, Hq, L, 4), dtype=torch.int32, device=dev())
+    assert kvq.kvq_debug_qk(case.cache, q16, Hq, tq, lens, L, None, qc, qs, sc) == "tcgen05"
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    nr = tq * Hq
+    rows = np.unique(np.concatenate([[0, 1, Hq - 1, nr - Hq, nr - 1], rng.integers(0, nr, 11)]))
+    # the oracle on just these rows: one query token whose heads are the sampled (token, head) rows
+    hm_full = np.arange(Hq) // (Hq // spec.n_kv_heads)
+    q_sub = case.q[0].reshape(nr, 128)[rows][None]
+    ref = oracle.decode_seq(case.oracle_cache(0), q_sub, hm_full[rows % Hq].astype(np.int32), False, SM_SCALE,
+                            spec.v_type, want_codes=True, want_scores=True, n_threads=8)
+    got_sc = sc.view(nr, L, 4)[torch.as_tensor(rows, device=dev())].cpu().numpy()
+    assert np.array_equal(qc.view(nr, 128).cpu().numpy()[rows], ref["q_codes"][0])
+    assert np.array_equal(qs.view(nr, 4).cpu().numpy().view(np.uint16)[rows], ref["q_scales"][0])
+    if not np.array_equal(got_sc, ref["scores"][0]):
+        bad = np.argwhere(got_sc != ref["scores"][0])
+        raise AssertionError("int32 block scores differ at %d places, first %s" % (len(bad), bad[:5].tolist()))
+    del sc
 
 
 def test_splits_past_a_row_tiles_causal_limit(monkeypatch):

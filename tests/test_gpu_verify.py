@@ -1,15 +1,12 @@
 """Multi-token verify over the quantized cache: calls with 9 to 32 query rows
 per kv head (t_q query tokens x the kv head's query heads).  They run on the
-split kernel's 16- and 32-row tiles, or with KVQ_VERIFY=1 on the tcgen05
-verify kernel (cache positions on the MMA's M, the rows on N, TMEM
-accumulators); every case below runs on both.  The cases cover row counts that are
-not multiples of 8, ragged and short contexts (tiles cut by segment ends, by
-the sequence length and by the causal tail), several splits merged by the
-combine, q8_0 V with x10 outlier channels, a non-causal call, uneven head maps,
-the step's tokens passed to the call (appended by a launch of their own ahead of
-the tcgen05 kernel), and a launch that mixes verify and decode calls.  All
-against the oracle on the same seeded inputs: cache bytes bit-exact, out within
-2e-3 and lse within 1e-4."""
+split kernel's 16- and 32-row tiles.  The cases cover row counts that are not
+multiples of 8, ragged and short contexts (tiles cut by segment ends, by the
+sequence length and by the causal tail), several splits merged by the combine,
+q8_0 V with x10 outlier channels, a non-causal call, uneven head maps, the
+step's tokens passed to the call (fused append), and a launch that mixes
+verify and decode calls.  All against the oracle on the same seeded inputs:
+cache bytes bit-exact, out within 2e-3 and lse within 1e-4."""
 
 import numpy as np
 import pytest
@@ -27,12 +24,6 @@ pytestmark = pytest.mark.gpu
 def _built():
     import __graft_entry__
     __graft_entry__.build()
-
-
-@pytest.fixture(params=["tcgen05", "rowtile"], autouse=True)
-def kernel(request, monkeypatch):
-    monkeypatch.setenv("KVQ_VERIFY", "1" if request.param == "tcgen05" else "0")
-    return request.param
 
 
 def _check_all(case, head_map=None):
@@ -163,8 +154,8 @@ def test_full_size_sampled_rows():
 
 def test_repeats_and_pdl_on_off_bitwise_equal(monkeypatch):
     """Five runs with programmatic dependent launch and three without give
-    identical bits (fixed-order reductions on both kernels), with a forced
-    split so the combine runs too."""
+    identical bits (fixed-order reductions), with a forced split so the
+    combine runs too."""
     monkeypatch.setenv("KVQ_SPLIT", "1024")
     spec = W.make_spec("verify", ctx=4000, n_seqs=2, v_type=1, outliers=4)[0]
     case = Case(spec).build()

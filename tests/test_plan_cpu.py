@@ -24,7 +24,7 @@ def _lib():
 
 @pytest.fixture(autouse=True)
 def _clean_env(monkeypatch):
-    for k in ("KVQ_SPLIT", "KVQ_SPLIT_WARPS", "KVQ_ROW_TILE", "KVQ_PREFILL", "KVQ_VERIFY"):
+    for k in ("KVQ_SPLIT", "KVQ_SPLIT_WARPS", "KVQ_ROW_TILE", "KVQ_PREFILL"):
         monkeypatch.delenv(k, raising=False)
 
 
@@ -79,17 +79,17 @@ def test_long_pair_fused_is_one_wave_of_16_warp_ctas():
     """Both caches in one launch: 12 splits of 11008 positions per kv head,
     (8 + 4) x 12 = 144 CTAs, one combine over the 40 + 16 query rows."""
     _, calls = calls_of("long", fused=True)
-    lns, ws, pre = plan(calls)
+    lns, ws = plan(calls)
     assert lns == [dict(kernel="split", n_tiles8=1, warps=16, chunk=11008, n_ctas=144, n_rows=56)]
-    assert ws > 0 and pre == 0
+    assert ws > 0
 
 
 def test_long_caches_one_call_each():
     """Per cache, as the per-cache variant of the bench launches them: the
     main cache fills the 152 SMs with 19 splits, the draft 148 with 37."""
     _, calls = calls_of("long", fused=False)
-    main, _, _ = plan(calls[:1])
-    draft, _, _ = plan(calls[1:])
+    main, _ = plan(calls[:1])
+    draft, _ = plan(calls[1:])
     assert (main[0]["warps"], main[0]["n_ctas"], main[0]["n_rows"]) == (16, 152, 40)
     assert (draft[0]["warps"], draft[0]["n_ctas"], draft[0]["n_rows"]) == (16, 148, 16)
 
@@ -98,7 +98,7 @@ def test_batched_takes_the_8_warp_form():
     """64 sequences x 8 kv heads need more than one wave of 16-warp CTAs, so
     the 8-warp form (two per SM) runs, with chunks in its 128-position granule."""
     specs, calls = calls_of("batched", fused=True)
-    lns, _, _ = plan(calls)
+    lns, _ = plan(calls)
     assert len(lns) == 1
     ln = lns[0]
     assert ln["kernel"] == "split" and ln["n_tiles8"] == 1 and ln["warps"] == 8
@@ -130,27 +130,22 @@ def test_single_and_tiny():
     """single: 16 splits of 512 positions (128 CTAs, the best of the chunk
     sweep); tiny: one split, so no combine launch and no workspace."""
     _, calls = calls_of("single", fused=True)
-    lns, ws, _ = plan(calls)
+    lns, ws = plan(calls)
     assert lns == [dict(kernel="split", n_tiles8=1, warps=16, chunk=512, n_ctas=128, n_rows=32)]
     _, calls = calls_of("tiny", fused=True)
-    lns, ws, _ = plan(calls)
+    lns, ws = plan(calls)
     assert len(lns) == 1 and lns[0]["n_ctas"] == 1 and lns[0]["n_rows"] == 0 and ws == 0
 
 
 def test_verify_shape(monkeypatch):
     """32 query rows per kv head: the 32-row tiles by default; KVQ_ROW_TILE=16
-    doubles the CTAs with 16-row tiles; KVQ_VERIFY=1 takes the tcgen05 verify
-    kernel, whose step tokens then go through a separate append launch."""
+    doubles the CTAs with 16-row tiles."""
     specs, calls = calls_of("verify", fused=True)
     ln = plan(calls)[0][0]
     assert (ln["kernel"], ln["n_tiles8"], ln["warps"]) == ("split", 4, 4)
     monkeypatch.setenv("KVQ_ROW_TILE", "16")
     ln16 = plan(calls)[0][0]
     assert (ln16["n_tiles8"], ln16["warps"]) == (2, 4)
-    monkeypatch.delenv("KVQ_ROW_TILE")
-    monkeypatch.setenv("KVQ_VERIFY", "1")
-    lns, _, pre = plan(calls)
-    assert lns[0]["kernel"] == "verify" and lns[0]["warps"] == 0 and pre == 1
 
 
 def test_prefill_chunk(monkeypatch):
@@ -158,7 +153,7 @@ def test_prefill_chunk(monkeypatch):
     kernel, one split on 128 CTAs (the best of the split sweep); KVQ_PREFILL=0
     sends it to the split kernel's 32-row tiles."""
     _, calls = calls_of("prefill", fused=False)
-    lns, ws, _ = plan(calls)
+    lns, ws = plan(calls)
     assert len(lns) == 1 and lns[0]["kernel"] == "prefill" and lns[0]["n_ctas"] == 128
     assert lns[0]["n_rows"] == 0 and ws == 0
     monkeypatch.setenv("KVQ_PREFILL", "0")
@@ -183,7 +178,7 @@ def test_workspace_is_the_split_partials():
     row's per-split partial output and lse (128 + 1 floats), each unit's block
     rounded up to 256 bytes."""
     specs, calls = calls_of("long", fused=True)
-    lns, ws, _ = plan(calls)
+    lns, ws = plan(calls)
     n_split = -(-131072 // lns[0]["chunk"])
     want = sum(-(-(s.n_seqs * s.t_q * s.n_q_heads * n_split * 129 * 4) // 256) * 256 for s in specs)
     assert ws == want
@@ -194,7 +189,7 @@ def test_more_than_64_sequences_take_several_launches():
     as a launch of 64 and one of 36, each planned on its own (the second fits
     one wave of 8-warp CTAs unsplit, so it needs no combine)."""
     specs, calls = calls_of("batched", fused=True, ctx=4096, n_seqs=100)
-    lns, _, _ = plan(calls)
+    lns, _ = plan(calls)
     H, Hq = specs[0].n_kv_heads, specs[0].n_q_heads
     assert len(lns) == 2 and all(ln["kernel"] == "split" for ln in lns)
     for ln, nb in zip(lns, (64, 36)):
@@ -208,5 +203,5 @@ def test_f16k_pair_without_fused_append():
     """F16 K decodes on the same split kernel (its own K format) once the
     step's tokens went in through kvq_append: one launch for both caches."""
     _, calls = calls_of("long_f16k", fused=False)
-    lns, _, pre = plan(calls)
-    assert len(lns) == 1 and lns[0]["kernel"] == "split" and lns[0]["n_rows"] == 56 and pre == 0
+    lns, _ = plan(calls)
+    assert len(lns) == 1 and lns[0]["kernel"] == "split" and lns[0]["n_rows"] == 56
