@@ -42,6 +42,7 @@ L2_BYTES = 129 * 1024 * 1024
 SPREAD_MIN_REPLAYS = 5      # replays behind the step-time spread
 SPREAD_MAX_REPLAYS = 4000
 SPREAD_SECONDS = 1.0        # length of the spread pass (clock samples every 100 ms)
+PRE_SLEEP_CYCLES = 4_000_000   # ~2 ms at 2 GHz, untimed, ahead of the timed region
 
 WORKLOADS = {
     "long": "long-context decode: main 40q/8kv heads + draft 16q/4kv heads, 131072 positions each "
@@ -473,6 +474,10 @@ def main():
     with ClockSampler(local) as clk:
         t_region = time.perf_counter()
         with torch.cuda.stream(stream):
+            # a short device-side sleep ahead of the start event keeps the
+            # GPU busy while the host enqueues the replays, so the timed
+            # region holds the K steps and not the host's launch latency
+            torch.cuda._sleep(PRE_SLEEP_CYCLES)
             e0.record(stream)
             for i in range(reps):
                 g_all.replay()

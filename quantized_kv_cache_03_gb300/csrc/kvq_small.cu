@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
     const float *ls = G.ws_lse + (size_t)row * n;
     const float4 *o = reinterpret_cast<const float4 *>(G.ws_o + (size_t)row * n * kD) + lane;
     float m = -INFINITY, W = 0.f;
+    bool poisoned = false;   // a split wrote NaN (its CTA lost a copy stage)
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = warp; s0 < n; s0 += 4 * kCombineWarps) {
         float lv[4];
@@ -86,6 +87,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
             const int s = s0 + k * kCombineWarps;
             lv[k] = (s < n) ? ls[s] : -INFINITY;
             v[k] = (s < n) ? o[(size_t)s * (kD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+            poisoned |= lv[k] != lv[k];
         }
         const float mx = fmaxf(fmaxf(m, fmaxf(lv[0], lv[1])), fmaxf(lv[2], lv[3]));
         if (mx == -INFINITY) continue;
@@ -104,6 +106,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
             }
         }
         m = mx;
+    }
+    if (poisoned) {   // m = +inf and W = NaN make the merged row NaN
+        m = INFINITY;
+        W = __int_as_float(0x7fc00000);
     }
     if (lane == 0) {
         sm_m[warp] = m;

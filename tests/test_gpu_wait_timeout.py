@@ -47,12 +47,16 @@ def test_a_lost_stage_gives_up_poisons_its_rows_and_counts(monkeypatch):
     lse = torch.zeros((1, 1, case.Hq), dtype=torch.float32, device=dev())
     n = kvq.kvq_decode_workspace_size(case.cache, case.Hq, 1, case.max_len)
     ws = torch.empty(n, dtype=torch.uint8, device=dev())
-    kvq.kvq_debug_lose_stage(case.cache, to_dev(case.q), case.Hq, 1, False, lens, case.max_len, None, SM_SCALE,
-                             out, lse, ws)
-    torch.cuda.synchronize()
-    count = ctypes.c_uint32(0)
-    st = kvq.load().kvq_wait_timeouts(ctypes.byref(count))
-    assert st == kvq.KVQ_ERR_TIMEOUT and count.value == 1, "status %d, count %d" % (st, count.value)
+    try:
+        kvq.kvq_debug_lose_stage(case.cache, to_dev(case.q), case.Hq, 1, False, lens, case.max_len, None,
+                                 SM_SCALE, out, lse, ws)
+        torch.cuda.synchronize()
+        count = ctypes.c_uint32(0)
+        st = kvq.load().kvq_wait_timeouts(ctypes.byref(count))
+        assert st == kvq.KVQ_ERR_TIMEOUT and count.value == 1, "status %d, count %d" % (st, count.value)
+    finally:
+        torch.cuda.synchronize()
+        kvq.kvq_reset_wait_timeouts()
     o, l = out.cpu().numpy()[0, 0], lse.cpu().numpy()[0, 0]
     group = case.Hq // spec.n_kv_heads
     lost = np.arange(case.Hq) < group                  # the query heads of kv head 0
