@@ -75,6 +75,9 @@ def parse():
     ap.add_argument("--mode", default="bench", choices=["bench", "profile"],
                     help="profile: one cache copy, a few directly launched steps, no timing (for ncu)")
     ap.add_argument("--ctx", type=int, default=None, help="shrink the workload's context (profile mode)")
+    ap.add_argument("--layout", default="auto", choices=["auto", "tiles", "rows"],
+                    help="segment layouts: auto = kvq_choose_layout per segment (the library's cost model), "
+                         "or every segment in tiles / rows")
     return ap.parse_args()
 
 
@@ -353,8 +356,9 @@ def main():
     # the step's appends run inside the attention kernel when every cache
     # takes at most KVQ_MAX_T_Q_APPEND tokens per step; else kvq_append first
     fusable = all(s.t_q <= kvq.MAX_T_Q_APPEND and s.k_type == W.K_I8 for s in specs)
+    layout = {"auto": "auto", "tiles": kvq.LAYOUT_TILES, "rows": kvq.LAYOUT_ROWS}[args.layout]
     if args.mode == "profile":
-        grp = [DecodeSet(d, dev) for d in data]
+        grp = [DecodeSet(d, dev, layout=layout) for d in data]
         for ds in grp:
             ds.staging = None
         fused = StepSet(grp, append=fusable)
@@ -373,8 +377,8 @@ def main():
         return
     n_rot = max(3, -(-3 * L2_BYTES // max(1, kv_bytes)))
     n_rot = min(n_rot, 64)
-    first = [DecodeSet(d, dev) for d in data]
-    sets = [first] + [[DecodeSet(d, dev, staging=f.staging) for d, f in zip(data, first)]
+    first = [DecodeSet(d, dev, layout=layout) for d in data]
+    sets = [first] + [[DecodeSet(d, dev, staging=f.staging, layout=layout) for d, f in zip(data, first)]
                       for _ in range(n_rot - 1)]
     for f in first:
         f.staging = None
@@ -637,6 +641,10 @@ def main():
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8+fp32", "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload], "parallelism": "replicas" if world > 1 else "single",
+                   "segment_layout": args.layout if args.layout != "auto" else
+                   "auto: kvq_choose_layout per segment -> " + "/".join(sorted({
+                       {kvq.LAYOUT_TILES: "tiles", kvq.LAYOUT_ROWS: "rows"}[ds.cache.seg(b, k).layout]
+                       for grp in sets for ds in grp for b in range(ds.B) for k in range(ds.cache.n_segs(b))})),
                    "l2": "rotating %d independent cache copies (%.0f MB each, L2 129 MB); CUDA-graph replays"
                          " of %d steps" % (n_rot, kv_bytes / 1e6, per_replay),
                    "timed": "%d replays of a %d-step graph + a %d-step graph; warm-up: %d steps in a graph after"

@@ -86,9 +86,35 @@ typedef enum kvq_ktype {
 } kvq_ktype;
 
 /*
+ * Segment layout (the stride-1 axis and packing of a segment's code bytes,
+ * chosen per segment: BitLLM summary, "How it works" and "What differs", where
+ * a layout is picked per sequence length by a cost model and a new layout only
+ * ever applies to a new append-only segment).
+ *   KVQ_LAYOUT_TILES  16-token tiles with the code bytes permuted into the
+ *                     order the attention kernel's MMA lanes read them (see
+ *                     "Tiles" below).  Every fragment read is one
+ *                     conflict-free 16-byte load; a tile is the unit of every
+ *                     copy, so a segment's last partly filled tile is read
+ *                     whole.  The default.
+ *   KVQ_LAYOUT_ROWS   one row per token in element order: K row j = code of
+ *                     element j, q4_0 V row = the 32-blocks' 16 bytes in the
+ *                     usual q4_0 order, q8_0 V row = codes in element order
+ *                     (the order of the row sizes below).  Copies move exactly
+ *                     the filled rows; the kernel then permutes each staged
+ *                     tile into the tile order in shared memory (extra unpack
+ *                     instructions).  int8 K only.
+ * kvq_layout_cost / kvq_choose_layout weigh the two per segment.
+ */
+typedef enum kvq_layout {
+    KVQ_LAYOUT_TILES = 0,
+    KVQ_LAYOUT_ROWS = 1
+} kvq_layout;
+
+/*
  * One append-only segment of one sequence.  All four arrays are device memory,
  * 16-byte aligned and head-major: kv head h owns cap token rows starting at row
- * h*cap, and token t of the segment is row t of its head.  Row sizes:
+ * h*cap, and token t of the segment is row t of its head.  Row sizes (and, for
+ * KVQ_LAYOUT_ROWS, the byte order of each row):
  *   k_q  int8 codes, head_dim bytes per row (F16 K: fp16 values, 2*head_dim
  *        bytes per row)
  *   k_s  fp16 scales, head_dim/32 per row, plain [kv_head][token][block] order
@@ -110,7 +136,9 @@ typedef enum kvq_ktype {
  * and for F16 K, with j the element (not byte) of the row, the fp16 value of
  * element j of token u sits at byte offset (a 4096-byte tile)
  *   k_q f16   (j/16)*512 + (4*(u%8) + (j%8)/2)*16 + 4*(u/8 + 2*((j%16)/8)) + 2*(j%2)
- * (head_dim 128).  Only kvq_append writes code bytes, so callers never see the
+ * (head_dim 128), for segments of KVQ_LAYOUT_TILES.  Segments of
+ * KVQ_LAYOUT_ROWS keep every row in the element order above.  Only kvq_append
+ * and the fused append write code bytes, so callers never see the
  * permutation unless they read the arrays themselves.
  * cap  : capacity in tokens, a positive multiple of KVQ_SEG_ALIGN.
  * len  : tokens filled, 0..cap (host bookkeeping; kvq_append advances it).
@@ -118,6 +146,8 @@ typedef enum kvq_ktype {
  *        must start where segment k ends: pos0[k+1] == pos0[k] + len[k]; the
  *        first segment starts at 0.  Only the last segment of a sequence is
  *        open for appends.
+ * layout: kvq_layout of this segment's code bytes (0 = KVQ_LAYOUT_TILES); the
+ *        segments of one sequence may differ.
  */
 typedef struct kvq_segment {
     void *k_q;
@@ -127,7 +157,7 @@ typedef struct kvq_segment {
     int32_t cap;
     int32_t len;
     int32_t pos0;
-    int32_t reserved;
+    int32_t layout;
 } kvq_segment;
 
 /*
@@ -325,6 +355,50 @@ kvq_status kvq_wait_timeouts(uint32_t *count);
  * no counterpart.
  */
 kvq_status kvq_reset_wait_timeouts(void);
+
+/*
+ * Per-segment layout cost model (BitLLM summary, "How it works": a layout is
+ * scored as alpha1 * Bytes / BW + alpha2 * UnpackOps, both weights fitted once
+ * per GPU by a microbenchmark; "What differs": the layout is chosen by the
+ * expected length, a new layout only for a new segment).  The library's
+ * terms for one kv head of a segment of n tokens read by the attention kernel:
+ *   Bytes      KVQ_LAYOUT_TILES: whole 16-token tiles, ceil(n/16)*16 rows;
+ *              KVQ_LAYOUT_ROWS: n code rows plus the scale rows rounded up
+ *              to a pair (a row: 128 K bytes + 64 (q4_0) or 128 (q8_0) V
+ *              bytes + 16 bytes of scales);
+ *   UnpackOps  tiles: 0; rows: ops_rows_per_tile per staged tile (the
+ *              in-shared-memory permute into the tile order).
+ * cost = us_per_byte * Bytes + us_per_op * UnpackOps, in microseconds; the
+ * layout-independent work (the same number of tiles computed either way) is
+ * left out.  kvq_layout_model_default() gives the coefficients fitted on a
+ * GB300 (layout_calib.py beside the package; its record layout_model.json
+ * holds every measured point).  On that GPU the tiles cost less at every
+ * segment length.
+ */
+typedef struct kvq_layout_model {
+    double us_per_byte;         /* time per HBM byte moved by the copies    */
+    double us_per_op;           /* time per unpack warp-instruction         */
+    double ops_rows_per_tile;   /* rows-layout unpack instructions per tile */
+} kvq_layout_model;
+
+/* The fitted GB300 coefficients.  m: host out. */
+kvq_status kvq_layout_model_default(kvq_layout_model *m);
+
+/*
+ * kvq_layout_cost -- modelled cost (us) of one attention pass over one kv head
+ * of a segment of n_tokens (>= 1) tokens in `layout` with V format v_type,
+ * under model m (NULL: the default).  cost_us: host out.
+ */
+kvq_status kvq_layout_cost(int32_t layout, int32_t v_type, int32_t n_tokens, const kvq_layout_model *m,
+                           double *cost_us);
+
+/*
+ * kvq_choose_layout -- the layout of lower modelled cost for a new segment
+ * expected to hold n_tokens tokens (ties and int8-K-only rules: F16 K and
+ * ties give KVQ_LAYOUT_TILES).  layout: host out.
+ */
+kvq_status kvq_choose_layout(int32_t k_type, int32_t v_type, int32_t n_tokens, const kvq_layout_model *m,
+                             int32_t *layout);
 
 /* Short English text of a status code (static storage). */
 const char *kvq_status_string(kvq_status s);

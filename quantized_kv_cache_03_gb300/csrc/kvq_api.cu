@@ -121,6 +121,8 @@ kvq_status check_cache(const kvq_cache *c)
             if (!aligned16(s.k_q) || !aligned16(s.k_s) || !aligned16(s.v_q) || !aligned16(s.v_s))
                 return KVQ_ERR_INVALID_ARG;
             if (s.cap <= 0 || s.cap % KVQ_SEG_ALIGN || s.len < 0 || s.len > s.cap) return KVQ_ERR_INVALID_ARG;
+            if (s.layout != KVQ_LAYOUT_TILES && s.layout != KVQ_LAYOUT_ROWS) return KVQ_ERR_INVALID_ARG;
+            if (s.layout == KVQ_LAYOUT_ROWS && f16k) return KVQ_ERR_UNSUPPORTED;   // rows layout: int8 K only
             const long long expect = k == 0 ? 0 : (long long)seg_of(c, b, k - 1).pos0 + seg_of(c, b, k - 1).len;
             if (s.pos0 != expect) return KVQ_ERR_INVALID_ARG;
             if ((long long)s.pos0 + s.cap > 0x7fffffffLL) return KVQ_ERR_INVALID_ARG;
@@ -144,6 +146,7 @@ struct Desc {
     const uint16_t *k_new, *v_new;   // fused append of t_q tokens per sequence, or null
     std::vector<int> kv;   // query head -> kv head
     int max_rows;          // query rows of the busiest kv head
+    bool has_rows;         // some segment of the cache keeps KVQ_LAYOUT_ROWS
 };
 
 // Validate one call's shape arguments and derive its head map.
@@ -172,6 +175,9 @@ kvq_status prepare_desc(Desc &d, const int32_t *head_map, bool need_ptrs, bool d
     int gmax = 0;
     for (int k = 0; k < H; ++k) gmax = std::max(gmax, cnt[k]);
     d.max_rows = gmax * d.t_q;   // at most 256 * 4096: row tiles of <= KVQ_MAX_ROWS
+    d.has_rows = false;
+    for (int b = 0; b < c->n_seqs; ++b)
+        for (int k = 0; k < c->n_segs[b]; ++k) d.has_rows = d.has_rows || seg_of(c, b, k).layout == KVQ_LAYOUT_ROWS;
     // F16 K: no fused append and no integer-score dump
     if (c->k_type == KVQ_K_F16 && (dump || d.k_new || d.v_new)) return KVQ_ERR_UNSUPPORTED;
     if ((d.k_new != nullptr) != (d.v_new != nullptr)) return KVQ_ERR_INVALID_ARG;
@@ -204,14 +210,15 @@ int tiles8_for(int rows)
 }
 
 
-// Calls with long query chunks go to the tcgen05 kernel unless KVQ_PREFILL=0.
-// The score dump takes the same route, so it tests the kernel the decode
-// call runs.
+// Calls with long query chunks go to the tcgen05 kernel unless KVQ_PREFILL=0
+// (it reads tile-layout segments only: caches holding a rows-layout segment
+// take the split kernel's row tiles).  The score dump takes the same route, so
+// it tests the kernel the decode call runs.
 bool prefill_kernel_for(const Desc &d)
 {
     const char *e = std::getenv("KVQ_PREFILL");
     const bool on = !(e && e[0] == '0');
-    return on && !d.k_new && d.c->k_type == KVQ_K_I8 && d.max_rows > KVQ_MAX_ROWS;
+    return on && !d.k_new && !d.has_rows && d.c->k_type == KVQ_K_I8 && d.max_rows > KVQ_MAX_ROWS;
 }
 int round_up(long long x, int m) { return (int)((x + m - 1) / m * m); }
 
@@ -479,6 +486,7 @@ void fill_launch(const std::vector<Desc> &ds, const Launch &ln, bool dump, void 
                 p.seg[nseg].vs = static_cast<const uint16_t *>(s.v_s);
                 p.seg[nseg].pos0 = s.pos0;
                 p.seg[nseg].cap = s.cap;
+                p.seg[nseg].layout = s.layout;
             }
         }
     }
@@ -631,6 +639,7 @@ kvq_status kvq_append(kvq_cache *c, int32_t n_seqs_in, const int32_t *seq_ids, c
                 e.dst = sg.len;
                 e.src = src;
                 e.n = n_new[i];
+                e.layout = sg.layout;
                 max_rows = std::max(max_rows, n_new[i] * c->n_kv_heads);
             }
             src += n_new[i];
@@ -829,6 +838,53 @@ extern "C" kvq_status kvq_reset_wait_timeouts(void)
         cudaGetLastError();
         return KVQ_ERR_CUDA;
     }
+    return KVQ_OK;
+}
+
+// Coefficients fitted by layout_calib.py on a GB300 (its record
+// layout_model.json: 256 kv heads x 60 segments of n tokens, n = 1..32, both
+// layouts, least squares of the measured decode times on bytes and unpack
+// instructions; the rows permute counted with ncu on the long-context step).
+static const kvq_layout_model kDefaultLayoutModel = {8.150755150671073e-08, 2.771975819748976e-06, 134.36};
+
+extern "C" kvq_status kvq_layout_model_default(kvq_layout_model *m)
+{
+    if (!m) return KVQ_ERR_INVALID_ARG;
+    *m = kDefaultLayoutModel;
+    return KVQ_OK;
+}
+
+extern "C" kvq_status kvq_layout_cost(int32_t layout, int32_t v_type, int32_t n_tokens, const kvq_layout_model *m,
+                                      double *cost_us)
+{
+    if (!cost_us || n_tokens < 1 || (layout != KVQ_LAYOUT_TILES && layout != KVQ_LAYOUT_ROWS) ||
+        (v_type != KVQ_V_Q4_0 && v_type != KVQ_V_Q8_0))
+        return KVQ_ERR_INVALID_ARG;
+    const kvq_layout_model &mm = m ? *m : kDefaultLayoutModel;
+    const double code = kD + (v_type == KVQ_V_Q4_0 ? kD / 2 : kD), scales = 2 * kNB * 2;   // bytes per row
+    const double tiles = (double)((n_tokens + kWTile - 1) / kWTile);
+    double bytes, ops;
+    if (layout == KVQ_LAYOUT_TILES) {
+        bytes = tiles * kWTile * (code + scales);
+        ops = 0.0;
+    } else {
+        bytes = n_tokens * code + (double)(n_tokens + (n_tokens & 1)) * scales;
+        ops = tiles * mm.ops_rows_per_tile;
+    }
+    *cost_us = mm.us_per_byte * bytes + mm.us_per_op * ops;
+    return KVQ_OK;
+}
+
+extern "C" kvq_status kvq_choose_layout(int32_t k_type, int32_t v_type, int32_t n_tokens, const kvq_layout_model *m,
+                                        int32_t *layout)
+{
+    if (!layout || (k_type != KVQ_K_I8 && k_type != KVQ_K_F16)) return KVQ_ERR_INVALID_ARG;
+    double ct = 0.0, cr = 0.0;
+    kvq_status st = kvq_layout_cost(KVQ_LAYOUT_TILES, v_type, n_tokens, m, &ct);
+    if (st != KVQ_OK) return st;
+    st = kvq_layout_cost(KVQ_LAYOUT_ROWS, v_type, n_tokens, m, &cr);
+    if (st != KVQ_OK) return st;
+    *layout = (k_type == KVQ_K_I8 && cr < ct) ? KVQ_LAYOUT_ROWS : KVQ_LAYOUT_TILES;
     return KVQ_OK;
 }
 

@@ -143,6 +143,22 @@ __device__ __forceinline__ void tile_issue(const Walk &w, int n, uint32_t dst, u
     bulk_g2s(dst + C::VS_OFF, w.gvs, n * C::TILE_S, bar);
 }
 
+// The same for a KVQ_LAYOUT_ROWS segment: only the rows [ra, rb) of the n
+// tiles (relative to the first tile's token 0) that the piece covers, at their
+// places in the slot; scale rows are copied in pairs (16-byte granules).  The
+// other rows of the slot keep stale bytes, which the masks never let through.
+template <int NT, int VT, int KT>
+__device__ __forceinline__ void rows_issue(const Walk &w, int ra, int rb, uint32_t dst, uint32_t bar)
+{
+    using C = SplitCfg<NT, VT, KT>;
+    const int sa = ra & ~1, sb = (rb + 1) & ~1;
+    mbar_arrive_expect_tx(bar, (rb - ra) * (C::KCODE + C::VCODE) + (sb - sa) * 2 * kNB * 2);
+    bulk_g2s(dst + C::K_OFF + ra * C::KCODE, w.gk + ra * C::KCODE, (rb - ra) * C::KCODE, bar);
+    bulk_g2s(dst + C::KS_OFF + sa * kNB * 2, w.gks + sa * kNB * 2, (sb - sa) * kNB * 2, bar);
+    bulk_g2s(dst + C::V_OFF + ra * C::VCODE, w.gv + ra * C::VCODE, (rb - ra) * C::VCODE, bar);
+    bulk_g2s(dst + C::VS_OFF + sa * kNB * 2, w.gvs + sa * kNB * 2, (sb - sa) * kNB * 2, bar);
+}
+
 // Head-dim index of accumulator row rho (0..15) of PV m-tile mt = 2*block + h2.
 template <int VT>
 __device__ __forceinline__ int pv_dim(int mt, int rho)
@@ -324,9 +340,12 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT, KT, W>::THREADS, SplitCfg<NT,
         if (lane == 0) {
             const int tb = pw.T * kWTile;
             tile_rec[slot] = make_int4(tb, pw.la, pw.le, pw.pos0 + tb);
-            stage_n[slot] = n;
+            stage_n[slot] = n | (pw.rows << 8);
             if (loser && issued == kLostStage)
                 mbar_arrive_expect_tx(bar_s + slot * 8, n * C::TILE);   // bytes that never come
+            else if (pw.rows)   // rows layout: the piece's rows of these tiles only
+                rows_issue<NT, VT, KT>(pw, max(pw.la, tb) - tb, min(pw.le, tb + n * kWTile) - tb,
+                                       ring_s + slot * C::STAGE, bar_s + slot * 8);
             else
                 tile_issue<NT, VT, KT>(pw, n, ring_s + slot * C::STAGE, bar_s + slot * 8);
         }
@@ -377,7 +396,12 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT, KT, W>::THREADS, SplitCfg<NT,
             const TokenRow t = quant_token<VT>(G.k_new + src, G.v_new + src, lane);
             const int local = na0 + i - sl.pos0, u = local % kWTile;
             const size_t tile = (size_t)h * sl.cap + local - u;
-            if (app_store)
+            if (app_store && sl.layout == KVQ_LAYOUT_ROWS)
+                store_token_rows<VT>(t, lane, const_cast<uint8_t *>(sl.kq) + (tile + u) * kD,
+                                     const_cast<uint16_t *>(sl.ks) + (tile + u) * kNB,
+                                     const_cast<uint8_t *>(sl.vq) + (tile + u) * C::VCODE,
+                                     const_cast<uint16_t *>(sl.vs) + (tile + u) * kNB);
+            else if (app_store)
                 store_token<VT>(t, u, lane, const_cast<uint8_t *>(sl.kq) + tile * kD,
                                 const_cast<uint16_t *>(sl.ks) + (tile + u) * kNB,
                                 const_cast<uint8_t *>(sl.vq) + tile * C::VCODE,
@@ -519,9 +543,15 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT, KT, W>::THREADS, SplitCfg<NT,
             if (lane == 0) fence_proxy_async_smem();
             issue(prev);
         }
-        const int ns = stage_n[slot];
+        const int ns = stage_n[slot] & 0xff;
         const uint8_t *stg = ring + slot * C::STAGE;
         const int4 rec0 = tile_rec[slot];
+        if (KT == KVQ_K_I8 && (stage_n[slot] >> 8)) {   // rows layout: permute the staged tiles into the tile order
+            for (int t = 0; t < ns; ++t) {
+                rows_to_tile_k(const_cast<uint8_t *>(stg) + C::K_OFF + t * C::TILE_K, lane);
+                rows_to_tile_v<VT>(const_cast<uint8_t *>(stg) + C::V_OFF + t * C::TILE_V, lane);
+            }
+        }
         prev = slot;
         if (++slot == S) {
             slot = 0;

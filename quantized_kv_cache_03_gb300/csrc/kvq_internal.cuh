@@ -84,6 +84,7 @@ struct SegDesc {
     const uint16_t *vs;   // [Hkv][cap][kNB]
     int pos0;             // absolute position of token 0
     int cap;              // tokens, multiple of KVQ_SEG_ALIGN
+    int layout;           // kvq_layout of the code bytes
 };
 
 // One work group of a split launch: sequences [b0, b0 + n_seqs) of one cache
@@ -153,6 +154,7 @@ struct AppendEntry {
     int dst;                               // first token slot written
     int src;                               // first input token row
     int n;                                 // tokens
+    int layout;                            // kvq_layout of the segment
 };
 
 struct AppendParams {
@@ -254,6 +256,7 @@ struct Walk {
     int T, Tend;      // next tile inside the segment, end tile (exclusive) of the piece
     int la, le;       // local range [la, le) of the current piece
     int pos0;
+    int rows;         // the segment keeps KVQ_LAYOUT_ROWS (rows in element order)
     const uint8_t *gk, *gks, *gv, *gvs;
 };
 
@@ -270,6 +273,7 @@ __device__ __forceinline__ void walk_seek(const AttnParams &p, int seg0, int nse
             w.T = w.la / kWTile;
             w.Tend = (w.le + kWTile - 1) / kWTile;
             w.pos0 = s.pos0;
+            w.rows = s.layout == KVQ_LAYOUT_ROWS;
             const size_t row = (size_t)h * s.cap + (size_t)w.T * kWTile;
             w.gk = reinterpret_cast<const uint8_t *>(s.kq) + row * kcode;
             w.gks = reinterpret_cast<const uint8_t *>(s.ks) + row * kNB * 2;
@@ -485,6 +489,81 @@ __device__ __forceinline__ void store_token(const TokenRow &t, int u, int lane, 
         *reinterpret_cast<uint16_t *>(vt + v4_tile_off(u, j + 2)) = (uint16_t)(t.vw >> 16);
     }
     if ((lane & 7) == 0) vsr[lane >> 3] = t.vs;
+}
+
+// The same row stored in KVQ_LAYOUT_ROWS order (global memory): kr, vr point
+// at the token's K and V code rows, ksr / vsr at its scale rows.
+template <int VT>
+__device__ __forceinline__ void store_token_rows(const TokenRow &t, int lane, uint8_t *kr, uint16_t *ksr, uint8_t *vr,
+                                                 uint16_t *vsr)
+{
+    *reinterpret_cast<uint32_t *>(kr + 4 * lane) = t.kw;
+    if ((lane & 7) == 0) ksr[lane >> 3] = t.ks;
+    if (VT == KVQ_V_Q8_0) {
+        *reinterpret_cast<uint32_t *>(vr + 4 * lane) = t.vw;
+    } else if ((lane & 7) < 4) {   // bytes 4(l%4)..+3 of block l/8
+        *reinterpret_cast<uint32_t *>(vr + 16 * (lane >> 3) + 4 * (lane & 3)) = t.vw;
+    }
+    if ((lane & 7) == 0) vsr[lane >> 3] = t.vs;
+}
+
+// ---- a staged tile of a KVQ_LAYOUT_ROWS segment -> the tile order ----
+// One warp permutes a tile's code bytes in shared memory in place: every lane
+// loads its 16-byte pieces of the row-order tile, the warp synchronizes, and
+// the lanes store them at their tile-order offsets (8-byte runs for K, 2-byte
+// runs for q4_0; for q8_0 the bytes of tokens 2i and 2i + 1 interleave, so a
+// lane pairs the same 4 bytes of both rows into one 8-byte run).
+static __device__ __noinline__ void rows_to_tile_k(uint8_t *t, int lane)
+{
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = *reinterpret_cast<const uint4 *>(t + (lane + 32 * k) * 16);
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int q = lane + 32 * k, u = q >> 3, j = (q & 7) * 16;   // token u, bytes j..j+15 of its row
+        *reinterpret_cast<uint2 *>(t + k_tile_off(u, j)) = make_uint2(v[k].x, v[k].y);
+        *reinterpret_cast<uint2 *>(t + k_tile_off(u, j + 8)) = make_uint2(v[k].z, v[k].w);
+    }
+    __syncwarp();
+}
+
+template <int VT>
+__device__ __noinline__ void rows_to_tile_v(uint8_t *t, int lane)
+{
+    if (VT == KVQ_V_Q4_0) {
+        uint4 v[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) v[k] = *reinterpret_cast<const uint4 *>(t + (lane + 32 * k) * 16);
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int q = lane + 32 * k, u = q >> 2, bb = q & 3;   // token u, block bb (16 bytes)
+            const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e)   // bytes 2e, 2e + 1 of the block
+                *reinterpret_cast<uint16_t *>(t + v4_tile_off(u, 16 * bb + 2 * e)) = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
+        }
+    } else {
+        uint4 a[2], b[2];   // the same 16 bytes of tokens 2p and 2p + 1
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int q = lane + 32 * k, p = q >> 3, c16 = q & 7;
+            a[k] = *reinterpret_cast<const uint4 *>(t + (2 * p) * kD + 16 * c16);
+            b[k] = *reinterpret_cast<const uint4 *>(t + (2 * p + 1) * kD + 16 * c16);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int q = lane + 32 * k, p = q >> 3, c16 = q & 7;
+            const uint32_t wa[4] = {a[k].x, a[k].y, a[k].z, a[k].w}, wb[4] = {b[k].x, b[k].y, b[k].z, b[k].w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w)   // bytes j..j+3 of both rows, interleaved token by token
+                *reinterpret_cast<uint2 *>(t + v8_tile_off(2 * p, 16 * c16 + 4 * w)) =
+                    make_uint2(__byte_perm(wa[w], wb[w], 0x5140), __byte_perm(wa[w], wb[w], 0x7362));
+        }
+    }
+    __syncwarp();
 }
 
 }  // namespace kvq

@@ -12,6 +12,8 @@ namespace kvq {
 // them as two byte pairs; q8_0 codes are stored byte by byte (the tile
 // interleaves neighbouring positions).  F16 K (KT = KVQ_K_F16): the lane's four
 // fp16 K values go to their places in the 4096-byte tile as two 32-bit pairs.
+// Segments of KVQ_LAYOUT_ROWS get the token's rows in element order instead
+// (store_token_rows: one 32-bit word per lane and array).
 // ---------------------------------------------------------------------------
 template <int VT, int KT>
 __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ AppendParams p)
@@ -28,8 +30,13 @@ __global__ void __launch_bounds__(128) append_kernel(const __grid_constant__ App
     const int u = (e.dst + tok) % kWTile;                      // position in its tile
     const size_t tile = (size_t)h * e.cap + e.dst + tok - u;    // first row of the tile
     const TokenRow t = quant_token<VT, KT>(p.k16 + src, p.v16 + src, lane);
-    store_token<VT, KT>(t, u, lane, e.kq + tile * kD * (KT == KVQ_K_F16 ? 2 : 1), e.ks + (tile + u) * kNB,
-                        e.vq + tile * (VT == KVQ_V_Q4_0 ? kD / 2 : kD), e.vs + (tile + u) * kNB);
+    constexpr int VCODE = VT == KVQ_V_Q4_0 ? kD / 2 : kD;
+    if (KT == KVQ_K_I8 && e.layout == KVQ_LAYOUT_ROWS)   // the token's own rows, element order
+        store_token_rows<VT>(t, lane, e.kq + (tile + u) * kD, e.ks + (tile + u) * kNB, e.vq + (tile + u) * VCODE,
+                             e.vs + (tile + u) * kNB);
+    else
+        store_token<VT, KT>(t, u, lane, e.kq + tile * kD * (KT == KVQ_K_F16 ? 2 : 1), e.ks + (tile + u) * kNB,
+                            e.vq + tile * VCODE, e.vs + (tile + u) * kNB);
 }
 
 cudaError_t launch_append(const AppendParams &p, int v_type, int k_type, int max_rows, cudaStream_t s, bool pdl)

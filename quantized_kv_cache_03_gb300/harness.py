@@ -27,7 +27,7 @@ class HostData:
 
 
 class DecodeSet:
-    def __init__(self, data: HostData, device=None, staging=None):
+    def __init__(self, data: HostData, device=None, staging=None, layout="auto"):
         s = self.spec = data.spec
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
         self.B, self.tq, self.Hq = s.n_seqs, s.t_q, s.n_q_heads
@@ -46,7 +46,7 @@ class DecodeSet:
             segs = s.segments[b]
             for j, n in enumerate(segs):
                 n = int(n)
-                self.cache.add_segment(b, n)
+                self.cache.add_segment(b, n, layout)
                 nb = n - (self.tq if j == len(segs) - 1 else 0)
                 if nb > 0:
                     kvq.kvq_append(self.cache, [b], [nb], k[pos:pos + nb], v[pos:pos + nb])

@@ -27,6 +27,8 @@ V_Q4_0 = 0
 V_Q8_0 = 1
 K_I8 = 0    # K: int8 codes + fp16 scale per 32 (query quantized the same way)
 K_F16 = 1   # K: fp16 values (query unquantized)
+LAYOUT_TILES = 0   # segment code bytes in 16-token tiles, fragment order
+LAYOUT_ROWS = 1    # one row per token in element order
 HEAD_DIM = 128
 SEG_ALIGN = 64
 QBLOCK = 32
@@ -34,7 +36,7 @@ QBLOCK = 32
 EXPORTED = ("kvq_append", "kvq_decode_attn", "kvq_decode_workspace_size", "kvq_decode_attn_multi",
             "kvq_decode_multi_workspace_size", "kvq_decode_attn_noalloc", "kvq_wait_timeouts",
             "kvq_reset_wait_timeouts", "kvq_status_string", "kvq_debug_qk", "kvq_debug_lose_stage",
-            "kvq_debug_plan")
+            "kvq_debug_plan", "kvq_layout_model_default", "kvq_layout_cost", "kvq_choose_layout")
 MAX_CALLS = 16
 MAX_T_Q = 4096
 MAX_T_Q_APPEND = 8
@@ -43,7 +45,7 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 
 class KvqSegment(ctypes.Structure):
     _fields_ = [("k_q", c_void_p), ("k_s", c_void_p), ("v_q", c_void_p), ("v_s", c_void_p),
-                ("cap", c_int32), ("len", c_int32), ("pos0", c_int32), ("reserved", c_int32)]
+                ("cap", c_int32), ("len", c_int32), ("pos0", c_int32), ("layout", c_int32)]
 
 
 class KvqCache(ctypes.Structure):
@@ -57,6 +59,11 @@ class KvqDecodeDesc(ctypes.Structure):
                 ("causal_tail", c_int32), ("seq_lens", c_void_p), ("max_len", c_int32),
                 ("head_map", POINTER(c_int32)), ("sm_scale", c_float), ("out", c_void_p), ("lse", c_void_p),
                 ("k16_new", c_void_p), ("v16_new", c_void_p)]
+
+
+class KvqLayoutModel(ctypes.Structure):
+    _fields_ = [("us_per_byte", ctypes.c_double), ("us_per_op", ctypes.c_double),
+                ("ops_rows_per_tile", ctypes.c_double)]
 
 
 class KvqPlanLaunch(ctypes.Structure):
@@ -106,6 +113,13 @@ def load():
             lib.kvq_wait_timeouts.argtypes = [POINTER(ctypes.c_uint32)]
             lib.kvq_reset_wait_timeouts.restype = c_int32
             lib.kvq_reset_wait_timeouts.argtypes = []
+            lib.kvq_layout_model_default.restype = c_int32
+            lib.kvq_layout_model_default.argtypes = [POINTER(KvqLayoutModel)]
+            lib.kvq_layout_cost.restype = c_int32
+            lib.kvq_layout_cost.argtypes = [c_int32, c_int32, c_int32, POINTER(KvqLayoutModel),
+                                            POINTER(ctypes.c_double)]
+            lib.kvq_choose_layout.restype = c_int32
+            lib.kvq_choose_layout.argtypes = [c_int32, c_int32, c_int32, POINTER(KvqLayoutModel), POINTER(c_int32)]
             lib.kvq_debug_lose_stage.restype = c_int32
             lib.kvq_debug_lose_stage.argtypes = lib.kvq_decode_attn.argtypes
             lib.kvq_debug_qk.restype = c_int32
@@ -164,8 +178,12 @@ class Cache:
     def n_segs(self, b: int) -> int:
         return self._nsegs[b]
 
-    def add_segment(self, b: int, cap: int):
-        """Open a new segment of `cap` tokens (rounded up to 64) for sequence b."""
+    def add_segment(self, b: int, cap: int, layout=LAYOUT_TILES):
+        """Open a new segment of `cap` tokens (rounded up to 64) for sequence b,
+        its code bytes in `layout` (LAYOUT_TILES, LAYOUT_ROWS, or "auto": the
+        layout kvq_choose_layout picks for `cap` expected tokens)."""
+        if layout == "auto":
+            layout = choose_layout(self.k_type, self.v_type, max(1, int(cap)))
         ns = self._nsegs[b]
         if ns >= self.max_segs:
             raise ValueError("sequence %d already has max_segs segments" % b)
@@ -183,7 +201,7 @@ class Cache:
             pos0 = prev.pos0 + prev.len
         s = self.seg(b, ns)
         s.k_q, s.k_s, s.v_q, s.v_s = (0 if t[n] is None else t[n].data_ptr() for n in ("k_q", "k_s", "v_q", "v_s"))
-        s.cap, s.len, s.pos0 = cap, 0, pos0
+        s.cap, s.len, s.pos0, s.layout = cap, 0, pos0, int(layout)
         self.tensors[b].append(t)
         self._nsegs[b] = ns + 1
         return t
@@ -202,8 +220,9 @@ class Cache:
         """Sequence b copied to host numpy arrays.  raw=False: the filled
         positions, [H][L][row] per array in logical row order.  raw=True: one
         dict per segment with the whole arrays as stored ([H][cap][row], code
-        bytes in their in-tile order) plus its "len".  F16 K caches give "k16"
-        (fp16 bits) instead of "kq" and "ks"."""
+        bytes in their in-tile order for tile-layout segments) plus its "len"
+        and "layout".  F16 K caches give "k16" (fp16 bits) instead of "kq" and
+        "ks"."""
         import numpy as np
         f16k = self.k_type == K_F16
         arrays = ((("k16", "k_q", np.uint16),) if f16k else (("kq", "k_q", np.uint8), ("ks", "k_s", np.uint16))) + \
@@ -212,11 +231,11 @@ class Cache:
         segs = []
         for k in range(self._nsegs[b]):
             s, t = self.seg(b, k), self.tensors[b][k]
-            seg = {"len": s.len}
+            seg = {"len": s.len, "layout": s.layout}
             for name, key, view in arrays:
                 a = t[key].cpu().numpy().view(view)
                 seg[name] = a
-                if not raw and name in ("kq", "vq", "k16"):
+                if not raw and name in ("kq", "vq", "k16") and s.layout == LAYOUT_TILES:
                     a = untile_codes(a, name, self.v_type)
                 parts[name].append(a[:, :s.len])
             segs.append(seg)
@@ -390,6 +409,35 @@ def kvq_wait_timeouts() -> int:
     if st not in (0, KVQ_ERR_TIMEOUT):
         raise KvqError(st, "kvq_wait_timeouts")
     return int(n.value)
+
+
+def layout_model_default() -> KvqLayoutModel:
+    """kvq_layout_model_default of include/kvq.h."""
+    m = KvqLayoutModel()
+    st = load().kvq_layout_model_default(ctypes.byref(m))
+    if st:
+        raise KvqError(st, "kvq_layout_model_default")
+    return m
+
+
+def layout_cost(layout: int, v_type: int, n_tokens: int, model: KvqLayoutModel | None = None) -> float:
+    """kvq_layout_cost of include/kvq.h (microseconds per kv head)."""
+    c = ctypes.c_double(0.0)
+    st = load().kvq_layout_cost(layout, v_type, n_tokens, None if model is None else ctypes.byref(model),
+                                ctypes.byref(c))
+    if st:
+        raise KvqError(st, "kvq_layout_cost")
+    return c.value
+
+
+def choose_layout(k_type: int, v_type: int, n_tokens: int, model: KvqLayoutModel | None = None) -> int:
+    """kvq_choose_layout of include/kvq.h."""
+    out = c_int32(-1)
+    st = load().kvq_choose_layout(k_type, v_type, n_tokens, None if model is None else ctypes.byref(model),
+                                  ctypes.byref(out))
+    if st:
+        raise KvqError(st, "kvq_choose_layout")
+    return out.value
 
 
 def kvq_reset_wait_timeouts() -> None:

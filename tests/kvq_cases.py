@@ -34,7 +34,9 @@ class Case:
         self.max_len = max(self.lens) if self.lens else 0
         self.cache = None
 
-    def build(self, append_step=True):
+    def build(self, append_step=True, layout_of=None):
+        """layout_of(b, k, n) -> kvq.LAYOUT_* of segment k (n tokens) of
+        sequence b (default: every segment in tiles)."""
         s = self.spec
         self.cache = kvq.Cache(self.B, s.n_kv_heads, s.v_type, max_segs=max(len(x) for x in s.segments),
                                k_type=s.k_type)
@@ -46,7 +48,7 @@ class Case:
             segs = s.segments[b]
             for j, n in enumerate(segs):
                 n = int(n)
-                self.cache.add_segment(b, n)
+                self.cache.add_segment(b, n, kvq.LAYOUT_TILES if layout_of is None else layout_of(b, j, n))
                 nb = n - (self.tq if j == len(segs) - 1 else 0)
                 if nb > 0:
                     kvq.kvq_append(self.cache, [b], [nb], to_dev(k[pos:pos + nb]), to_dev(v[pos:pos + nb]))
@@ -165,7 +167,9 @@ def export_logical(cache, b):
         n = seg["len"]
         for name in parts:
             a = seg[name]
-            if name in ("kq", "vq"):
+            if name in ("kq", "vq") and seg["layout"] == kvq.LAYOUT_ROWS:
+                a = a.view(np.uint8)                  # rows layout: element order as stored
+            elif name in ("kq", "vq"):
                 a = logical_codes(a.view(np.uint8), name, cache.v_type)
             elif name == "k16":
                 a = logical_codes(a.view(np.uint16), name, cache.v_type)

@@ -205,3 +205,31 @@ def test_f16k_pair_without_fused_append():
     _, calls = calls_of("long_f16k", fused=False)
     lns, _ = plan(calls)
     assert len(lns) == 1 and lns[0]["kernel"] == "split" and lns[0]["n_rows"] == 56
+
+
+def test_rows_segments_route_long_chunks_to_the_row_tiles():
+    """The tcgen05 prefill kernel reads tile-layout segments only: a chunk over
+    a cache with a rows-layout segment plans on the split kernel's 32-row
+    tiles; decode calls keep their plan."""
+    _, calls = calls_of("prefill", fused=False)
+    assert plan(calls)[0][0]["kernel"] == "prefill"
+    calls[0]["cache"].segs[1].layout = kvq.LAYOUT_ROWS
+    ln = plan(calls)[0][0]
+    assert (ln["kernel"], ln["n_tiles8"]) == ("split", 4)
+    _, dec = calls_of("long", fused=True)
+    before = plan(dec)
+    dec[0]["cache"].segs[2].layout = kvq.LAYOUT_ROWS
+    assert plan(dec) == before
+
+
+def test_segment_layout_is_checked():
+    _, calls = calls_of("long", fused=False)
+    calls[0]["cache"].segs[0].layout = 2
+    with pytest.raises(kvq.KvqError) as e:
+        plan(calls)
+    assert e.value.status == kvq.KVQ_ERR_INVALID_ARG
+    _, f16 = calls_of("long_f16k", fused=False)
+    f16[0]["cache"].segs[0].layout = kvq.LAYOUT_ROWS      # rows layout: int8 K only
+    with pytest.raises(kvq.KvqError) as e:
+        plan(f16)
+    assert e.value.status == kvq.KVQ_ERR_UNSUPPORTED
