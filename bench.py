@@ -567,7 +567,12 @@ def main():
     # A step's inputs (q, new K, new V of every cache) sit in one pinned host
     # buffer and go over in one H2D copy; its results (out, lse of every
     # cache) come back in one D2H copy.  Each piece starts on a 256-byte
-    # boundary (the API wants 16).
+    # boundary (the API wants 16).  The stagings are double-buffered, as a
+    # serving loop keeps them: the copies run on a second stream, so step
+    # i + 1's inputs go over and step i's results come back while the
+    # kernels run; events order every copy against the steps that write or
+    # read its buffer.  Steps rotate over the cache copies like the timed
+    # region, and the region holds every step's copies.
     grp = sets[0]
 
     def pack(tensors):
@@ -581,45 +586,78 @@ def main():
     outs = [t for ds in grp for t in (ds.out, ds.lse)]
     in_offs, in_bytes = pack(ins)
     out_offs, out_bytes = pack(outs)
-    h_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
-    for t, o in zip(ins, in_offs):
-        nb = t.numel() * t.element_size()
-        h_in[o:o + nb].copy_(t.detach().contiguous().view(-1).view(torch.uint8).cpu())
-    d_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
-    d_out = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
-    h_out = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+    NBUF = 2
+    h_in = [torch.zeros(in_bytes, dtype=torch.uint8).pin_memory() for _ in range(NBUF)]
+    for hb in h_in:
+        for t, o in zip(ins, in_offs):
+            nb = t.numel() * t.element_size()
+            hb[o:o + nb].copy_(t.detach().contiguous().view(-1).view(torch.uint8).cpu())
+    d_in = [torch.empty(in_bytes, dtype=torch.uint8, device=dev) for _ in range(NBUF)]
+    d_out = [torch.empty(out_bytes, dtype=torch.uint8, device=dev) for _ in range(NBUF)]
+    h_out = [torch.empty(out_bytes, dtype=torch.uint8).pin_memory() for _ in range(NBUF)]
 
     def view(buf, t, off):
         nb = t.numel() * t.element_size()
         return buf[off:off + nb].view(t.dtype).view(t.shape)
 
-    dv_in = [view(d_in, t, o) for t, o in zip(ins, in_offs)]
-    dv_out = [view(d_out, t, o) for t, o in zip(outs, out_offs)]
     h2d, d2h = in_bytes, out_bytes
-    kv_in = list(zip(dv_in[1::3], dv_in[2::3]))
-    e2e_call = StepSet(grp, q16=dv_in[0::3], append=fusable, kv_new=kv_in,
-                       outs=list(zip(dv_out[0::2], dv_out[1::2])))
+    e2e_calls = []   # [copy r][buffer j]
+    for r in range(n_rot):
+        row = []
+        for j in range(NBUF):
+            dv_in = [view(d_in[j], t, o) for t, o in zip(ins, in_offs)]
+            dv_out = [view(d_out[j], t, o) for t, o in zip(outs, out_offs)]
+            kv_in = list(zip(dv_in[1::3], dv_in[2::3]))
+            row.append((StepSet(sets[r], q16=dv_in[0::3], append=fusable, kv_new=kv_in,
+                                outs=list(zip(dv_out[0::2], dv_out[1::2]))), kv_in))
+        e2e_calls.append(row)
+    cs = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(NBUF)]     # inputs of the buffer's step on the device
+    ev_done = [torch.cuda.Event() for _ in range(NBUF)]   # the buffer's step finished
+    ev_out = [torch.cuda.Event() for _ in range(NBUF)]    # its results are on the host
 
-    def e2e_step():
-        d_in.copy_(h_in, non_blocking=True)
-        if not fusable:
-            for ds, (k, v) in zip(grp, kv_in):
-                ds.append_step(k_new=k, v_new=v, stream=stream)
-        e2e_call.decode(stream=stream)
-        h_out.copy_(d_out, non_blocking=True)
-        for ds in grp:
-            ds.rewind()
+    def e2e_run(n, start=None):
+        with torch.cuda.stream(cs):
+            if start is not None:
+                cs.wait_event(start)
+            d_in[0].copy_(h_in[0], non_blocking=True)
+            ev_in[0].record(cs)
+        for i in range(n):
+            j, r = i % NBUF, i % n_rot
+            fz, kv_in = e2e_calls[r][j]
+            stream.wait_event(ev_in[j])
+            if i >= NBUF:
+                stream.wait_event(ev_out[j])    # step i - 2's results have left d_out[j]
+            with torch.cuda.stream(stream):
+                if not fusable:
+                    for ds, (k, v) in zip(sets[r], kv_in):
+                        ds.append_step(k_new=k, v_new=v, stream=stream)
+                fz.decode(stream=stream)
+                ev_done[j].record(stream)
+            for ds in sets[r]:
+                ds.rewind()
+            with torch.cuda.stream(cs):
+                if i + 1 < n:
+                    jn = (i + 1) % NBUF
+                    if i >= 1:
+                        cs.wait_event(ev_done[jn])   # step i - 1 has read d_in[jn]
+                    d_in[jn].copy_(h_in[jn], non_blocking=True)
+                    ev_in[jn].record(cs)
+                cs.wait_event(ev_done[j])
+                h_out[j].copy_(d_out[j], non_blocking=True)
+                ev_out[j].record(cs)
+        stream.wait_event(ev_out[(n - 1) % NBUF])
 
+    e2e_run(6)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        for _ in range(5):
-            e2e_step()
-        stream.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(PRE_SLEEP_CYCLES)
         a.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
+    e2e_run(args.e2e_steps, start=a)
+    with torch.cuda.stream(stream):
         b.record(stream)
-        stream.synchronize()
+    torch.cuda.synchronize()
     e2e_ms = a.elapsed_time(b) / args.e2e_steps
 
     # ---- CPU baseline: the oracle on this host's cores (rank 0, N = 1 only) ----
@@ -676,7 +714,9 @@ def main():
         "per_cache_calls_ms_per_step": sep_ms_per_step,
         "append_alone_ms_per_step": app_ms_per_step,
         "e2e": {"value": tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "method": "kvq_decode_attn_multi per step (appends fused), eager launches; pinned host "
+                          "stagings double-buffered, H2D / D2H on a second stream ordered by events"},
         "gpu_launches": launches_per_step * steps,
         "clocks": dict(clk.summary(), window="timed region + the spread pass after it (%.2f s)"
                        % (clk.region_s,)),
