@@ -454,7 +454,8 @@ kvq_status kvq_debug_lose_stage(const kvq_cache *c, const void *q16, int32_t n_q
  *   i = 0  the <= 8-row kernel, 16 warps;  1  the same with 8 warps;
  *   i = 2  16-row tiles;                   3  32-row tiles.
  * It reads the calls' host descriptors and the same environment knobs as the
- * decode call (KVQ_SPLIT, KVQ_SPLIT_WARPS, KVQ_ROW_TILE, KVQ_PREFILL).  It
+ * decode call (KVQ_SPLIT, KVQ_SPLIT_WARPS, KVQ_ROW_TILE, KVQ_PREFILL,
+ * KVQ_TC_ROWS).  It
  * touches no device and dereferences no device pointer, so segments and
  * k16_new / v16_new may hold any non-null 16-byte-aligned address; q16,
  * seq_lens, out and lse may be NULL.
@@ -463,9 +464,11 @@ kvq_status kvq_debug_lose_stage(const kvq_cache *c, const void *q16, int32_t n_q
  *                   launch order (may be NULL when max_out is 0)
  *  n_out            host: launches of the plan
  *  workspace_bytes  host: what kvq_decode_multi_workspace_size would report
+ *  n_pre_appends    host: calls whose step tokens go through a separate append
+ *                   launch first (the tcgen05 kernel has no fused append)
  * Errors: the argument checks of kvq_decode_attn_multi (pointers aside), and
  * KVQ_ERR_INVALID_ARG for n_sms < 1, ctas_per_sm NULL or an entry < 1, or a
- * NULL n_out / workspace_bytes.
+ * NULL n_out / workspace_bytes / n_pre_appends.
  */
 typedef struct kvq_plan_launch {
     int32_t kernel;     /* 0 split kernel, 1 tcgen05 prefill kernel */
@@ -478,7 +481,8 @@ typedef struct kvq_plan_launch {
 
 kvq_status kvq_debug_plan(int32_t n, const kvq_decode_desc *calls, int32_t n_sms,
                           const int32_t *ctas_per_sm, kvq_plan_launch *out,
-                          int32_t max_out, int32_t *n_out, size_t *workspace_bytes);
+                          int32_t max_out, int32_t *n_out, size_t *workspace_bytes,
+                          int32_t *n_pre_appends);
 
 #ifdef __cplusplus
 }

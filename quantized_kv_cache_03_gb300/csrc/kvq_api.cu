@@ -210,15 +210,77 @@ int tiles8_for(int rows)
 }
 
 
-// Calls with long query chunks go to the tcgen05 kernel unless KVQ_PREFILL=0
-// (it reads tile-layout segments only: caches holding a rows-layout segment
-// take the split kernel's row tiles).  The score dump takes the same route, so
-// it tests the kernel the decode call runs.
-bool prefill_kernel_for(const Desc &d)
+// Query rows per kv head from which a call runs on the tcgen05 kernel (one CTA
+// per 128-row tile; a tile with fewer rows leaves the softmax warps of its
+// empty TMEM lane quarters idle): chunks of more than 32 rows.  The verify
+// shape (32 rows per kv head) measured 1007 us there against 520 us on the
+// split kernel's 32-row tiles: the tcgen05 kernel's per-tile period is set by
+// one lane quarter's softmax latency, which 32 rows do not shorten.
+// KVQ_TC_ROWS=<rows> moves the threshold; KVQ_PREFILL=0 keeps every call on
+// the split kernel.
+constexpr int kTcMinRows = KVQ_MAX_ROWS + 1;
+int tc_min_rows()
+{
+    const char *e = std::getenv("KVQ_TC_ROWS");
+    return (e && std::atoi(e) > 0) ? std::atoi(e) : kTcMinRows;
+}
+// The tcgen05 kernel reads tile-layout segments only (caches holding a
+// rows-layout segment take the split kernel's row tiles) and has no fused
+// append (a call carrying its step's tokens gets an append launch first).  The
+// score dump takes the same route, so it tests the kernel the decode call runs.
+bool tc_rows(const Desc &d)
 {
     const char *e = std::getenv("KVQ_PREFILL");
     const bool on = !(e && e[0] == '0');
-    return on && !d.k_new && !d.has_rows && d.c->k_type == KVQ_K_I8 && d.max_rows > KVQ_MAX_ROWS;
+    return on && !d.has_rows && d.c->k_type == KVQ_K_I8 && d.max_rows >= tc_min_rows();
+}
+bool prefill_kernel_for(const Desc &d) { return !d.k_new && tc_rows(d); }
+
+// The step's tokens of call d (t_q per sequence, token-major as kvq_append
+// takes them) through the append kernel, for a call whose attention runs on
+// the tcgen05 kernel.  The caller bumps the host lengths.
+cudaError_t launch_step_append(const Desc &d, cudaStream_t s, bool pdl)
+{
+    static thread_local AppendParams p;
+    const kvq_cache *c = d.c;
+    int b = 0;
+    while (b < c->n_seqs) {
+        std::memset(&p, 0, sizeof(p));
+        p.k16 = d.k_new;
+        p.v16 = d.v_new;
+        p.n_kv_heads = c->n_kv_heads;
+        while (b < c->n_seqs && p.n_entries < kMaxSeqsLaunch) {
+            const kvq_segment &sg = seg_of(c, b, c->n_segs[b] - 1);
+            AppendEntry &e = p.e[p.n_entries++];
+            e.kq = static_cast<uint8_t *>(sg.k_q);
+            e.ks = static_cast<uint16_t *>(sg.k_s);
+            e.vq = static_cast<uint8_t *>(sg.v_q);
+            e.vs = static_cast<uint16_t *>(sg.v_s);
+            e.cap = sg.cap;
+            e.dst = sg.len;
+            e.src = b * d.t_q;
+            e.n = d.t_q;
+            e.layout = sg.layout;
+            ++b;
+        }
+        const cudaError_t err = launch_append(p, c->v_type, c->k_type, d.t_q * c->n_kv_heads, s, pdl);
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
+// Calls whose rows go to the tcgen05 kernel take their step's tokens through
+// an append launch first: dsp is ds with those calls' k_new / v_new cleared,
+// pre their indices.
+void split_off_pre_appends(const std::vector<Desc> &ds, std::vector<Desc> &dsp, std::vector<int> &pre)
+{
+    dsp = ds;
+    pre.clear();
+    for (size_t i = 0; i < ds.size(); ++i)
+        if (ds[i].k_new && ds[i].c->n_seqs > 0 && tc_rows(ds[i])) {
+            dsp[i].k_new = dsp[i].v_new = nullptr;
+            pre.push_back((int)i);
+        }
 }
 int round_up(long long x, int m) { return (int)((x + m - 1) / m * m); }
 
@@ -507,9 +569,12 @@ kvq_status run(std::vector<Desc> &ds, bool dump, void *workspace, size_t workspa
     }
     kvq_status st = device_setup(&dev);
     if (st != KVQ_OK) return st;
+    std::vector<Desc> dsp;
+    std::vector<int> pre;
+    split_off_pre_appends(ds, dsp, pre);
     std::vector<Launch> lns;
     size_t ws = 0;
-    st = plan(ds, dev, dump, lns, ws);
+    st = plan(dsp, dev, dump, lns, ws);
     if (st != KVQ_OK) return st;
     if (kernel_out) *kernel_out = (!lns.empty() && lns[0].prefill) ? 1 : 0;
     if (lose_stage)   // the test flavour exists for one form of the split kernel
@@ -529,8 +594,13 @@ kvq_status run(std::vector<Desc> &ds, bool dump, void *workspace, size_t workspa
     static thread_local AttnParams p;        // ~6 KB; kept off the stack
     static thread_local CombineParams cp;
     const bool pdl = pdl_enabled();
+    for (int i : pre)
+        if (launch_step_append(ds[i], stream, pdl) != cudaSuccess) {
+            cudaGetLastError();
+            return KVQ_ERR_CUDA;
+        }
     for (const Launch &ln : lns) {
-        fill_launch(ds, ln, dump, workspace, dev->timeouts, p, cp);
+        fill_launch(dsp, ln, dump, workspace, dev->timeouts, p, cp);
         cudaError_t e;
         if (ln.prefill)
             e = (ln.v_type == KVQ_V_Q4_0) ? launch_prefill_q4(p, ln.n_ctas, dump, stream, pdl)
@@ -700,10 +770,11 @@ kvq_status kvq_decode_multi_workspace_size(int32_t n, const kvq_decode_desc *cal
 }
 
 kvq_status kvq_debug_plan(int32_t n, const kvq_decode_desc *calls, int32_t n_sms, const int32_t *ctas_per_sm,
-                          kvq_plan_launch *out, int32_t max_out, int32_t *n_out, size_t *workspace_bytes)
+                          kvq_plan_launch *out, int32_t max_out, int32_t *n_out, size_t *workspace_bytes,
+                          int32_t *n_pre_appends)
 {
     if (n < 0 || n > KVQ_MAX_CALLS || (n > 0 && !calls) || n_sms < 1 || !ctas_per_sm || max_out < 0 ||
-        (max_out > 0 && !out) || !n_out || !workspace_bytes)
+        (max_out > 0 && !out) || !n_out || !workspace_bytes || !n_pre_appends)
         return KVQ_ERR_INVALID_ARG;
     for (int i = 0; i < 4; ++i)
         if (ctas_per_sm[i] < 1) return KVQ_ERR_INVALID_ARG;
@@ -723,9 +794,12 @@ kvq_status kvq_debug_plan(int32_t n, const kvq_decode_desc *calls, int32_t n_sms
             dev.ctas[kt][vt][2] = ctas_per_sm[2];
             dev.ctas[kt][vt][4] = ctas_per_sm[3];
         }
+    std::vector<Desc> dsp;
+    std::vector<int> pre;
+    split_off_pre_appends(ds, dsp, pre);
     std::vector<Launch> lns;
     size_t ws = 0;
-    const kvq_status st = plan(ds, &dev, false, lns, ws);
+    const kvq_status st = plan(dsp, &dev, false, lns, ws);
     if (st != KVQ_OK) return st;
     for (int i = 0; i < (int)lns.size() && i < max_out; ++i) {
         const Launch &ln = lns[i];
@@ -739,6 +813,7 @@ kvq_status kvq_debug_plan(int32_t n, const kvq_decode_desc *calls, int32_t n_sms
     }
     *n_out = (int32_t)lns.size();
     *workspace_bytes = ws;
+    *n_pre_appends = (int32_t)pre.size();
     return KVQ_OK;
 }
 

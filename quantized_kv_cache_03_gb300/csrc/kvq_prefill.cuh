@@ -627,6 +627,24 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
         // each KV tile, head-dim columns 64hf..64hf+63 of O.  The two halves of
         // a row agree on its reference max through the tile-max exchange, and
         // keep their own partial sums l.
+        if (32 * quarter >= R) {
+            // No query row in this TMEM lane quarter (a tile of up to 32 rows,
+            // or the ragged last one): keep the barrier phases in step with
+            // the live warps and do nothing else.  Per tile: S(j) complete,
+            // the two arrivals the issuers count (S read, P written; the rows
+            // here feed nothing the output keeps), then the P-ready phase's
+            // completion, so that no arrival for tile j + 1 lands in phase j.
+            for (int j = 0; j < n_tiles; ++j) {
+                if (wbad()) break;
+                if (!wwait_poll(bar(C::B_SFULL), j & 1)) { give_up(); break; }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(C::B_SFREE + (j & 1)));
+                    mbar_arrive(bar(C::B_PREADY));
+                }
+                if (!wwait_poll(bar(C::B_PREADY), j & 1)) { give_up(); break; }
+            }
+        } else {
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
         float qsl[kNB];   // block scale * sm_scale * log2(e)
         {
@@ -837,6 +855,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
                 else G.ws_lse[orow * G.n_split + split] = lse;
             }
         }
+        }   // live quarter
     }
     tc_fence_before();
     __syncthreads();

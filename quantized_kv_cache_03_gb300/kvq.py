@@ -128,7 +128,8 @@ def load():
                                          c_void_p]
             lib.kvq_debug_plan.restype = c_int32
             lib.kvq_debug_plan.argtypes = [c_int32, POINTER(KvqDecodeDesc), c_int32, POINTER(c_int32),
-                                           POINTER(KvqPlanLaunch), c_int32, POINTER(c_int32), POINTER(c_size_t)]
+                                           POINTER(KvqPlanLaunch), c_int32, POINTER(c_int32), POINTER(c_size_t),
+                                           POINTER(c_int32)]
             _lib = lib
     return _lib
 
@@ -468,13 +469,15 @@ def kvq_debug_plan(calls, n_sms: int, ctas_per_sm=(1, 2, 2, 2), max_out: int = 6
     """kvq_debug_plan of include/kvq.h (test hook): the launches the decode
     call would make for `calls` (dicts as for kvq_decode_attn_multi; only the
     caches' host descriptors are read) on a described device.  Returns
-    (launches as dicts, workspace bytes)."""
+    (launches as dicts, workspace bytes); the calls whose step tokens get an
+    append launch of their own first are in kvq_debug_plan.n_pre_appends."""
     arr, keep = _descs(calls)
     ctas = _i32(ctas_per_sm)
     out = (KvqPlanLaunch * max(1, max_out))()
-    n_out, ws = c_int32(0), c_size_t(0)
+    n_out, ws, n_pre = c_int32(0), c_size_t(0), c_int32(0)
     st = load().kvq_debug_plan(len(calls), arr, int(n_sms), ctas, out, max_out, ctypes.byref(n_out),
-                               ctypes.byref(ws))
+                               ctypes.byref(ws), ctypes.byref(n_pre))
+    kvq_debug_plan.n_pre_appends = int(n_pre.value)
     if st:
         raise KvqError(st, "kvq_debug_plan")
     launches = [dict(kernel=PLAN_KERNELS[r.kernel], n_tiles8=r.n_tiles8, warps=r.warps, chunk=r.chunk,

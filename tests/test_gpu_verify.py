@@ -5,7 +5,10 @@ multiples of 8, ragged and short contexts (tiles cut by segment ends, by the
 sequence length and by the causal tail), several splits merged by the combine,
 q8_0 V with x10 outlier channels, a non-causal call, uneven head maps, the
 step's tokens passed to the call (fused append), and a launch that mixes
-verify and decode calls.  All against the oracle on the same seeded inputs:
+verify and decode calls.  With KVQ_TC_ROWS=17 the same calls run on the
+tcgen05 kernel (one 128-row tile whose idle lane quarters keep only the
+barrier phases, the step's tokens appended by a launch of their own first);
+the tests marked below run both ways.  All against the oracle on the same seeded inputs:
 cache bytes bit-exact, out within 2e-3 and lse within 1e-4."""
 
 import numpy as np
@@ -26,6 +29,13 @@ def _built():
     __graft_entry__.build()
 
 
+@pytest.fixture(params=["rowtile", "tcgen05"])
+def route(request, monkeypatch):
+    if request.param == "tcgen05":
+        monkeypatch.setenv("KVQ_TC_ROWS", "17")
+    return request.param
+
+
 def _check_all(case, head_map=None):
     out, lse = case.decode(head_map=head_map)
     for b in range(case.B):
@@ -37,7 +47,7 @@ def _check_all(case, head_map=None):
 
 
 @pytest.mark.parametrize("vt", [0, 1])
-def test_verify_shape_two_sequences(vt):
+def test_verify_shape_two_sequences(vt, route):
     # 4 causal tokens x 8 query heads = 32 rows per kv head, 3000 positions
     spec = W.make_spec("verify", ctx=3000, n_seqs=2, v_type=vt)[0]
     _check_all(Case(spec).build())
@@ -50,7 +60,7 @@ def test_row_counts_not_multiples_of_eight(tq, hq, hkv):
     _check_all(Case(spec).build())
 
 
-def test_ragged_short_contexts_and_segments():
+def test_ragged_short_contexts_and_segments(route):
     """Four sequences of very different lengths (one shorter than a KV tile),
     three segments each: KV tiles cut by segment ends and sequence lengths."""
     spec = W.make_spec("verify", ctx=2600, n_seqs=4, n_seg=3, v_type=1, outliers=4)[0]
@@ -86,7 +96,7 @@ def test_uneven_head_map():
     _check_all(Case(spec).build(), head_map=hm)
 
 
-def test_step_tokens_passed_to_the_call():
+def test_step_tokens_passed_to_the_call(route):
     """k16_new / v16_new with a verify call: the tokens are appended (cache
     bytes as kvq_append writes them), the host lengths advance, and the
     attention sees them."""
@@ -152,7 +162,7 @@ def test_full_size_sampled_rows():
     assert kvq.kvq_wait_timeouts() == 0
 
 
-def test_repeats_and_pdl_on_off_bitwise_equal(monkeypatch):
+def test_repeats_and_pdl_on_off_bitwise_equal(monkeypatch, route):
     """Five runs with programmatic dependent launch and three without give
     identical bits (fixed-order reductions), with a forced split so the
     combine runs too."""

@@ -24,7 +24,7 @@ def _lib():
 
 @pytest.fixture(autouse=True)
 def _clean_env(monkeypatch):
-    for k in ("KVQ_SPLIT", "KVQ_SPLIT_WARPS", "KVQ_ROW_TILE", "KVQ_PREFILL"):
+    for k in ("KVQ_SPLIT", "KVQ_SPLIT_WARPS", "KVQ_ROW_TILE", "KVQ_PREFILL", "KVQ_TC_ROWS"):
         monkeypatch.delenv(k, raising=False)
 
 
@@ -146,6 +146,12 @@ def test_verify_shape(monkeypatch):
     monkeypatch.setenv("KVQ_ROW_TILE", "16")
     ln16 = plan(calls)[0][0]
     assert (ln16["n_tiles8"], ln16["warps"]) == (2, 4)
+    monkeypatch.delenv("KVQ_ROW_TILE")
+    assert kvq.kvq_debug_plan.n_pre_appends == 0
+    # KVQ_TC_ROWS=17: the tcgen05 kernel, its step tokens through an append launch first
+    monkeypatch.setenv("KVQ_TC_ROWS", "17")
+    ln = plan(calls)[0][0]
+    assert ln["kernel"] == "prefill" and ln["n_ctas"] == 16 * 8 and kvq.kvq_debug_plan.n_pre_appends == 1
 
 
 def test_prefill_chunk(monkeypatch):
