@@ -474,7 +474,11 @@ typedef struct kvq_plan_launch {
     int32_t kernel;     /* 0 split kernel, 1 tcgen05 prefill kernel */
     int32_t n_tiles8;   /* split kernel: 8-row query tiles per CTA (1, 2 or 4); else 0 */
     int32_t warps;      /* split kernel: warps per CTA; else 0 */
-    int32_t chunk;      /* kv positions per split */
+    int32_t chunk;      /* kv positions per split (after the first, see chunk0) */
+    int32_t chunk0;     /* kv positions of the first split: chunk, except on a
+                           one-wave tcgen05 launch split unevenly (large first
+                           pieces on every busy SM, small second pieces taken
+                           by the SMs that would idle) */
     int32_t n_ctas;     /* CTAs of the attention launch */
     int32_t n_rows;     /* query rows of the combine launch (0: no combine launch) */
 } kvq_plan_launch;

@@ -311,6 +311,8 @@ struct Launch {
     int warps = 0;   // warps per split CTA (split_warps(nt), or kWarpsHalf for the 8-row kernel)
     bool prefill = false;
     int chunk = KVQ_SEG_ALIGN;
+    int chunk0 = KVQ_SEG_ALIGN;   // split 0's positions (chunk unless the launch is split unevenly)
+    bool split_major = false;     // CTAs ordered split first (the uneven split's large pieces first)
     int n_ctas = 0, n_rows = 0;   // split CTAs, combine rows
     std::vector<Unit> units;
 };
@@ -328,6 +330,41 @@ int tile_rows(const Launch &ln) { return ln.prefill ? kPrefillRows : 8 * ln.nt; 
 // CTA) and at least 256 positions; KVQ_SPLIT forces a chunk (rounded to the
 // 64-position segment alignment).
 constexpr int kOverhead = 512;
+
+// Uneven two-way split of a one-wave tcgen05 launch.  With U CTAs of one
+// group on S SMs (S / 2 < U < S; one CTA per SM), S - U SMs idle for the whole
+// launch.  Splitting every unit at c0 instead gives U large CTAs [0, c0),
+// dispatched first, and U small ones [c0, reach) that the S - U idle SMs take
+// k = ceil(U / (S - U)) at a time; the combine merges the two partials.
+// c0 balances the large CTAs' time c0 + o against k (reach - c0 + o), o the
+// fixed cost of one CTA in positions.  KVQ_PREFILL_BALANCE=0 turns it off, a
+// positive value forces k.  Returns false (launch unchanged) when it does not
+// pay by at least 5 %.
+constexpr int kPrefillCtaCost = 256;
+bool uneven_split(const std::vector<Desc> &ds, Launch &ln, int n_sms)
+{
+    if (!ln.prefill || ln.units.size() != 1) return false;
+    const char *fs = std::getenv("KVQ_SPLIT");
+    if (fs && std::atoi(fs) > 0) return false;
+    const char *env = std::getenv("KVQ_PREFILL_BALANCE");
+    const int forced = env ? std::atoi(env) : -1;
+    if (forced == 0) return false;
+    const Unit &u = ln.units[0];
+    const Desc &d = ds[u.d];
+    const int lmax = u.reach;
+    if (lmax <= 0 || ln.chunk < lmax) return false;   // already split evenly
+    const long long U = (long long)((d.max_rows + kPrefillRows - 1) / kPrefillRows) * d.c->n_kv_heads * u.nb;
+    if (U >= n_sms || 2 * U <= n_sms) return false;
+    const long long k = forced > 0 ? forced : (U + (n_sms - U) - 1) / (n_sms - U);
+    const char *ce = std::getenv("KVQ_PREFILL_CTA_COST");
+    const long long o = (ce && std::atoi(ce) >= 0) ? std::atoi(ce) : kPrefillCtaCost;
+    const int c0 = round_up((int)((k * lmax + (k - 1) * o + k) / (k + 1)), kPrefillPositions);
+    if (c0 >= lmax || (double)(c0 + o) > 0.95 * (double)(lmax + o)) return false;
+    ln.chunk0 = c0;
+    ln.chunk = round_up(lmax - c0, kPrefillPositions);
+    ln.split_major = true;
+    return true;
+}
 int choose_chunk(const std::vector<Desc> &ds, const Launch &ln, int slots, int gran)
 {
     int lmax = 0;
@@ -448,9 +485,11 @@ kvq_status plan(std::vector<Desc> &ds, DeviceInfo *dev, bool dump, std::vector<L
                 ln.chunk = choose_chunk(ds, ln, dev->n_sms * half_ctas, kWarpsHalf * kWTile);
             }
         }
+        ln.chunk0 = ln.chunk;
+        if (tc) uneven_split(ds, ln, dev->n_sms);
         for (Unit &u : ln.units) {
             const Desc &d = ds[u.d];
-            u.n_split = std::max(1, (u.reach + ln.chunk - 1) / ln.chunk);
+            u.n_split = u.reach <= ln.chunk0 ? 1 : 1 + (u.reach - ln.chunk0 + ln.chunk - 1) / ln.chunk;
             u.n_rt = (d.max_rows + tile_rows(ln) - 1) / tile_rows(ln);   // 1 unless rows exceed the tile
             const long long n = (long long)u.n_rt * u.n_split * d.c->n_kv_heads * u.nb;
             if (ln.n_ctas + n > INT_MAX) return KVQ_ERR_UNSUPPORTED;
@@ -509,6 +548,8 @@ void fill_launch(const std::vector<Desc> &ds, const Launch &ln, bool dump, void 
         G.n_split = u.n_split;
         G.n_rt = u.n_rt;
         G.chunk = ln.chunk;
+        G.chunk0 = ln.chunk0;
+        G.split_major = ln.split_major ? 1 : 0;
         G.qk_scale_log2 = d.sm_scale * 1.4426950408889634f;
         if (dump) {
             G.dbg_qc = d.dbg_qc + r0 * kD;
@@ -808,6 +849,7 @@ kvq_status kvq_debug_plan(int32_t n, const kvq_decode_desc *calls, int32_t n_sms
         r.n_tiles8 = ln.prefill ? 0 : ln.nt;
         r.warps = ln.warps;
         r.chunk = ln.chunk;
+        r.chunk0 = ln.chunk0;
         r.n_ctas = ln.n_ctas;
         r.n_rows = ln.n_rows;
     }

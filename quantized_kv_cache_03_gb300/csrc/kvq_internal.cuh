@@ -109,7 +109,13 @@ struct GroupDesc {
     int head0;                             // first entry of grp_begin (this cache's kv heads)
     int n_seqs, n_kv_heads, n_q_heads, t_q, causal;
     int max_len;                           // positions >= max_len are ignored
-    int n_split, chunk;                    // split s covers [s*chunk, (s+1)*chunk)
+    int n_split, chunk;                    // split s covers [s*chunk, (s+1)*chunk) ...
+    int chunk0;                            // ... when chunk0 == chunk; else split 0 covers [0, chunk0)
+                                           // and split s >= 1 [chunk0 + (s-1)*chunk, chunk0 + s*chunk)
+                                           // (the tcgen05 kernel's uneven split; the split kernel
+                                           // always gets chunk0 == chunk)
+    int split_major;                       // CTA order split, seq, kv head, row tile (else seq, kv head,
+                                           // split, row tile); tcgen05 kernel only
     int n_rt;                              // row tiles of 8*NT query rows per kv head
     float qk_scale_log2;                   // sm_scale * log2(e)
 };

@@ -227,8 +227,20 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
         if ((int)blockIdx.x >= p.grp[k].cta0) gi = k;
     const GroupDesc &G = p.grp[gi];
     const int lb = (int)blockIdx.x - G.cta0;
-    const int rt = lb % G.n_rt, ls = lb / G.n_rt;
-    const int split = ls % G.n_split, h = (ls / G.n_split) % G.n_kv_heads, b = ls / G.n_split / G.n_kv_heads;
+    int rt, split, h, b;
+    if (G.split_major) {   // every unit's split 0 first (the large pieces of an uneven split)
+        const int per = G.n_rt * G.n_kv_heads * G.n_seqs, x = lb % per;
+        split = lb / per;
+        rt = x % G.n_rt;
+        h = (x / G.n_rt) % G.n_kv_heads;
+        b = x / G.n_rt / G.n_kv_heads;
+    } else {
+        const int ls = lb / G.n_rt;
+        rt = lb % G.n_rt;
+        split = ls % G.n_split;
+        h = (ls / G.n_split) % G.n_kv_heads;
+        b = ls / G.n_split / G.n_kv_heads;
+    }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gb = p.grp_begin[G.head0 + h], gsz = p.grp_begin[G.head0 + h + 1] - gb;
     const int row0 = rt * kPM;
@@ -242,8 +254,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
     const int L = max(0, min(G.seq_lens[b], lcap));
     // the split's positions, cut at the sequence length and, under the causal
     // tail, after the last position the tile's last query token sees
-    const int r0 = split * G.chunk;
-    int r1 = min(L, r0 + G.chunk);
+    const int r0 = split == 0 ? 0 : G.chunk0 + (split - 1) * G.chunk;
+    int r1 = min(L, split == 0 ? G.chunk0 : r0 + G.chunk);
     if (G.causal) r1 = min(r1, L - G.t_q + (row0 + R - 1) / gsz + 1);
     if (r0 >= r1) {   // nothing visible in this split
         if (!DUMP && tid < R) {

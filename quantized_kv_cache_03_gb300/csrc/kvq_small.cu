@@ -145,10 +145,70 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
     }
 }
 
+// The same merge for launches whose rows have at most kNarrowSplits splits
+// each (long query chunks: thousands of rows, two or three splits): one warp
+// per row, eight rows per CTA, the splits merged one after another in split
+// order with the same running (max, weight sum, weighted o).  One CTA per row
+// would leave most warps idle and make the launch a stream of tiny CTAs.
+constexpr int kNarrowSplits = 8;
+
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_rows_kernel(const __grid_constant__ CombineParams p,
+                                                                          int n_rows)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = (int)blockIdx.x * kCombineWarps + warp;
+    pdl_wait();
+    pdl_trigger();
+    if (r >= n_rows) return;
+    int gi = 0;
+#pragma unroll 1
+    for (int k = 1; k < p.n_groups; ++k)
+        if (r >= p.grp[k].row0) gi = k;
+    const CombineGroup &G = p.grp[gi];
+    const int row = r - G.row0, n = G.n_split;
+    const float *ls = G.ws_lse + (size_t)row * n;
+    const float4 *o = reinterpret_cast<const float4 *>(G.ws_o + (size_t)row * n * kD) + lane;
+    float lv[kNarrowSplits];
+    float4 v[kNarrowSplits];
+#pragma unroll
+    for (int k = 0; k < kNarrowSplits; ++k) {   // every split's lse and o in one round trip
+        lv[k] = (k < n) ? ls[k] : -INFINITY;
+        v[k] = (k < n) ? o[(size_t)k * (kD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float m = -INFINITY, W = 0.f;
+    bool poisoned = false;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kNarrowSplits; ++k) {
+        poisoned |= lv[k] != lv[k];
+        if (lv[k] == -INFINITY || lv[k] != lv[k]) continue;
+        const float mx = fmaxf(m, lv[k]);
+        const float a = (m == -INFINITY) ? 0.f : expf(m - mx), w = expf(lv[k] - mx);
+        W = fmaf(W, a, w);
+        acc.x = fmaf(w, v[k].x, acc.x * a);
+        acc.y = fmaf(w, v[k].y, acc.y * a);
+        acc.z = fmaf(w, v[k].z, acc.z * a);
+        acc.w = fmaf(w, v[k].w, acc.w * a);
+        m = mx;
+    }
+    if (poisoned) {   // a split that lost a copy stage: the merged row is NaN
+        m = INFINITY;
+        W = __int_as_float(0x7fc00000);
+    }
+    const bool any = !(W <= 0.f);
+    const float inv = any ? 1.f / W : 0.f;
+    reinterpret_cast<float4 *>(G.out + (size_t)row * kD)[lane] =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (lane == 0) G.lse[row] = any ? m + logf(W) : -INFINITY;
+}
+
 cudaError_t launch_combine(const CombineParams &p, int n_rows, cudaStream_t s, bool pdl)
 {
+    int max_split = 0;
+    for (int k = 0; k < p.n_groups; ++k) max_split = max(max_split, p.grp[k].n_split);
+    const bool narrow = max_split <= kNarrowSplits;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(n_rows);
+    cfg.gridDim = dim3(narrow ? (n_rows + kCombineWarps - 1) / kCombineWarps : n_rows);
     cfg.blockDim = dim3(kCombineWarps * 32);
     cfg.stream = s;
     cudaLaunchAttribute at[1];
@@ -156,6 +216,7 @@ cudaError_t launch_combine(const CombineParams &p, int n_rows, cudaStream_t s, b
     at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = at;
     cfg.numAttrs = 1;
+    if (narrow) return cudaLaunchKernelEx(&cfg, combine_rows_kernel, p, n_rows);
     return cudaLaunchKernelEx(&cfg, combine_kernel, p);
 }
 

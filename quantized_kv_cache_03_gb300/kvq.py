@@ -68,7 +68,7 @@ class KvqLayoutModel(ctypes.Structure):
 
 class KvqPlanLaunch(ctypes.Structure):
     _fields_ = [("kernel", c_int32), ("n_tiles8", c_int32), ("warps", c_int32), ("chunk", c_int32),
-                ("n_ctas", c_int32), ("n_rows", c_int32)]
+                ("chunk0", c_int32), ("n_ctas", c_int32), ("n_rows", c_int32)]
 
 
 class KvqError(RuntimeError):
@@ -481,5 +481,5 @@ def kvq_debug_plan(calls, n_sms: int, ctas_per_sm=(1, 2, 2, 2), max_out: int = 6
     if st:
         raise KvqError(st, "kvq_debug_plan")
     launches = [dict(kernel=PLAN_KERNELS[r.kernel], n_tiles8=r.n_tiles8, warps=r.warps, chunk=r.chunk,
-                     n_ctas=r.n_ctas, n_rows=r.n_rows) for r in out[:min(n_out.value, max_out)]]
+                     chunk0=r.chunk0, n_ctas=r.n_ctas, n_rows=r.n_rows) for r in out[:min(n_out.value, max_out)]]
     return launches, int(ws.value)

@@ -229,6 +229,53 @@ def test_chunk_full_size_sampled_rows():
     assert_close(out[0], lse[0], ref, rows=rows, what="prefill full size")
 
 
+def test_uneven_split_of_a_one_wave_launch(kernel, monkeypatch):
+    """A 512-token chunk over 3000 positions, 8 kv heads x 16 row tiles: 128
+    units on 152 SMs, so the launch splits every unit unevenly (large pieces
+    first, small ones on the spare SMs, then the combine).  The first row
+    tiles' causal limit falls before the split point, so their small pieces see
+    nothing.  Sampled rows of every row tile against the oracle, the int32 block
+    scores of the same rows bit for bit, and the same rows with the split off
+    (KVQ_PREFILL_BALANCE=0) also within the tolerance."""
+    if kernel != "tcgen05":
+        pytest.skip("the uneven split is a tcgen05 launch policy")
+    spec = W.make_spec("prefill", ctx=3000, v_type=1)[0]
+    case = Case(spec).build()
+    call = dict(cache=case.cache, n_q_heads=case.Hq, t_q=case.tq, causal_tail=True, max_len=case.max_len,
+                head_map=None, sm_scale=SM_SCALE)
+    ln = kvq.kvq_debug_plan([call], 152)[0][0]
+    L, tq, Hq = case.lens[0], case.tq, case.Hq
+    assert ln["kernel"] == "prefill" and ln["n_ctas"] == 256 and ln["chunk0"] < L
+    assert ln["chunk0"] > L - tq + 32   # row tile 0 (tokens 0-31) ends before the split point
+    nr = tq * Hq
+    rng = np.random.default_rng(3)
+    # rows of every row tile (128 rows = 32 tokens x 4 heads per kv head)
+    rows = np.unique(np.concatenate([[0, 1, nr - 1], (np.arange(16) * 32 + 31) * Hq + 5, rng.integers(0, nr, 40)]))
+    mask = np.zeros(nr, np.uint8)
+    mask[rows] = 1
+    ref = case.oracle_decode(0, row_mask=mask)
+    out, lse = case.decode()
+    assert_close(out[0], lse[0], ref, rows=rows, what="uneven split")
+    # the dump runs on the same plan: int32 block scores of the sampled rows
+    q16 = to_dev(case.q)
+    lens = torch.tensor(case.lens, dtype=torch.int32, device=dev())
+    qc = torch.zeros((1, tq, Hq, 128), dtype=torch.int8, device=dev())
+    qs = torch.zeros((1, tq, Hq, 4), dtype=torch.int16, device=dev())
+    sc = torch.zeros((1, tq, Hq, L, 4), dtype=torch.int32, device=dev())
+    assert kvq.kvq_debug_qk(case.cache, q16, Hq, tq, lens, L, None, qc, qs, sc) == "tcgen05"
+    torch.cuda.synchronize()
+    hm_full = np.arange(Hq) // (Hq // spec.n_kv_heads)
+    q_sub = case.q[0].reshape(nr, 128)[rows][None]
+    refs = oracle.decode_seq(case.oracle_cache(0), q_sub, hm_full[rows % Hq].astype(np.int32), False, SM_SCALE,
+                             spec.v_type, want_scores=True, n_threads=8)
+    got_sc = sc.view(nr, L, 4)[torch.as_tensor(rows, device=dev())].cpu().numpy()
+    assert np.array_equal(got_sc, refs["scores"][0])
+    monkeypatch.setenv("KVQ_PREFILL_BALANCE", "0")
+    assert kvq.kvq_debug_plan([call], 152)[0][0]["n_ctas"] == 128
+    out0, lse0 = case.decode()
+    assert_close(out0[0], lse0[0], ref, rows=rows, what="one split")
+
+
 def test_repeats_and_pdl_on_off_bitwise_equal(monkeypatch):
     """Five runs with programmatic dependent launch and three without give
     identical bits: every reduction has a fixed order, so a stale read through

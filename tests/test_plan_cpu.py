@@ -80,7 +80,7 @@ def test_long_pair_fused_is_one_wave_of_16_warp_ctas():
     (8 + 4) x 12 = 144 CTAs, one combine over the 40 + 16 query rows."""
     _, calls = calls_of("long", fused=True)
     lns, ws = plan(calls)
-    assert lns == [dict(kernel="split", n_tiles8=1, warps=16, chunk=11008, n_ctas=144, n_rows=56)]
+    assert lns == [dict(kernel="split", n_tiles8=1, warps=16, chunk=11008, chunk0=11008, n_ctas=144, n_rows=56)]
     assert ws > 0
 
 
@@ -131,7 +131,7 @@ def test_single_and_tiny():
     sweep); tiny: one split, so no combine launch and no workspace."""
     _, calls = calls_of("single", fused=True)
     lns, ws = plan(calls)
-    assert lns == [dict(kernel="split", n_tiles8=1, warps=16, chunk=512, n_ctas=128, n_rows=32)]
+    assert lns == [dict(kernel="split", n_tiles8=1, warps=16, chunk=512, chunk0=512, n_ctas=128, n_rows=32)]
     _, calls = calls_of("tiny", fused=True)
     lns, ws = plan(calls)
     assert len(lns) == 1 and lns[0]["n_ctas"] == 1 and lns[0]["n_rows"] == 0 and ws == 0
@@ -149,19 +149,43 @@ def test_verify_shape(monkeypatch):
     monkeypatch.delenv("KVQ_ROW_TILE")
     assert kvq.kvq_debug_plan.n_pre_appends == 0
     # KVQ_TC_ROWS=17: the tcgen05 kernel, its step tokens through an append launch first
+    # (128 one-tile units on 152 SMs: split unevenly in two)
     monkeypatch.setenv("KVQ_TC_ROWS", "17")
     ln = plan(calls)[0][0]
-    assert ln["kernel"] == "prefill" and ln["n_ctas"] == 16 * 8 and kvq.kvq_debug_plan.n_pre_appends == 1
+    assert ln["kernel"] == "prefill" and ln["n_ctas"] == 2 * 16 * 8 and kvq.kvq_debug_plan.n_pre_appends == 1
+    assert ln["n_rows"] == 16 * 4 * 64
 
 
 def test_prefill_chunk(monkeypatch):
     """A 512-token chunk (2048 rows per kv head) runs on the tcgen05 prefill
-    kernel, one split on 128 CTAs (the best of the split sweep); KVQ_PREFILL=0
-    sends it to the split kernel's 32-row tiles."""
-    _, calls = calls_of("prefill", fused=False)
+    kernel.  Its 128 units (8 kv heads x 16 row tiles) on 152 SMs would leave 24
+    SMs idle, so every unit is split unevenly: 128 large CTAs [0, chunk0), then
+    128 small ones [chunk0, reach) that the 24 spare SMs take six at a time, and
+    a combine over all 16384 rows.  chunk0 balances one large CTA against six
+    small ones (256 positions of fixed cost each).  KVQ_PREFILL_BALANCE=0 keeps
+    one split on 128 CTAs; KVQ_PREFILL=0 sends the chunk to the split kernel's
+    32-row tiles."""
+    specs, calls = calls_of("prefill", fused=False)
+    reach = max(specs[0].lengths)
     lns, ws = plan(calls)
-    assert len(lns) == 1 and lns[0]["kernel"] == "prefill" and lns[0]["n_ctas"] == 128
-    assert lns[0]["n_rows"] == 0 and ws == 0
+    assert len(lns) == 1 and lns[0]["kernel"] == "prefill" and lns[0]["n_ctas"] == 256
+    ln = lns[0]
+    c0, c1 = ln["chunk0"], ln["chunk"]
+    assert c0 % 64 == 0 and c1 % 64 == 0 and c0 < reach <= c0 + c1 < reach + 64
+    k, o = 6, 256
+    assert k * (reach - c0 + o) <= c0 + o < k * (reach - c0 + o) + (k + 1) * 64
+    assert ln["n_rows"] == 512 * 32 and ws == (512 * 32 * 2 * 129 * 4 + 255) // 256 * 256
+    monkeypatch.setenv("KVQ_PREFILL_BALANCE", "3")
+    ln3 = plan(calls)[0][0]
+    assert ln3["n_ctas"] == 256 and ln3["chunk0"] < c0 and 3 * (reach - ln3["chunk0"] + o) <= ln3["chunk0"] + o
+    monkeypatch.setenv("KVQ_PREFILL_BALANCE", "0")
+    lns, ws = plan(calls)
+    assert lns[0]["n_ctas"] == 128 and lns[0]["chunk0"] == lns[0]["chunk"] and lns[0]["n_rows"] == 0 and ws == 0
+    monkeypatch.delenv("KVQ_PREFILL_BALANCE")
+    monkeypatch.setenv("KVQ_SPLIT", "8192")   # a forced chunk keeps even splits
+    ln = plan(calls)[0][0]
+    assert ln["chunk0"] == ln["chunk"] == 8192 and ln["n_ctas"] == 128 * ((reach + 8191) // 8192)
+    monkeypatch.delenv("KVQ_SPLIT")
     monkeypatch.setenv("KVQ_PREFILL", "0")
     ln = plan(calls)[0][0]
     assert (ln["kernel"], ln["n_tiles8"]) == ("split", 4)
