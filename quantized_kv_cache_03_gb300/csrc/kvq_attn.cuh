@@ -127,20 +127,21 @@ struct SplitCfg {
     static_assert(SMEM <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
 };
 
-// Lane 0 fills ring slot `dst` (shared address) with n consecutive tiles of
-// one segment starting at the walk's next tile: four contiguous bulk copies
-// whose bytes complete on the slot's barrier.  Positions of a tile outside
-// [la, le) are copied too (they are cache rows of the same segment, possibly
-// never written) and masked where they are used.
+// The warp (converged; one elected lane issues) fills ring slot `dst`
+// (shared address) with n consecutive tiles of one segment starting at the
+// walk's next tile: four contiguous bulk copies whose bytes complete on the
+// slot's barrier.  Positions of a tile outside [la, le) are copied too (they
+// are cache rows of the same segment, possibly never written) and masked where
+// they are used.
 template <int NT, int VT, int KT>
 __device__ __forceinline__ void tile_issue(const Walk &w, int n, uint32_t dst, uint32_t bar)
 {
     using C = SplitCfg<NT, VT, KT>;
-    mbar_arrive_expect_tx(bar, n * C::TILE);
-    bulk_g2s(dst + C::K_OFF, w.gk, n * C::TILE_K, bar);
-    if (C::TILE_KS) bulk_g2s(dst + C::KS_OFF, w.gks, n * C::TILE_KS, bar);
-    bulk_g2s(dst + C::V_OFF, w.gv, n * C::TILE_V, bar);
-    bulk_g2s(dst + C::VS_OFF, w.gvs, n * C::TILE_S, bar);
+    mbar_arrive_expect_tx_w(bar, n * C::TILE);
+    bulk_g2s_w(dst + C::K_OFF, w.gk, n * C::TILE_K, bar);
+    if (C::TILE_KS) bulk_g2s_w(dst + C::KS_OFF, w.gks, n * C::TILE_KS, bar);
+    bulk_g2s_w(dst + C::V_OFF, w.gv, n * C::TILE_V, bar);
+    bulk_g2s_w(dst + C::VS_OFF, w.gvs, n * C::TILE_S, bar);
 }
 
 // The same for a KVQ_LAYOUT_ROWS segment: only the rows [ra, rb) of the n
@@ -152,11 +153,11 @@ __device__ __forceinline__ void rows_issue(const Walk &w, int ra, int rb, uint32
 {
     using C = SplitCfg<NT, VT, KT>;
     const int sa = ra & ~1, sb = (rb + 1) & ~1;
-    mbar_arrive_expect_tx(bar, (rb - ra) * (C::KCODE + C::VCODE) + (sb - sa) * 2 * kNB * 2);
-    bulk_g2s(dst + C::K_OFF + ra * C::KCODE, w.gk + ra * C::KCODE, (rb - ra) * C::KCODE, bar);
-    bulk_g2s(dst + C::KS_OFF + sa * kNB * 2, w.gks + sa * kNB * 2, (sb - sa) * kNB * 2, bar);
-    bulk_g2s(dst + C::V_OFF + ra * C::VCODE, w.gv + ra * C::VCODE, (rb - ra) * C::VCODE, bar);
-    bulk_g2s(dst + C::VS_OFF + sa * kNB * 2, w.gvs + sa * kNB * 2, (sb - sa) * kNB * 2, bar);
+    mbar_arrive_expect_tx_w(bar, (rb - ra) * (C::KCODE + C::VCODE) + (sb - sa) * 2 * kNB * 2);
+    bulk_g2s_w(dst + C::K_OFF + ra * C::KCODE, w.gk + ra * C::KCODE, (rb - ra) * C::KCODE, bar);
+    bulk_g2s_w(dst + C::KS_OFF + sa * kNB * 2, w.gks + sa * kNB * 2, (sb - sa) * kNB * 2, bar);
+    bulk_g2s_w(dst + C::V_OFF + ra * C::VCODE, w.gv + ra * C::VCODE, (rb - ra) * C::VCODE, bar);
+    bulk_g2s_w(dst + C::VS_OFF + sa * kNB * 2, w.gvs + sa * kNB * 2, (sb - sa) * kNB * 2, bar);
 }
 
 // Head-dim index of accumulator row rho (0..15) of PV m-tile mt = 2*block + h2.
@@ -337,18 +338,19 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT, KT, W>::THREADS, SplitCfg<NT,
     const bool loser = LOSE && blockIdx.x == 0 && warp == 0;
     auto issue = [&](int slot) {
         const int n = min(C::TPS, pw.Tend - pw.T);
+        const int tb = pw.T * kWTile;
         if (lane == 0) {
-            const int tb = pw.T * kWTile;
             tile_rec[slot] = make_int4(tb, pw.la, pw.le, pw.pos0 + tb);
             stage_n[slot] = n | (pw.rows << 8);
-            if (loser && issued == kLostStage)
-                mbar_arrive_expect_tx(bar_s + slot * 8, n * C::TILE);   // bytes that never come
-            else if (pw.rows)   // rows layout: the piece's rows of these tiles only
-                rows_issue<NT, VT, KT>(pw, max(pw.la, tb) - tb, min(pw.le, tb + n * kWTile) - tb,
-                                       ring_s + slot * C::STAGE, bar_s + slot * 8);
-            else
-                tile_issue<NT, VT, KT>(pw, n, ring_s + slot * C::STAGE, bar_s + slot * 8);
         }
+        // the whole warp from here (every condition is warp-uniform)
+        if (loser && issued == kLostStage)
+            mbar_arrive_expect_tx_w(bar_s + slot * 8, n * C::TILE);   // bytes that never come
+        else if (pw.rows)   // rows layout: the piece's rows of these tiles only
+            rows_issue<NT, VT, KT>(pw, max(pw.la, tb) - tb, min(pw.le, tb + n * kWTile) - tb,
+                                   ring_s + slot * C::STAGE, bar_s + slot * 8);
+        else
+            tile_issue<NT, VT, KT>(pw, n, ring_s + slot * C::STAGE, bar_s + slot * 8);
         pw.T += n;
         pw.gk += n * C::TILE_K;
         pw.gks += n * C::TILE_S;
@@ -540,7 +542,9 @@ __global__ void __launch_bounds__(SplitCfg<NT, VT, KT, W>::THREADS, SplitCfg<NT,
         }
         __syncwarp();   // every lane is done with the previous stage, whose slot is refilled next
         if (pw.k < nseg) {
-            if (lane == 0) fence_proxy_async_smem();
+            // every lane (the elected issuing lane among them): the lanes'
+            // generic reads of the slot before the copy engine's writes
+            fence_proxy_async_smem();
             issue(prev);
         }
         const int ns = stage_n[slot] & 0xff;

@@ -236,6 +236,23 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
+// Warp-collective forms of the two calls above: every lane of a converged
+// warp passes the same (warp-uniform) operands and one elected lane issues.
+// Issuing from inside a lane-0 branch instead costs more per instruction (the
+// uniform operands have to be taken out of a divergent lane).
+__device__ __forceinline__ void mbar_arrive_expect_tx_w(uint32_t bar, uint32_t tx)
+{
+    asm volatile("{\n .reg .pred e;\n .reg .b64 st;\n elect.sync _|e, 0xffffffff;\n"
+                 " @e mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(bar), "r"(tx)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_w(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+                 " @e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n}"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 // Wait for phase `parity` of the barrier to complete, giving up after
 // kMbarSpins polls (each poll may suspend the thread for a short while).
 constexpr uint32_t kMbarSpins = 1u << 22;

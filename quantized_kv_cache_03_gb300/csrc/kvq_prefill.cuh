@@ -126,26 +126,25 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int m, int n)
 {
     return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+// D (+)= A.B, kind::f16, A in tensor memory (row r in lane r, two fp16 k
+// elements per 32-bit column, k-step columns [a, a + 8)), B a shared-memory
+// descriptor.  Issued by one elected lane of a converged warp whose lanes all
+// pass the same (warp-uniform) operands: cheaper to issue than from inside a
+// lane-0 branch, which has to take the uniform operands out of a divergent lane.
+__device__ __forceinline__ void umma_f16_ta_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc)
 {
-    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-                 " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-                 "l"(a), "l"(b), "r"(idesc), "r"(acc)
-                 : "memory");
-}
-// The same with A in tensor memory (row r in lane r, two fp16 k elements per
-// 32-bit column, k-step columns [a, a + 8)).
-__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc)
-{
-    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-                 " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+    asm volatile("{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+                 " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
                  "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
                  : "memory");
 }
-// Arrive once on `bar` when every tcgen05 operation this thread issued so far is done.
-__device__ __forceinline__ void umma_commit(uint32_t bar)
+// Arrive once on `bar` when every tcgen05 operation issued so far by this
+// warp's elected lane is done (elect.sync picks the same lane each time for
+// the same full warp, so it is the lane that issued the MMAs).
+__device__ __forceinline__ void umma_commit_w(uint32_t bar)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+    asm volatile("{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+                 " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(bar)
                  : "memory");
 }
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
@@ -378,8 +377,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
     __syncthreads();   // the Q operand and the query scales in place
     tc_fence_after();
 
+    // called by whole warps (a uniform decision): counted once per warp
     auto give_up = [&]() {
-        if (!*bad) {
+        if (lane == 0 && !*bad) {
             *bad = 1;
             atomicAdd(p.timeouts, 1u);
         }
@@ -396,93 +396,92 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
     auto wbad = [&]() { return __any_sync(0xffffffffu, *bad != 0); };
 
     if (warp == kPCtlWarp) {
-        // ================= QK MMAs =================
-        if (lane == 0) {
-            // descriptors of the k16 steps differ from a base only in the start
-            // address (16-byte units, no carry out of its 14 bits)
-            const uint64_t dK0 = umma_desc(sbase + C::K_OFF, C::K_LBO, C::K_SBO);
-            const uint64_t dK1 = umma_desc(sbase + C::K_OFF + C::KBUF, C::K_LBO, C::K_SBO);
-            for (int j = 0; j < n_tiles; ++j) {
-                if (*bad) break;
-                if (!mbar_wait(bar(C::B_KR + (j & 1)), (j >> 1) & 1)) { give_up(); break; }
-                if (j > 0 && !mbar_wait_poll(bar(C::B_SFREE + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { give_up(); break; }
-                tc_fence_after();
-                const uint64_t dK = (j & 1) ? dK1 : dK0;
+        // ================= QK MMAs (the warp runs the loop, one elected lane
+        // issues) =================
+        // descriptors of the k16 steps differ from a base only in the start
+        // address (16-byte units, no carry out of its 14 bits)
+        const uint64_t dK0 = umma_desc(sbase + C::K_OFF, C::K_LBO, C::K_SBO);
+        const uint64_t dK1 = umma_desc(sbase + C::K_OFF + C::KBUF, C::K_LBO, C::K_SBO);
+        for (int j = 0; j < n_tiles; ++j) {
+            if (wbad()) break;
+            if (!wwait(bar(C::B_KR + (j & 1)), (j >> 1) & 1)) { give_up(); break; }
+            if (j > 0 && !wwait_poll(bar(C::B_SFREE + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { give_up(); break; }
+            tc_fence_after();
+            const uint64_t dK = (j & 1) ? dK1 : dK0;
 #pragma unroll
-                for (int bb = 0; bb < kNB; ++bb)
+            for (int bb = 0; bb < kNB; ++bb)
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const uint64_t o = (uint64_t)((4 * bb + 2 * kk) * (C::K_LBO / 16));
-                        umma_f16_ta(tS + kPN * bb, tQ + 16 * bb + 8 * kk, dK + o, kIdQK, kk);
-                    }
-                umma_commit(bar(C::B_SFULL));
-            }
-            umma_commit(bar(C::B_FIN));
-            if (!mbar_wait(bar(C::B_FIN), 0)) give_up();
+                for (int kk = 0; kk < 2; ++kk) {
+                    const uint64_t o = (uint64_t)((4 * bb + 2 * kk) * (C::K_LBO / 16));
+                    umma_f16_ta_w(tS + kPN * bb, tQ + 16 * bb + 8 * kk, dK + o, kIdQK, kk);
+                }
+            umma_commit_w(bar(C::B_SFULL));
         }
-        __syncwarp();
+        umma_commit_w(bar(C::B_FIN));
+        if (!wwait(bar(C::B_FIN), 0)) give_up();
     } else if (warp == kPPvWarp) {
         // ================= P.V MMAs as soon as each tile's P and V are in
-        // place; the bulk copies of the tiles RS ahead =================
-        if (lane == 0) {
-            int4 *rec = reinterpret_cast<int4 *>(smem + C::REC_OFF);
-            int *nsub = reinterpret_cast<int *>(smem + C::NSUB_OFF);
-            Walk w;
-            walk_seek(p, seg0, nseg, h, r0, r1, 0, C::VCODE, w);
-            int issued = 0;
-            auto issue = [&]() {
-                const int st = issued % C::RS;
-                const int n = min(kPSub, w.Tend - w.T);
+        // place; the bulk copies of the tiles RS ahead (the warp runs the
+        // loop, one elected lane issues) =================
+        int4 *rec = reinterpret_cast<int4 *>(smem + C::REC_OFF);
+        int *nsub = reinterpret_cast<int *>(smem + C::NSUB_OFF);
+        Walk w;
+        walk_seek(p, seg0, nseg, h, r0, r1, 0, C::VCODE, w);
+        int issued = 0;
+        auto issue = [&]() {
+            const int st = issued % C::RS;
+            const int n = min(kPSub, w.Tend - w.T);
+            if (lane == 0) {
                 for (int k = 0; k < kPSub; ++k) {
                     const int tb = (w.T + k) * kWTile;
                     rec[st * kPSub + k] = make_int4(tb, w.la, w.le, w.pos0 + tb);
                 }
                 nsub[st] = n;
-                const uint32_t dst = sbase + C::RAW_OFF + st * C::RAW, bw = bar(C::B_RAW + st);
-                mbar_arrive_expect_tx(bw, n * C::TILE);
-                bulk_g2s(dst + C::R_K, w.gk, n * C::TILE_K, bw);
-                bulk_g2s(dst + C::R_KS, w.gks, n * C::TILE_S, bw);
-                bulk_g2s(dst + C::R_V, w.gv, n * C::TILE_V, bw);
-                bulk_g2s(dst + C::R_VS, w.gvs, n * C::TILE_S, bw);
-                w.T += n;
-                w.gk += n * C::TILE_K;
-                w.gks += n * C::TILE_S;
-                w.gv += n * C::TILE_V;
-                w.gvs += n * C::TILE_S;
-                if (w.T >= w.Tend) walk_seek(p, seg0, nseg, h, r0, r1, w.k + 1, C::VCODE, w);
-                ++issued;
-            };
-            while (issued < min(C::RS, n_tiles)) issue();
-            const uint64_t dVH0 = umma_desc(sbase + C::VH_OFF, 128, C::V_SBO);
-            const uint64_t dVH1 = umma_desc(sbase + C::VH_OFF + C::VBUF, 128, C::V_SBO);
-            const uint64_t dVL0 = umma_desc(sbase + C::VL_OFF, 128, C::V_SBO);
-            const uint64_t dVL1 = umma_desc(sbase + C::VL_OFF + C::VBUF, 128, C::V_SBO);
-            for (int j = 0; j < n_tiles; ++j) {
-                if (*bad) break;
-                if (!mbar_wait_poll(bar(C::B_PREADY), j & 1) || !mbar_wait(bar(C::B_VR + (j & 1)), (j >> 1) & 1)) {
-                    give_up();
-                    break;
-                }
-                tc_fence_after();
-                const uint64_t dVH = (j & 1) ? dVH1 : dVH0, dVL = (j & 1) ? dVL1 : dVL0;
-#pragma unroll
-                for (int ks = 0; ks < kPN / 16; ++ks) {
-                    const uint64_t o = (uint64_t)(16 * ks);   // 2 ks * 128 bytes
-                    umma_f16_ta(tO, tPH + 8 * ks, dVH + o, kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
-                    umma_f16_ta(tO, tPL + 8 * ks, dVH + o, kIdPV, 1u);
-                    umma_f16_ta(tO, tPH + 8 * ks, dVL + o, kIdPV, 1u);
-                }
-                umma_commit(bar(C::B_PV + (j & 1)));
-                // both converters are done with tile j's stage (the V warps
-                // said so; the K warps before the softmax passed tile j)
-                if (issued < n_tiles) issue();
             }
-            // drain: every MMA issued here, and the copies no converter took
-            umma_commit(bar(C::B_FIN));
-            if (!mbar_wait(bar(C::B_FIN), 0)) give_up();
-            for (int k = max(0, issued - C::RS); k < issued; ++k) mbar_wait(bar(C::B_RAW + k % C::RS), (k / C::RS) & 1);
+            __syncwarp();   // the records before the (elected lane's) arrival that publishes them
+            const uint32_t dst = sbase + C::RAW_OFF + st * C::RAW, bw = bar(C::B_RAW + st);
+            mbar_arrive_expect_tx_w(bw, n * C::TILE);
+            bulk_g2s_w(dst + C::R_K, w.gk, n * C::TILE_K, bw);
+            bulk_g2s_w(dst + C::R_KS, w.gks, n * C::TILE_S, bw);
+            bulk_g2s_w(dst + C::R_V, w.gv, n * C::TILE_V, bw);
+            bulk_g2s_w(dst + C::R_VS, w.gvs, n * C::TILE_S, bw);
+            w.T += n;
+            w.gk += n * C::TILE_K;
+            w.gks += n * C::TILE_S;
+            w.gv += n * C::TILE_V;
+            w.gvs += n * C::TILE_S;
+            if (w.T >= w.Tend) walk_seek(p, seg0, nseg, h, r0, r1, w.k + 1, C::VCODE, w);
+            ++issued;
+        };
+        while (issued < min(C::RS, n_tiles)) issue();
+        const uint64_t dVH0 = umma_desc(sbase + C::VH_OFF, 128, C::V_SBO);
+        const uint64_t dVH1 = umma_desc(sbase + C::VH_OFF + C::VBUF, 128, C::V_SBO);
+        const uint64_t dVL0 = umma_desc(sbase + C::VL_OFF, 128, C::V_SBO);
+        const uint64_t dVL1 = umma_desc(sbase + C::VL_OFF + C::VBUF, 128, C::V_SBO);
+        for (int j = 0; j < n_tiles; ++j) {
+            if (wbad()) break;
+            if (!wwait_poll(bar(C::B_PREADY), j & 1) || !wwait(bar(C::B_VR + (j & 1)), (j >> 1) & 1)) {
+                give_up();
+                break;
+            }
+            tc_fence_after();
+            const uint64_t dVH = (j & 1) ? dVH1 : dVH0, dVL = (j & 1) ? dVL1 : dVL0;
+#pragma unroll
+            for (int ks = 0; ks < kPN / 16; ++ks) {
+                const uint64_t o = (uint64_t)(16 * ks);   // 2 ks * 128 bytes
+                umma_f16_ta_w(tO, tPH + 8 * ks, dVH + o, kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
+                umma_f16_ta_w(tO, tPL + 8 * ks, dVH + o, kIdPV, 1u);
+                umma_f16_ta_w(tO, tPH + 8 * ks, dVL + o, kIdPV, 1u);
+            }
+            umma_commit_w(bar(C::B_PV + (j & 1)));
+            // both converters are done with tile j's stage (the V warps
+            // said so; the K warps before the softmax passed tile j)
+            if (issued < n_tiles) issue();
         }
-        __syncwarp();
+        // drain: every MMA issued here, and the copies no converter took
+        umma_commit_w(bar(C::B_FIN));
+        if (!wwait(bar(C::B_FIN), 0)) give_up();
+        for (int k = max(0, issued - C::RS); k < issued; ++k) mbar_wait(bar(C::B_RAW + k % C::RS), (k / C::RS) & 1);
     } else if (warp >= kPKWarp0) {
         // ================= convert: cache codes -> fp16 operands =================
         // K warps: K codes, K scales, the slot records (K(j) may overwrite
