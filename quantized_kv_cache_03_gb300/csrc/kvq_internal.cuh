@@ -307,22 +307,6 @@ __device__ __forceinline__ void walk_seek(const AttnParams &p, int seg0, int nse
     }
 }
 
-// The same wait by polling mbarrier.test_wait (no suspension between polls,
-// for waits on the critical path of a pipeline), giving up after
-// kMbarPolls polls.
-constexpr uint32_t kMbarPolls = 1u << 26;
-__device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity)
-{
-    for (uint32_t i = 0; i < kMbarPolls; ++i) {
-        uint32_t done;
-        asm volatile("{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-                     : "=r"(done)
-                     : "r"(bar), "r"(parity)
-                     : "memory");
-        if (done) return true;
-    }
-    return false;
-}
 
 // D = A(16x16 f16, row) * B(16x8 f16, col) + C, C given as four floats (bit patterns).
 __device__ __forceinline__ void mma_f16_16816_c4(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,

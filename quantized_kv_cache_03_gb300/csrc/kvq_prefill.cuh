@@ -384,13 +384,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
             atomicAdd(p.timeouts, 1u);
         }
     };
-    // warp-uniform forms for the warps that run warp-collective tcgen05 loads
+    // Warp-uniform wait.  Every wait of this kernel suspends the warp
+    // (try_wait) rather than spinning on test_wait: four roles share each
+    // SMSP, and a spinning waiter takes issue slots from the softmax warps
+    // beside it (measured: the attention call 723 -> 711 us with the issuers'
+    // and the softmax's waits suspending instead of spinning).
     auto wwait = [&](uint32_t b_, uint32_t parity) {
         const bool okw = mbar_wait(b_, parity);
-        return __all_sync(0xffffffffu, okw);
-    };
-    auto wwait_poll = [&](uint32_t b_, uint32_t parity) {
-        const bool okw = mbar_wait_poll(b_, parity);
         return __all_sync(0xffffffffu, okw);
     };
     auto wbad = [&]() { return __any_sync(0xffffffffu, *bad != 0); };
@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
         for (int j = 0; j < n_tiles; ++j) {
             if (wbad()) break;
             if (!wwait(bar(C::B_KR + (j & 1)), (j >> 1) & 1)) { give_up(); break; }
-            if (j > 0 && !wwait_poll(bar(C::B_SFREE + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { give_up(); break; }
+            if (j > 0 && !wwait(bar(C::B_SFREE + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { give_up(); break; }
             tc_fence_after();
             const uint64_t dK = (j & 1) ? dK1 : dK0;
 #pragma unroll
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
         const uint64_t dVL1 = umma_desc(sbase + C::VL_OFF + C::VBUF, 128, C::V_SBO);
         for (int j = 0; j < n_tiles; ++j) {
             if (wbad()) break;
-            if (!wwait_poll(bar(C::B_PREADY), j & 1) || !wwait(bar(C::B_VR + (j & 1)), (j >> 1) & 1)) {
+            if (!wwait(bar(C::B_PREADY), j & 1) || !wwait(bar(C::B_VR + (j & 1)), (j >> 1) & 1)) {
                 give_up();
                 break;
             }
@@ -647,13 +647,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
             // completion, so that no arrival for tile j + 1 lands in phase j.
             for (int j = 0; j < n_tiles; ++j) {
                 if (wbad()) break;
-                if (!wwait_poll(bar(C::B_SFULL), j & 1)) { give_up(); break; }
+                if (!wwait(bar(C::B_SFULL), j & 1)) { give_up(); break; }
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(bar(C::B_SFREE + (j & 1)));
                     mbar_arrive(bar(C::B_PREADY));
                 }
-                if (!wwait_poll(bar(C::B_PREADY), j & 1)) { give_up(); break; }
+                if (!wwait(bar(C::B_PREADY), j & 1)) { give_up(); break; }
             }
         } else {
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
@@ -671,7 +671,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
             const int ob = j & 1;
             // this tile's scores, and (directly from the converters) its K
             // scales and slot records
-            if (!wwait_poll(bar(C::B_SFULL), j & 1) || !wwait(bar(C::B_KR + ob), (j >> 1) & 1)) { give_up(); break; }
+            if (!wwait(bar(C::B_SFULL), j & 1) || !wwait(bar(C::B_KR + ob), (j >> 1) & 1)) { give_up(); break; }
             tc_fence_after();
             const float *skf = reinterpret_cast<const float *>(smem + C::SKF_OFF) + ob * kNB * kPN + HP * hf;
             float s[HP];
@@ -757,7 +757,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
             xm[(ob * 2 + hf) * kPM + row] = mx;
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_X + quarter));
-            if (!wwait_poll(bar(C::B_X + quarter), j & 1)) { give_up(); break; }
+            if (!wwait(bar(C::B_X + quarter), j & 1)) { give_up(); break; }
             mx = fmaxf(mx, xm[(ob * 2 + (hf ^ 1)) * kPM + row]);
             const bool need = mx > m + kSlack;
             const bool wneed = o_live && __any_sync(0xffffffffu, need);   // rescale O (whole warp)
@@ -781,7 +781,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
             l += lsum.x + lsum.y;
             // P(j) may overwrite P(j-1) once P.V(j-1) is done; O is then stable
             if (j > 0) {
-                if (!wwait_poll(bar(C::B_PV + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { give_up(); break; }
+                if (!wwait(bar(C::B_PV + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { give_up(); break; }
                 tc_fence_after();
             }
             if (wneed) {   // O *= alpha on this half's columns (1 on the rows that keep their max)
