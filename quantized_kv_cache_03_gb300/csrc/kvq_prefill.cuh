@@ -299,12 +299,17 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
         fence_mbar_init();
     }
 
-    // ---- softmax warps: warp w takes tile rows 32(w%4)..+31 (its TMEM lane
-    // quarter) and, of each KV tile, positions 32(w/4)..+31; in the prologue
-    // it quantizes blocks 2(w/4), 2(w/4)+1 of its row ----
+    // ---- softmax warps: warp w takes the 32 tile rows of its TMEM lane
+    // quarter w%4 and, of each KV tile, positions 32(w/4)..+31; in the
+    // prologue it quantizes blocks 2(w/4), 2(w/4)+1 of its row.  Rows are
+    // numbered from lane quarter 2 on (rows 0-31 in lanes 64-95, 32-63 in
+    // 96-127, then 0-31 and 32-63): a tile of up to 64 rows then runs its
+    // softmax on SMSPs 2 and 3, beside the issuer warps, rather than on 0 and
+    // 1, beside the K converters ----
     const bool srole = warp < kPSoftWarps;
     const int quarter = warp & 3, hf = (warp >> 2) & 1;
-    const int row = 32 * quarter + lane;
+    const int rq = (quarter + 2) & 3;        // the quarter's place in the row order
+    const int row = 32 * rq + lane;
     const bool row_ok = srole && row < R;
     int lim = -1;                            // last visible position of the row
     size_t orow = 0;
@@ -638,7 +643,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_attn_kernel(const __grid
         // each KV tile, head-dim columns 64hf..64hf+63 of O.  The two halves of
         // a row agree on its reference max through the tile-max exchange, and
         // keep their own partial sums l.
-        if (32 * quarter >= R) {
+        if (32 * rq >= R) {
             // No query row in this TMEM lane quarter (a tile of up to 32 rows,
             // or the ragged last one): keep the barrier phases in step with
             // the live warps and do nothing else.  Per tile: S(j) complete,
