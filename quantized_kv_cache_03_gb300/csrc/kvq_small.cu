@@ -146,11 +146,15 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
 }
 
 // The same merge for launches whose rows have at most kNarrowSplits splits
-// each (long query chunks: thousands of rows, two or three splits): one warp
-// per row, eight rows per CTA, the splits merged one after another in split
-// order with the same running (max, weight sum, weighted o).  One CTA per row
-// would leave most warps idle and make the launch a stream of tiny CTAs.
-constexpr int kNarrowSplits = 8;
+// each (long query chunks: thousands of rows, two splits; the long-context
+// step: 56 rows, 12 splits): one warp per row, eight rows per CTA, the splits
+// merged one after another in split order with the same running (max, weight
+// sum, weighted o).  One CTA per row would leave most warps idle and make the
+// launch a stream of tiny CTAs.  Measured: the prefill chunk's 16384 rows x 2
+// splits 31 -> 8 us; the long-context step 65.78 -> 65.47 us; 32 rows x 16
+// splits slower this way (11.85 -> 12.5 us per step), so more splits keep
+// one CTA per row.
+constexpr int kNarrowSplits = 12;
 
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_rows_kernel(const __grid_constant__ CombineParams p,
                                                                           int n_rows)

@@ -29,11 +29,14 @@ def _built():
     __graft_entry__.build()
 
 
-def test_a_lost_stage_gives_up_poisons_its_rows_and_counts(monkeypatch):
+@pytest.mark.parametrize("ctx", [6000, 28000])
+def test_a_lost_stage_gives_up_poisons_its_rows_and_counts(ctx, monkeypatch):
     # 2048-position splits of 16 warps: warp 0 of each CTA streams 128
-    # positions, four copy stages, so its second stage exists
+    # positions, four copy stages, so its second stage exists.  3 splits per
+    # kv head at 6000 positions (the combine's row-per-warp form), 14 at 28000
+    # (one CTA per row): both forms must carry the poisoned partial into NaN.
     monkeypatch.setenv("KVQ_SPLIT", "2048")
-    spec = W.make_spec("long", ctx=6000)[0]          # 40 query / 8 kv heads, q4_0 V, 4 segments
+    spec = W.make_spec("long", ctx=ctx)[0]           # 40 query / 8 kv heads, q4_0 V, 4 segments
     case = Case(spec).build()
     call = dict(cache=case.cache, n_q_heads=case.Hq, t_q=1, causal_tail=False, max_len=case.max_len,
                 head_map=None, sm_scale=SM_SCALE)
