@@ -136,16 +136,19 @@ KERNEL_SOURCES = {
 
 
 _COMMENT = re.compile(rb"/\*.*?\*/|//[^\n]*", re.S)
+_SPACE = re.compile(rb"\s+")
 
 
 def kernel_source_hash(kernel="split_attn"):
-    """Hash of the kernel's source files with C comments removed, so that
-    counters taken on a kernel stay valid across comment-only edits."""
+    """Hash of the kernel's source files with C comments removed and every run
+    of white space collapsed to one blank, so that counters taken on a kernel
+    stay valid across comment-only and layout-only edits."""
     h = hashlib.sha256()
     pkg = os.path.join(ROOT, "quantized_kv_cache_03_gb300")
     for f in KERNEL_SOURCES[kernel] + ["../include/kvq.h"]:
         with open(os.path.normpath(os.path.join(pkg, f)), "rb") as fh:
-            h.update(_COMMENT.sub(b"", fh.read()))
+            h.update(_SPACE.sub(b" ", _COMMENT.sub(b"", fh.read())).strip())
+            h.update(b"\n")
     return h.hexdigest()[:16]
 
 

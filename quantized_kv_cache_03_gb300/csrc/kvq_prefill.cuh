@@ -1,12 +1,13 @@
 // kvq_prefill.cuh -- attention over the quantized cache for long query chunks
 // (chunked prefill) on the sm_103a tensor cores (tcgen05, accumulators in TMEM).
 //
-// One CTA = (row tile, split s, kv head h, sequence b) of a work group, indexed
-// like the split kernel's CTAs: it attends kPM = 128 query rows of kv head h
-// (row g = query token g / group, query head grp_q[g % group]) over the
-// positions [s*chunk, (s+1)*chunk) of sequence b, 64 positions (one KV tile)
-// at a time, and writes the final output (one split) or a partial (normalised
-// o, lse) for the combine kernel.
+// One CTA = (row tile, split s, kv head h, sequence b) of a work group: it
+// attends kPM = 128 query rows of kv head h (row g = query token g / group,
+// query head grp_q[g % group]) over split s's positions of sequence b ([0,
+// chunk0) for s = 0, then chunk-sized pieces), 64 positions (one KV tile) at a
+// time, and writes the final output (one split) or a partial (normalised o,
+// lse) for the combine kernel.  CTAs are ordered like the split kernel's, or
+// split first when the launch is split unevenly (large first pieces ahead).
 //
 // What it computes is the split kernel's arithmetic (scheme of the quantized
 // KV cache pages: per-32 int8 K and Q with fp16 scales, integer block dot,
@@ -24,20 +25,25 @@
 //     bits of every product.  (The 1/2 keeps d * code inside fp16's range
 //     when the q8_0 scale rounded up; it is undone at the end.)
 //
-// Warp roles (288 threads):
-//   warps 0-3  softmax: Q quantization, score assembly from TMEM, softmax,
-//              P (hi, lo) to shared memory, the final O read-out;
-//   warps 4-7  convert: one KV tile's cache codes (copied in by bulk copies)
-//              to the fp16 operand layouts (K codes, V hi / lo), zero where a
-//              slot holds no visible cache row;
-//   warp 8     control: TMEM allocation; lane 0 walks the segments, issues
-//              the bulk copies and every tcgen05.mma.
-// Per KV tile j the control lane issues QK(j) as soon as the softmax warps
-// have read S(j-1), then P.V(j-1), so the tensor core computes the next scores
-// while the softmax works on the current ones.  Every wait is bounded: a wait
-// that gives up marks the CTA, the roles leave their loops, in-flight copies
-// and MMAs are waited for (bounded), TMEM is released and the CTA's rows are
-// written as NaN.
+// Warp roles (512 threads, one CTA per SM, all 512 TMEM columns):
+//   warps 0-7   softmax: two per TMEM lane quarter (positions 0-31 / 32-63 of
+//               a tile); Q quantization into TMEM, score assembly from the
+//               four S_b, softmax, P (hi, lo) into TMEM, O rescale and the
+//               final O read-out;
+//   warps 8-9   K converters: K codes to the fp16 operand layout, K scales,
+//               the slot records;
+//   warps 10-13 V converters: V codes to v/2 hi and lo;
+//   warp 14     QK issuer (and the TMEM allocation);
+//   warp 15     P.V issuer; it also walks the segments and issues the bulk
+//               copies of the raw tiles, three stages ahead.
+// The issuers run their loops as converged warps and issue every MMA, commit
+// and copy from one lane elected inside the instruction's asm.  QK(j+1) is
+// issued once K(j+1) is converted and the softmax has read S(j); P.V(j) once
+// P(j) is in TMEM and V(j) converted, so the tensor core computes the next
+// scores while the softmax works on the current ones.  Every wait suspends
+// the warp (try_wait) and is bounded: a wait that gives up marks the CTA, the
+// roles leave their loops, in-flight copies and MMAs are waited for (bounded),
+// TMEM is released and the CTA's rows are written as NaN.
 //
 // Operands live in shared memory, K-major without swizzle: 8 rows x 16 bytes
 // core matrices, a row group's core matrices LBO bytes apart along K (128 for
