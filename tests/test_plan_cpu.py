@@ -191,6 +191,22 @@ def test_prefill_chunk(monkeypatch):
     assert (ln["kernel"], ln["n_tiles8"]) == ("split", 4)
 
 
+def test_uneven_split_only_for_one_partial_wave_of_one_group():
+    """The uneven split applies to a one-group tcgen05 launch whose units fill
+    more than half but not all of the SMs.  At most half (4 kv heads x 16 row
+    tiles = 64 units) the even split already fills the machine (2 x 64 CTAs);
+    more units than SMs (10 kv heads: 160) take even splits over several
+    waves; two calls in one launch (two work groups) keep even splits too."""
+    for kw, units in ((dict(n_q_heads=16, n_kv_heads=4), 64), (dict(n_q_heads=40, n_kv_heads=10), 160)):
+        _, calls = calls_of("prefill", fused=False, **kw)
+        ln = plan(calls)[0][0]
+        assert ln["kernel"] == "prefill" and ln["chunk0"] == ln["chunk"], kw
+        assert ln["n_ctas"] % units == 0 and ln["n_ctas"] > units, kw
+    _, calls = calls_of("prefill", fused=False)
+    ln = plan(calls + calls)[0][0]
+    assert ln["kernel"] == "prefill" and ln["chunk0"] == ln["chunk"] and ln["n_ctas"] % 256 == 0
+
+
 def test_bad_arguments():
     _, calls = calls_of("tiny", fused=True)
     with pytest.raises(kvq.KvqError):
