@@ -29,7 +29,13 @@
  * asynchronous: no call synchronizes the host.  Kernels are chained with
  * programmatic dependent launch (set KVQ_PDL=0 in the environment to launch
  * them plainly); calls can be captured into CUDA graphs once the first call on
- * the device has run outside capture (it caches device attributes).
+ * the device has run outside capture (it caches device attributes).  Other
+ * environment knobs steer the launch plan only, never the arithmetic's
+ * definition: KVQ_SPLIT (force the split chunk), KVQ_SPLIT_WARPS, KVQ_ROW_TILE,
+ * KVQ_PREFILL=0 and KVQ_TC_ROWS (which kernel takes long query chunks), and
+ * KVQ_PREFILL_BALANCE / KVQ_PREFILL_CTA_COST (the uneven two-way split of a
+ * one-wave tcgen05 launch).  A plan with more splits changes the order of the
+ * fp32 sums, within the stated tolerance.
  *
  * Errors.  Arguments are validated before anything is enqueued; a failed
  * validation returns a status and changes no state (kvq_append bumps segment
@@ -455,7 +461,7 @@ kvq_status kvq_debug_lose_stage(const kvq_cache *c, const void *q16, int32_t n_q
  *   i = 2  16-row tiles;                   3  32-row tiles.
  * It reads the calls' host descriptors and the same environment knobs as the
  * decode call (KVQ_SPLIT, KVQ_SPLIT_WARPS, KVQ_ROW_TILE, KVQ_PREFILL,
- * KVQ_TC_ROWS).  It
+ * KVQ_TC_ROWS, KVQ_PREFILL_BALANCE, KVQ_PREFILL_CTA_COST).  It
  * touches no device and dereferences no device pointer, so segments and
  * k16_new / v16_new may hold any non-null 16-byte-aligned address; q16,
  * seq_lens, out and lse may be NULL.
