@@ -222,30 +222,19 @@ __device__ __forceinline__ void fence_mbar_init()
 // Order this thread's earlier generic-proxy shared accesses before later
 // async-proxy ones (a bulk copy into a stage the warp has just read).
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// Issued by a converged warp: every lane passes the same (warp-uniform)
+// operands and one lane, elected inside the asm, issues.  (Issuing from inside
+// a lane-0 branch costs more per instruction: the uniform operands have to be
+// taken out of a divergent lane.)
 // One arrival that also announces tx bytes still to land on the barrier.
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t tx)
-{
-    asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(bar), "r"(tx)
-                 : "memory");
-}
-// Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses
-// 16-byte aligned) that completes its bytes on barrier `bar`.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-// Warp-collective forms of the two calls above: every lane of a converged
-// warp passes the same (warp-uniform) operands and one elected lane issues.
-// Issuing from inside a lane-0 branch instead costs more per instruction (the
-// uniform operands have to be taken out of a divergent lane).
 __device__ __forceinline__ void mbar_arrive_expect_tx_w(uint32_t bar, uint32_t tx)
 {
     asm volatile("{\n .reg .pred e;\n .reg .b64 st;\n elect.sync _|e, 0xffffffff;\n"
                  " @e mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(bar), "r"(tx)
                  : "memory");
 }
+// Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses
+// 16-byte aligned) that completes its bytes on barrier `bar`.
 __device__ __forceinline__ void bulk_g2s_w(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
 {
     asm volatile("{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
