@@ -156,6 +156,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
 // one CTA per row.
 constexpr int kNarrowSplits = 12;
 
+// NS: the most splits a row of the launch has room for (4 or kNarrowSplits):
+// every lane loads NS slots, so a launch of two-split rows takes the small form.
+template <int NS>
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_rows_kernel(const __grid_constant__ CombineParams p,
                                                                           int n_rows)
 {
@@ -172,10 +175,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_rows_kernel(const 
     const int row = r - G.row0, n = G.n_split;
     const float *ls = G.ws_lse + (size_t)row * n;
     const float4 *o = reinterpret_cast<const float4 *>(G.ws_o + (size_t)row * n * kD) + lane;
-    float lv[kNarrowSplits];
-    float4 v[kNarrowSplits];
+    float lv[NS];
+    float4 v[NS];
 #pragma unroll
-    for (int k = 0; k < kNarrowSplits; ++k) {   // every split's lse and o in one round trip
+    for (int k = 0; k < NS; ++k) {   // every split's lse and o in one round trip
         lv[k] = (k < n) ? ls[k] : -INFINITY;
         v[k] = (k < n) ? o[(size_t)k * (kD / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_rows_kernel(const 
     bool poisoned = false;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < kNarrowSplits; ++k) {
+    for (int k = 0; k < NS; ++k) {
         poisoned |= lv[k] != lv[k];
         if (lv[k] == -INFINITY || lv[k] != lv[k]) continue;
         const float mx = fmaxf(m, lv[k]);
@@ -220,7 +223,8 @@ cudaError_t launch_combine(const CombineParams &p, int n_rows, cudaStream_t s, b
     at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    if (narrow) return cudaLaunchKernelEx(&cfg, combine_rows_kernel, p, n_rows);
+    if (narrow && max_split <= 4) return cudaLaunchKernelEx(&cfg, combine_rows_kernel<4>, p, n_rows);
+    if (narrow) return cudaLaunchKernelEx(&cfg, combine_rows_kernel<kNarrowSplits>, p, n_rows);
     return cudaLaunchKernelEx(&cfg, combine_kernel, p);
 }
 
