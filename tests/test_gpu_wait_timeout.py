@@ -29,12 +29,13 @@ def _built():
     __graft_entry__.build()
 
 
-@pytest.mark.parametrize("ctx", [6000, 28000])
+@pytest.mark.parametrize("ctx", [6000, 16000, 28000])
 def test_a_lost_stage_gives_up_poisons_its_rows_and_counts(ctx, monkeypatch):
     # 2048-position splits of 16 warps: warp 0 of each CTA streams 128
     # positions, four copy stages, so its second stage exists.  3 splits per
-    # kv head at 6000 positions (the combine's row-per-warp form), 14 at 28000
-    # (one CTA per row): both forms must carry the poisoned partial into NaN.
+    # kv head at 6000 positions and 8 at 16000 (the combine's row-per-warp
+    # form with 4 and with 12 slots), 14 at 28000 (one CTA per row): every
+    # form must carry the poisoned partial into NaN.
     monkeypatch.setenv("KVQ_SPLIT", "2048")
     spec = W.make_spec("long", ctx=ctx)[0]           # 40 query / 8 kv heads, q4_0 V, 4 segments
     case = Case(spec).build()
