@@ -330,41 +330,6 @@ int tile_rows(const Launch &ln) { return ln.prefill ? kPrefillRows : 8 * ln.nt; 
 // CTA) and at least 256 positions; KVQ_SPLIT forces a chunk (rounded to the
 // 64-position segment alignment).
 constexpr int kOverhead = 512;
-
-// Uneven two-way split of a one-wave tcgen05 launch.  With U CTAs of one
-// group on S SMs (S / 2 < U < S; one CTA per SM), S - U SMs idle for the whole
-// launch.  Splitting every unit at c0 instead gives U large CTAs [0, c0),
-// dispatched first, and U small ones [c0, reach) that the S - U idle SMs take
-// k = ceil(U / (S - U)) at a time; the combine merges the two partials.
-// c0 balances the large CTAs' time c0 + o against k (reach - c0 + o), o the
-// fixed cost of one CTA in positions.  KVQ_PREFILL_BALANCE=0 turns it off, a
-// positive value forces k.  Returns false (launch unchanged) when it does not
-// pay by at least 5 %.
-constexpr int kPrefillCtaCost = 256;
-bool uneven_split(const std::vector<Desc> &ds, Launch &ln, int n_sms)
-{
-    if (!ln.prefill || ln.units.size() != 1) return false;
-    const char *fs = std::getenv("KVQ_SPLIT");
-    if (fs && std::atoi(fs) > 0) return false;
-    const char *env = std::getenv("KVQ_PREFILL_BALANCE");
-    const int forced = env ? std::atoi(env) : -1;
-    if (forced == 0) return false;
-    const Unit &u = ln.units[0];
-    const Desc &d = ds[u.d];
-    const int lmax = u.reach;
-    if (lmax <= 0 || ln.chunk < lmax) return false;   // already split evenly
-    const long long U = (long long)((d.max_rows + kPrefillRows - 1) / kPrefillRows) * d.c->n_kv_heads * u.nb;
-    if (U >= n_sms || 2 * U <= n_sms) return false;
-    const long long k = forced > 0 ? forced : (U + (n_sms - U) - 1) / (n_sms - U);
-    const char *ce = std::getenv("KVQ_PREFILL_CTA_COST");
-    const long long o = (ce && std::atoi(ce) >= 0) ? std::atoi(ce) : kPrefillCtaCost;
-    const int c0 = round_up((int)((k * lmax + (k - 1) * o + k) / (k + 1)), kPrefillPositions);
-    if (c0 >= lmax || (double)(c0 + o) > 0.95 * (double)(lmax + o)) return false;
-    ln.chunk0 = c0;
-    ln.chunk = round_up(lmax - c0, kPrefillPositions);
-    ln.split_major = true;
-    return true;
-}
 int choose_chunk(const std::vector<Desc> &ds, const Launch &ln, int slots, int gran)
 {
     int lmax = 0;
@@ -406,6 +371,42 @@ int choose_chunk(const std::vector<Desc> &ds, const Launch &ln, int slots, int g
     }
     if ((lmax + chunk - 1) / chunk > 1024) chunk = round_up((lmax + 1023) / 1024, gran);
     return chunk;
+}
+
+// Uneven two-way split of a one-wave tcgen05 launch.  With U CTAs of one
+// group on S SMs (S / 2 < U < S; one CTA per SM), S - U SMs idle for the whole
+// launch.  Splitting every unit at c0 instead gives U large CTAs [0, c0),
+// dispatched first, and U small ones [c0, reach) that the S - U idle SMs take
+// k = ceil(U / (S - U)) at a time; the combine merges the two partials.
+// c0 balances the large CTAs' time c0 + o against k (reach - c0 + o), o the
+// fixed cost of one CTA in positions (KVQ_PREFILL_CTA_COST overrides it).
+// KVQ_PREFILL_BALANCE=0 turns the split off, a positive value forces k.  A
+// chunk forced by KVQ_SPLIT keeps even splits.  Returns false (launch
+// unchanged) when the split does not pay by at least 5 %.
+constexpr int kPrefillCtaCost = 256;
+bool uneven_split(const std::vector<Desc> &ds, Launch &ln, int n_sms)
+{
+    if (!ln.prefill || ln.units.size() != 1) return false;
+    const char *fs = std::getenv("KVQ_SPLIT");
+    if (fs && std::atoi(fs) > 0) return false;
+    const char *env = std::getenv("KVQ_PREFILL_BALANCE");
+    const int forced = env ? std::atoi(env) : -1;
+    if (forced == 0) return false;
+    const Unit &u = ln.units[0];
+    const Desc &d = ds[u.d];
+    const int lmax = u.reach;
+    if (lmax <= 0 || ln.chunk < lmax) return false;   // already split evenly
+    const long long U = (long long)((d.max_rows + kPrefillRows - 1) / kPrefillRows) * d.c->n_kv_heads * u.nb;
+    if (U >= n_sms || 2 * U <= n_sms) return false;
+    const long long k = forced > 0 ? forced : (U + (n_sms - U) - 1) / (n_sms - U);
+    const char *ce = std::getenv("KVQ_PREFILL_CTA_COST");
+    const long long o = (ce && std::atoi(ce) >= 0) ? std::atoi(ce) : kPrefillCtaCost;
+    const int c0 = round_up((int)((k * lmax + (k - 1) * o + k) / (k + 1)), kPrefillPositions);
+    if (c0 >= lmax || (double)(c0 + o) > 0.95 * (double)(lmax + o)) return false;
+    ln.chunk0 = c0;
+    ln.chunk = round_up(lmax - c0, kPrefillPositions);
+    ln.split_major = true;
+    return true;
 }
 
 // Pack the calls' sequences into launches (tables of AttnParams bound the
