@@ -270,6 +270,14 @@ def test_uneven_split_of_a_one_wave_launch(kernel, monkeypatch):
                              spec.v_type, want_scores=True, n_threads=8)
     got_sc = sc.view(nr, L, 4)[torch.as_tensor(rows, device=dev())].cpu().numpy()
     assert np.array_equal(got_sc, refs["scores"][0])
+    # the split-major CTA order and the two-partial combine repeat bit for
+    # bit, with and without programmatic dependent launch
+    again = [case.decode() for _ in range(2)]
+    monkeypatch.setenv("KVQ_PDL", "0")
+    again.append(case.decode())
+    monkeypatch.delenv("KVQ_PDL")
+    for o2, l2 in again:
+        assert np.array_equal(o2, out) and np.array_equal(l2, lse)
     monkeypatch.setenv("KVQ_PREFILL_BALANCE", "0")
     assert kvq.kvq_debug_plan([call], 152)[0][0]["n_ctas"] == 128
     out0, lse0 = case.decode()
